@@ -72,7 +72,7 @@ def _bind(lib):
     P = ctypes.c_void_p
     i = ctypes.c_int
     lib.oracle_attention_rows.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.c_double,
-                                          P, P, P, P, P, P, P, ctypes.c_int64, P, P, P]
+                                          P, P, P, P, P, P, P, ctypes.c_int64, P, P, P, P, P]
     lib.oracle_attention_rows.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
@@ -90,12 +90,15 @@ def _c(a: np.ndarray, dtype) -> np.ndarray:
 def attention_rows(*, num_q_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                    rel_extent: int, window: int, sm_scale: float,
                    cu_q, seq_lens, q_bits, k_bits, v_bits, block_table, rel,
-                   rows_t, rows_h, lib=None) -> np.ndarray:
+                   rows_t, rows_h, q_rows_bits=None, rel_rows=None, lib=None) -> np.ndarray:
     """fp64 output rows ``[n_rows, D]`` for the (packed row, head) pairs given.
 
     ``q_bits``/``k_bits``/``v_bits`` are bf16 bit patterns (uint16 arrays) shaped
     ``[total_q, Hq, D]`` and ``[num_pages, Hkv, P, D]``; ``rel`` is fp32
     ``[total_q, Hq, E]``; ``block_table`` is int32 ``[B, max_pages]``.
+    ``q_rows_bits`` ``[n_rows, D]`` and ``rel_rows`` ``[n_rows, E]``, when given, are the
+    query vectors and bias rows of the requested rows (``q_bits``/``rel`` may then be
+    empty placeholders).
     """
     lib = lib or load()
     cu_q = _c(cu_q, np.int32)
@@ -107,17 +110,23 @@ def attention_rows(*, num_q_heads: int, num_kv_heads: int, head_dim: int, page_s
     rel = _c(rel, np.float32)
     rows_t = _c(rows_t, np.int32)
     rows_h = _c(rows_h, np.int32)
+    if q_rows_bits is not None:
+        q_rows_bits = _c(q_rows_bits, np.uint16)
+        assert q_rows_bits.shape == (rows_t.shape[0], head_dim)
+    if rel_rows is not None:
+        rel_rows = _c(rel_rows, np.float32)
+        assert rel_rows.shape == (rows_t.shape[0], rel_extent)
     num_seqs = seq_lens.shape[0]
     num_pages = k_bits.shape[0]
     max_pages = block_table.shape[1] if block_table.ndim == 2 else 0
     n = rows_t.shape[0]
     out = np.zeros((n, head_dim), dtype=np.float64)
-    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    ptr = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
     st = lib.oracle_attention_rows(num_seqs, num_q_heads, num_kv_heads, head_dim, page_size,
                                    max_pages, num_pages, rel_extent, window, float(sm_scale),
                                    ptr(cu_q), ptr(seq_lens), ptr(q_bits), ptr(k_bits),
                                    ptr(v_bits), ptr(block_table), ptr(rel), n, ptr(rows_t),
-                                   ptr(rows_h), ptr(out))
+                                   ptr(rows_h), ptr(q_rows_bits), ptr(rel_rows), ptr(out))
     if st != 0:
         raise ValueError(f"oracle rejected the inputs (status {st})")
     return out

@@ -90,6 +90,10 @@ static int owner_of_row(const int32_t* cu_q, int num_seqs, int64_t t) {
  * k_cache/v_cache: [num_pages, Hkv, P, D] bf16 bits
  * block_table: [num_seqs, max_pages] int32
  * rel:         [total_q, Hq, E] fp32
+ * q_rows, rel_rows: optional (may be NULL).  When given, the query vector and bias row
+ *              of output row r are q_rows[r*D ..] and rel_rows[r*E ..] instead of
+ *              q[t, h, :] and rel[t, h, :] (lets a caller pass only the sampled rows of a
+ *              problem too large to copy whole; q / rel are then unused).
  */
 int oracle_attention_rows(
     int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -99,6 +103,7 @@ int oracle_attention_rows(
     const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
     const int32_t* block_table, const float* rel,
     int64_t n_rows, const int32_t* row_t, const int32_t* row_h,
+    const uint16_t* q_rows, const float* rel_rows,
     double* out)
 {
     if (num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1) return -1;
@@ -142,8 +147,10 @@ int oracle_attention_rows(
                 cap = n_vis;
                 s = (double*)malloc((size_t)cap * sizeof(double));
             }
-            const uint16_t* qrow = q + (t * num_q_heads + h) * (int64_t)head_dim;
-            const float* brow = rel + (t * num_q_heads + h) * (int64_t)rel_extent;
+            const uint16_t* qrow = q_rows ? q_rows + r * (int64_t)head_dim
+                                          : q + (t * num_q_heads + h) * (int64_t)head_dim;
+            const float* brow = rel_rows ? rel_rows + r * (int64_t)rel_extent
+                                         : rel + (t * num_q_heads + h) * (int64_t)rel_extent;
             int bad = 0;
             double m = -INFINITY;
             for (int64_t k = lo; k <= p; ++k) {
