@@ -1,0 +1,443 @@
+"""Benchmark of the paged relative-bias GQA attention path on GB300.
+
+Default (N=1): the SWA-layer decode workload (batch 64, 64 query heads over 16 KV heads,
+head_dim 128, window 512, contexts U{1024..8192}, page 64, fp32 bias [64, 64, 512]) is
+the headline step: one decode call, i.e. one pass of every step of the hot path (page
+walk, scores, bias gather, mask, online softmax, PV, split-K merge, store).  The same
+run also reports the other workloads (global decode, SWA prefill tiny, global prefill,
+mixed 5 SWA + 1 global serving step) under "workloads".
+
+One JSON line is printed by rank 0.  `--impl reference` times the fp64 CPU oracle on
+the same workload instead (a bounded row sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import shutil
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_attention_relative_gqa_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode attn HBM GB/s (% of 8 TB/s); prefill attn TFLOP/s (% bf16 peak); tok/s"
+HEADLINE = "swa_decode"
+
+
+# ---------------------------------------------------------------- algorithmic work
+
+def visible_ranges(prob):
+    """Per new token: (p, lo) of its visible keys."""
+    out = []
+    for n, L in zip(prob.q_lens, prob.seq_lens_list):
+        pos = np.arange(L - n, L, dtype=np.int64)
+        lo = np.zeros_like(pos) if prob.window <= 0 else np.maximum(0, pos - prob.window + 1)
+        out.append((pos, lo))
+    return out
+
+
+def decode_bytes(prob) -> int:
+    """K+V of visible keys, bias buckets used, Q and out, table entries and lengths read."""
+    D, Hq, Hkv, E, P = prob.head_dim, prob.num_q_heads, prob.num_kv_heads, prob.rel_extent, prob.page_size
+    total = 0
+    for (pos, lo) in visible_ranges(prob):
+        for p, l in zip(pos.tolist(), lo.tolist()):
+            vis = p - l + 1
+            total += vis * Hkv * D * 2 * 2
+            total += Hq * min(vis, E) * 4
+            total += ((p // P) - (l // P) + 1) * 4
+    total += prob.total_q * Hq * D * 2 * 2 + prob.num_seqs * 4
+    return total
+
+
+def prefill_work(prob):
+    """(FLOPs, bytes): 4*D per visible (row, key, head); bias read once, Q/out, K/V once."""
+    D, Hq, Hkv, E = prob.head_dim, prob.num_q_heads, prob.num_kv_heads, prob.rel_extent
+    flops = 0
+    bias = 0
+    for (pos, lo) in visible_ranges(prob):
+        vis = pos - lo + 1
+        flops += int(vis.sum()) * 4 * D * Hq
+        bias += int(np.minimum(vis, E).sum()) * Hq * 4
+    kv = sum(prob.seq_lens_list) * Hkv * D * 2 * 2
+    qo = prob.total_q * Hq * D * 2 * 2
+    return flops, bias + kv + qo
+
+
+# ---------------------------------------------------------------- GPU timing helpers
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        smi = shutil.which("nvidia-smi")
+        if not smi:
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.proc = subprocess.Popen([smi, "-i", str(self.index), f"--query-gpu={self.Q}",
+                                      "--format=csv,noheader,nounits", "-lms", "100"],
+                                     stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        time.sleep(0.3)
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def time_steps(fns, steps, warmup, stream):
+    """Warm up, then time exactly `steps` calls (cycling through `fns`) with CUDA events
+    on `stream`; returns ms per step."""
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            fns[i % len(fns)]()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(steps):
+            fns[i % len(fns)]()
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash(name: str) -> str:
+    p = os.path.join(ROOT, "paged_attention_relative_gqa_gb300", "csrc", name)
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            t = json.load(f)
+        e = t[workload]
+        if e.get("source_sha256_16") == kernel_source_hash(kernel_file):
+            return int(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- our arm
+
+def make_call(binding, prob, out, ws):
+    params = binding.params_of(prob)
+    if prob.is_decode:
+        return lambda: binding.inkling_attn_decode(params, prob.q, prob.k_cache, prob.v_cache,
+                                                   prob.block_table, prob.seq_lens, prob.rel_logits,
+                                                   out, ws)
+    return lambda: binding.inkling_attn_prefill(params, prob.q, prob.cu_q_lens, prob.max_q_len,
+                                                prob.k_cache, prob.v_cache, prob.block_table,
+                                                prob.seq_lens, prob.rel_logits, out, ws)
+
+
+def instances(factory, dev, n):
+    """`n` independently seeded instances of a workload: alternating them keeps each
+    step's inputs out of L2 (every instance is larger than the 129 MB L2)."""
+    return [factory(dev, seed) for seed in range(n)]
+
+
+def bench_workload(binding, probs, steps, warmup, stream):
+    calls = []
+    keep = []
+    for prob in probs:
+        params = binding.params_of(prob)
+        ws = binding.alloc_workspace(params, True, prob.q.device)
+        out = torch.empty_like(prob.q)
+        keep.append((ws, out))
+        calls.append(make_call(binding, prob, out, ws))
+    ms = time_steps(calls, steps, warmup, stream)
+    for (ws, _) in keep:
+        assert binding.inkling_attn_read_device_error(ws) == 0
+    return ms
+
+
+def e2e_decode(binding, prob, steps, warmup, stream):
+    """Through the C ABI with host buffers: each step copies the step's inputs (q, bias,
+    block table, lengths) from pinned host memory, runs decode, and reads the output
+    back.  The K/V pool is the resident cache."""
+    dev = prob.q.device
+    host = {k: getattr(prob, k).cpu().pin_memory() for k in ("q", "rel_logits", "block_table", "seq_lens")}
+    dbuf = {k: torch.empty_like(getattr(prob, k)) for k in host}
+    out = torch.empty_like(prob.q)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    params = binding.params_of(prob)
+    ws = binding.alloc_workspace(params, True, dev)
+
+    def step():
+        for k in host:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        binding.inkling_attn_decode(params, dbuf["q"], prob.k_cache, prob.v_cache, dbuf["block_table"],
+                                    dbuf["seq_lens"], dbuf["rel_logits"], out, ws)
+        out_h.copy_(out, non_blocking=True)
+
+    ms = time_steps([step], steps, warmup, stream)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    return ms, h2d, d2h
+
+
+def cpu_baseline_decode(prob_cpu, seconds: float = 10.0):
+    """The fp64 oracle on whole passes of the workload, repeated for about `seconds`."""
+    import oracle
+    kw = prob_cpu.oracle_kwargs()
+    nbytes = decode_bytes(prob_cpu)
+    t_sum, passes = 0.0, 0
+    while t_sum < seconds:
+        t0 = time.perf_counter()
+        oracle.attention(**kw)
+        t_sum += time.perf_counter() - t0
+        passes += 1
+    gbs = nbytes * passes / t_sum / 1e9
+    return gbs, t_sum, passes, oracle.num_threads()
+
+
+def run_ours(args, rank, world, local_rank):
+    from paged_attention_relative_gqa_gb300 import binding, build
+
+    build.build()
+    binding.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    hbm_peak, bf16_peak, peak_src = peaks()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ---- headline: SWA decode (two alternating instances, each > L2)
+    probs = instances(lambda d, s: W.swa_decode(d, seed=2 + 1000 * s), dev, 2)
+    nbytes = decode_bytes(probs[0])
+    clocks = Clocks(local_rank)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    ms = bench_workload(binding, probs, args.steps, args.warmup, stream)
+    clk = clocks.stop()
+    barrier()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = e2e_decode(binding, probs[0], max(10, args.steps // 2), args.warmup, stream)
+    e2e_gbs = nbytes / (e2e_ms * 1e-3) / 1e9
+    tok_s = probs[0].num_seqs / (ms * 1e-3)
+    B = probs[0].num_seqs
+    line = {
+        "metric": METRIC, "value": round(gbs * world, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; Q/K/V ~N(0,1) bf16, bias ~N(0,0.5) fp32)",
+        "config": {"workload": "swa_decode: batch 64, 64 q heads / 16 kv heads, head_dim 128, "
+                               "window 512, contexts U{1024..8192}, page 64, bias [64,64,512] fp32",
+                   "global_batch": B * world, "seq_len": "1024-8192 (context)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: two alternating 0.3 GB instances"},
+        "tok_s": round(tok_s * world, 1),
+        "hbm_frac": round(gbs / hbm_peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(gbs / hbm_peak, 4), "peak_source": peak_src,
+                     "traffic": profiled_traffic("decode.cu", "swa_decode"),
+                     "algorithmic_bytes": nbytes, "kernel": "decode_splitk_kernel<128,3>"},
+        "e2e": {"value": round(e2e_gbs * world, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    del probs
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads (rank 0 view; each rank runs its own replica)
+    if not args.no_extra:
+        wl = {}
+        steps_x = max(5, args.steps // 4)
+        g = [W.global_decode(dev, seed=3), W.global_decode(dev, seed=1003)]
+        b_ = decode_bytes(g[0])
+        m = bench_workload(binding, g, steps_x, args.warmup, stream)
+        wl["global_decode"] = {"ms": round(m, 4), "GB/s": round(b_ / m / 1e6, 1),
+                               "hbm_frac": round(b_ / m / 1e6 / hbm_peak, 4),
+                               "tok_s": round(g[0].num_seqs / m * 1e3, 1), "bytes": b_}
+        del g
+        t1 = [W.swa_prefill_tiny(dev, seed=0)]
+        f1, by1 = prefill_work(t1[0])
+        m = bench_workload(binding, t1, steps_x, args.warmup, stream)
+        wl["swa_prefill_tiny"] = {"ms": round(m, 4), "TFLOP/s": round(f1 / m / 1e9, 2),
+                                  "tok_s": round(t1[0].total_q / m * 1e3, 1)}
+        del t1
+        torch.cuda.empty_cache()
+        gp = [W.global_prefill(dev, seed=4)]
+        f4, by4 = prefill_work(gp[0])
+        m = bench_workload(binding, gp, max(3, steps_x // 2), min(args.warmup, 3), stream)
+        wl["global_prefill"] = {"ms": round(m, 3), "TFLOP/s": round(f4 / m / 1e9, 1),
+                                "tensor_frac": round(f4 / m / 1e9 / bf16_peak, 4),
+                                "GB/s": round(by4 / m / 1e6, 1),
+                                "hbm_frac": round(by4 / m / 1e6 / hbm_peak, 4),
+                                "tok_s": round(gp[0].total_q / m * 1e3, 1), "flops": f4, "bytes": by4}
+        del gp
+        torch.cuda.empty_cache()
+        # mixed serving step: 6 layers x (prefill 8x2048 + decode 128)
+        layers = [W.mixed_layer(k, i, dev) for i, k in enumerate(W.MIXED_STACK)]
+        calls, keep, per_layer = [], [], []
+        for pre, dec in layers:
+            for prob in (pre, dec):
+                params = binding.params_of(prob)
+                ws = binding.alloc_workspace(params, True, dev)
+                out = torch.empty_like(prob.q)
+                keep.append((ws, out))
+                calls.append(make_call(binding, prob, out, ws))
+
+        def mixed_step():
+            for c in calls:
+                c()
+
+        m = time_steps([mixed_step], max(3, steps_x // 2), min(args.warmup, 3), stream)
+        for j, c in enumerate(calls):
+            per_layer.append(round(time_steps([c], 3, 1, stream), 4))
+        # every token of the step passes through all 6 layers once
+        ntok = layers[0][0].total_q + layers[0][1].total_q
+        wl["mixed_5swa_1global"] = {"ms": round(m, 3), "tok_s": round(ntok / m * 1e3, 1),
+                                    "tokens_per_step": ntok,
+                                    "per_call_ms(prefill,decode)xlayer": per_layer}
+        del layers, calls, keep
+        torch.cuda.empty_cache()
+        line["workloads"] = wl
+
+    # ---- CPU baseline (rank 0, N=1): the oracle on a bounded sample
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        prob_cpu = W.swa_decode("cpu", seed=2)
+        gbs_cpu, secs, passes, cores = cpu_baseline_decode(prob_cpu)
+        line["cpu_baseline"] = {"value": round(gbs_cpu, 4), "unit": "GB/s", "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"{passes} whole passes of swa_decode (seed 2) in {secs:.1f} s"}
+    return line
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    prob = W.swa_decode("cpu", seed=2)
+    kw = prob.oracle_kwargs()
+    B, Hq = prob.num_seqs, prob.num_q_heads
+    total_rows = B * Hq
+    nbytes = decode_bytes(prob)
+    rows_per_step = total_rows  # a whole decode step is cheap enough for the oracle
+    rng = np.random.default_rng(0)
+
+    def step():
+        idx = rng.choice(total_rows, size=rows_per_step, replace=False)
+        oracle.attention_rows(**kw, rows_t=(idx // Hq).astype(np.int32), rows_h=(idx % Hq).astype(np.int32))
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    secs = time.perf_counter() - t0
+    ms = secs / args.steps * 1e3
+    gbs = nbytes * (rows_per_step / total_rows) / (secs / args.steps) / 1e9
+    cores = oracle.num_threads()
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": "swa_decode: batch 64, 64 q heads / 16 kv heads, head_dim 128, "
+                               "window 512, contexts U{1024..8192}, page 64, bias [64,64,512] fp32",
+                   "global_batch": B, "seq_len": "1024-8192 (context)", "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_per_step} of {total_rows} (sequence, head) rows per step "
+                                   "(the whole workload)"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,159 @@
+/*
+ * inkling_attn.h -- C ABI of libinkling_attn.so: paged prefill and decode attention
+ * with a per-token relative-position bias, grouped-query heads, and sliding-window or
+ * full-causal masking, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the attention of the RoPE-free hybrid model described in
+ * "Support Inkling-NVFP4 model" (TensorRT-LLM PR #17062):
+ *   - section "Architecture": position enters only through a learned bias per
+ *     (query token, head, relative distance) added to the scores before the softmax;
+ *     local layers attend over a 512-key sliding window (16 KV heads), global layers
+ *     are full causal (8 KV heads);
+ *   - section "Implementation", row attention_backend/inkling_triton.py: paged prefill
+ *     and decode kernels apply the bias as a score modifier; rel_logits has a static
+ *     shape so decode can be captured in a CUDA graph;
+ *   - review of _build_rel_logits: the bias tensor is [tokens, heads, rel_extent] fp32.
+ * and in "Inkling attn backend cleanup fake registry" (TensorRT-LLM PR #17860):
+ *   - commit on GQA input checks: query head h reads KV head h / (Hq / Hkv); a
+ *     non-divisible head pair is an error;
+ *   - commit moving attention into the backend: per-layer scalars sm_scale,
+ *     rel_extent, window_left (-1 on global layers);
+ *   - commits on borrowing the base page table: key k lives in page
+ *     block_table[b][k / page_size] (a positional table), and k < seq_len bounds every
+ *     access, so entries past a sequence's own blocks are never read.
+ *
+ * Definition (exact; the kernels compute it in fp32 with bf16 inputs):
+ *   sequence b has L_b = seq_lens[b] keys; its n_b new query tokens are the last n_b
+ *   positions, so new token i sits at p = L_b - n_b + i.
+ *   visible keys:  0 <= k <= p, and p - k <= window - 1 when window > 0
+ *   s_k = sm_scale * <q[t,h,:], K[k,h/G,:]> + rel_logits[t, h, min(p - k, E - 1)]
+ *   out[t,h,:] = sum_k softmax(s)_k * V[k,h/G,:]          (bf16, round to nearest even)
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" must point to GPU memory of the current device; the
+ *     caller owns every buffer.  Calls never allocate, free or synchronise: they enqueue
+ *     kernels on `stream` (a cudaStream_t; NULL = legacy default stream) and return.
+ *   - Host-side validation reads only the scalars and pointer values.  On failure the
+ *     call returns an error code and launches nothing.
+ *   - Device-side problems (a page id outside [0, num_pages) for a key that must be
+ *     read, more new tokens than history, a bounded wait that ran out) never fault:
+ *     the kernel skips the access, treats the affected keys as masked, and ORs a bit
+ *     into the sticky error word in the workspace (INK_DEVERR_*), which
+ *     inkling_attn_read_device_error() returns.
+ *   - Keys that sit in a loaded page but are not visible get weight exactly 0 and
+ *     their V rows are zeroed before use, so any bit pattern (NaN included) may sit
+ *     there.  Pages that hold no visible key are never read.
+ *   - A sequence with seq_lens[b] == 0 writes zeros to its output rows.
+ */
+#ifndef INKLING_ATTN_H
+#define INKLING_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  INK_OK = 0,
+  INK_ERR_NULL_PTR = 1,        /* a required pointer is NULL */
+  INK_ERR_BAD_SHAPE = 2,       /* Hq % Hkv != 0, head_dim not 64/128, non-positive sizes */
+  INK_ERR_BAD_PAGE_SIZE = 3,   /* page_size not a power of two in [8, 2^20] */
+  INK_ERR_WORKSPACE = 4,       /* workspace smaller than inkling_attn_workspace_bytes() */
+  INK_ERR_ALIGNMENT = 5,       /* q/k/v/out not 16-byte aligned, or index arrays not 4-byte */
+  INK_ERR_CUDA = 6,            /* a CUDA runtime call failed (launch, attribute, ...) */
+  INK_ERR_TOO_LARGE = 7        /* an index would overflow the 32-bit coordinates used */
+} ink_status_t;
+
+/* Sticky device error bits (see inkling_attn_read_device_error). */
+#define INK_DEVERR_PAGE_OUT_OF_RANGE 0x1u  /* block_table entry outside [0, num_pages) */
+#define INK_DEVERR_QLEN_EXCEEDS_KV   0x2u  /* cu_q_lens gives more new tokens than seq_lens */
+#define INK_DEVERR_WAIT_TIMEOUT      0x4u  /* a bounded wait on a copy ran out */
+#define INK_DEVERR_QLEN_EXCEEDS_MAX  0x8u  /* a sequence has more new tokens than max_q_len */
+
+/* Per-call shape and layer scalars.  All sizes are element counts. */
+typedef struct {
+  int32_t num_seqs;           /* B */
+  int32_t num_q_heads;        /* Hq */
+  int32_t num_kv_heads;       /* Hkv; Hq % Hkv == 0 */
+  int32_t head_dim;           /* D: 64 or 128 */
+  int32_t page_size;          /* P: power of two, >= 8 */
+  int32_t max_pages_per_seq;  /* row stride of block_table */
+  int32_t num_pages;          /* pages in each K/V pool */
+  int32_t rel_extent;         /* E >= 1: distances >= E-1 use bucket E-1 */
+  int32_t window;             /* > 0: keys at distances 0..window-1; <= 0: full causal */
+  float sm_scale;             /* multiplies q.k only; the bias is added unscaled */
+} ink_attn_params_t;
+
+/*
+ * Bytes of device workspace a call needs.  is_decode != 0 sizes it for
+ * inkling_attn_decode (split-K partials and tickets), else for inkling_attn_prefill.
+ * Returns 0 if the parameters are invalid.  A buffer sized for decode also serves
+ * prefill with the same params.
+ */
+size_t inkling_attn_workspace_bytes(const ink_attn_params_t* params, int is_decode);
+
+/*
+ * Zero a workspace (error word and split-K tickets) on `stream`.  Must be called once
+ * after allocating a workspace and before its first use; the kernels leave the tickets
+ * at zero when they finish, so later calls need no re-initialisation.
+ */
+ink_status_t inkling_attn_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Paged prefill (context phase), any number of new tokens per sequence.
+ *   q          device, bf16 [total_q, Hq, D], rows packed by sequence
+ *   cu_q_lens  device, int32 [B+1], cu_q_lens[0] = 0, non-decreasing; n_b = cu[b+1]-cu[b]
+ *   max_q_len  host int >= every n_b (sizes the grid; larger n_b set INK_DEVERR_QLEN_EXCEEDS_MAX)
+ *   k_cache, v_cache  device, bf16 [num_pages, Hkv, P, D]; the step's K/V must already
+ *              be written (new tokens are the last n_b of seq_lens[b])
+ *   block_table device, int32 [B, max_pages_per_seq], positional page ids
+ *   seq_lens   device, int32 [B], KV length including the new tokens
+ *   rel_logits device, fp32 [total_q, Hq, E]
+ *   out        device, bf16 [total_q, Hq, D]
+ *   workspace  device, >= inkling_attn_workspace_bytes(params, 0), initialised once
+ */
+ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q,
+                                  const int32_t* cu_q_lens, int32_t max_q_len,
+                                  const void* k_cache, const void* v_cache,
+                                  const int32_t* block_table, const int32_t* seq_lens,
+                                  const float* rel_logits, void* out, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
+ * Paged decode: one new token per sequence (row b of q is sequence b, at p = L_b - 1).
+ *   q          device, bf16 [B, Hq, D]
+ *   rel_logits device, fp32 [B, Hq, E]
+ *   out        device, bf16 [B, Hq, D]
+ *   workspace  device, >= inkling_attn_workspace_bytes(params, 1), initialised once.
+ *              Calls that share a workspace must not overlap on the GPU (the split-K
+ *              partials and tickets live there).
+ * Other arguments as for prefill.  Stream-ordered, no allocation, no host sync: the
+ * call can be captured in a CUDA graph.
+ */
+ink_status_t inkling_attn_decode(const ink_attn_params_t* params, const void* q,
+                                 const void* k_cache, const void* v_cache,
+                                 const int32_t* block_table, const int32_t* seq_lens,
+                                 const float* rel_logits, void* out, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, copy the sticky device error word (INK_DEVERR_* bits) to
+ * *err_out, and clear it when `clear` is non-zero.  This is the only entry point that
+ * blocks the host.
+ */
+ink_status_t inkling_attn_read_device_error(void* workspace, size_t workspace_bytes,
+                                            void* stream, uint32_t* err_out, int clear);
+
+/* Static, human-readable name of a status code. */
+const char* inkling_attn_status_string(ink_status_t status);
+
+/* ABI version of the library (major * 100 + minor). */
+int32_t inkling_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* INKLING_ATTN_H */

@@ -1,0 +1,277 @@
+// api.cu -- the C ABI of libinkling_attn.so (declared in include/inkling_attn.h):
+// argument validation, workspace layout, TMA tensor-map encoding and kernel launch.
+// Host code here touches only scalars and pointer values; it never synchronises,
+// allocates or copies (except inkling_attn_read_device_error, which is documented to).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <cstring>
+
+#include "../../include/inkling_attn.h"
+#include "kernels.h"
+
+namespace {
+
+using ink::DecodeArgs;
+using ink::PrefillArgs;
+
+constexpr size_t kHeaderBytes = 256;  // error word lives at offset 0
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int ilog2(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+
+ink_status_t validate(const ink_attn_params_t* p) {
+  if (!p) return INK_ERR_NULL_PTR;
+  if (p->num_seqs < 0 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->rel_extent < 1 ||
+      p->max_pages_per_seq < 1 || p->num_pages < 1)
+    return INK_ERR_BAD_SHAPE;
+  if (p->num_q_heads % p->num_kv_heads != 0) return INK_ERR_BAD_SHAPE;
+  if (p->head_dim != 64 && p->head_dim != 128) return INK_ERR_BAD_SHAPE;
+  if (!is_pow2(p->page_size) || p->page_size < 8 || p->page_size > (1 << 20))
+    return INK_ERR_BAD_PAGE_SIZE;
+  // TMA row coordinates and in-kernel row arithmetic are 32-bit
+  const long long rows = (long long)p->num_pages * p->num_kv_heads * p->page_size;
+  if (rows >= (1ll << 31)) return INK_ERR_TOO_LARGE;
+  if ((long long)p->max_pages_per_seq * p->page_size >= (1ll << 31)) return INK_ERR_TOO_LARGE;
+  if (!(p->sm_scale == p->sm_scale)) return INK_ERR_BAD_SHAPE;  // NaN scale
+  return INK_OK;
+}
+
+struct DecodePlan {
+  int head_chunks, tiles_per_split, num_splits;
+};
+
+// Split-K plan for decode.  Visible keys of one sequence span at most `max_tiles`
+// 64-key tiles (window-limited on sliding-window layers).  Tiles are cut into
+// splits of roughly equal size so that the grid holds enough CTAs to fill the GPU
+// several times over even for small batches.
+DecodePlan plan_decode(const ink_attn_params_t* p) {
+  DecodePlan d;
+  const int G = p->num_q_heads / p->num_kv_heads;
+  d.head_chunks = (G + 15) / 16;
+  const long long max_keys = (long long)p->max_pages_per_seq * p->page_size;
+  long long max_tiles = (max_keys + ink::TILE_KEYS - 1) / ink::TILE_KEYS;
+  if (p->window > 0) {
+    const long long wt = (p->window + ink::TILE_KEYS - 1) / ink::TILE_KEYS + 1;
+    if (wt < max_tiles) max_tiles = wt;
+  }
+  if (max_tiles < 1) max_tiles = 1;
+  const long long units = (long long)(p->num_seqs > 0 ? p->num_seqs : 1) * p->num_kv_heads * d.head_chunks;
+  const long long want_ctas = 2048;
+  long long tps = (units * max_tiles + want_ctas - 1) / want_ctas;
+  if (tps < 2) tps = 2;
+  if (tps > 16) tps = 16;
+  long long splits = (max_tiles + tps - 1) / tps;
+  if (splits > ink::MAX_DECODE_SPLITS) splits = ink::MAX_DECODE_SPLITS;
+  tps = (max_tiles + splits - 1) / splits;  // rebalance
+  splits = (max_tiles + tps - 1) / tps;
+  d.tiles_per_split = (int)tps;
+  d.num_splits = (int)splits;
+  return d;
+}
+
+struct DecodeLayout {
+  size_t tickets_off, part_o_off, part_ml_off, total;
+};
+
+DecodeLayout decode_layout(const ink_attn_params_t* p, const DecodePlan& d) {
+  DecodeLayout l;
+  const size_t B = (size_t)(p->num_seqs > 0 ? p->num_seqs : 1);
+  const size_t nt = B * p->num_kv_heads * d.head_chunks;
+  l.tickets_off = kHeaderBytes;
+  l.part_o_off = align_up(l.tickets_off + nt * sizeof(int32_t), 256);
+  const size_t rows = B * p->num_q_heads * (size_t)d.num_splits;
+  l.part_ml_off = align_up(l.part_o_off + rows * p->head_dim * sizeof(float), 256);
+  l.total = align_up(l.part_ml_off + rows * 2 * sizeof(float), 256);
+  return l;
+}
+
+// ---- TMA tensor maps over a K or V pool viewed as [num_pages*Hkv*P rows, D] bf16
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool make_pool_map(CUtensorMap* map, const void* base, const ink_attn_params_t* p) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t rows = (cuuint64_t)p->num_pages * p->num_kv_heads * p->page_size;
+  cuuint64_t dims[2] = {(cuuint64_t)p->head_dim, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)p->head_dim * 2};
+  const int box_rows = p->page_size < ink::TILE_KEYS ? p->page_size : ink::TILE_KEYS;
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t inkling_attn_version(void) { return 100; }
+
+const char* inkling_attn_status_string(ink_status_t s) {
+  switch (s) {
+    case INK_OK: return "ok";
+    case INK_ERR_NULL_PTR: return "null pointer argument";
+    case INK_ERR_BAD_SHAPE: return "bad shape (heads not divisible, head_dim not 64/128, or non-positive size)";
+    case INK_ERR_BAD_PAGE_SIZE: return "page_size must be a power of two >= 8";
+    case INK_ERR_WORKSPACE: return "workspace too small";
+    case INK_ERR_ALIGNMENT: return "misaligned pointer (16 bytes for q/k/v/out, 4 for index and bias arrays)";
+    case INK_ERR_CUDA: return "CUDA runtime error";
+    case INK_ERR_TOO_LARGE: return "sizes overflow 32-bit coordinates";
+  }
+  return "unknown status";
+}
+
+size_t inkling_attn_workspace_bytes(const ink_attn_params_t* params, int is_decode) {
+  if (validate(params) != INK_OK) return 0;
+  if (!is_decode) return kHeaderBytes;
+  return decode_layout(params, plan_decode(params)).total;
+}
+
+ink_status_t inkling_attn_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace) return INK_ERR_NULL_PTR;
+  if (workspace_bytes < kHeaderBytes) return INK_ERR_WORKSPACE;
+  if (cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream) != cudaSuccess)
+    return INK_ERR_CUDA;
+  return INK_OK;
+}
+
+ink_status_t inkling_attn_read_device_error(void* workspace, size_t workspace_bytes, void* stream,
+                                            uint32_t* err_out, int clear) {
+  if (!workspace || !err_out) return INK_ERR_NULL_PTR;
+  if (workspace_bytes < kHeaderBytes) return INK_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return INK_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return INK_ERR_CUDA;
+  *err_out = v;
+  if (clear) {
+    if (cudaMemsetAsync(workspace, 0, sizeof v, st) != cudaSuccess) return INK_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return INK_ERR_CUDA;
+  }
+  return INK_OK;
+}
+
+ink_status_t inkling_attn_decode(const ink_attn_params_t* params, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* block_table,
+                                 const int32_t* seq_lens, const float* rel_logits, void* out,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  ink_status_t st = validate(params);
+  if (st != INK_OK) return st;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !rel_logits || !out || !workspace)
+    return INK_ERR_NULL_PTR;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(rel_logits, 4) ||
+      !aligned(workspace, 256))
+    return INK_ERR_ALIGNMENT;
+  const DecodePlan plan = plan_decode(params);
+  const DecodeLayout lay = decode_layout(params, plan);
+  if (workspace_bytes < lay.total) return INK_ERR_WORKSPACE;
+  if (params->num_seqs == 0) return INK_OK;
+  CUtensorMap tmK, tmV;
+  if (!make_pool_map(&tmK, k_cache, params) || !make_pool_map(&tmV, v_cache, params))
+    return INK_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeArgs a;
+  a.q = q;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.rel = rel_logits;
+  a.out = out;
+  a.part_o = reinterpret_cast<float*>(ws + lay.part_o_off);
+  a.part_ml = reinterpret_cast<float*>(ws + lay.part_ml_off);
+  a.tickets = reinterpret_cast<int32_t*>(ws + lay.tickets_off);
+  a.err = reinterpret_cast<uint32_t*>(ws);
+  a.B = params->num_seqs;
+  a.Hq = params->num_q_heads;
+  a.Hkv = params->num_kv_heads;
+  a.G = params->num_q_heads / params->num_kv_heads;
+  a.head_chunks = plan.head_chunks;
+  a.log2_page = ilog2(params->page_size);
+  a.max_pages = params->max_pages_per_seq;
+  a.num_pages = params->num_pages;
+  a.E = params->rel_extent;
+  a.W = params->window;
+  a.scale_log2 = params->sm_scale * 1.4426950408889634f;
+  a.tiles_per_split = plan.tiles_per_split;
+  a.num_splits = plan.num_splits;
+  if (ink::launch_decode(tmK, tmV, a, params->head_dim, (cudaStream_t)stream) != cudaSuccess)
+    return INK_ERR_CUDA;
+  return INK_OK;
+}
+
+ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q,
+                                  const int32_t* cu_q_lens, int32_t max_q_len, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_table,
+                                  const int32_t* seq_lens, const float* rel_logits, void* out,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  ink_status_t st = validate(params);
+  if (st != INK_OK) return st;
+  if (!q || !cu_q_lens || !k_cache || !v_cache || !block_table || !seq_lens || !rel_logits ||
+      !out || !workspace)
+    return INK_ERR_NULL_PTR;
+  if (max_q_len < 0) return INK_ERR_BAD_SHAPE;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(cu_q_lens, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+      !aligned(rel_logits, 4) || !aligned(workspace, 256))
+    return INK_ERR_ALIGNMENT;
+  if (workspace_bytes < kHeaderBytes) return INK_ERR_WORKSPACE;
+  if (params->num_seqs == 0 || max_q_len == 0) return INK_OK;
+  const int num_q_tiles = (max_q_len + 63) / 64;
+  if (num_q_tiles > 65535 || params->num_seqs > 65535) return INK_ERR_TOO_LARGE;
+  CUtensorMap tmK, tmV;
+  if (!make_pool_map(&tmK, k_cache, params) || !make_pool_map(&tmV, v_cache, params))
+    return INK_ERR_CUDA;
+  PrefillArgs a;
+  a.q = q;
+  a.cu_q = cu_q_lens;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.rel = rel_logits;
+  a.out = out;
+  a.err = reinterpret_cast<uint32_t*>(workspace);
+  a.B = params->num_seqs;
+  a.Hq = params->num_q_heads;
+  a.Hkv = params->num_kv_heads;
+  a.G = params->num_q_heads / params->num_kv_heads;
+  a.log2_page = ilog2(params->page_size);
+  a.max_pages = params->max_pages_per_seq;
+  a.num_pages = params->num_pages;
+  a.E = params->rel_extent;
+  a.W = params->window;
+  a.scale_log2 = params->sm_scale * 1.4426950408889634f;
+  a.max_q_len = max_q_len;
+  a.num_q_tiles = num_q_tiles;
+  if (ink::launch_prefill(tmK, tmV, a, params->head_dim, (cudaStream_t)stream) != cudaSuccess)
+    return INK_ERR_CUDA;
+  return INK_OK;
+}
+
+}  // extern "C"

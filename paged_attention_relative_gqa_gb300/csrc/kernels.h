@@ -1,0 +1,52 @@
+// kernels.h -- argument blocks and launchers shared between the host API (api.cu)
+// and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ink {
+
+// Keys per K/V tile: one TMA box is 64 rows of 128 bytes (64 bf16 of head_dim).
+constexpr int TILE_KEYS = 64;
+
+// Largest number of key splits a decode launch may use (bounds the merge scratch).
+constexpr int MAX_DECODE_SPLITS = 64;
+
+struct DecodeArgs {
+  const void* q;              // bf16 [B, Hq, D]
+  const int32_t* block_table; // [B, max_pages]
+  const int32_t* seq_lens;    // [B]
+  const float* rel;           // fp32 [B, Hq, E]
+  void* out;                  // bf16 [B, Hq, D]
+  float* part_o;              // fp32 [B, Hq, num_splits, D]
+  float* part_ml;             // fp32 [B, Hq, num_splits, 2] (running max in log2 units, sum)
+  int32_t* tickets;           // [B, Hkv * head_chunks]
+  uint32_t* err;              // sticky error word
+  int B, Hq, Hkv, G, head_chunks;
+  int log2_page, max_pages, num_pages, E, W;
+  float scale_log2;           // sm_scale * log2(e)
+  int tiles_per_split, num_splits;
+};
+
+struct PrefillArgs {
+  const void* q;              // bf16 [total_q, Hq, D]
+  const int32_t* cu_q;        // [B+1]
+  const int32_t* block_table; // [B, max_pages]
+  const int32_t* seq_lens;    // [B]
+  const float* rel;           // fp32 [total_q, Hq, E]
+  void* out;                  // bf16 [total_q, Hq, D]
+  uint32_t* err;
+  int B, Hq, Hkv, G;
+  int log2_page, max_pages, num_pages, E, W;
+  float scale_log2;
+  int max_q_len, num_q_tiles;
+};
+
+cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeArgs& a,
+                          int head_dim, cudaStream_t stream);
+cudaError_t launch_prefill(const CUtensorMap& tmK, const CUtensorMap& tmV, const PrefillArgs& a,
+                           int head_dim, cudaStream_t stream);
+
+}  // namespace ink

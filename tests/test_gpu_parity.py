@@ -1,0 +1,277 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances (bf16 output vs fp64): max-abs <= 2e-2 and relative RMS <= 5e-3 on every
+workload; page/index bookkeeping (probes, page permutation, masking) bit-exact.
+Each comparison prints how many rows it compared; zero rows fails.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from paged_attention_relative_gqa_gb300 import binding
+from paged_attention_relative_gqa_gb300 import workloads as W
+from tests.parity import bits, compare, gpu_rows, oracle_full, oracle_rows, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load_library()
+    yield
+    torch.cuda.empty_cache()
+
+
+DEV = "cuda"
+
+
+def full_check(prob, label):
+    out, _ = run_gpu(prob)
+    ref = oracle_full(prob)
+    return compare(out.float().cpu().numpy(), ref, label)
+
+
+# ------------------------------------------------------------------ the five workloads
+
+def test_swa_prefill_tiny_every_row():
+    full_check(W.swa_prefill_tiny(DEV), "swa_prefill_tiny (1x1024, 8q/2kv, D64, W512, P16)")
+
+
+def test_swa_decode_every_row():
+    full_check(W.swa_decode(DEV), "swa_decode (B64, 64q/16kv, D128, W512)")
+
+
+def test_global_decode_every_row():
+    full_check(W.global_decode(DEV), "global_decode (B32, 64q/8kv, ctx 8k-32k, E4096)")
+
+
+def test_global_prefill_sampled_rows():
+    prob = W.global_prefill(DEV)
+    out, _ = run_gpu(prob)
+    rows = W.sample_rows(prob, per_seq=1024, seed=44)
+    compare(gpu_rows(out, rows), oracle_rows(prob, rows), "global_prefill (4x8192, sampled)")
+    assert torch.isfinite(out.float()).all()
+    del prob, out
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("layer", range(6))
+def test_mixed_stack_layer(layer):
+    kind = W.MIXED_STACK[layer]
+    pre, dec = W.mixed_layer(kind, layer, DEV)
+    out, _ = run_gpu(pre)
+    rows = W.sample_rows(pre, per_seq=256, seed=layer)
+    compare(gpu_rows(out, rows), oracle_rows(pre, rows), f"mixed layer {layer} ({kind}) prefill, sampled")
+    assert torch.isfinite(out.float()).all()
+    full_check(dec, f"mixed layer {layer} ({kind}) decode")
+    del pre, dec, out
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ shapes and edge cases
+
+EDGE = [
+    # (Hq, Hkv, D, P, W, E, q_lens, seq_lens)
+    (8, 2, 64, 8, -1, 7, [1, 5, 70], [1, 40, 200]),            # ragged, P8, small E (clamp)
+    (8, 8, 128, 16, 5, 16, [33, 1, 64], [33, 2, 300]),         # MHA, tiny window, cached prefix
+    (16, 1, 128, 32, 64, 600, [65, 129], [100, 129]),          # G16, window == tile
+    (32, 1, 64, 128, -1, 1, [1, 1, 1], [1, 127, 1000]),        # G32 (two head chunks), E1
+    (4, 2, 128, 64, 1, 4, [70, 3], [70, 90]),                   # window 1: own value
+    (8, 2, 128, 256, 512, 512, [300, 1], [1500, 777]),          # P256, SWA
+    (8, 4, 64, 64, -1, 100, [0, 17, 1], [0, 17, 0]),            # zero-length sequences
+]
+
+
+@pytest.mark.parametrize("case", range(len(EDGE)))
+def test_edge_shapes_prefill(case):
+    Hq, Hkv, D, P, Wn, E, ql, sl = EDGE[case]
+    ql = [0 if L == 0 else n for n, L in zip(ql, sl)]
+    prob = W.make_problem(num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P, rel_extent=E,
+                          window=Wn, q_lens=ql, seq_lens=sl, seed=100 + case, device=DEV,
+                          max_pages=max(-(-L // P) for L in sl) + 3)
+    full_check(prob, f"edge prefill {EDGE[case]}")
+
+
+@pytest.mark.parametrize("case", range(len(EDGE)))
+def test_edge_shapes_decode(case):
+    Hq, Hkv, D, P, Wn, E, _, sl = EDGE[case]
+    prob = W.make_problem(num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P, rel_extent=E,
+                          window=Wn, q_lens=[1 if L > 0 else 0 for L in sl], seq_lens=sl,
+                          seed=200 + case, device=DEV, max_pages=max(-(-L // P) for L in sl) + 3)
+    if not prob.is_decode:  # zero-length rows: decode layout needs one row per sequence
+        prob = W.make_problem(num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P,
+                              rel_extent=E, window=Wn, q_lens=[1] * len(sl),
+                              seq_lens=[max(L, 1) for L in sl], seed=200 + case, device=DEV)
+    full_check(prob, f"edge decode {EDGE[case]}")
+
+
+def test_decode_zero_length_rows_are_zero():
+    prob = W.make_problem(num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=64, rel_extent=64,
+                          window=-1, q_lens=[1, 1, 1], seq_lens=[5, 1, 300], seed=3, device=DEV)
+    prob.seq_lens[1] = 0
+    out, _ = run_gpu(prob)
+    assert torch.all(out[1] == 0)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_long_decode_many_splits():
+    # one very long sequence among short ones: many splits + ticket merge
+    prob = W.make_problem(num_q_heads=16, num_kv_heads=2, head_dim=128, page_size=64, rel_extent=4096,
+                          window=-1, q_lens=[1, 1, 1], seq_lens=[65536, 3, 4097], seed=9, device=DEV)
+    full_check(prob, "long decode 64k")
+
+
+# ------------------------------------------------------------------ invariants on the GPU
+
+def _mid_problem(window=48, decode=False, seed=21):
+    ql = [1, 1, 1] if decode else [40, 1, 97]
+    return W.make_problem(num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16, rel_extent=40,
+                          window=window, q_lens=ql, seq_lens=[90, 200, 97], seed=seed, device=DEV)
+
+
+@pytest.mark.parametrize("decode", [False, True])
+def test_repeated_calls_are_bitwise_identical(decode):
+    prob = _mid_problem(decode=decode)
+    a, _ = run_gpu(prob)
+    b, _ = run_gpu(prob)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("decode", [False, True])
+def test_page_permutation_is_bitwise_invariant(decode):
+    prob = _mid_problem(decode=decode)
+    a, _ = run_gpu(prob)
+    N = prob.num_pages
+    extra = 9
+    g = torch.Generator().manual_seed(3)
+    perm = torch.randperm(N + extra, generator=g).to(DEV)
+    shape = (N + extra,) + tuple(prob.k_cache.shape[1:])
+    k2 = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=DEV)
+    v2 = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=DEV)
+    k2[perm[:N]] = prob.k_cache
+    v2[perm[:N]] = prob.v_cache
+    bt = prob.block_table.clone()
+    valid = bt < N
+    bt[valid] = perm[bt[valid].long()].to(torch.int32)
+    prob.k_cache, prob.v_cache, prob.block_table = k2, v2, bt
+    b, _ = run_gpu(prob)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("decode", [False, True])
+def test_invisible_keys_and_bias_buckets_do_not_matter(decode):
+    """NaN in every K/V slot no new row can see (same page or not), junk in unused
+    bias buckets: output bitwise unchanged."""
+    prob = _mid_problem(decode=decode)
+    a, _ = run_gpu(prob)
+    P = prob.page_size
+    for b, (n, L) in enumerate(zip(prob.q_lens, prob.seq_lens_list)):
+        lo = max(0, L - n - prob.window + 1)
+        for k in list(range(0, lo)) + list(range(L, -(-L // P) * P)):
+            pg = int(prob.block_table[b, k // P])
+            prob.k_cache[pg, :, k % P] = float("nan")
+            prob.v_cache[pg, :, k % P] = float("nan")
+        t0 = int(prob.cu_q_lens[b])
+        for i in range(n):
+            p = L - n + i
+            far = min(p, prob.window - 1) + 1
+            prob.rel_logits[t0 + i, :, far:] = float("nan")
+    b_, _ = run_gpu(prob)
+    assert torch.equal(a, b_)
+
+
+def test_argmax_probe_is_exact_on_gpu():
+    L = n = 300
+    prob = W.make_problem(num_q_heads=4, num_kv_heads=1, head_dim=128, page_size=16, rel_extent=64,
+                          window=100, q_lens=[n], seq_lens=[L], seed=5, device=DEV)
+    prob.q.zero_()
+    k = torch.arange(L, device=DEV)
+    pages = prob.block_table[0, (k // 16)].long()
+    prob.v_cache[pages, 0, k % 16, 0] = (k // 256).to(torch.bfloat16)
+    prob.v_cache[pages, 0, k % 16, 1] = (k % 256).to(torch.bfloat16)
+    rng = np.random.default_rng(1)
+    jstar = rng.integers(0, 64, size=n)
+    prob.rel_logits.fill_(-30.0)
+    prob.rel_logits[torch.arange(n), :, torch.from_numpy(jstar).to(DEV)] = 30.0
+    out, _ = run_gpu(prob)
+    checked = 0
+    for i in range(n):
+        lo = max(0, i - 99)
+        fav = [kk for kk in range(lo, i + 1) if min(i - kk, 63) == jstar[i]]
+        if len(fav) == 1:
+            got = int(round(out[i, 2, 0].item())) * 256 + int(round(out[i, 2, 1].item()))
+            assert got == fav[0]
+            checked += 1
+    print(f"argmax probe: {checked} rows checked")
+    assert checked > 200
+
+
+def test_count_probe_recovers_visible_key_count_on_gpu():
+    """q = 0, bias 0, V[k,0] = 1, V[k,1] = [k == 0]: rows whose visible range starts at
+    key 0 output 1/|Vis| in column 1, which identifies |Vis| exactly up to 128 keys."""
+    L = n = 200
+    checked = 0
+    for window in (-1, 37):
+        prob = W.make_problem(num_q_heads=2, num_kv_heads=1, head_dim=64, page_size=8, rel_extent=512,
+                              window=window, q_lens=[n], seq_lens=[L], seed=6, device=DEV)
+        prob.q.zero_()
+        prob.rel_logits.zero_()
+        k = torch.arange(L, device=DEV)
+        pages = prob.block_table[0, (k // 8)].long()
+        prob.v_cache[pages, 0, k % 8] = 0
+        prob.v_cache[pages, 0, k % 8, 0] = 1.0
+        prob.v_cache[pages[0], 0, 0, 1] = 1.0
+        out, _ = run_gpu(prob)
+        for i in range(n):
+            lo = 0 if window <= 0 else max(0, i - window + 1)
+            if lo == 0 and i + 1 <= 128:
+                assert round(1.0 / out[i, 0, 1].float().item()) == i + 1
+                checked += 1
+            assert out[i, 0, 0].float().item() == 1.0
+    print(f"count probe: {checked} rows checked")
+    assert checked > 150
+
+
+def test_decode_matches_last_row_of_prefill_on_gpu():
+    pre = W.make_problem(num_q_heads=16, num_kv_heads=2, head_dim=128, page_size=64, rel_extent=300,
+                         window=-1, q_lens=[700], seq_lens=[700], seed=8, device=DEV)
+    out_p, _ = run_gpu(pre)
+    for p in (0, 63, 64, 299, 699):
+        dec = W.make_problem(num_q_heads=16, num_kv_heads=2, head_dim=128, page_size=64, rel_extent=300,
+                             window=-1, q_lens=[1], seq_lens=[p + 1], seed=1, device=DEV)
+        dec.k_cache, dec.v_cache = pre.k_cache, pre.v_cache
+        dec.block_table = pre.block_table[:, : -(-(p + 1) // 64)].contiguous()
+        dec.q = pre.q[p:p + 1].contiguous()
+        dec.rel_logits = pre.rel_logits[p:p + 1].contiguous()
+        out_d, _ = run_gpu(dec)
+        compare(out_d[0].float().cpu().numpy(), out_p[p].float().cpu().numpy(), f"decode==prefill row {p}")
+
+
+def test_window_and_global_parameters_give_different_results():
+    prob = W.make_problem(num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=64, rel_extent=512,
+                          window=512, q_lens=[1, 1], seq_lens=[3000, 2000], seed=10, device=DEV)
+    a, _ = run_gpu(prob)
+    prob.window = -1
+    b, _ = run_gpu(prob)
+    assert (a.float() - b.float()).abs().max().item() > 1e-2
+
+
+def test_bad_page_id_sets_error_word_and_output_stays_finite():
+    for decode in (False, True):
+        prob = _mid_problem(window=-1, decode=decode)
+        L = prob.seq_lens_list[1]
+        prob.block_table[1, (L - 1) // prob.page_size] = prob.num_pages + 1000
+        prob.block_table[0, 0] = -5
+        out, err = run_gpu(prob, check_error=False)
+        assert err & binding.DEVERR_PAGE_OUT_OF_RANGE
+        assert torch.isfinite(out.float()).all()
+
+
+def test_error_word_is_clear_after_good_calls():
+    prob = _mid_problem()
+    _, err = run_gpu(prob)
+    assert err == 0
