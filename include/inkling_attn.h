@@ -139,6 +139,34 @@ ink_status_t inkling_attn_decode(const ink_attn_params_t* params, const void* q,
                                  size_t workspace_bytes, void* stream);
 
 /*
+ * inkling_attn_decode without a workspace argument, for callers that cannot allocate
+ * device memory: for example a plugin whose host framework owns every device buffer
+ * and hands out only fixed-size tensors, or a serving loop that must not grow its
+ * memory after start-up.  Such a caller has no way to create the workspace that
+ * inkling_attn_decode needs.  The pages this library follows have no counterpart to
+ * this entry point.
+ *   - Scratch: a 64 MiB device array inside the library, held by every GPU that loads
+ *     it until the process exits.  A call whose workspace need
+ *     (inkling_attn_workspace_bytes(params, 1)) exceeds 64 MiB returns
+ *     INK_ERR_WORKSPACE and launches nothing.
+ *   - The call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *     routine.  It clears the array's error word and split-K tickets on `stream`
+ *     (cudaMemsetAsync), then runs the same kernel as inkling_attn_decode.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current.  Make that first call before any
+ *     stream capture.
+ *   - All calls on a device share the array, which keeps the last call's contents.
+ *     Calls that overlap on the GPU (different streams, no ordering between them) race
+ *     on it and give wrong results.  Device-side error bits are kept in the array and
+ *     not reported.
+ * Other arguments and results as for inkling_attn_decode.
+ */
+ink_status_t inkling_attn_decode_noalloc(const ink_attn_params_t* params, const void* q,
+                                         const void* k_cache, const void* v_cache,
+                                         const int32_t* block_table, const int32_t* seq_lens,
+                                         const float* rel_logits, void* out, void* stream);
+
+/*
  * Synchronise `stream`, copy the sticky device error word (INK_DEVERR_* bits) to
  * *err_out, and clear it when `clear` is non-zero.  This is the only entry point that
  * blocks the host.

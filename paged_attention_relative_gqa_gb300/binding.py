@@ -27,7 +27,7 @@ DEVERR_WAIT_TIMEOUT = 0x4
 DEVERR_QLEN_EXCEEDS_MAX = 0x8
 
 EXPORTED_SYMBOLS = ("inkling_attn_workspace_bytes", "inkling_attn_workspace_init",
-                    "inkling_attn_prefill", "inkling_attn_decode",
+                    "inkling_attn_prefill", "inkling_attn_decode", "inkling_attn_decode_noalloc",
                     "inkling_attn_read_device_error", "inkling_attn_status_string",
                     "inkling_attn_version")
 
@@ -70,6 +70,8 @@ def load_library(path: Optional[str] = None):
     lib.inkling_attn_prefill.restype = ctypes.c_int
     lib.inkling_attn_decode.argtypes = [PP, V, V, V, V, V, V, V, V, S, V]
     lib.inkling_attn_decode.restype = ctypes.c_int
+    lib.inkling_attn_decode_noalloc.argtypes = [PP, V, V, V, V, V, V, V, V]
+    lib.inkling_attn_decode_noalloc.restype = ctypes.c_int
     lib.inkling_attn_read_device_error.argtypes = [V, S, V, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
     lib.inkling_attn_read_device_error.restype = ctypes.c_int
     lib.inkling_attn_status_string.argtypes = [ctypes.c_int]
@@ -169,6 +171,19 @@ def inkling_attn_decode(params, q, k_cache, v_cache, block_table, seq_lens, rel_
         _dev(out, "out", torch.bfloat16), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), _stream_handle(stream))
     _check(code, "inkling_attn_decode")
+    return out
+
+
+def inkling_attn_decode_noalloc(params, q, k_cache, v_cache, block_table, seq_lens, rel_logits,
+                                out, stream=None):
+    """Decode without a workspace (the library's own fixed device scratch is used)."""
+    lib = load_library()
+    code = lib.inkling_attn_decode_noalloc(
+        ctypes.byref(params), _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache", torch.bfloat16),
+        _dev(v_cache, "v_cache", torch.bfloat16), _dev(block_table, "block_table", torch.int32),
+        _dev(seq_lens, "seq_lens", torch.int32), _dev(rel_logits, "rel_logits", torch.float32),
+        _dev(out, "out", torch.bfloat16), _stream_handle(stream))
+    _check(code, "inkling_attn_decode_noalloc")
     return out
 
 
