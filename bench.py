@@ -185,12 +185,6 @@ def make_call(binding, prob, out, ws):
                                                 prob.seq_lens, prob.rel_logits, out, ws)
 
 
-def instances(factory, dev, n):
-    """`n` independently seeded instances of a workload: alternating them keeps each
-    step's inputs out of L2 (every instance is larger than the 129 MB L2)."""
-    return [factory(dev, seed) for seed in range(n)]
-
-
 def bench_workload(binding, probs, steps, warmup, stream):
     calls = []
     keep = []
@@ -246,94 +240,43 @@ def cpu_baseline_decode(prob_cpu, seconds: float = 10.0):
     return gbs, t_sum, passes, oracle.num_threads()
 
 
-def run_ours(args, rank, world, local_rank):
-    from paged_attention_relative_gqa_gb300 import binding, build
+WORKLOAD_DESC = {
+    "swa_decode": "swa_decode: batch 64, 64 q heads / 16 kv heads, head_dim 128, window 512, "
+                  "contexts U{1024..8192}, page 64, bias [64,64,512] fp32",
+    "global_decode": "global_decode: batch 32, 64 q heads / 8 kv heads, head_dim 128, full causal, "
+                     "contexts U{8192..32768}, page 64, bias [32,64,4096] fp32 (clamped)",
+    "swa_prefill_tiny": "swa_prefill_tiny: 1 x 1024 tokens, 8 q heads / 2 kv heads, head_dim 64, "
+                        "window 512, page 16, bias [1024,8,512] fp32",
+    "global_prefill": "global_prefill: 4 x 8192 tokens, 64 q heads / 8 kv heads, head_dim 128, "
+                      "full causal, page 64, bias [32768,64,4096] fp32 (clamped)",
+    "global_prefill_small": "global_prefill_small (profiling size): 1 x 2048 tokens, 64 q heads / "
+                            "8 kv heads, head_dim 128, full causal, page 64, bias [2048,64,4096] fp32",
+    "mixed": "mixed serving step: 5 SWA + 1 global layer, each one prefill call (8 x 2048 tokens) "
+             "and one decode call (128 requests, contexts log-uniform 512..16384)",
+}
 
-    build.build()
-    binding.load_library()
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.Stream(dev)
-    hbm_peak, bf16_peak, peak_src = peaks()
 
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
+def workload_instances(name, dev):
+    """Problems of one workload; decode workloads get two instances (each > L2) that
+    alternate between steps so no step finds its inputs in L2."""
+    if name == "swa_decode":
+        return [W.swa_decode(dev, seed=2), W.swa_decode(dev, seed=1002)]
+    if name == "global_decode":
+        return [W.global_decode(dev, seed=3), W.global_decode(dev, seed=1003)]
+    if name == "swa_prefill_tiny":
+        return [W.swa_prefill_tiny(dev, seed=s) for s in range(8)]  # 8 x 17 MB > L2
+    if name == "global_prefill":
+        return [W.global_prefill(dev, seed=4)]                       # 36 GB > L2
+    if name == "global_prefill_small":
+        return [W.global_prefill(dev, seed=4, batch=1, tokens=2048)]  # 2.2 GB > L2
+    raise ValueError(name)
 
-    # ---- headline: SWA decode (two alternating instances, each > L2)
-    probs = instances(lambda d, s: W.swa_decode(d, seed=2 + 1000 * s), dev, 2)
-    nbytes = decode_bytes(probs[0])
-    clocks = Clocks(local_rank)
-    barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    ms = bench_workload(binding, probs, args.steps, args.warmup, stream)
-    clk = clocks.stop()
-    barrier()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    e2e_ms, h2d, d2h = e2e_decode(binding, probs[0], max(10, args.steps // 2), args.warmup, stream)
-    e2e_gbs = nbytes / (e2e_ms * 1e-3) / 1e9
-    tok_s = probs[0].num_seqs / (ms * 1e-3)
-    B = probs[0].num_seqs
-    line = {
-        "metric": METRIC, "value": round(gbs * world, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded; Q/K/V ~N(0,1) bf16, bias ~N(0,0.5) fp32)",
-        "config": {"workload": "swa_decode: batch 64, 64 q heads / 16 kv heads, head_dim 128, "
-                               "window 512, contexts U{1024..8192}, page 64, bias [64,64,512] fp32",
-                   "global_batch": B * world, "seq_len": "1024-8192 (context)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2: two alternating 0.3 GB instances"},
-        "tok_s": round(tok_s * world, 1),
-        "hbm_frac": round(gbs / hbm_peak, 4),
-        "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(gbs / hbm_peak, 4), "peak_source": peak_src,
-                     "traffic": profiled_traffic("decode.cu", "swa_decode"),
-                     "algorithmic_bytes": nbytes, "kernel": "decode_splitk_kernel<128,3>"},
-        "e2e": {"value": round(e2e_gbs * world, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
-        "clocks": clk,
-    }
-    del probs
-    torch.cuda.empty_cache()
 
-    # ---- the other workloads (rank 0 view; each rank runs its own replica)
-    if not args.no_extra:
-        wl = {}
-        steps_x = max(5, args.steps // 4)
-        g = [W.global_decode(dev, seed=3), W.global_decode(dev, seed=1003)]
-        b_ = decode_bytes(g[0])
-        m = bench_workload(binding, g, steps_x, args.warmup, stream)
-        wl["global_decode"] = {"ms": round(m, 4), "GB/s": round(b_ / m / 1e6, 1),
-                               "hbm_frac": round(b_ / m / 1e6 / hbm_peak, 4),
-                               "tok_s": round(g[0].num_seqs / m * 1e3, 1), "bytes": b_}
-        del g
-        t1 = [W.swa_prefill_tiny(dev, seed=0)]
-        f1, by1 = prefill_work(t1[0])
-        m = bench_workload(binding, t1, steps_x, args.warmup, stream)
-        wl["swa_prefill_tiny"] = {"ms": round(m, 4), "TFLOP/s": round(f1 / m / 1e9, 2),
-                                  "tok_s": round(t1[0].total_q / m * 1e3, 1)}
-        del t1
-        torch.cuda.empty_cache()
-        gp = [W.global_prefill(dev, seed=4)]
-        f4, by4 = prefill_work(gp[0])
-        m = bench_workload(binding, gp, max(3, steps_x // 2), min(args.warmup, 3), stream)
-        wl["global_prefill"] = {"ms": round(m, 3), "TFLOP/s": round(f4 / m / 1e9, 1),
-                                "tensor_frac": round(f4 / m / 1e9 / bf16_peak, 4),
-                                "GB/s": round(by4 / m / 1e6, 1),
-                                "hbm_frac": round(by4 / m / 1e6 / hbm_peak, 4),
-                                "tok_s": round(gp[0].total_q / m * 1e3, 1), "flops": f4, "bytes": by4}
-        del gp
-        torch.cuda.empty_cache()
-        # mixed serving step: 6 layers x (prefill 8x2048 + decode 128)
+def measure(binding, name, dev, steps, warmup, stream, hbm_peak, bf16_peak):
+    """Time one workload; returns a dict of its numbers (value in its own unit)."""
+    if name == "mixed":
         layers = [W.mixed_layer(k, i, dev) for i, k in enumerate(W.MIXED_STACK)]
-        calls, keep, per_layer = [], [], []
+        calls, keep = [], []
         for pre, dec in layers:
             for prob in (pre, dec):
                 params = binding.params_of(prob)
@@ -346,26 +289,157 @@ def run_ours(args, rank, world, local_rank):
             for c in calls:
                 c()
 
-        m = time_steps([mixed_step], max(3, steps_x // 2), min(args.warmup, 3), stream)
-        for j, c in enumerate(calls):
-            per_layer.append(round(time_steps([c], 3, 1, stream), 4))
+        m = time_steps([mixed_step], steps, warmup, stream)
+        per_call = [round(time_steps([c], 3, 1, stream), 4) for c in calls]
+        for ws, _ in keep:
+            assert binding.inkling_attn_read_device_error(ws) == 0
         # every token of the step passes through all 6 layers once
         ntok = layers[0][0].total_q + layers[0][1].total_q
-        wl["mixed_5swa_1global"] = {"ms": round(m, 3), "tok_s": round(ntok / m * 1e3, 1),
-                                    "tokens_per_step": ntok,
-                                    "per_call_ms(prefill,decode)xlayer": per_layer}
-        del layers, calls, keep
-        torch.cuda.empty_cache()
+        return {"ms": m, "value": ntok / m * 1e3, "unit": "tok/s", "tok_s": ntok / m * 1e3,
+                "tokens_per_step": ntok, "launches_per_step": len(calls),
+                "per_call_ms(prefill,decode)xlayer": per_call}
+    probs = workload_instances(name, dev)
+    m = bench_workload(binding, probs, steps, warmup, stream)
+    p0 = probs[0]
+    if p0.is_decode:
+        nbytes = decode_bytes(p0)
+        gbs = nbytes / m / 1e6
+        return {"ms": m, "value": gbs, "unit": "GB/s", "GB/s": gbs, "hbm_frac": gbs / hbm_peak,
+                "tok_s": p0.num_seqs / m * 1e3, "bytes": nbytes, "launches_per_step": 1,
+                "bound": "hbm", "probs": probs}
+    flops, nbytes = prefill_work(p0)
+    tfs = flops / m / 1e9
+    return {"ms": m, "value": tfs, "unit": "TFLOP/s", "TFLOP/s": tfs, "tensor_frac": tfs / bf16_peak,
+            "GB/s": nbytes / m / 1e6, "hbm_frac": nbytes / m / 1e6 / hbm_peak,
+            "tok_s": p0.total_q / m * 1e3, "flops": flops, "bytes": nbytes, "launches_per_step": 1,
+            "bound": "tensor", "probs": probs}
+
+
+def run_ours(args, rank, world, local_rank):
+    from paged_attention_relative_gqa_gb300 import binding, build
+
+    build.build()
+    binding.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    hbm_peak, bf16_peak, peak_src = peaks()
+    name = args.workload
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    clocks = Clocks(local_rank)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    r = measure(binding, name, dev, args.steps, args.warmup, stream, hbm_peak, bf16_peak)
+    clk = clocks.stop()
+    barrier()
+    ms = r["ms"]
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    scale = r["ms"] / ms  # value recomputed at the slowest rank's time
+    value = r["value"] * scale * world
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": r["unit"], "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; Q/K/V ~N(0,1) bf16, bias ~N(0,0.5) fp32)",
+        "config": {"workload": WORKLOAD_DESC[name],
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (decode: two alternating 0.3-2.7 GB instances)"},
+        "tok_s": round(r["tok_s"] * scale * world, 1),
+        "gpu_launches": args.steps * r["launches_per_step"],
+        "clocks": clk,
+    }
+    if name != "mixed":
+        if r["bound"] == "hbm":
+            line["roofline"] = {"bound": "hbm", "achieved": round(r["GB/s"], 2), "peak": hbm_peak,
+                                "unit": "GB/s", "frac": round(r["GB/s"] / hbm_peak, 4),
+                                "peak_source": peak_src,
+                                "traffic": profiled_traffic("decode.cu", name),
+                                "algorithmic_bytes": r["bytes"], "kernel": "decode_persistent_kernel"}
+        else:
+            line["roofline"] = {"bound": "tensor", "achieved": round(r["TFLOP/s"], 2), "peak": bf16_peak,
+                                "unit": "TFLOP/s", "frac": round(r["TFLOP/s"] / bf16_peak, 4),
+                                "peak_source": peak_src,
+                                "traffic": profiled_traffic("prefill_mma.cu", name),
+                                "algorithmic_flops": r["flops"], "algorithmic_bytes": r["bytes"],
+                                "hbm_frac": round(r["hbm_frac"], 4), "kernel": "prefill_mma_kernel"}
+        probs = r.pop("probs")
+        if probs[0].is_decode:
+            e2e_ms, h2d, d2h = e2e_decode(binding, probs[0], max(10, args.steps // 2), args.warmup, stream)
+            line["e2e"] = {"value": round(r["bytes"] / e2e_ms / 1e6 * world, 2), "unit": "GB/s",
+                           "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                           "d2h_bytes_per_step": d2h}
+        elif probs[0].rel_logits.numel() * 4 > (4 << 30):
+            line["e2e"] = {"value": None, "unit": "TFLOP/s",
+                           "skipped": "inputs above 4 GB are not staged through pinned host memory"}
+        else:
+            e2e_ms, h2d, d2h = e2e_prefill(binding, probs[0], max(3, args.steps // 4), 3, stream)
+            line["e2e"] = {"value": round(r["flops"] / e2e_ms / 1e9 * world, 2), "unit": "TFLOP/s",
+                           "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                           "d2h_bytes_per_step": d2h}
+        del probs
+    else:
+        line["e2e"] = None
+        line["mixed"] = {k: v for k, v in r.items() if k not in ("value", "unit")}
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads, reported beside the headline
+    if not args.no_extra:
+        wl = {}
+        steps_x = max(5, args.steps // 4)
+        for other in ("global_decode", "swa_prefill_tiny", "global_prefill", "mixed"):
+            if other == name:
+                continue
+            st = steps_x if other in ("global_decode", "swa_prefill_tiny") else max(3, steps_x // 2)
+            o = measure(binding, other, dev, st, min(args.warmup, 3), stream, hbm_peak, bf16_peak)
+            o.pop("probs", None)
+            wl[other] = {k: (round(v, 5) if isinstance(v, float) else v) for k, v in o.items()
+                         if k not in ("value", "unit", "bound", "launches_per_step")}
+            torch.cuda.empty_cache()
         line["workloads"] = wl
 
-    # ---- CPU baseline (rank 0, N=1): the oracle on a bounded sample
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    # ---- CPU baseline (rank 0, N=1): the oracle, timed on the host cores
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and name == "swa_decode":
         prob_cpu = W.swa_decode("cpu", seed=2)
         gbs_cpu, secs, passes, cores = cpu_baseline_decode(prob_cpu)
         line["cpu_baseline"] = {"value": round(gbs_cpu, 4), "unit": "GB/s", "cores": cores,
                                 "kind": "oracle",
                                 "sample": f"{passes} whole passes of swa_decode (seed 2) in {secs:.1f} s"}
     return line
+
+
+def e2e_prefill(binding, prob, steps, warmup, stream):
+    """Prefill through the C ABI with host buffers: q, bias, table, lengths and query
+    offsets copied in from pinned memory each step, output copied back."""
+    dev = prob.q.device
+    keys = ("q", "rel_logits", "block_table", "seq_lens", "cu_q_lens")
+    host = {k: getattr(prob, k).cpu().pin_memory() for k in keys}
+    dbuf = {k: torch.empty_like(getattr(prob, k)) for k in keys}
+    out = torch.empty_like(prob.q)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    params = binding.params_of(prob)
+    ws = binding.alloc_workspace(params, False, dev)
+
+    def step():
+        for k in keys:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        binding.inkling_attn_prefill(params, dbuf["q"], dbuf["cu_q_lens"], prob.max_q_len, prob.k_cache,
+                                     prob.v_cache, dbuf["block_table"], dbuf["seq_lens"],
+                                     dbuf["rel_logits"], out, ws)
+        out_h.copy_(out, non_blocking=True)
+
+    ms = time_steps([step], steps, warmup, stream)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    del host, dbuf
+    return ms, h2d, d2h
 
 
 # ---------------------------------------------------------------- reference arm (the oracle)
@@ -416,7 +490,9 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOAD_DESC),
+                    help="workload of the timed line (default: the SWA decode headline)")
+    ap.add_argument("--no-extra", action="store_true", help="timed workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

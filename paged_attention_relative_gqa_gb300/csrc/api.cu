@@ -51,9 +51,13 @@ struct DecodePlan {
 };
 
 // Split-K plan for decode.  Visible keys of one sequence span at most `max_tiles`
-// 64-key tiles (window-limited on sliding-window layers).  Tiles are cut into
-// splits of roughly equal size so that the grid holds enough CTAs to fill the GPU
-// several times over even for small batches.
+// 64-key tiles (window-limited on sliding-window layers).  The persistent decode kernel
+// runs one CTA per SM over work units (split, sequence, KV head, head chunk); the tiles
+// of a sequence are cut into splits so that there are about kTargetUnits units in the
+// worst case, enough for an even spread over the SMs, while each split keeps at least
+// two tiles.
+constexpr long long kTargetUnits = 608;  // 4 units per SM on a 152-SM GB300
+
 DecodePlan plan_decode(const ink_attn_params_t* p) {
   DecodePlan d;
   const int G = p->num_q_heads / p->num_kv_heads;
@@ -66,10 +70,9 @@ DecodePlan plan_decode(const ink_attn_params_t* p) {
   }
   if (max_tiles < 1) max_tiles = 1;
   const long long units = (long long)(p->num_seqs > 0 ? p->num_seqs : 1) * p->num_kv_heads * d.head_chunks;
-  const long long want_ctas = 2048;
-  long long tps = (units * max_tiles + want_ctas - 1) / want_ctas;
+  long long tps = (units * max_tiles + kTargetUnits - 1) / kTargetUnits;
   if (tps < 2) tps = 2;
-  if (tps > 16) tps = 16;
+  if (tps > 64) tps = 64;
   long long splits = (max_tiles + tps - 1) / tps;
   if (splits > ink::MAX_DECODE_SPLITS) splits = ink::MAX_DECODE_SPLITS;
   tps = (max_tiles + splits - 1) / splits;  // rebalance
@@ -111,19 +114,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_pool_map(CUtensorMap* map, const void* base, const ink_attn_params_t* p) {
+// A bf16 matrix [rows, D] (row pitch D*2 bytes) with boxes of 64 columns x box_rows
+// rows, 128-byte swizzle.
+bool make_rows_map(CUtensorMap* map, const void* base, uint64_t rows, int head_dim, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t rows = (cuuint64_t)p->num_pages * p->num_kv_heads * p->page_size;
-  cuuint64_t dims[2] = {(cuuint64_t)p->head_dim, rows};
-  cuuint64_t strides[1] = {(cuuint64_t)p->head_dim * 2};
-  const int box_rows = p->page_size < ink::TILE_KEYS ? p->page_size : ink::TILE_KEYS;
+  cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+uint64_t pool_rows(const ink_attn_params_t* p) {
+  return (uint64_t)p->num_pages * p->num_kv_heads * p->page_size;
+}
+
+// K or V pool as [num_pages*Hkv*P rows, D], boxes of min(P, box_cap) rows.
+bool make_pool_map(CUtensorMap* map, const void* base, const ink_attn_params_t* p, int box_cap) {
+  const int box_rows = p->page_size < box_cap ? p->page_size : box_cap;
+  return make_rows_map(map, base, pool_rows(p), p->head_dim, box_rows);
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -195,8 +208,13 @@ ink_status_t inkling_attn_decode(const ink_attn_params_t* params, const void* q,
   const DecodeLayout lay = decode_layout(params, plan);
   if (workspace_bytes < lay.total) return INK_ERR_WORKSPACE;
   if (params->num_seqs == 0) return INK_OK;
-  CUtensorMap tmK, tmV;
-  if (!make_pool_map(&tmK, k_cache, params) || !make_pool_map(&tmV, v_cache, params))
+  ink::DecodeMaps maps;
+  if (!make_pool_map(&maps.k, k_cache, params, ink::TILE_KEYS) ||
+      !make_pool_map(&maps.v, v_cache, params, ink::TILE_KEYS) ||
+      !make_pool_map(&maps.k_seg, k_cache, params, 16) ||
+      !make_pool_map(&maps.v_seg, v_cache, params, 16) ||
+      !make_rows_map(&maps.q, q, (uint64_t)params->num_seqs * params->num_q_heads,
+                     params->head_dim, 16))
     return INK_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodeArgs a;
@@ -222,7 +240,7 @@ ink_status_t inkling_attn_decode(const ink_attn_params_t* params, const void* q,
   a.scale_log2 = params->sm_scale * 1.4426950408889634f;
   a.tiles_per_split = plan.tiles_per_split;
   a.num_splits = plan.num_splits;
-  if (ink::launch_decode(tmK, tmV, a, params->head_dim, (cudaStream_t)stream) != cudaSuccess)
+  if (ink::launch_decode(maps, a, params->head_dim, (cudaStream_t)stream) != cudaSuccess)
     return INK_ERR_CUDA;
   return INK_OK;
 }
@@ -247,7 +265,8 @@ ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q
   const int num_q_tiles = (max_q_len + 63) / 64;
   if (num_q_tiles > 65535 || params->num_seqs > 65535) return INK_ERR_TOO_LARGE;
   CUtensorMap tmK, tmV;
-  if (!make_pool_map(&tmK, k_cache, params) || !make_pool_map(&tmV, v_cache, params))
+  if (!make_pool_map(&tmK, k_cache, params, ink::TILE_KEYS) ||
+      !make_pool_map(&tmV, v_cache, params, ink::TILE_KEYS))
     return INK_ERR_CUDA;
   PrefillArgs a;
   a.q = q;

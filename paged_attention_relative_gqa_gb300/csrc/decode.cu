@@ -1,22 +1,35 @@
-// decode.cu -- split-K flash-decode over a paged K/V cache with a per-token
+// decode.cu -- persistent split-K flash-decode over a paged K/V cache with a per-token
 // relative-position bias ("Support Inkling-NVFP4 model", TensorRT-LLM PR #17062,
 // sections "Architecture" and "Implementation": one new token per request attends to
-// its paged history, bias added before the softmax).
+// its paged history, the bias rel[b, h, distance] added before the softmax; 512-key
+// windows on local layers, full causal on global layers).
 //
-// Grid: (split, KV head x head-chunk, sequence).  One CTA owns up to 16 query heads
-// that share one KV head (GQA, query head h reads KV head h / G) and a contiguous run
-// of 64-key tiles of one sequence.  Per tile:
-//   * thread 0 reads the block-table entries (positional: page of key k is
-//     block_table[b][k / P]) and issues 2-D TMA loads of the K and V rows into a ring
-//     of NSTAGE shared-memory stages (128-byte swizzle, completion on an mbarrier);
-//   * each of the 4 warps takes 16 keys: S = Q K^T with mma.sync (query heads are the
-//     16 MMA rows), scale, add the gathered bias rel[b, h, min(p - k, E - 1)], mask
-//     keys outside [lo, p] (window) or in unreadable pages, online softmax in base 2;
-//     O += P V with mma.sync, V rows of masked keys zeroed in registers.
-// The 4 warps' (max, sum, O) are merged in shared memory.  A sequence that needs more
-// than one split writes fp32 partials to the workspace; the last CTA of that sequence
-// to finish (atomic ticket, no spinning) merges the partials in split order, so the
-// result does not depend on which CTA finishes last, and resets the ticket to 0.
+// Work unit: (split s, sequence b, KV head, chunk of <= 16 query heads sharing that KV
+// head).  A split is a run of `tiles_per_split` 64-key tiles of the sequence's visible
+// range [lo, p], p = L - 1.  One CTA per SM walks units blockIdx.x, +gridDim.x, ...;
+// units whose split lies past the sequence's visible range are skipped by every warp
+// alike, so the producer and consumers need no unit hand-off.
+//
+// Two CTAs per SM.  Warp roles:
+//   warp 4 (producer, one lane): block-table walk (page of key k is
+//     block_table[b][k / P]; entries past the sequence's own pages are never read),
+//     then 2-D TMA loads of K and V rows into a ring of NSTAGE shared-memory stages
+//     (128-byte swizzle, full/empty mbarriers).  Whole 64-key tiles use 64-row boxes;
+//     tiles cut by the window start or the sequence end load only the 16-row segments
+//     that hold visible keys.  The first tile of a unit also carries the unit's query
+//     rows (TMA over q viewed as [B*Hq, D]).  The producer runs ahead across units.
+//   warps 0-3 (consumers): each takes 16 keys of every tile: S = Q K^T (mma.sync,
+//     query heads are the 16 MMA rows), s2 = S * sm_scale * log2(e) + bias * log2(e),
+//     keys outside [lo, p] or in unreadable pages -> -inf, online softmax in base 2,
+//     O += P V with V rows of masked keys zeroed in registers.  The bias values of the
+//     next tile are prefetched into registers while the current one is computed.
+// Unit epilogue: the 4 warps' (max, sum, O) are merged through shared memory; a
+// sequence with one split writes bf16 output, otherwise fp32 partials go to the
+// workspace and the last CTA to finish that sequence (atomic ticket, no spinning)
+// merges all partials in split order -- the result does not depend on arrival order --
+// and resets the ticket.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -24,368 +37,670 @@ namespace ink {
 
 namespace {
 
-constexpr int DEC_WARPS = 4;
-constexpr int DEC_THREADS = DEC_WARPS * 32;
+constexpr int DEC_CONSUMERS = 4;
+// With at most 8 query heads per unit two CTAs share an SM: 8 consumer warps per SM hide
+// each other's latencies, which matters more than a deeper ring (registers are capped
+// at 65536 / (2 * 160) = 204).  16-head units need the room of a whole SM.
+template <int HB>
+constexpr int dec_ctas_per_sm() { return HB == 8 ? 2 : 1; }
+constexpr int DEC_THREADS = (DEC_CONSUMERS + 1) * 32;
+constexpr int QROWS = 16;       // query-head rows per unit (MMA M)
+constexpr int SEG_ROWS = 16;    // fine TMA box rows for partial tiles
+constexpr int PTAB = 576;       // staged block-table entries per unit (>= 64 tiles x 64/8 + 2)
 
 template <int D>
-struct DecodeShape {
-  static constexpr int COL_BLOCKS = D / 64;               // 128-byte column blocks
-  static constexpr int SUB_BYTES = TILE_KEYS * 128;       // one column block of a tile
+struct DecShape {
+  static constexpr int COL_BLOCKS = D / 64;             // 128-byte column blocks
+  static constexpr int SUB_BYTES = TILE_KEYS * 128;     // one column block of a 64-key tile
   static constexpr int TILE_BYTES = COL_BLOCKS * SUB_BYTES;
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;      // K tile + V tile
-  static constexpr int OPITCH = D + 4;                    // fp32 merge buffer row pitch
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // K tile + V tile
+  static constexpr int QSUB_BYTES = QROWS * 128;        // one column block of the query rows
+  static constexpr int QSLOT_BYTES = COL_BLOCKS * QSUB_BYTES;
+  static constexpr int OPITCH = D + 4;                  // fp32 merge buffer row pitch
 };
 
-template <int D, int NSTAGE>
-constexpr size_t decode_smem_bytes() {
-  using S = DecodeShape<D>;
-  return 1024 /* alignment slack */ + (size_t)NSTAGE * S::STAGE_BYTES +
-         NSTAGE * 16 /* barriers + masks */ + 2 * DEC_WARPS * 16 * 4 +
-         16 * MAX_DECODE_SPLITS * 4 + 16;
+constexpr int BIAS_DIST = 3;               // tiles a consumer warp stages its bias ahead of use
+constexpr int BIAS_SLOTS = BIAS_DIST + 1;
+constexpr int BIAS_PITCH = 20;             // floats per staged (head) row of a warp's 16 keys
+
+template <int D, int NSTAGE, int HB>
+struct DecSmem {
+  using S = DecShape<D>;
+  static constexpr size_t stages = 0;
+  static constexpr size_t q = stages + (size_t)NSTAGE * S::STAGE_BYTES;
+  static constexpr size_t bias = q + 2 * S::QSLOT_BYTES;
+  static constexpr size_t obuf = bias + (size_t)DEC_CONSUMERS * BIAS_SLOTS * HB * BIAS_PITCH * 4;
+  static constexpr size_t red = obuf + (size_t)DEC_CONSUMERS * HB * S::OPITCH * 4;
+  static constexpr size_t wts = red + 2 * DEC_CONSUMERS * 16 * 4;
+  static constexpr size_t bars = wts + 16 * MAX_DECODE_SPLITS * 4;  // 8-byte aligned
+  static constexpr size_t badmask = bars + (2 * NSTAGE + 4 + DEC_CONSUMERS * BIAS_SLOTS) * 8;
+  static constexpr size_t flags = badmask + NSTAGE * 8;
+  static constexpr size_t ptab = flags + 16;
+  static constexpr size_t total = ptab + 3 * PTAB * 4;
+  static constexpr size_t alloc = total + 1024;  // base alignment slack
+};
+
+struct Unit {
+  int b, kvh, hc, s, h0, nh, L, p, lo, tb, n_my, nact;
+};
+
+// Decode potential unit u.  Returns false when the unit has nothing to do.  A sequence
+// with L <= 0 yields one unit (split 0) with n_my = 0: its output rows are zeroed.
+__device__ __forceinline__ bool get_unit(const DecodeArgs& a, int u, Unit& w) {
+  const int per_s = a.B * a.Hkv * a.head_chunks;
+  w.s = u / per_s;
+  int r = u - w.s * per_s;
+  const int per_b = a.Hkv * a.head_chunks;
+  w.b = r / per_b;
+  r -= w.b * per_b;
+  w.kvh = r / a.head_chunks;
+  w.hc = r - w.kvh * a.head_chunks;
+  w.h0 = w.kvh * a.G + w.hc * QROWS;
+  w.nh = min(QROWS, a.G - w.hc * QROWS);
+  int L = __ldg(a.seq_lens + w.b);
+  if (L <= 0) {
+    w.L = 0;
+    w.n_my = 0;
+    w.nact = 1;
+    return w.s == 0;
+  }
+  const long long cap = (long long)a.max_pages << a.log2_page;
+  if (L > cap) L = (int)cap;  // keys past the table's reach are not readable (error recorded)
+  w.L = L;
+  w.p = L - 1;
+  w.lo = a.W > 0 ? max(0, w.p - a.W + 1) : 0;
+  const int t_first = w.lo / TILE_KEYS, t_last = w.p / TILE_KEYS;
+  const int ntiles = t_last - t_first + 1;
+  w.nact = min((ntiles + a.tiles_per_split - 1) / a.tiles_per_split, a.num_splits);
+  if (w.s >= w.nact) return false;
+  w.tb = t_first + w.s * a.tiles_per_split;
+  w.n_my = (w.s == w.nact - 1) ? (t_last + 1 - w.tb) : a.tiles_per_split;
+  return true;
 }
 
-template <int D, int NSTAGE>
-__global__ void __launch_bounds__(DEC_THREADS, 2)
-decode_splitk_kernel(const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
-  using S = DecodeShape<D>;
-  static_assert(NSTAGE >= 2, "merge buffer reuses two stages");
-  static_assert(DEC_WARPS * 16 * S::OPITCH * 4 <= NSTAGE * S::STAGE_BYTES, "merge buffer");
+// First and last block-table index a unit reads (pages holding its visible keys).
+__device__ __forceinline__ void unit_page_span(const DecodeArgs& a, const Unit& w, int& first, int& count) {
+  const int kf = max(w.tb * TILE_KEYS, w.lo);
+  const int kl = min((w.tb + w.n_my) * TILE_KEYS - 1, w.p);
+  first = kf >> a.log2_page;
+  count = (kl >> a.log2_page) - first + 1;
+}
+
+// Segments of tile i of unit w to fetch: `whole` (one 64-row box) when every key of the
+// tile is visible and the page holds the whole tile, else 16-row (or P-row) segments
+// that hold at least one visible key.  rows[sg] is the pool row of segment sg, or -1
+// (nothing to fetch), or -2 (unreadable page: its keys are masked).  Page ids come from
+// the unit's slice of the block table, staged in shared memory (ptab[j] = entry first+j).
+struct TilePlan {
+  bool whole;
+  int sk, nseg;
+  int rows[TILE_KEYS / 8];
+};
+
+__device__ __forceinline__ void plan_tile(const DecodeArgs& a, const Unit& w, int i, const int* ptab,
+                                          int pfirst, TilePlan& t) {
+  const int P = 1 << a.log2_page;
+  const int seg = P < SEG_ROWS ? P : SEG_ROWS;
+  const int k0 = (w.tb + i) * TILE_KEYS;
+  const int kfirst = max(k0, w.lo), klast = min(k0 + TILE_KEYS - 1, w.p);
+  t.whole = kfirst == k0 && klast == k0 + TILE_KEYS - 1 && P >= TILE_KEYS;
+  t.sk = t.whole ? TILE_KEYS : seg;
+  t.nseg = TILE_KEYS / t.sk;
+  for (int sg = 0; sg < t.nseg; ++sg) {
+    const int ks = k0 + sg * t.sk;
+    t.rows[sg] = -1;
+    if (ks > klast || ks + t.sk - 1 < kfirst) continue;
+    const int page = ptab[(ks >> a.log2_page) - pfirst];
+    if (page < 0 || page >= a.num_pages) {
+      t.rows[sg] = -2;
+      continue;
+    }
+    t.rows[sg] = ((page * a.Hkv + w.kvh) << a.log2_page) + (ks & (P - 1));
+  }
+}
+
+// Does tile k0 of unit w need its own bias values?  Not when every visible key of the
+// tile is at distance >= E - 1: those all read the clamped bucket E - 1.
+__device__ __forceinline__ bool tile_needs_bias(const Unit& w, int k0, int E) {
+  return max(w.p - (k0 + TILE_KEYS - 1), 0) < E - 1;
+}
+
+__device__ __forceinline__ void named_barrier_consumers() {
+  asm volatile("bar.sync 1, %0;" ::"n"(DEC_CONSUMERS * 32) : "memory");
+}
+
+// Wait on an mbarrier phase unless the CTA has aborted; on timeout, record the error
+// and abort the CTA (every later wait returns at once).
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              uint32_t* err) {
+  if (*abort_flag) return false;
+  if (mbar_wait_bounded(bar, parity)) return true;
+  record_error(err, INK_DEVERR_WAIT_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
+template <int D, int NSTAGE, int HB>
+__global__ void __launch_bounds__(DEC_THREADS, dec_ctas_per_sm<HB>())
+decode_persistent_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmKs, const __grid_constant__ CUtensorMap tmVs,
+                         const __grid_constant__ CUtensorMap tmQ, const DecodeArgs a) {
+  using S = DecShape<D>;
+  using L_ = DecSmem<D, NSTAGE, HB>;
   constexpr int KSTEPS = D / 16;
-  constexpr int DBLK = D / 8;
+  static_assert(HB == 8 || HB == 16, "heads per unit");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NSTAGE * S::STAGE_BYTES);
-  uint64_t* badmask = full + NSTAGE;
-  float* red_m = reinterpret_cast<float*>(badmask + NSTAGE);
-  float* red_l = red_m + DEC_WARPS * 16;
-  float* wts = red_l + DEC_WARPS * 16;
-  int* flags = reinterpret_cast<int*>(wts + 16 * MAX_DECODE_SPLITS);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L_::bars);
+  uint64_t* empty = full + NSTAGE;
+  uint64_t* qempty = empty + NSTAGE;  // [2]
+  uint64_t* badmask = reinterpret_cast<uint64_t*>(smem + L_::badmask);
+  int* flags = reinterpret_cast<int*>(smem + L_::flags);  // [0] ticket winner, [1] abort
+  float* red_m = reinterpret_cast<float*>(smem + L_::red);
+  float* red_l = red_m + DEC_CONSUMERS * 16;
+  float* obuf = reinterpret_cast<float*>(smem + L_::obuf);
+  float* wts = reinterpret_cast<float*>(smem + L_::wts);
+  volatile int* abort_flag = flags + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gq = lane >> 2, cq = lane & 3;  // mma fragment row / column-pair
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y / a.head_chunks, hc = blockIdx.y % a.head_chunks;
-  const int b = blockIdx.z;
-  const int h0 = kvh * a.G + hc * 16;
-  const int nh = min(16, a.G - hc * 16);
   const int P = 1 << a.log2_page;
-
-  int L = a.seq_lens[b];
-  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-  if (L <= 0) {  // padding row: zeros, nothing read
-    if (split == 0)
-      for (int i = tid; i < nh * D; i += DEC_THREADS)
-        out[((size_t)b * a.Hq + h0 + i / D) * D + i % D] = __float2bfloat16(0.f);
-    return;
-  }
-  const long long cap = (long long)a.max_pages * P;
-  if (L > cap) {  // history longer than the table row: use what the table covers
-    if (split == 0 && blockIdx.y == 0 && tid == 0) record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
-    L = (int)cap;
-  }
-  const int p = L - 1;
-  const int lo = a.W > 0 ? max(0, p - a.W + 1) : 0;
-  const int t_first = lo / TILE_KEYS, t_last = p / TILE_KEYS;
-  const int ntiles = t_last - t_first + 1;
-  const int nact = min((ntiles + a.tiles_per_split - 1) / a.tiles_per_split, a.num_splits);
-  if (split >= nact) return;
-  const int tb = t_first + split * a.tiles_per_split;
-  const int n_my = (split == nact - 1) ? (t_last + 1 - tb) : a.tiles_per_split;
+  const int total_units = a.num_splits * a.B * a.Hkv * a.head_chunks;
 
   if (tid == 0) {
-    for (int s = 0; s < NSTAGE; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], DEC_CONSUMERS);
+    }
+    mbar_init(&qempty[0], DEC_CONSUMERS);
+    mbar_init(&qempty[1], DEC_CONSUMERS);
+    for (int x = 0; x < DEC_CONSUMERS * BIAS_SLOTS; ++x) mbar_init(&qempty[2 + x], 32);
     fence_mbar_init();
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
     flags[0] = 0;
     flags[1] = 0;
   }
   __syncthreads();
 
-  // Producer: block-table walk + TMA for tile index i (relative to tb) into stage s.
-  auto issue = [&](int i, int s) {
-    const int k0 = (tb + i) * TILE_KEYS;
-    uint8_t* kdst = smem + s * S::STAGE_BYTES;
-    uint8_t* vdst = kdst + S::TILE_BYTES;
-    const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
-    uint64_t bad = 0;
-    uint32_t bytes = 0;
-    const int seg_keys = P < TILE_KEYS ? P : TILE_KEYS;
-    const int nseg = TILE_KEYS / seg_keys;
-    int rows[TILE_KEYS / 8];
-    for (int sg = 0; sg < nseg; ++sg) {
-      const int ks = k0 + sg * seg_keys;
-      rows[sg] = -1;
-      if (ks > p || ks + seg_keys - 1 < lo) continue;  // no visible key in this segment
-      const int pidx = ks >> a.log2_page;
-      const int page = bt[pidx];
-      if (page < 0 || page >= a.num_pages) {
-        bad |= (seg_keys == 64 ? ~0ull : (((1ull << seg_keys) - 1) << (sg * seg_keys)));
-        record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
-        continue;
-      }
-      rows[sg] = ((page * a.Hkv + kvh) << a.log2_page) + (ks & (P - 1));
-      bytes += 2u * seg_keys * D * 2u;
+  if (warp == DEC_CONSUMERS) {
+    // ------------------------------------------------------------------ producer
+    // The warp stages each unit's slice of the block table into shared memory with
+    // cp.async two units ahead (3-slot ring), so no tile waits on a table read; lane 0
+    // alone then issues the unit's tiles into the shared-memory ring.  Whole tiles take
+    // a short path (one page lookup, four TMA copies for D = 128).
+    int* ptab = reinterpret_cast<int*>(smem + L_::ptab);
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      prefetch_tensormap(&tmKs);
+      prefetch_tensormap(&tmVs);
+      prefetch_tensormap(&tmQ);
     }
-    badmask[s] = bad;
-    mbar_arrive_expect_tx(&full[s], bytes);
-    for (int sg = 0; sg < nseg; ++sg) {
-      if (rows[sg] < 0) continue;
+    const int per_b = a.Hkv * a.head_chunks, per_s = a.B * per_b;
+    auto next_active = [&](int u, Unit& w) -> int {
+      for (; u < total_units; u += gridDim.x) {
+        // warm L1 with the length of the unit four strides on (read by every warp later)
+        const int uf = u + 4 * (int)gridDim.x;
+        if (uf < total_units) prefetch_l1(a.seq_lens + (uf % per_s) / per_b);
+        if (get_unit(a, u, w) && w.n_my > 0) return u;
+      }
+      return total_units;
+    };
+    auto stage_ptab = [&](const Unit* w, int slot) {  // w == nullptr: empty group
+      if (w) {
+        int first, count;
+        unit_page_span(a, *w, first, count);
+        const int32_t* src = a.block_table + (size_t)w->b * a.max_pages + first;
+        const uint32_t dst = smem_u32(ptab + slot * PTAB);
+        for (int j = lane; j < count; j += 32) cp_async_4(dst + 4 * j, src + j);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    Unit cur, nxt, nxt2;
+    int ucur = next_active(blockIdx.x, cur);
+    int unxt = ucur < total_units ? next_active(ucur + gridDim.x, nxt) : total_units;
+    stage_ptab(ucur < total_units ? &cur : nullptr, 0);
+    stage_ptab(unxt < total_units ? &nxt : nullptr, 1);
+    int n = 0, uc = 0;
+    bool go = true;
+    while (ucur < total_units && go) {
+      const int unxt2 = unxt < total_units ? next_active(unxt + gridDim.x, nxt2) : total_units;
+      stage_ptab(unxt2 < total_units ? &nxt2 : nullptr, (uc + 2) % 3);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      __syncwarp();
+      const int slot = uc & 1;  // Q slot
+      const int* tab = ptab + (uc % 3) * PTAB;
+      int pfirst, pcount;
+      unit_page_span(a, cur, pfirst, pcount);
+      const int row_kv = cur.kvh << a.log2_page;       // + page * Hkv * P
+      const int hkvp = a.Hkv << a.log2_page;
+      constexpr uint32_t WHOLE_BYTES = 2u * TILE_KEYS * D * 2u;
+      if (uc >= 2) {
+        if (lane == 0) go = wait_or_abort(&qempty[slot], (uint32_t)((uc >> 1) - 1) & 1u, abort_flag, a.err);
+        go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+      }
+      for (int i = 0; i < cur.n_my && go; ++i, ++n) {
+        const int st = n % NSTAGE;
+        if (n >= NSTAGE) {
+          if (lane == 0) go = wait_or_abort(&empty[st], (uint32_t)((n / NSTAGE) - 1) & 1u, abort_flag, a.err);
+          go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
+          if (!go) break;
+        }
+        const int k0 = (cur.tb + i) * TILE_KEYS;
+        if (lane == 0) {
+          uint8_t* kdst = smem + L_::stages + (size_t)st * S::STAGE_BYTES;
+          uint8_t* vdst = kdst + S::TILE_BYTES;
+          const uint32_t qbytes = i == 0 ? (uint32_t)(S::COL_BLOCKS * QROWS * 128) : 0u;
+          if (P >= TILE_KEYS && k0 >= cur.lo && k0 + TILE_KEYS - 1 <= cur.p) {
+            const int page = tab[(k0 >> a.log2_page) - pfirst];
+            const bool okp = page >= 0 && page < a.num_pages;
+            badmask[st] = okp ? 0ull : ~0ull;
+            if (!okp) record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
+            mbar_arrive_expect_tx(&full[st], (okp ? WHOLE_BYTES : 0u) + qbytes);
+            if (okp) {
+              const int row = page * hkvp + row_kv + (k0 & (P - 1));
 #pragma unroll
-      for (int cb = 0; cb < S::COL_BLOCKS; ++cb) {
-        tma_load_2d(kdst + cb * S::SUB_BYTES + sg * seg_keys * 128, &tmK, cb * 64, rows[sg], &full[s]);
-        tma_load_2d(vdst + cb * S::SUB_BYTES + sg * seg_keys * 128, &tmV, cb * 64, rows[sg], &full[s]);
+              for (int cb = 0; cb < S::COL_BLOCKS; ++cb) {
+                tma_load_2d(kdst + cb * S::SUB_BYTES, &tmK, cb * 64, row, &full[st]);
+                tma_load_2d(vdst + cb * S::SUB_BYTES, &tmV, cb * 64, row, &full[st]);
+              }
+            }
+          } else {
+            TilePlan t;
+            plan_tile(a, cur, i, tab, pfirst, t);
+            uint64_t bad = 0;
+            uint32_t bytes = qbytes;
+            for (int sg = 0; sg < t.nseg; ++sg) {
+              if (t.rows[sg] == -2) {
+                bad |= (t.sk == 64 ? ~0ull : (((1ull << t.sk) - 1) << (sg * t.sk)));
+                record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
+              } else if (t.rows[sg] >= 0) {
+                bytes += 2u * t.sk * D * 2u;
+              }
+            }
+            badmask[st] = bad;
+            mbar_arrive_expect_tx(&full[st], bytes);
+            for (int sg = 0; sg < t.nseg; ++sg) {
+              if (t.rows[sg] < 0) continue;
+#pragma unroll
+              for (int cb = 0; cb < S::COL_BLOCKS; ++cb) {
+                tma_load_2d(kdst + cb * S::SUB_BYTES + sg * t.sk * 128, t.whole ? &tmK : &tmKs, cb * 64,
+                            t.rows[sg], &full[st]);
+                tma_load_2d(vdst + cb * S::SUB_BYTES + sg * t.sk * 128, t.whole ? &tmV : &tmVs, cb * 64,
+                            t.rows[sg], &full[st]);
+              }
+            }
+          }
+          if (i == 0) {
+            uint8_t* qdst = smem + L_::q + slot * S::QSLOT_BYTES;
+#pragma unroll
+            for (int cb = 0; cb < S::COL_BLOCKS; ++cb)
+              tma_load_2d(qdst + cb * S::QSUB_BYTES, &tmQ, cb * 64, cur.b * a.Hq + cur.h0, &full[st]);
+          }
+        }
       }
+      ++uc;
+      cur = nxt;
+      ucur = unxt;
+      nxt = nxt2;
+      unxt = unxt2;
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    // drain: the last load issued into each stage must land before the CTA exits
+    if (lane == 0)
+      for (int k = max(0, n - NSTAGE); k < n; ++k)
+        (void)mbar_wait_bounded(&full[k % NSTAGE], (uint32_t)(k / NSTAGE) & 1u);
+    return;
+  }
+
+  // -------------------------------------------------------------------- consumers
+  // Transposed products, so no MMA row is padding: S^T = K Q^T has the warp's 16 keys as
+  // MMA rows and the unit's query heads as MMA columns (NB blocks of 8), and
+  // O^T = V^T P^T.  A thread owns keys (gq, gq + 8) and heads (8j + 2cq, 8j + 2cq + 1):
+  // the same two heads in its S^T and O^T fragments, so each thread keeps the running
+  // max / sum of exactly the heads whose O^T columns it rescales.
+  constexpr int NB = HB / 8;
+  const int gq = lane >> 2, cq = lane & 3, mi = lane >> 3;
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+  int n = 0, uc = 0;
+
+  // find the first unit with tiles (or a zero-length unit) starting at u
+  auto next_unit = [&](int u, Unit& w) -> int {
+    for (; u < total_units; u += gridDim.x)
+      if (get_unit(a, u, w)) return u;
+    return total_units;
   };
 
-  if (tid == 0)
-    for (int i = 0; i < min(NSTAGE, n_my); ++i) issue(i, i);
+  Unit cur, nxt;
+  int ucur = next_unit(blockIdx.x, cur);
 
-  // Q fragments (A operand, 16 heads x D), loaded once.
-  const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)b * a.Hq + h0) * D;
-  uint32_t qa[KSTEPS][4];
+  // Bias ring of this warp: for stream position t (the t-th tile this CTA consumes) the
+  // lanes copy rel[b, h0 + r, min(p - k, E - 1)] for the warp's 16 keys k and the unit's
+  // heads r into slot t % BIAS_SLOTS with 4-byte cp.async, BIAS_DIST tiles ahead of use;
+  // completion is counted on the slot's mbarrier (32 arrivals, one per lane).
+  float* bring = reinterpret_cast<float*>(smem + L_::bias) + warp * BIAS_SLOTS * HB * BIAS_PITCH;
+  uint64_t* bfull = qempty + 2 + warp * BIAS_SLOTS;
+  Unit bu = cur;          // unit of the next position to stage
+  int bu_idx = ucur, bi = 0, bpos = 0;
+  auto stage_bias = [&]() {
+    // skip zero-length units: they have no tiles in the stream
+    while (bu_idx < total_units && bi >= bu.n_my) {
+      bu_idx = next_unit(bu_idx + gridDim.x, bu);
+      bi = 0;
+    }
+    const int slot = bpos % BIAS_SLOTS;
+    if (bu_idx < total_units) {
+      const int k0 = (bu.tb + bi) * TILE_KEYS;
+      if (tile_needs_bias(bu, k0, a.E)) {
+        const uint32_t dst = smem_u32(bring + slot * HB * BIAS_PITCH);
+        const int kw = k0 + 16 * warp;
+        const float* relu = a.rel + ((size_t)bu.b * a.Hq + bu.h0) * a.E;
+        for (int idx = lane; idx < bu.nh * 16; idx += 32) {
+          const int r = idx >> 4, kk = idx & 15, k = kw + kk;
+          if (k >= bu.lo && k <= bu.p)
+            cp_async_4(dst + (uint32_t)((r * BIAS_PITCH + kk) * 4), relu + (size_t)r * a.E + min(bu.p - k, a.E - 1));
+        }
+      }
+      ++bi;
+    }
+    cp_async_mbar_arrive_noinc(&bfull[slot]);
+    ++bpos;
+  };
+  for (int x = 0; x < BIAS_DIST; ++x) stage_bias();
+
+  while (ucur < total_units) {
+    const int unxt = next_unit(ucur + gridDim.x, nxt);
+    if (cur.n_my == 0) {  // zero-length sequence: zeros, nothing read
+      for (int i = tid; i < cur.nh * D; i += DEC_CONSUMERS * 32)
+        out[((size_t)cur.b * a.Hq + cur.h0 + i / D) * D + i % D] = __float2bfloat16(0.f);
+      cur = nxt;
+      ucur = unxt;
+      continue;
+    }
+    // bucket E - 1 of this thread's heads: the bias of every key at distance >= E - 1
+    float clampv[NB][2];
 #pragma unroll
-  for (int kk = 0; kk < KSTEPS; ++kk) {
-    const int c0 = kk * 16 + 2 * cq;
-    qa[kk][0] = gq < nh ? *reinterpret_cast<const uint32_t*>(qb + gq * D + c0) : 0u;
-    qa[kk][1] = gq + 8 < nh ? *reinterpret_cast<const uint32_t*>(qb + (gq + 8) * D + c0) : 0u;
-    qa[kk][2] = gq < nh ? *reinterpret_cast<const uint32_t*>(qb + gq * D + c0 + 8) : 0u;
-    qa[kk][3] = gq + 8 < nh ? *reinterpret_cast<const uint32_t*>(qb + (gq + 8) * D + c0 + 8) : 0u;
-  }
-  const float* rel0 = a.rel + ((size_t)b * a.Hq + h0 + gq) * a.E;
-  const float* rel1 = rel0 + (size_t)8 * a.E;
-  const bool row0 = gq < nh, row1 = gq + 8 < nh;
-
-  float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
-  float o[DBLK][4];
-#pragma unroll
-  for (int n = 0; n < DBLK; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-
-  bool timed_out = false;
-  for (int i = 0; i < n_my; ++i) {
-    const int s = i % NSTAGE;
-    const uint32_t par = (uint32_t)(i / NSTAGE) & 1u;
-    const int kw = (tb + i) * TILE_KEYS + 16 * warp;  // this warp's first key
-
-    // bias gather for this warp's 4 keys per thread, issued before the wait
-    float bias[2][2][2];
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb)
+    for (int j = 0; j < NB; ++j)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int k = kw + 8 * nb + 2 * cq + e;
-        const bool vis = k >= lo && k <= p;
-        const int d = min(p - k, a.E - 1);
-        bias[nb][e][0] = (vis && row0) ? __ldg(rel0 + d) : 0.f;
-        bias[nb][e][1] = (vis && row1) ? __ldg(rel1 + d) : 0.f;
+        const int h = 8 * j + 2 * cq + e;
+        clampv[j][e] = h < cur.nh ? __ldg(a.rel + ((size_t)cur.b * a.Hq + cur.h0 + h) * a.E + a.E - 1) : 0.f;
       }
+    const int qslot = uc & 1;
+    uint32_t qb[NB][KSTEPS][2];  // B fragments of Q^T
+    float m_r[NB][2], l_r[NB][2];
+    float o[D / 16][NB][4];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      m_r[j][0] = m_r[j][1] = -INFINITY;
+      l_r[j][0] = l_r[j][1] = 0.f;
+    }
+#pragma unroll
+    for (int dn = 0; dn < D / 16; ++dn)
+#pragma unroll
+      for (int j = 0; j < NB; ++j) o[dn][j][0] = o[dn][j][1] = o[dn][j][2] = o[dn][j][3] = 0.f;
 
-    if (!mbar_wait_bounded(&full[s], par)) {
-      timed_out = true;
-      record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
-      flags[1] = 1;
-    }
-    const uint64_t bad = badmask[s];
-    uint32_t valid16 = 0;
+    for (int i = 0; i < cur.n_my; ++i, ++n) {
+      const int st = n % NSTAGE;
+      const bool ok = wait_or_abort(&full[st], (uint32_t)(n / NSTAGE) & 1u, abort_flag, a.err) &&
+                      wait_or_abort(&bfull[n % BIAS_SLOTS], (uint32_t)(n / BIAS_SLOTS) & 1u, abort_flag, a.err);
+      if (i == 0) {
+        const uint32_t qbase = smem_u32(smem + L_::q + qslot * S::QSLOT_BYTES);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int k = kw + j;
-      const bool ok = k >= lo && k <= p && !((bad >> (16 * warp + j)) & 1ull);
-      valid16 |= (ok ? 1u : 0u) << j;
-    }
-    if (!timed_out && valid16 != 0) {
-      const uint32_t kbase = smem_u32(smem + s * S::STAGE_BYTES);
-      const uint32_t vbase = kbase + S::TILE_BYTES;
-      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const int mi = lane >> 3;
+        for (int j = 0; j < NB; ++j) {
+          const bool hv = ok && 8 * j + gq < cur.nh;
 #pragma unroll
-      for (int kk = 0; kk < KSTEPS; ++kk) {
-        const int krow = 16 * warp + (mi >> 1) * 8 + (lane & 7);
-        const int chunk = 2 * kk + (mi & 1);
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(kbase + (chunk >> 3) * S::SUB_BYTES + swz128(krow, chunk & 7), b0, b1, b2, b3);
-        mma_bf16_16816(sacc[0], qa[kk], b0, b1);
-        mma_bf16_16816(sacc[1], qa[kk], b2, b3);
-      }
-      // scores in log2 units, masked keys -> -inf
-      float sc[2][4];
-#pragma unroll
-      for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const bool ok = (valid16 >> (8 * nb + 2 * cq + e)) & 1u;
-          sc[nb][e] = ok ? fmaf(sacc[nb][e], a.scale_log2, bias[nb][e][0] * LOG2E) : -INFINITY;
-          sc[nb][2 + e] = ok ? fmaf(sacc[nb][2 + e], a.scale_log2, bias[nb][e][1] * LOG2E) : -INFINITY;
+          for (int kk = 0; kk < KSTEPS; kk += 2) {
+            const int row = 8 * j + (lane & 7);
+            const int chunk = 2 * kk + mi;
+            uint32_t r0, r1, r2, r3;
+            ldmatrix_x4(qbase + (chunk >> 3) * S::QSUB_BYTES + swz128(row, chunk & 7), r0, r1, r2, r3);
+            qb[j][kk][0] = hv ? r0 : 0u;
+            qb[j][kk][1] = hv ? r1 : 0u;
+            qb[j][kk + 1][0] = hv ? r2 : 0u;
+            qb[j][kk + 1][1] = hv ? r3 : 0u;
+          }
         }
-      float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-      float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m_r[0], mx0), mn1 = fmaxf(m_r[1], mx1);
-      const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = fast_exp2(m_r[0] - mu0), al1 = fast_exp2(m_r[1] - mu1);
-      m_r[0] = mn0;
-      m_r[1] = mn1;
-      float pr[2][4];
-      float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-      for (int nb = 0; nb < 2; ++nb) {
-        pr[nb][0] = fast_exp2(sc[nb][0] - mu0);
-        pr[nb][1] = fast_exp2(sc[nb][1] - mu0);
-        pr[nb][2] = fast_exp2(sc[nb][2] - mu1);
-        pr[nb][3] = fast_exp2(sc[nb][3] - mu1);
-        rs0 += pr[nb][0] + pr[nb][1];
-        rs1 += pr[nb][2] + pr[nb][3];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qempty[qslot]);
       }
-      l_r[0] = l_r[0] * al0 + rs0;
-      l_r[1] = l_r[1] * al1 + rs1;
+      const int kw = (cur.tb + i) * TILE_KEYS + 16 * warp;
+      const uint64_t bad = ok ? badmask[st] : ~0ull;
+      // keys kw + j (j < 16) with lo <= key <= p, minus keys of unreadable pages
+      const int jlo = max(cur.lo - kw, 0), jhi = min(cur.p - kw, 15);
+      uint32_t valid16 = jhi >= jlo ? ((0xFFFFu >> (15 - jhi)) & (0xFFFFu << jlo)) : 0u;
+      valid16 &= ~(uint32_t)(bad >> (16 * warp)) & 0xFFFFu;
+      if (valid16 != 0) {
+        const uint32_t kbase = smem_u32(smem + L_::stages + (size_t)st * S::STAGE_BYTES);
+        const uint32_t vbase = kbase + S::TILE_BYTES;
+        float acc[NB][4];
 #pragma unroll
-      for (int n = 0; n < DBLK; ++n) {
-        o[n][0] *= al0; o[n][1] *= al0;
-        o[n][2] *= al1; o[n][3] *= al1;
+        for (int j = 0; j < NB; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+          const int krow = 16 * warp + (mi & 1) * 8 + (lane & 7);
+          const int chunk = 2 * kk + (mi >> 1);
+          uint32_t ka[4];
+          ldmatrix_x4(kbase + (chunk >> 3) * S::SUB_BYTES + swz128(krow, chunk & 7), ka[0], ka[1], ka[2], ka[3]);
+#pragma unroll
+          for (int j = 0; j < NB; ++j) mma_bf16_16816(acc[j], ka, qb[j][kk][0], qb[j][kk][1]);
+        }
+        // V fragments (A operand of O^T = V^T P^T) into registers, masked keys zeroed;
+        // then the stage goes back to the producer before the softmax and PV run
+        const bool all_valid = valid16 == 0xFFFFu;
+        const uint32_t mlo = pair_mask((valid16 >> (2 * cq)) & 1u, (valid16 >> (2 * cq + 1)) & 1u);
+        const uint32_t mhi = pair_mask((valid16 >> (8 + 2 * cq)) & 1u, (valid16 >> (9 + 2 * cq)) & 1u);
+        uint32_t va[D / 16][4];
+#pragma unroll
+        for (int dn = 0; dn < D / 16; ++dn) {
+          const int vrow = 16 * warp + (mi >> 1) * 8 + (lane & 7);
+          const int chunk = 2 * dn + (mi & 1);
+          ldmatrix_x4_trans(vbase + (chunk >> 3) * S::SUB_BYTES + swz128(vrow, chunk & 7), va[dn][0], va[dn][1],
+                            va[dn][2], va[dn][3]);
+          if (!all_valid) { va[dn][0] &= mlo; va[dn][1] &= mlo; va[dn][2] &= mhi; va[dn][3] &= mhi; }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        const bool v0 = (valid16 >> gq) & 1u, v1 = (valid16 >> (gq + 8)) & 1u;
+        // bias: this warp's staged rows [head][key], or the clamped bucket
+        float bias[NB][4];
+        if (tile_needs_bias(cur, (cur.tb + i) * TILE_KEYS, a.E)) {
+          const float* bsm = bring + (n % BIAS_SLOTS) * HB * BIAS_PITCH + gq;
+#pragma unroll
+          for (int j = 0; j < NB; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const bool hv = 8 * j + 2 * cq + e < cur.nh;  // rows past nh are never staged
+              const float* br = bsm + (8 * j + 2 * cq + e) * BIAS_PITCH;
+              bias[j][e] = hv ? br[0] : 0.f;
+              bias[j][2 + e] = hv ? br[8] : 0.f;
+            }
+        } else {
+#pragma unroll
+          for (int j = 0; j < NB; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) bias[j][e] = bias[j][2 + e] = clampv[j][e];
+        }
+        uint32_t pb0[NB], pb1[NB];
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          float pr[4];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float s0 = v0 ? fmaf(acc[j][e], a.scale_log2, bias[j][e] * LOG2E) : -INFINITY;
+            const float s1 = v1 ? fmaf(acc[j][2 + e], a.scale_log2, bias[j][2 + e] * LOG2E) : -INFINITY;
+            float mx = fmaxf(s0, s1);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mn = fmaxf(m_r[j][e], mx);
+            const float mu = mn == -INFINITY ? 0.f : mn;
+            const float al = fast_exp2(m_r[j][e] - mu);
+            m_r[j][e] = mn;
+            pr[e] = fast_exp2(s0 - mu);
+            pr[2 + e] = fast_exp2(s1 - mu);
+            l_r[j][e] = l_r[j][e] * al + pr[e] + pr[2 + e];
+#pragma unroll
+            for (int dn = 0; dn < D / 16; ++dn) {
+              o[dn][j][e] *= al;
+              o[dn][j][2 + e] *= al;
+            }
+          }
+          // P^T into the B-fragment layout: thread (g, c) needs keys 2c, 2c+1 (and +8) of head g
+          const uint32_t X = pack_bf16(pr[0], pr[1]);  // key gq,   heads 2cq, 2cq+1
+          const uint32_t Y = pack_bf16(pr[2], pr[3]);  // key gq+8, heads 2cq, 2cq+1
+          const int src0 = 8 * cq + (gq >> 1), src1 = src0 + 4;
+          const uint32_t x0 = __shfl_sync(0xffffffffu, X, src0), x1 = __shfl_sync(0xffffffffu, X, src1);
+          const uint32_t y0 = __shfl_sync(0xffffffffu, Y, src0), y1 = __shfl_sync(0xffffffffu, Y, src1);
+          const uint32_t sel = (gq & 1) ? 0x7632u : 0x5410u;
+          pb0[j] = __byte_perm(x0, x1, sel);
+          pb1[j] = __byte_perm(y0, y1, sel);
+        }
+#pragma unroll
+        for (int dn = 0; dn < D / 16; ++dn)
+#pragma unroll
+          for (int j = 0; j < NB; ++j) mma_bf16_16816(o[dn][j], va[dn], pb0[j], pb1[j]);
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
       }
-      uint32_t pa[4];
-      pa[0] = pack_bf16(pr[0][0], pr[0][1]);
-      pa[1] = pack_bf16(pr[0][2], pr[0][3]);
-      pa[2] = pack_bf16(pr[1][0], pr[1][1]);
-      pa[3] = pack_bf16(pr[1][2], pr[1][3]);
-      const bool all_valid = valid16 == 0xFFFFu;
-      const uint32_t mlo = pair_mask((valid16 >> (2 * cq)) & 1u, (valid16 >> (2 * cq + 1)) & 1u);
-      const uint32_t mhi = pair_mask((valid16 >> (8 + 2 * cq)) & 1u, (valid16 >> (9 + 2 * cq)) & 1u);
+      stage_bias();  // position n + BIAS_DIST reuses the slot just read
+    }
+    ++uc;
+
+    // ---- unit epilogue: merge the 4 warps' partial softmax states
 #pragma unroll
-      for (int dn = 0; dn < D / 16; ++dn) {
-        const int vrow = 16 * warp + (mi & 1) * 8 + (lane & 7);
-        const int chunk = 2 * dn + (mi >> 1);
-        uint32_t v0, v1, v2, v3;
-        ldmatrix_x4_trans(vbase + (chunk >> 3) * S::SUB_BYTES + swz128(vrow, chunk & 7), v0, v1, v2, v3);
-        if (!all_valid) { v0 &= mlo; v1 &= mhi; v2 &= mlo; v3 &= mhi; }
-        mma_bf16_16816(o[2 * dn], pa, v0, v1);
-        mma_bf16_16816(o[2 * dn + 1], pa, v2, v3);
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float l = l_r[j][e];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        l_r[j][e] = l;
+        if (gq == 0) {
+          red_m[warp * 16 + 8 * j + 2 * cq + e] = m_r[j][e];
+          red_l[warp * 16 + 8 * j + 2 * cq + e] = l;
+        }
+      }
+    named_barrier_consumers();
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int h = 8 * j + 2 * cq + e;
+        if (h >= cur.nh) continue;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < DEC_CONSUMERS; ++w) M = fmaxf(M, red_m[w * 16 + h]);
+        const float f = fast_exp2(m_r[j][e] - (M == -INFINITY ? 0.f : M));
+        float* row = obuf + (warp * HB + h) * S::OPITCH;
+#pragma unroll
+        for (int dn = 0; dn < D / 16; ++dn) {
+          row[16 * dn + gq] = o[dn][j][e] * f;
+          row[16 * dn + gq + 8] = o[dn][j][2 + e] * f;
+        }
+      }
+    named_barrier_consumers();
+    const bool single = cur.nact == 1;
+    const size_t rowbase = (size_t)cur.b * a.Hq + cur.h0;
+    for (int idx = tid; idx < cur.nh * D; idx += DEC_CONSUMERS * 32) {
+      const int r = idx / D, d = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < DEC_CONSUMERS; ++w) M = fmaxf(M, red_m[w * 16 + r]);
+      const float Mu = M == -INFINITY ? 0.f : M;
+      float acc = 0.f, Lt = 0.f;
+#pragma unroll
+      for (int w = 0; w < DEC_CONSUMERS; ++w) {
+        acc += obuf[(w * HB + r) * S::OPITCH + d];
+        Lt += red_l[w * 16 + r] * fast_exp2(red_m[w * 16 + r] - Mu);
+      }
+      if (single) {
+        out[(rowbase + r) * D + d] = __float2bfloat16(Lt > 0.f ? acc / Lt : 0.f);
+      } else {
+        const size_t pi = (rowbase + r) * a.num_splits + cur.s;
+        a.part_o[pi * D + d] = acc;
+        if (d == 0) {
+          a.part_ml[pi * 2 + 0] = M;
+          a.part_ml[pi * 2 + 1] = Lt;
+        }
       }
     }
-    __syncthreads();  // every warp is done with stage s
-    if (tid == 0 && !flags[1] && i + NSTAGE < n_my) issue(i + NSTAGE, s);
-  }
-  if (flags[1] && tid == 0) {
-    // a copy never completed: give the outstanding ones one more bounded wait
-    for (int i = max(0, n_my - NSTAGE); i < n_my; ++i)
-      (void)mbar_wait_bounded(&full[i % NSTAGE], (uint32_t)(i / NSTAGE) & 1u);
-  }
-
-  // ---- merge the 4 warps' partial softmax states
-  l_r[0] += __shfl_xor_sync(0xffffffffu, l_r[0], 1);
-  l_r[0] += __shfl_xor_sync(0xffffffffu, l_r[0], 2);
-  l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], 1);
-  l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], 2);
-  if (cq == 0) {
-    red_m[warp * 16 + gq] = m_r[0];
-    red_m[warp * 16 + gq + 8] = m_r[1];
-    red_l[warp * 16 + gq] = l_r[0];
-    red_l[warp * 16 + gq + 8] = l_r[1];
-  }
-  __syncthreads();
-  float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < DEC_WARPS; ++w) {
-    M0 = fmaxf(M0, red_m[w * 16 + gq]);
-    M1 = fmaxf(M1, red_m[w * 16 + gq + 8]);
-  }
-  const float f0 = fast_exp2(m_r[0] - (M0 == -INFINITY ? 0.f : M0));
-  const float f1 = fast_exp2(m_r[1] - (M1 == -INFINITY ? 0.f : M1));
-  float* obuf = reinterpret_cast<float*>(smem);
-#pragma unroll
-  for (int n = 0; n < DBLK; ++n) {
-    const int col = 8 * n + 2 * cq;
-    float* r0p = obuf + (warp * 16 + gq) * S::OPITCH + col;
-    float* r1p = obuf + (warp * 16 + gq + 8) * S::OPITCH + col;
-    r0p[0] = o[n][0] * f0; r0p[1] = o[n][1] * f0;
-    r1p[0] = o[n][2] * f1; r1p[1] = o[n][3] * f1;
-  }
-  __syncthreads();
-
-  const bool single = nact == 1;
-  const size_t rowbase = (size_t)b * a.Hq + h0;
-  for (int idx = tid; idx < nh * D; idx += DEC_THREADS) {
-    const int r = idx / D, d = idx % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, red_m[w * 16 + r]);
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float acc = 0.f, Lt = 0.f;
-#pragma unroll
-    for (int w = 0; w < DEC_WARPS; ++w) {
-      acc += obuf[(w * 16 + r) * S::OPITCH + d];
-      Lt += red_l[w * 16 + r] * fast_exp2(red_m[w * 16 + r] - Mu);
-    }
-    if (single) {
-      out[(rowbase + r) * D + d] = __float2bfloat16(Lt > 0.f ? acc / Lt : 0.f);
-    } else {
-      const size_t pi = (rowbase + r) * a.num_splits + split;
-      a.part_o[pi * D + d] = acc;
-      if (d == 0) {
-        a.part_ml[pi * 2 + 0] = M;
-        a.part_ml[pi * 2 + 1] = Lt;
+    if (!single) {
+      // split-K ticket: the last CTA of this (sequence, KV head, head chunk) merges
+      __threadfence();
+      named_barrier_consumers();
+      const size_t ticket = ((size_t)cur.b * a.Hkv + cur.kvh) * a.head_chunks + cur.hc;
+      if (tid == 0) flags[0] = (atomicAdd(&a.tickets[ticket], 1) == cur.nact - 1);
+      named_barrier_consumers();
+      if (flags[0]) {
+        __threadfence();
+        if (tid < cur.nh) {
+          const size_t pi0 = (rowbase + tid) * a.num_splits;
+          float M = -INFINITY;
+          for (int sp = 0; sp < cur.nact; ++sp) M = fmaxf(M, __ldcg(a.part_ml + (pi0 + sp) * 2));
+          const float Mu = M == -INFINITY ? 0.f : M;
+          float Lt = 0.f;
+          for (int sp = 0; sp < cur.nact; ++sp)
+            Lt += __ldcg(a.part_ml + (pi0 + sp) * 2 + 1) * fast_exp2(__ldcg(a.part_ml + (pi0 + sp) * 2) - Mu);
+          const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+          for (int sp = 0; sp < cur.nact; ++sp)
+            wts[tid * MAX_DECODE_SPLITS + sp] = fast_exp2(__ldcg(a.part_ml + (pi0 + sp) * 2) - Mu) * inv;
+        }
+        named_barrier_consumers();
+        for (int idx = tid; idx < cur.nh * D; idx += DEC_CONSUMERS * 32) {
+          const int r = idx / D, d = idx % D;
+          const size_t pi0 = (rowbase + r) * a.num_splits;
+          float acc = 0.f;
+          for (int sp = 0; sp < cur.nact; ++sp)
+            acc += wts[r * MAX_DECODE_SPLITS + sp] * __ldcg(a.part_o + (pi0 + sp) * D + d);
+          out[(rowbase + r) * D + d] = __float2bfloat16(acc);
+        }
+        if (tid == 0) a.tickets[ticket] = 0;  // ready for the next call
       }
     }
+    named_barrier_consumers();  // red/obuf/wts/flags are reused by the next unit
+    cur = nxt;
+    ucur = unxt;
   }
-  if (single) return;
-
-  // ---- split-K ticket: the last CTA of this (sequence, head chunk) merges
-  __threadfence();
-  __syncthreads();
-  const size_t ticket = (size_t)b * gridDim.y + blockIdx.y;
-  if (tid == 0) flags[0] = (atomicAdd(&a.tickets[ticket], 1) == nact - 1);
-  __syncthreads();
-  if (!flags[0]) return;
-  __threadfence();
-  if (tid < nh) {
-    const size_t pi0 = (rowbase + tid) * a.num_splits;
-    float M = -INFINITY;
-    for (int sp = 0; sp < nact; ++sp) M = fmaxf(M, __ldcg(a.part_ml + (pi0 + sp) * 2));
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float Lt = 0.f;
-    for (int sp = 0; sp < nact; ++sp)
-      Lt += __ldcg(a.part_ml + (pi0 + sp) * 2 + 1) * fast_exp2(__ldcg(a.part_ml + (pi0 + sp) * 2) - Mu);
-    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
-    for (int sp = 0; sp < nact; ++sp)
-      wts[tid * MAX_DECODE_SPLITS + sp] = fast_exp2(__ldcg(a.part_ml + (pi0 + sp) * 2) - Mu) * inv;
-  }
-  __syncthreads();
-  for (int idx = tid; idx < nh * D; idx += DEC_THREADS) {
-    const int r = idx / D, d = idx % D;
-    const size_t pi0 = (rowbase + r) * a.num_splits;
-    float acc = 0.f;
-    for (int sp = 0; sp < nact; ++sp)
-      acc += wts[r * MAX_DECODE_SPLITS + sp] * __ldcg(a.part_o + (pi0 + sp) * D + d);
-    out[(rowbase + r) * D + d] = __float2bfloat16(acc);
-  }
-  if (tid == 0) a.tickets[ticket] = 0;  // ready for the next call
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-template <int D, int NSTAGE>
-cudaError_t launch_decode_t(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeArgs& a,
-                            cudaStream_t stream) {
-  constexpr size_t smem = decode_smem_bytes<D, NSTAGE>();
-  cudaError_t e = cudaFuncSetAttribute(decode_splitk_kernel<D, NSTAGE>,
+int num_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+template <int D, int NSTAGE, int HB>
+cudaError_t launch_decode_t(const DecodeMaps& m, const DecodeArgs& a, cudaStream_t stream) {
+  constexpr size_t smem = DecSmem<D, NSTAGE, HB>::alloc;
+  constexpr int ctas = dec_ctas_per_sm<HB>();
+  static_assert(smem * ctas <= 228 * 1024 - ctas * 1024, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(decode_persistent_kernel<D, NSTAGE, HB>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.num_splits, a.Hkv * a.head_chunks, a.B);
-  decode_splitk_kernel<D, NSTAGE><<<grid, DEC_THREADS, smem, stream>>>(tmK, tmV, a);
+  const long long units = (long long)a.num_splits * a.B * a.Hkv * a.head_chunks;
+  const int grid = (int)std::min<long long>(units, (long long)dec_ctas_per_sm<HB>() * num_sms());
+  decode_persistent_kernel<D, NSTAGE, HB><<<grid, DEC_THREADS, smem, stream>>>(m.k, m.v, m.k_seg, m.v_seg,
+                                                                              m.q, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeArgs& a,
-                          int head_dim, cudaStream_t stream) {
-  if (head_dim == 128) return launch_decode_t<128, 3>(tmK, tmV, a, stream);
-  return launch_decode_t<64, 4>(tmK, tmV, a, stream);
+cudaError_t launch_decode(const DecodeMaps& m, const DecodeArgs& a, int head_dim, cudaStream_t stream) {
+  const bool narrow = a.G <= 8;  // one 8-wide column block of query heads per unit
+  if (head_dim == 128)
+    return narrow ? launch_decode_t<128, 2, 8>(m, a, stream) : launch_decode_t<128, 4, 16>(m, a, stream);
+  return narrow ? launch_decode_t<64, 4, 8>(m, a, stream) : launch_decode_t<64, 8, 16>(m, a, stream);
 }
 
 }  // namespace ink

@@ -44,8 +44,15 @@ struct PrefillArgs {
   int max_q_len, num_q_tiles;
 };
 
-cudaError_t launch_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeArgs& a,
-                          int head_dim, cudaStream_t stream);
+// TMA descriptors of one decode call: K/V pools viewed as [num_pages*Hkv*P rows, D]
+// with 64-row boxes (whole tiles) and 16-row boxes (tiles cut by the window start or
+// the sequence end), and q viewed as [B*Hq rows, D] with 16-row boxes.
+struct DecodeMaps {
+  CUtensorMap k, v, k_seg, v_seg, q;
+};
+
+cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& a, int head_dim,
+                          cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap& tmK, const CUtensorMap& tmV, const PrefillArgs& a,
                            int head_dim, cudaStream_t stream);
 
