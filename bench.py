@@ -367,9 +367,9 @@ def run_ours(args, rank, world, local_rank):
             line["roofline"] = {"bound": "tensor", "achieved": round(r["TFLOP/s"], 2), "peak": bf16_peak,
                                 "unit": "TFLOP/s", "frac": round(r["TFLOP/s"] / bf16_peak, 4),
                                 "peak_source": peak_src,
-                                "traffic": profiled_traffic("prefill_mma.cu", name),
+                                "traffic": profiled_traffic("prefill_tc.cu", name),
                                 "algorithmic_flops": r["flops"], "algorithmic_bytes": r["bytes"],
-                                "hbm_frac": round(r["hbm_frac"], 4), "kernel": "prefill_mma_kernel"}
+                                "hbm_frac": round(r["hbm_frac"], 4), "kernel": "prefill_tc_kernel"}
         probs = r.pop("probs")
         if probs[0].is_decode:
             e2e_ms, h2d, d2h = e2e_decode(binding, probs[0], max(10, args.steps // 2), args.warmup, stream)

@@ -106,6 +106,8 @@ ink_status_t inkling_attn_workspace_init(void* workspace, size_t workspace_bytes
  *   q          device, bf16 [total_q, Hq, D], rows packed by sequence
  *   cu_q_lens  device, int32 [B+1], cu_q_lens[0] = 0, non-decreasing; n_b = cu[b+1]-cu[b]
  *   max_q_len  host int >= every n_b (sizes the grid; larger n_b set INK_DEVERR_QLEN_EXCEEDS_MAX)
+ *   total_q    host int = cu_q_lens[B], the number of rows of q, rel_logits and out (bounds
+ *              the tensor-memory copies of q; rows past it are never read)
  *   k_cache, v_cache  device, bf16 [num_pages, Hkv, P, D]; the step's K/V must already
  *              be written (new tokens are the last n_b of seq_lens[b])
  *   block_table device, int32 [B, max_pages_per_seq], positional page ids
@@ -115,7 +117,7 @@ ink_status_t inkling_attn_workspace_init(void* workspace, size_t workspace_bytes
  *   workspace  device, >= inkling_attn_workspace_bytes(params, 0), initialised once
  */
 ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q,
-                                  const int32_t* cu_q_lens, int32_t max_q_len,
+                                  const int32_t* cu_q_lens, int32_t max_q_len, int32_t total_q,
                                   const void* k_cache, const void* v_cache,
                                   const int32_t* block_table, const int32_t* seq_lens,
                                   const float* rel_logits, void* out, void* workspace,

@@ -66,7 +66,7 @@ def load_library(path: Optional[str] = None):
     lib.inkling_attn_workspace_bytes.restype = S
     lib.inkling_attn_workspace_init.argtypes = [V, S, V]
     lib.inkling_attn_workspace_init.restype = ctypes.c_int
-    lib.inkling_attn_prefill.argtypes = [PP, V, V, I32, V, V, V, V, V, V, V, S, V]
+    lib.inkling_attn_prefill.argtypes = [PP, V, V, I32, I32, V, V, V, V, V, V, V, S, V]
     lib.inkling_attn_prefill.restype = ctypes.c_int
     lib.inkling_attn_decode.argtypes = [PP, V, V, V, V, V, V, V, V, S, V]
     lib.inkling_attn_decode.restype = ctypes.c_int
@@ -153,7 +153,8 @@ def inkling_attn_prefill(params, q, cu_q_lens, max_q_len, k_cache, v_cache, bloc
     lib = load_library()
     code = lib.inkling_attn_prefill(
         ctypes.byref(params), _dev(q, "q", torch.bfloat16), _dev(cu_q_lens, "cu_q_lens", torch.int32),
-        int(max_q_len), _dev(k_cache, "k_cache", torch.bfloat16), _dev(v_cache, "v_cache", torch.bfloat16),
+        int(max_q_len), int(q.shape[0]), _dev(k_cache, "k_cache", torch.bfloat16),
+        _dev(v_cache, "v_cache", torch.bfloat16),
         _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
         _dev(rel_logits, "rel_logits", torch.float32), _dev(out, "out", torch.bfloat16),
         _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream_handle(stream))

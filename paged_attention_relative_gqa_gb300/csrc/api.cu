@@ -114,13 +114,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A bf16 matrix [rows, D] (row pitch D*2 bytes) with boxes of 64 columns x box_rows
+// A bf16 matrix [rows, cols] (row pitch cols*2 bytes) with boxes of 64 columns x box_rows
 // rows, 128-byte swizzle.
-bool make_rows_map(CUtensorMap* map, const void* base, uint64_t rows, int head_dim, int box_rows) {
+bool make_rows_map(CUtensorMap* map, const void* base, uint64_t rows, int cols, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
@@ -140,6 +140,21 @@ bool make_pool_map(CUtensorMap* map, const void* base, const ink_attn_params_t* 
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// rel_logits [total_q, Hq, E] fp32 as a 3-D tensor {E, Hq, total_q}; boxes of
+// BIAS_BOX_COLS buckets x 1 head x BIAS_BOX_ROWS tokens, out-of-range elements read as 0.
+bool make_bias_map(CUtensorMap* map, const float* rel, const ink_attn_params_t* p, int total_q) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)p->rel_extent, (cuuint64_t)p->num_q_heads, (cuuint64_t)total_q};
+  cuuint64_t strides[2] = {(cuuint64_t)p->rel_extent * 4, (cuuint64_t)p->rel_extent * 4 * p->num_q_heads};
+  cuuint32_t box[3] = {(cuuint32_t)ink::BIAS_BOX_COLS, 1, (cuuint32_t)ink::BIAS_BOX_ROWS};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(rel), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -246,7 +261,8 @@ ink_status_t inkling_attn_decode(const ink_attn_params_t* params, const void* q,
 }
 
 ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q,
-                                  const int32_t* cu_q_lens, int32_t max_q_len, const void* k_cache,
+                                  const int32_t* cu_q_lens, int32_t max_q_len, int32_t total_q,
+                                  const void* k_cache,
                                   const void* v_cache, const int32_t* block_table,
                                   const int32_t* seq_lens, const float* rel_logits, void* out,
                                   void* workspace, size_t workspace_bytes, void* stream) {
@@ -255,18 +271,20 @@ ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q
   if (!q || !cu_q_lens || !k_cache || !v_cache || !block_table || !seq_lens || !rel_logits ||
       !out || !workspace)
     return INK_ERR_NULL_PTR;
-  if (max_q_len < 0) return INK_ERR_BAD_SHAPE;
+  if (max_q_len < 0 || total_q < 0) return INK_ERR_BAD_SHAPE;
+  if ((long long)total_q * params->num_q_heads >= (1ll << 31)) return INK_ERR_TOO_LARGE;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(cu_q_lens, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
       !aligned(rel_logits, 4) || !aligned(workspace, 256))
     return INK_ERR_ALIGNMENT;
   if (workspace_bytes < kHeaderBytes) return INK_ERR_WORKSPACE;
-  if (params->num_seqs == 0 || max_q_len == 0) return INK_OK;
+  if (params->num_seqs == 0 || max_q_len == 0 || total_q == 0) return INK_OK;
   const int num_q_tiles = (max_q_len + 63) / 64;
   if (num_q_tiles > 65535 || params->num_seqs > 65535) return INK_ERR_TOO_LARGE;
-  CUtensorMap tmK, tmV;
-  if (!make_pool_map(&tmK, k_cache, params, ink::TILE_KEYS) ||
-      !make_pool_map(&tmV, v_cache, params, ink::TILE_KEYS))
+  ink::PrefillMaps maps;
+  if (!make_pool_map(&maps.k, k_cache, params, ink::TILE_KEYS) ||
+      !make_pool_map(&maps.v, v_cache, params, ink::TILE_KEYS) ||
+      !make_rows_map(&maps.q, q, (uint64_t)total_q, params->num_q_heads * params->head_dim, 128))
     return INK_ERR_CUDA;
   PrefillArgs a;
   a.q = q;
@@ -288,7 +306,10 @@ ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q
   a.scale_log2 = params->sm_scale * 1.4426950408889634f;
   a.max_q_len = max_q_len;
   a.num_q_tiles = num_q_tiles;
-  if (ink::launch_prefill(tmK, tmV, a, params->head_dim, (cudaStream_t)stream) != cudaSuccess)
+  a.bias_bulk = (params->rel_extent % 4 == 0) && aligned(rel_logits, 16);
+  std::memset(&maps.bias, 0, sizeof maps.bias);
+  if (a.bias_bulk && !make_bias_map(&maps.bias, rel_logits, params, total_q)) return INK_ERR_CUDA;
+  if (ink::launch_prefill_tc(maps, a, params->head_dim, (cudaStream_t)stream) != cudaSuccess)
     return INK_ERR_CUDA;
   return INK_OK;
 }

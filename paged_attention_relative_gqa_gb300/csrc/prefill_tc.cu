@@ -1,0 +1,700 @@
+// prefill_tc.cu -- paged prefill on the 5th-generation tensor cores (tcgen05 + TMEM),
+// with the relative-position bias and the window / causal mask fused into the score
+// tile ("Support Inkling-NVFP4 model", TensorRT-LLM PR #17062, sections "Architecture"
+// and "Implementation": the bias rel[t, h, distance] is added before the softmax; local
+// layers see a 512-key window, global layers are full causal).  New tokens are the last
+// n_b positions of the history and K/V are read through the positional block table
+// ("Inkling attn backend cleanup fake registry", TensorRT-LLM PR #17860).
+//
+// Work item: 128 consecutive new tokens of one sequence and one query head.  One CTA
+// per SM walks items in order of decreasing causal length (static round-robin).
+// Warp roles (384 threads):
+//   warps 0, 3  producers: TMA of the item's 128 query rows (q viewed as [tokens, Hq*D])
+//           and of 64-key K tiles (warp 0) and V tiles (warp 3) into separate rings (K is
+//           freed when S = Q K^T is done, V when O += P V is done; 128-byte swizzle);
+//           block-table entries are held 32 at a time in lanes and looked up by shuffle.
+//   warp 1  MMA: one lane issues S = Q K^T (M 128, N 64, fp32 in TMEM, double-buffered)
+//           and O[g % 2] += P V (P bf16 from TMEM, V from shared memory, fp32 O in TMEM).  Its
+//           lanes zero the V rows of keys no row of the item may see (edges of the
+//           window, the sequence end, unreadable pages) before P V reads them, so any
+//           bit pattern there is harmless.
+//   warp 2  bias: one 3-D TMA box (100 buckets x 8 tokens) per group of 8 rows, skewed
+//           so the row-per-thread reads are free of bank conflicts (4-byte cp.async when
+//           rows of rel are not 16-byte aligned)
+//           into a skewed fp32 ring that a row-per-thread read sees without bank
+//           conflicts; keys at distance >= E - 1 use the row's bucket E - 1 instead.
+//   warps 4-11  softmax, two warpgroups taking alternate key tiles: thread r of a
+//           warpgroup owns row r (TMEM lane r): reads its 64 scores, adds bias, masks,
+//           keeps the running max/sum in base 2 and writes P (bf16) back to TMEM; each
+//           warpgroup accumulates into its own O, rescaled in TMEM only when a row's max
+//           grows by more than 2^8.  Epilogue: the two partial results are merged,
+//           O / l -> bf16 -> out.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ink {
+
+namespace {
+
+constexpr int PT_ROWS = 128;
+constexpr int PT_THREADS = 384;
+constexpr int PT_BIAS_SLOTS = 2;
+// Bias slot: 16 groups of 8 rows (tokens); group g at float 800 g, row i of it at +100 i.
+// A group holds buckets [x_g, x_g + 100) of its 8 rows, x_g = 4*floor((dmin0 + 8g)/4)
+// - 8*(g mod 4), where dmin0 = pos0 - (k0 + 63) is row 0's smallest distance in the tile.
+// Row r = 8g + i then finds the bucket of key k0 + c at offset boff + 63 - c with
+// boff = (dmin0 mod 4) + i + 8*(g mod 4) <= 34, so 98 columns suffice, and a
+// row-per-thread read of one c touches 32 different banks.
+constexpr int PT_BIAS_GROUP = BIAS_BOX_ROWS * BIAS_BOX_COLS;   // floats per group
+constexpr int PT_BIAS_SLOT_FLOATS = 16 * PT_BIAS_GROUP;
+constexpr uint32_t TM_S = 0;     // S[2]: 64 fp32 columns each
+constexpr uint32_t TM_P = 128;   // P[2]: 32 columns (64 bf16) each
+constexpr uint32_t TM_O = 256;   // O[2]: D fp32 columns each (one per softmax warpgroup)
+constexpr uint32_t TM_COLS = 512;
+constexpr float RESCALE_LOG2 = 8.f;
+
+template <int D>
+struct PtShape {
+  static constexpr int CB = D / 64;
+  static constexpr int Q_SUB = PT_ROWS * 128;
+  static constexpr int Q_BYTES = CB * Q_SUB;
+  static constexpr int KV_SUB = TILE_KEYS * 128;
+  static constexpr int KV_TILE = CB * KV_SUB;   // one K or one V tile
+  static constexpr int NK = D == 128 ? 3 : 4;    // K ring: freed once S = Q K^T is done
+  static constexpr int NV = D == 128 ? 2 : 4;    // V ring: freed once O += P V is done
+  static constexpr int BIAS_SLOT = PT_BIAS_SLOT_FLOATS * 4;
+};
+
+template <int D>
+struct PtSmem {
+  using S = PtShape<D>;
+  static constexpr size_t q = 0;
+  static constexpr size_t kst = q + S::Q_BYTES;
+  static constexpr size_t vst = kst + (size_t)S::NK * S::KV_TILE;
+  static constexpr size_t bias = vst + (size_t)S::NV * S::KV_TILE;
+  static constexpr size_t bars = bias + (size_t)PT_BIAS_SLOTS * S::BIAS_SLOT;
+  // q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2],
+  // s_empty[2], p_full[2], o_done[2], o_free, b_full[NB], b_empty[NB], ml_full, ml_free
+  static constexpr int NBAR = 2 + 2 * S::NK + 2 * S::NV + 2 + 2 + 2 + 2 + 1 + 2 * PT_BIAS_SLOTS + 2;
+  static constexpr size_t vbad = bars + NBAR * 8;
+  static constexpr size_t ml1 = vbad + S::NV * 8;          // float2 [128]
+  static constexpr size_t misc = ml1 + PT_ROWS * 8;
+  static constexpr size_t total = misc + 32;
+  static constexpr size_t alloc = total + 1024;
+};
+
+struct PItem {
+  int b, h, kvh, t0, rows, n, L, pos0, lo_min, k_hi, kt0, ntile;
+  bool bad_len;
+};
+
+__device__ __forceinline__ bool get_item(const PrefillArgs& a, int i, PItem& it) {
+  const int per_qt = a.B * a.Hq;
+  const int qrev = i / per_qt;
+  const int r = i - qrev * per_qt;
+  it.b = r / a.Hq;
+  it.h = r - it.b * a.Hq;
+  it.kvh = it.h / a.G;
+  const int qt = a.num_q_tiles - 1 - qrev;
+  const int cu0 = __ldg(a.cu_q + it.b);
+  it.n = __ldg(a.cu_q + it.b + 1) - cu0;
+  if (qt * PT_ROWS >= it.n) return false;
+  it.L = __ldg(a.seq_lens + it.b);
+  it.t0 = cu0 + qt * PT_ROWS;
+  it.rows = min(PT_ROWS, it.n - qt * PT_ROWS);
+  it.bad_len = it.n > it.L;
+  if (it.bad_len) {
+    it.ntile = 0;
+    return true;
+  }
+  it.pos0 = it.L - it.n + qt * PT_ROWS;
+  const int p_max = it.pos0 + it.rows - 1;
+  it.lo_min = a.W > 0 ? max(0, it.pos0 - a.W + 1) : 0;
+  const long long cap = (long long)a.max_pages << a.log2_page;
+  const int k_reach = (int)min((long long)it.L, cap) - 1;
+  it.k_hi = min(p_max, k_reach);
+  it.kt0 = it.lo_min / TILE_KEYS;
+  it.ntile = it.k_hi >= it.lo_min ? it.k_hi / TILE_KEYS - it.kt0 + 1 : 0;
+  return true;
+}
+
+// First bucket held by bias group g of a tile (may be negative or past E: read as 0).
+__device__ __forceinline__ int bias_group_x(int dmin0, int g) {
+  return ((dmin0 + 8 * g) & ~3) - 8 * (g & 3);
+}
+
+// Visible keys of row position pr within tile k0 (kmin > kmax: none).
+__device__ __forceinline__ void row_tile_keys(const PrefillArgs& a, const PItem& it, int pr, int k0, int& kmin,
+                                              int& kmax) {
+  const int lor = a.W > 0 ? max(0, pr - a.W + 1) : 0;
+  kmin = max(k0, lor);
+  kmax = min(min(k0 + TILE_KEYS - 1, pr), it.k_hi);
+}
+
+// Every visible (row, key) pair of tile k0 lies at distance >= E - 1 (row 0 has the
+// smallest position, key k0 + 63 the largest index): the whole tile reads bucket E - 1.
+__device__ __forceinline__ bool tile_needs_bias(int pos0, int k0, int E) {
+  return pos0 - (k0 + TILE_KEYS - 1) < E - 1;
+}
+
+__device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err) {
+  if (*abort_flag) return false;
+  if (mbar_wait_bounded(bar, parity)) return true;
+  record_error(err, INK_DEVERR_WAIT_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
+template <int D>
+__global__ void __launch_bounds__(PT_THREADS, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmB,
+                  const PrefillArgs a) {
+  using S = PtShape<D>;
+  using L_ = PtSmem<D>;
+  constexpr int NK = S::NK, NV = S::NV;
+  constexpr uint32_t IDESC_S = umma_idesc_bf16(PT_ROWS, TILE_KEYS, false, false);
+  constexpr uint32_t IDESC_PV = umma_idesc_bf16(PT_ROWS, D, false, true);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L_::bars);
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
+  uint64_t* k_empty = k_full + NK;
+  uint64_t* v_full = k_empty + NK;
+  uint64_t* v_empty = v_full + NV;
+  uint64_t* s_full = v_empty + NV;
+  uint64_t* s_empty = s_full + 2;
+  uint64_t* p_full = s_empty + 2;
+  uint64_t* o_done = p_full + 2;
+  uint64_t* o_free = o_done + 2;
+  uint64_t* b_full = o_free + 1;
+  uint64_t* b_empty = b_full + PT_BIAS_SLOTS;
+  uint64_t* ml_full = b_empty + PT_BIAS_SLOTS;
+  uint64_t* ml_free = ml_full + 1;
+  float2* ml1 = reinterpret_cast<float2*>(smem + L_::ml1);
+  uint64_t* vbad = reinterpret_cast<uint64_t*>(smem + L_::vbad);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L_::misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L_::misc + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int P = 1 << a.log2_page;
+  const int total_items = a.num_q_tiles * a.B * a.Hq;
+
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int x = 0; x < NK; ++x) {
+      mbar_init(&k_full[x], 1);
+      mbar_init(&k_empty[x], 1);
+    }
+    for (int x = 0; x < NV; ++x) {
+      mbar_init(&v_full[x], 1);
+      mbar_init(&v_empty[x], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&s_empty[x], 4);
+      mbar_init(&p_full[x], 4);
+      mbar_init(&o_done[x], 1);
+    }
+    mbar_init(o_free, 4);
+    mbar_init(ml_full, 4);
+    mbar_init(ml_free, 4);
+    for (int x = 0; x < PT_BIAS_SLOTS; ++x) {
+      mbar_init(&b_full[x], a.bias_bulk ? 1 : 32);
+      mbar_init(&b_empty[x], 4);
+    }
+    fence_mbar_init();
+    *abort_flag = 0;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "n"(TM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 || warp == 3) {
+    // -------------------------------------------------------------- producers (TMA)
+    // warp 0 loads the query tile of each item and the K tiles, warp 3 the V tiles;
+    // each walks the block table on its own (entries held 32 at a time in lanes).
+    const bool is_k = warp == 0;
+    const int NR = is_k ? NK : NV;
+    uint64_t* full = is_k ? k_full : v_full;
+    uint64_t* empty = is_k ? k_empty : v_empty;
+    const CUtensorMap* tm = is_k ? &tmK : &tmV;
+    uint8_t* ring = smem + (is_k ? L_::kst : L_::vst);
+    if (lane == 0) {
+      prefetch_tensormap(tm);
+      if (is_k) prefetch_tensormap(&tmQ);
+    }
+    int icount = 0, g = 0;
+    int chunk_b = -1, chunk_base = 0, chunk_val = -1;
+    const int seg = P < TILE_KEYS ? P : TILE_KEYS;
+    const int nseg = TILE_KEYS / seg;
+    for (int i = blockIdx.x; i < total_items && !*abort_flag; i += gridDim.x) {
+      PItem it;
+      if (!get_item(a, i, it) || it.ntile == 0) continue;
+      if (is_k && lane == 0) {
+        bool ok = icount == 0 || wait_flag(q_empty, (uint32_t)(icount - 1) & 1u, abort_flag, a.err);
+        if (ok) {
+          mbar_arrive_expect_tx(q_full, (uint32_t)S::Q_BYTES);
+#pragma unroll
+          for (int cb = 0; cb < S::CB; ++cb)
+            tma_load_2d(smem + L_::q + cb * S::Q_SUB, &tmQ, it.h * D + cb * 64, it.t0, q_full);
+        }
+      }
+      const int32_t* bt = a.block_table + (size_t)it.b * a.max_pages;
+      const int last_idx = it.k_hi >> a.log2_page;  // never read the table past here
+      for (int j = 0; j < it.ntile; ++j, ++g) {
+        const int st = g % NR;
+        bool ok = true;
+        if (lane == 0 && g >= NR) ok = wait_flag(&empty[st], (uint32_t)((g / NR) - 1) & 1u, abort_flag, a.err);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const int k0 = (it.kt0 + j) * TILE_KEYS;
+        int rows[TILE_KEYS / 8];
+        uint64_t bad = 0;
+        uint32_t bytes = 0;
+        for (int sg = 0; sg < nseg; ++sg) {
+          const int ks = k0 + sg * seg;
+          rows[sg] = -1;
+          if (ks > it.k_hi || ks + seg - 1 < it.lo_min) continue;
+          const int pidx = ks >> a.log2_page;
+          if (chunk_b != it.b || pidx < chunk_base || pidx >= chunk_base + 32) {
+            chunk_b = it.b;
+            chunk_base = pidx;
+            const int idx = chunk_base + lane;
+            chunk_val = idx <= last_idx ? __ldg(bt + idx) : -1;
+          }
+          const int page = __shfl_sync(0xffffffffu, chunk_val, pidx - chunk_base);
+          if (page < 0 || page >= a.num_pages) {
+            bad |= (seg == 64 ? ~0ull : (((1ull << seg) - 1) << (sg * seg)));
+            if (lane == 0 && is_k) record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
+            continue;
+          }
+          rows[sg] = ((page * a.Hkv + it.kvh) << a.log2_page) + (ks & (P - 1));
+          bytes += (uint32_t)(seg * D * 2);
+        }
+        if (lane == 0) {
+          if (!is_k) vbad[st] = bad;
+          mbar_arrive_expect_tx(&full[st], bytes);
+          uint8_t* dst = ring + (size_t)st * S::KV_TILE;
+          for (int sg = 0; sg < nseg; ++sg) {
+            if (rows[sg] < 0) continue;
+#pragma unroll
+            for (int cb = 0; cb < S::CB; ++cb)
+              tma_load_2d(dst + cb * S::KV_SUB + sg * seg * 128, tm, cb * 64, rows[sg], &full[st]);
+          }
+        }
+        __syncwarp();
+      }
+      ++icount;
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    int icount = 0, g = 0;
+    // O[gg & 1] += P(gg) V(gg); tile index j of the item (the two warpgroups' first tiles
+    // of an item, j = 0 and 1, start their accumulators from zero)
+    auto issue_pv = [&](const PItem& it, int gg, int j, int icnt) {
+      const bool first = j < 2;
+      const int vs = gg % NV;
+      bool ok = wait_flag(&v_full[vs], (uint32_t)(gg / NV) & 1u, abort_flag, a.err);
+      // zero the V rows of keys that no row of this item may read
+      const int k0 = (it.kt0 + j) * TILE_KEYS;
+      const uint64_t bad = ok ? vbad[vs] : ~0ull;
+      uint8_t* vt = smem + L_::vst + (size_t)vs * S::KV_TILE;
+      if (k0 < it.lo_min || k0 + TILE_KEYS - 1 > it.k_hi || bad) {
+        for (int rr = lane; rr < TILE_KEYS; rr += 32) {
+          const int k = k0 + rr;
+          if (k < it.lo_min || k > it.k_hi || ((bad >> rr) & 1ull)) {
+#pragma unroll
+            for (int cb = 0; cb < S::CB; ++cb) {
+              uint4* row = reinterpret_cast<uint4*>(vt + cb * S::KV_SUB + rr * 128);
+#pragma unroll
+              for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+      }
+      ok = wait_flag(&p_full[gg & 1], (uint32_t)(gg >> 1) & 1u, abort_flag, a.err) && ok;
+      // the previous item's epilogue has read both O accumulators
+      if (ok && j == 0 && icnt > 0) ok = wait_flag(o_free, (uint32_t)(icnt - 1) & 1u, abort_flag, a.err);
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t vbase = smem_u32(vt);
+        if (ok) {
+#pragma unroll
+          for (int ks = 0; ks < TILE_KEYS / 16; ++ks) {
+            const uint64_t bdesc = umma_desc_sw128(vbase + ks * 16 * 128, S::KV_SUB, 1024);
+            umma_ts(tmem + TM_O + (uint32_t)((gg & 1) * D), tmem + TM_P + (gg & 1) * 32 + ks * 8, bdesc,
+                    IDESC_PV, (first && ks == 0) ? 0u : 1u);
+          }
+        }
+        umma_commit(&v_empty[vs]);
+        umma_commit(&o_done[gg & 1]);
+      }
+      __syncwarp();
+    };
+    for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
+      PItem it;
+      if (!get_item(a, i, it) || it.ntile == 0) continue;
+      (void)wait_flag(q_full, (uint32_t)icount & 1u, abort_flag, a.err);
+      for (int j = 0; j < it.ntile; ++j, ++g) {
+        const int ks_ = g % NK;
+        (void)wait_flag(&k_full[ks_], (uint32_t)(g / NK) & 1u, abort_flag, a.err);
+        if (g >= 2) (void)wait_flag(&s_empty[g & 1], (uint32_t)((g >> 1) - 1) & 1u, abort_flag, a.err);
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t qbase = smem_u32(smem + L_::q);
+          const uint32_t kbase = smem_u32(smem + L_::kst + (size_t)ks_ * S::KV_TILE);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ad = umma_desc_sw128(qbase + (kk >> 2) * S::Q_SUB + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = umma_desc_sw128(kbase + (kk >> 2) * S::KV_SUB + (kk & 3) * 32, 16, 1024);
+            umma_ss(tmem + TM_S + (g & 1) * 64, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[g & 1]);
+          umma_commit(&k_empty[ks_]);
+        }
+        __syncwarp();
+        if (j > 0) issue_pv(it, g - 1, j - 1, icount);
+      }
+      issue_pv(it, g - 1, it.ntile - 1, icount);
+      if (lane == 0) umma_commit(q_empty);
+      __syncwarp();
+      ++icount;
+    }
+  } else if (warp == 2) {
+    // -------------------------------------------------------------- bias loader
+    // Fast path (rows of rel 16-byte aligned): one lane issues one 3-D TMA box per group
+    // of 8 tokens (100 buckets x 8 rows, skewed start so the softmax reads are free of
+    // bank conflicts); out-of-range buckets arrive as zeros and are never used.
+    // Otherwise the warp copies the visible buckets with 4-byte cp.async into the same
+    // layout.  Buckets at distance >= E - 1 are never read: the softmax uses the row's
+    // bucket E - 1 for those keys.
+    // Slot s serves the tiles of softmax warpgroup s (tiles g with g % 2 == s), so each
+    // slot has one consumer that takes its tiles in order.
+    int bcnt[PT_BIAS_SLOTS] = {0, 0};
+    int g = 0;
+    if (lane == 0) prefetch_tensormap(&tmB);
+    for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
+      PItem it;
+      if (!get_item(a, i, it) || it.ntile == 0) continue;
+      for (int j = 0; j < it.ntile; ++j, ++g) {
+        const int k0 = (it.kt0 + j) * TILE_KEYS;
+        if (!tile_needs_bias(it.pos0, k0, a.E)) continue;
+        const int slot = g & 1;
+        const int use = bcnt[slot]++;
+        if (use >= 1) (void)wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err);
+        float* sb = reinterpret_cast<float*>(smem + L_::bias + (size_t)slot * S::BIAS_SLOT);
+        const int dmin0 = it.pos0 - (k0 + TILE_KEYS - 1);
+        if (a.bias_bulk) {
+          if (lane == 0) {
+            uint32_t need = 0;
+            for (int gr = 0; gr < 16; ++gr) {
+              const int r0 = 8 * gr;
+              if (r0 >= it.rows) break;
+              const int p_lo = it.pos0 + r0, p_hi = it.pos0 + min(r0 + 7, it.rows - 1);
+              // union of the group's visible ranges is [window start of p_lo, p_hi]
+              const int lo_lo = a.W > 0 ? max(0, p_lo - a.W + 1) : 0;
+              const bool any_key = p_hi >= k0 && lo_lo <= min(k0 + TILE_KEYS - 1, it.k_hi);
+              const bool all_clamped = p_lo - (k0 + TILE_KEYS - 1) >= a.E - 1;
+              if (any_key && !all_clamped) need |= 1u << gr;
+            }
+            mbar_arrive_expect_tx(&b_full[slot], (uint32_t)__popc(need) * (uint32_t)(PT_BIAS_GROUP * 4));
+            for (int gr = 0; gr < 16; ++gr)
+              if ((need >> gr) & 1u)
+                tma_load_3d(sb + gr * PT_BIAS_GROUP, &tmB, bias_group_x(dmin0, gr), it.h, it.t0 + 8 * gr,
+                            &b_full[slot]);
+          }
+        } else {
+          for (int r = 0; r < it.rows; ++r) {
+            const int pr = it.pos0 + r;
+            int kmin, kmax;
+            row_tile_keys(a, it, pr, k0, kmin, kmax);
+            const float* srcr = a.rel + ((size_t)(it.t0 + r) * a.Hq + it.h) * a.E;
+            const int gr = r >> 3, ii = r & 7;
+            const int xg = bias_group_x(dmin0, gr);
+            // bucket d sits at group_base + ii*100 + (d - x_g); visible keys give d >= x_g
+            const uint32_t rb = smem_u32(sb + gr * PT_BIAS_GROUP + ii * BIAS_BOX_COLS);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int c = lane + 32 * half;
+              const int k = k0 + c;
+              const int d = pr - k;
+              if (k >= kmin && k <= kmax && d < a.E - 1) cp_async_4(rb + (uint32_t)((d - xg) * 4), srcr + d);
+            }
+          }
+          cp_async_mbar_arrive_noinc(&b_full[slot]);
+        }
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else {
+    // -------------------------------------------------------------- softmax warpgroups
+    // Warpgroup wg (warps 4-7: wg 0, warps 8-11: wg 1) owns the tiles g with g % 2 == wg
+    // and its own O accumulator in TMEM; thread r of a warpgroup owns row r.  At the end
+    // of an item wg 1 hands (max, sum) of its rows to wg 0 through shared memory and wg 0
+    // merges both partial results and writes the output.
+    const int wg = (warp - 4) >> 2;
+    const int sw = (warp - 4) & 3;
+    const int r = sw * 32 + lane;
+    const uint32_t tlane = tmem + ((uint32_t)(sw * 32) << 16);
+    const uint32_t tm_o = tlane + TM_O + (uint32_t)(wg * D);
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+    int icount = 0, g = 0, buse = 0;  // buse: bias tiles this warpgroup has consumed
+    for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
+      PItem it;
+      if (!get_item(a, i, it)) continue;
+      const bool rv = r < it.rows;
+      if (wg == 0 && sw == 0 && lane == 0 && it.t0 == __ldg(a.cu_q + it.b) && it.h == 0) {
+        if (it.n > a.max_q_len) record_error(a.err, INK_DEVERR_QLEN_EXCEEDS_MAX);
+        if (it.bad_len) record_error(a.err, INK_DEVERR_QLEN_EXCEEDS_KV);
+        else if ((long long)it.L > ((long long)a.max_pages << a.log2_page))
+          record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
+      }
+      if (it.ntile == 0) {  // nothing visible (inconsistent lengths or no readable key): zeros
+        if (wg == 0 && rv) {
+          uint4* o = reinterpret_cast<uint4*>(out + ((size_t)(it.t0 + r) * a.Hq + it.h) * D);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) o[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        continue;
+      }
+      const int pr = it.pos0 + r;
+      const float* relrow = a.rel + ((size_t)(it.t0 + r) * a.Hq + it.h) * a.E;
+      const float clampv = rv ? __ldg(relrow + a.E - 1) * LOG2E : 0.f;
+      const int32_t* bt = a.block_table + (size_t)it.b * a.max_pages;
+      const int seg = P < TILE_KEYS ? P : TILE_KEYS;
+      // unreadable pages of a tile (same rule as the producers: segments holding a key
+      // some row of the item may see, with a page id outside the pool)
+      auto tile_bad = [&](int k0) {
+        uint64_t bad = 0;
+        for (int sg = 0; sg < TILE_KEYS / seg; ++sg) {
+          const int ks = k0 + sg * seg;
+          if (ks > it.k_hi || ks + seg - 1 < it.lo_min) continue;
+          const int page = __ldg(bt + (ks >> a.log2_page));
+          if (page < 0 || page >= a.num_pages) bad |= (seg == 64 ? ~0ull : (((1ull << seg) - 1) << (sg * seg)));
+        }
+        return bad;
+      };
+      const int g0 = g;
+      float m = -INFINITY, l = 0.f;
+      bool fresh = true;  // no tile of this item seen yet by this warpgroup
+      for (int j = 0; j < it.ntile; ++j, ++g) {
+        const int k0 = (it.kt0 + j) * TILE_KEYS;
+        const bool needs = tile_needs_bias(it.pos0, k0, a.E);
+        if ((g & 1) != wg) continue;  // the other warpgroup's tile
+        uint64_t bad = tile_bad(k0);
+        bool ok = wait_flag(&s_full[g & 1], (uint32_t)(g >> 1) & 1u, abort_flag, a.err);
+        tc_fence_after();
+        uint32_t sr[64];
+        {
+          uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+          uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+          tmem_ld32(tlane + TM_S + (g & 1) * 64, lo);
+          tmem_ld32(tlane + TM_S + (g & 1) * 64 + 32, hi);
+          tmem_wait_ld();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[g & 1]);
+        if (!ok) bad = ~0ull;
+        int kmin, kmax;
+        row_tile_keys(a, it, pr, k0, kmin, kmax);
+        if (!rv) kmax = kmin - 1;
+        const int dmin = pr - (k0 + TILE_KEYS - 1);   // distance of key c is dmin + 63 - c
+        const float* brow = nullptr;
+        if (needs) {
+          const int slot = wg;
+          (void)wait_flag(&b_full[slot], (uint32_t)buse & 1u, abort_flag, a.err);
+          // bucket of key c is d = dmin + 63 - c, stored at group_base + i*100 + (d - x_g)
+          const int gr = r >> 3;
+          brow = reinterpret_cast<const float*>(smem + L_::bias + (size_t)slot * S::BIAS_SLOT) + gr * PT_BIAS_GROUP +
+                 (r & 7) * BIAS_BOX_COLS + (dmin - bias_group_x(dmin - r, gr)) + (TILE_KEYS - 1);
+        }
+        // fast path: every key of the tile visible to every row of the warp, no clamping
+        const bool fast_row = kmin == k0 && kmax == k0 + TILE_KEYS - 1 && bad == 0 && dmin + TILE_KEYS - 1 < a.E - 1;
+        float mxv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (__all_sync(0xffffffffu, fast_row)) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const float sv = fmaf(__uint_as_float(sr[c]), a.scale_log2, brow[-c] * LOG2E);
+            sr[c] = __float_as_uint(sv);
+            mxv[c & 3] = fmaxf(mxv[c & 3], sv);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const int k = k0 + c;
+            const bool v = k >= kmin && k <= kmax && !((bad >> c) & 1ull);
+            const bool clamped = dmin + (TILE_KEYS - 1) - c >= a.E - 1;
+            const float bsv = (needs && !clamped) ? brow[-c] * LOG2E : clampv;
+            const float sv = v ? fmaf(__uint_as_float(sr[c]), a.scale_log2, bsv) : -INFINITY;
+            sr[c] = __float_as_uint(sv);
+            mxv[c & 3] = fmaxf(mxv[c & 3], sv);
+          }
+        }
+        const float mx = fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3]));
+        if (needs) {
+          // every bias value this thread read is consumed (mx depends on all of them)
+          asm volatile("" ::"f"(mx) : "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&b_empty[wg]);
+          ++buse;
+        }
+        const float m_new = fmaxf(m, mx);
+        if (fresh) {
+          m = m_new;
+        } else {
+          const bool mine = m_new > m + RESCALE_LOG2;
+          if (__any_sync(0xffffffffu, mine)) {
+            // this warpgroup's O must be stable: its previous P V product (tile g - 2) is done
+            (void)wait_flag(&o_done[g & 1], (uint32_t)((g - 2) >> 1) & 1u, abort_flag, a.err);
+            tc_fence_after();
+            const float f = mine ? fast_exp2(m - m_new) : 1.f;
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t ov[32];
+              tmem_ld32(tm_o + cc * 32, ov);
+              tmem_wait_ld();
+#pragma unroll
+              for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * f);
+              tmem_st32(tm_o + cc * 32, ov);
+            }
+            tmem_wait_st();
+            l *= f;
+            if (mine) m = m_new;
+          }
+        }
+        const float mu = m == -INFINITY ? 0.f : m;
+        uint32_t pk[32];
+        float lsv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = fast_exp2(__uint_as_float(sr[2 * c]) - mu);
+          const float p1 = fast_exp2(__uint_as_float(sr[2 * c + 1]) - mu);
+          lsv[c & 3] += p0 + p1;
+          pk[c] = pack_bf16(p0, p1);
+        }
+        l += (lsv[0] + lsv[1]) + (lsv[2] + lsv[3]);
+        // P buffer g & 1 was last read by the P V product of tile g - 2
+        if (g >= 2) (void)wait_flag(&o_done[g & 1], (uint32_t)((g - 2) >> 1) & 1u, abort_flag, a.err);
+        tmem_st32(tlane + TM_P + (g & 1) * 32, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[g & 1]);
+        fresh = false;
+      }
+      // ---- item epilogue
+      const int g_last = g - 1;
+      if (wg == 1) {
+        if (icount > 0) (void)wait_flag(ml_free, (uint32_t)(icount - 1) & 1u, abort_flag, a.err);
+        ml1[r] = make_float2(m, l);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ml_full);
+      } else {
+        // Warpgroup 1 first: once it has stored its last P it has waited for its P V
+        // product two tiles back, so o_done[1] is at most one phase short of the count
+        // awaited below.  Waiting on o_done[1] earlier could see a phase two behind,
+        // whose parity matches, and read O_1 before its last product lands.
+        (void)wait_flag(ml_full, (uint32_t)icount & 1u, abort_flag, a.err);
+        // both warpgroups' last P V products of the item are done
+        (void)wait_flag(&o_done[g_last & 1], (uint32_t)(g_last >> 1) & 1u, abort_flag, a.err);
+        if (g_last > g0)
+          (void)wait_flag(&o_done[(g_last - 1) & 1], (uint32_t)((g_last - 1) >> 1) & 1u, abort_flag, a.err);
+        tc_fence_after();
+        const float2 o1 = ml1[r];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ml_free);
+        const float M = fmaxf(m, o1.x);
+        const float Mu = M == -INFINITY ? 0.f : M;
+        const bool has0 = l > 0.f, has1 = o1.y > 0.f;   // a warpgroup without tiles holds stale O
+        const float f0 = has0 ? fast_exp2(m - Mu) : 0.f;
+        const float f1 = has1 ? fast_exp2(o1.x - Mu) : 0.f;
+        const float Lt = l * f0 + o1.y * f1;
+        const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+        const float c0 = f0 * inv, c1 = f1 * inv;
+        uint4* orow = reinterpret_cast<uint4*>(out + ((size_t)(it.t0 + r) * a.Hq + it.h) * D);
+        const uint32_t t_o0 = tlane + TM_O, t_o1 = tlane + TM_O + D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 16; ++cc) {
+          uint32_t ov[16], ow[16];
+          tmem_ld16(t_o0 + cc * 16, ov);
+          tmem_ld16(t_o1 + cc * 16, ow);
+          tmem_wait_ld();
+          if (rv) {
+#pragma unroll
+            for (int q4 = 0; q4 < 2; ++q4) {
+              float y[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float a0 = has0 ? __uint_as_float(ov[8 * q4 + e]) * c0 : 0.f;
+                const float a1 = has1 ? __uint_as_float(ow[8 * q4 + e]) * c1 : 0.f;
+                y[e] = a0 + a1;
+              }
+              uint4 v;
+              v.x = pack_bf16(y[0], y[1]);
+              v.y = pack_bf16(y[2], y[3]);
+              v.z = pack_bf16(y[4], y[5]);
+              v.w = pack_bf16(y[6], y[7]);
+              orow[cc * 2 + q4] = v;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);
+      }
+      ++icount;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(TM_COLS));
+  }
+}
+
+int num_sms_pf() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+template <int D>
+cudaError_t launch_prefill_tc_t(const PrefillMaps& m, const PrefillArgs& a, cudaStream_t stream) {
+  constexpr size_t smem = PtSmem<D>::alloc;
+  static_assert(smem <= 227 * 1024, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const long long items = (long long)a.num_q_tiles * a.B * a.Hq;
+  const int grid = (int)std::min<long long>(items, num_sms_pf());
+  prefill_tc_kernel<D><<<grid, PT_THREADS, smem, stream>>>(m.k, m.v, m.q, m.bias, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PrefillMaps& m, const PrefillArgs& a, int head_dim, cudaStream_t stream) {
+  if (head_dim == 128) return launch_prefill_tc_t<128>(m, a, stream);
+  return launch_prefill_tc_t<64>(m, a, stream);
+}
+
+}  // namespace ink

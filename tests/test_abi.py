@@ -80,7 +80,7 @@ def test_invalid_params_are_rejected_without_launch(lib, bad, code):
     r = lib.inkling_attn_decode(ctypes.byref(params), fake, fake, fake, fake, fake, fake, fake,
                                 fake, 1 << 30, None)
     assert r == code
-    r = lib.inkling_attn_prefill(ctypes.byref(params), fake, fake, 16, fake, fake, fake, fake, fake,
+    r = lib.inkling_attn_prefill(ctypes.byref(params), fake, fake, 16, 64, fake, fake, fake, fake, fake,
                                  fake, fake, 1 << 30, None)
     assert r == code
 
