@@ -304,6 +304,7 @@ ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q
   a.E = params->rel_extent;
   a.W = params->window;
   a.scale_log2 = params->sm_scale * 1.4426950408889634f;
+  a.sm_scale = params->sm_scale;
   a.max_q_len = max_q_len;
   a.num_q_tiles = num_q_tiles;
   a.bias_bulk = (params->rel_extent % 4 == 0) && aligned(rel_logits, 16);

@@ -41,6 +41,7 @@ struct PrefillArgs {
   int B, Hq, Hkv, G;
   int log2_page, max_pages, num_pages, E, W;
   float scale_log2;
+  float sm_scale;             // multiplies q.k (the bias is added unscaled)
   int max_q_len, num_q_tiles;
   int bias_bulk;              // rows of rel are 16-byte aligned (E % 4 == 0, aligned base)
 };

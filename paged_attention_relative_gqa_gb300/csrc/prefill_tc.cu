@@ -53,7 +53,7 @@ constexpr uint32_t TM_S = 0;     // S[2]: 64 fp32 columns each
 constexpr uint32_t TM_P = 128;   // P[2]: 32 columns (64 bf16) each
 constexpr uint32_t TM_O = 256;   // O[2]: D fp32 columns each (one per softmax warpgroup)
 constexpr uint32_t TM_COLS = 512;
-constexpr float RESCALE_LOG2 = 8.f;
+constexpr float RESCALE_NAT = 5.545177444479562f;   // rescale O when a max grows by > 2^8
 
 template <int D>
 struct PtShape {
@@ -118,6 +118,16 @@ __device__ __forceinline__ bool get_item(const PrefillArgs& a, int i, PItem& it)
   it.kt0 = it.lo_min / TILE_KEYS;
   it.ntile = it.k_hi >= it.lo_min ? it.k_hi / TILE_KEYS - it.kt0 + 1 : 0;
   return true;
+}
+
+// Key tiles of all items this CTA takes.
+__device__ int cta_tiles(const PrefillArgs& a, int total_items) {
+  int n = 0;
+  PItem it;
+#pragma unroll 1
+  for (int i = blockIdx.x; i < total_items; i += gridDim.x)
+    if (get_item(a, i, it)) n += it.ntile;
+  return n;
 }
 
 // First bucket held by bias group g of a tile (may be negative or past E: read as 0).
@@ -262,39 +272,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         const int k0 = (it.kt0 + j) * TILE_KEYS;
-        int rows[TILE_KEYS / 8];
-        uint64_t bad = 0;
-        uint32_t bytes = 0;
-        for (int sg = 0; sg < nseg; ++sg) {
-          const int ks = k0 + sg * seg;
-          rows[sg] = -1;
-          if (ks > it.k_hi || ks + seg - 1 < it.lo_min) continue;
-          const int pidx = ks >> a.log2_page;
-          if (chunk_b != it.b || pidx < chunk_base || pidx >= chunk_base + 32) {
-            chunk_b = it.b;
-            chunk_base = pidx;
-            const int idx = chunk_base + lane;
-            chunk_val = idx <= last_idx ? __ldg(bt + idx) : -1;
-          }
-          const int page = __shfl_sync(0xffffffffu, chunk_val, pidx - chunk_base);
-          if (page < 0 || page >= a.num_pages) {
-            bad |= (seg == 64 ? ~0ull : (((1ull << seg) - 1) << (sg * seg)));
-            if (lane == 0 && is_k) record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
-            continue;
-          }
-          rows[sg] = ((page * a.Hkv + it.kvh) << a.log2_page) + (ks & (P - 1));
-          bytes += (uint32_t)(seg * D * 2);
+        // lane sg < nseg takes segment sg of the tile: seg keys on one page
+        const int pfirst = k0 >> a.log2_page, plast = (k0 + TILE_KEYS - 1) >> a.log2_page;
+        if (chunk_b != it.b || pfirst < chunk_base || plast >= chunk_base + 32) {
+          chunk_b = it.b;
+          chunk_base = pfirst;
+          const int idx = chunk_base + lane;
+          chunk_val = idx <= last_idx ? __ldg(bt + idx) : -1;
         }
+        const int ks = k0 + lane * seg;
+        const bool want = lane < nseg && ks <= it.k_hi && ks + seg - 1 >= it.lo_min;
+        const int page = __shfl_sync(0xffffffffu, chunk_val, min(max((ks >> a.log2_page) - chunk_base, 0), 31));
+        const bool bad_seg = want && (page < 0 || page >= a.num_pages);
+        const bool load = want && !bad_seg;
+        const uint32_t lmask = __ballot_sync(0xffffffffu, load);
+        const uint32_t bmask = __ballot_sync(0xffffffffu, bad_seg);
         if (lane == 0) {
-          if (!is_k) vbad[st] = bad;
-          mbar_arrive_expect_tx(&full[st], bytes);
-          uint8_t* dst = ring + (size_t)st * S::KV_TILE;
-          for (int sg = 0; sg < nseg; ++sg) {
-            if (rows[sg] < 0) continue;
-#pragma unroll
-            for (int cb = 0; cb < S::CB; ++cb)
-              tma_load_2d(dst + cb * S::KV_SUB + sg * seg * 128, tm, cb * 64, rows[sg], &full[st]);
+          if (bmask && is_k) record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
+          if (!is_k) {
+            uint64_t bad = 0;
+#pragma unroll 1
+            for (uint32_t mm = bmask; mm; mm &= mm - 1)
+              bad |= seg == 64 ? ~0ull : (((1ull << seg) - 1) << ((__ffs(mm) - 1) * seg));
+            vbad[st] = bad;
           }
+          mbar_arrive_expect_tx(&full[st], (uint32_t)__popc(lmask) * (uint32_t)(seg * D * 2));
+        }
+        __syncwarp();
+        if (load) {
+          const int row = ((page * a.Hkv + it.kvh) << a.log2_page) + (ks & (P - 1));
+          uint8_t* dst = ring + (size_t)st * S::KV_TILE + lane * seg * 128;
+#pragma unroll
+          for (int cb = 0; cb < S::CB; ++cb) tma_load_2d(dst + cb * S::KV_SUB, tm, cb * 64, row, &full[st]);
         }
         __syncwarp();
       }
@@ -302,22 +311,67 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
-    int icount = 0, g = 0;
-    // O[gg & 1] += P(gg) V(gg); tile index j of the item (the two warpgroups' first tiles
-    // of an item, j = 0 and 1, start their accumulators from zero)
-    auto issue_pv = [&](const PItem& it, int gg, int j, int icnt) {
-      const bool first = j < 2;
+    // Static order over this CTA's tiles g (all items, in sequence): step g issues
+    // S(g) = Q K(g)^T, then O[(g-2) % 2] += P(g-2) V(g-2).  S(g) reuses the S buffer
+    // of tile g - 2, which its warpgroup empties as soon as it starts that tile, so each
+    // warpgroup finds its next S already computed when it finishes a P.  Every wait of
+    // step g depends only on earlier steps.  At the first tile of an item the product
+    // P V of step g goes first: S(g) waits for the item's query tile, which is loaded
+    // only once every S of the previous item is done.
+    const int total = cta_tiles(a, total_items);
+    PItem its{}, itp{};
+    int is = blockIdx.x - (int)gridDim.x, ip = is;
+    int js = 0, jp = 0, ics = -1, icp = -1;   // tile within item, items started
+    int ns = 0, np = 0;                        // tiles of the current S / PV item
+    auto issue_s = [&](int g) {
+      if (js == ns) {  // next item with tiles
+        do { is += gridDim.x; } while (!(get_item(a, is, its) && its.ntile > 0));
+        js = 0;
+        ns = its.ntile;
+        ++ics;
+        (void)wait_flag(q_full, (uint32_t)ics & 1u, abort_flag, a.err);
+      }
+      const int ks_ = g % NK;
+      (void)wait_flag(&k_full[ks_], (uint32_t)(g / NK) & 1u, abort_flag, a.err);
+      if (g >= 2) (void)wait_flag(&s_empty[g & 1], (uint32_t)((g >> 1) - 1) & 1u, abort_flag, a.err);
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t qbase = smem_u32(smem + L_::q);
+        const uint32_t kbase = smem_u32(smem + L_::kst + (size_t)ks_ * S::KV_TILE);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = umma_desc_sw128(qbase + (kk >> 2) * S::Q_SUB + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = umma_desc_sw128(kbase + (kk >> 2) * S::KV_SUB + (kk & 3) * 32, 16, 1024);
+          umma_ss(tmem + TM_S + (g & 1) * 64, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[g & 1]);
+        umma_commit(&k_empty[ks_]);
+        if (js == ns - 1) umma_commit(q_empty);   // the item's last S: Q may be replaced
+      }
+      __syncwarp();
+      ++js;
+    };
+    // O[gg % 2] += P(gg) V(gg); the two warpgroups' first tiles of an item (jp 0 and 1)
+    // start their accumulators from zero
+    auto issue_pv = [&](int gg) {
+      if (jp == np) {
+        do { ip += gridDim.x; } while (!(get_item(a, ip, itp) && itp.ntile > 0));
+        jp = 0;
+        np = itp.ntile;
+        ++icp;
+      }
       const int vs = gg % NV;
       bool ok = wait_flag(&v_full[vs], (uint32_t)(gg / NV) & 1u, abort_flag, a.err);
       // zero the V rows of keys that no row of this item may read
-      const int k0 = (it.kt0 + j) * TILE_KEYS;
+      const int k0 = (itp.kt0 + jp) * TILE_KEYS;
       const uint64_t bad = ok ? vbad[vs] : ~0ull;
       uint8_t* vt = smem + L_::vst + (size_t)vs * S::KV_TILE;
-      if (k0 < it.lo_min || k0 + TILE_KEYS - 1 > it.k_hi || bad) {
+      if (k0 < itp.lo_min || k0 + TILE_KEYS - 1 > itp.k_hi || bad) {
+#pragma unroll 1
         for (int rr = lane; rr < TILE_KEYS; rr += 32) {
           const int k = k0 + rr;
-          if (k < it.lo_min || k > it.k_hi || ((bad >> rr) & 1ull)) {
-#pragma unroll
+          if (k < itp.lo_min || k > itp.k_hi || ((bad >> rr) & 1ull)) {
+#pragma unroll 1
             for (int cb = 0; cb < S::CB; ++cb) {
               uint4* row = reinterpret_cast<uint4*>(vt + cb * S::KV_SUB + rr * 128);
 #pragma unroll
@@ -330,7 +384,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       }
       ok = wait_flag(&p_full[gg & 1], (uint32_t)(gg >> 1) & 1u, abort_flag, a.err) && ok;
       // the previous item's epilogue has read both O accumulators
-      if (ok && j == 0 && icnt > 0) ok = wait_flag(o_free, (uint32_t)(icnt - 1) & 1u, abort_flag, a.err);
+      if (ok && jp == 0 && icp > 0) ok = wait_flag(o_free, (uint32_t)(icp - 1) & 1u, abort_flag, a.err);
       if (lane == 0) {
         tc_fence_after();
         const uint32_t vbase = smem_u32(vt);
@@ -339,42 +393,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
           for (int ks = 0; ks < TILE_KEYS / 16; ++ks) {
             const uint64_t bdesc = umma_desc_sw128(vbase + ks * 16 * 128, S::KV_SUB, 1024);
             umma_ts(tmem + TM_O + (uint32_t)((gg & 1) * D), tmem + TM_P + (gg & 1) * 32 + ks * 8, bdesc,
-                    IDESC_PV, (first && ks == 0) ? 0u : 1u);
+                    IDESC_PV, (jp < 2 && ks == 0) ? 0u : 1u);
           }
         }
         umma_commit(&v_empty[vs]);
         umma_commit(&o_done[gg & 1]);
       }
       __syncwarp();
+      ++jp;
     };
-    for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
-      PItem it;
-      if (!get_item(a, i, it) || it.ntile == 0) continue;
-      (void)wait_flag(q_full, (uint32_t)icount & 1u, abort_flag, a.err);
-      for (int j = 0; j < it.ntile; ++j, ++g) {
-        const int ks_ = g % NK;
-        (void)wait_flag(&k_full[ks_], (uint32_t)(g / NK) & 1u, abort_flag, a.err);
-        if (g >= 2) (void)wait_flag(&s_empty[g & 1], (uint32_t)((g >> 1) - 1) & 1u, abort_flag, a.err);
-        if (lane == 0) {
-          tc_fence_after();
-          const uint32_t qbase = smem_u32(smem + L_::q);
-          const uint32_t kbase = smem_u32(smem + L_::kst + (size_t)ks_ * S::KV_TILE);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad = umma_desc_sw128(qbase + (kk >> 2) * S::Q_SUB + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = umma_desc_sw128(kbase + (kk >> 2) * S::KV_SUB + (kk & 3) * 32, 16, 1024);
-            umma_ss(tmem + TM_S + (g & 1) * 64, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(&s_full[g & 1]);
-          umma_commit(&k_empty[ks_]);
+#pragma unroll 1
+    for (int g = 0; g < total + 2 && !*abort_flag; ++g) {
+      const bool do_s = g < total, do_pv = g >= 2;
+      const bool pv_first = do_pv && do_s && js == ns;   // S(g) opens a new item
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        if ((half == 0) == pv_first) {
+          if (do_pv) issue_pv(g - 2);
+        } else if (do_s) {
+          issue_s(g);
         }
-        __syncwarp();
-        if (j > 0) issue_pv(it, g - 1, j - 1, icount);
       }
-      issue_pv(it, g - 1, it.ntile - 1, icount);
-      if (lane == 0) umma_commit(q_empty);
-      __syncwarp();
-      ++icount;
     }
   } else if (warp == 2) {
     // -------------------------------------------------------------- bias loader
@@ -403,6 +442,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         if (a.bias_bulk) {
           if (lane == 0) {
             uint32_t need = 0;
+#pragma unroll 1
             for (int gr = 0; gr < 16; ++gr) {
               const int r0 = 8 * gr;
               if (r0 >= it.rows) break;
@@ -414,12 +454,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
               if (any_key && !all_clamped) need |= 1u << gr;
             }
             mbar_arrive_expect_tx(&b_full[slot], (uint32_t)__popc(need) * (uint32_t)(PT_BIAS_GROUP * 4));
+#pragma unroll 1
             for (int gr = 0; gr < 16; ++gr)
               if ((need >> gr) & 1u)
                 tma_load_3d(sb + gr * PT_BIAS_GROUP, &tmB, bias_group_x(dmin0, gr), it.h, it.t0 + 8 * gr,
                             &b_full[slot]);
           }
         } else {
+#pragma unroll 1
           for (int r = 0; r < it.rows; ++r) {
             const int pr = it.pos0 + r;
             int kmin, kmax;
@@ -475,13 +517,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       }
       const int pr = it.pos0 + r;
       const float* relrow = a.rel + ((size_t)(it.t0 + r) * a.Hq + it.h) * a.E;
-      const float clampv = rv ? __ldg(relrow + a.E - 1) * LOG2E : 0.f;
+      const float clampv = rv ? __ldg(relrow + a.E - 1) : 0.f;   // bucket of distances >= E - 1
       const int32_t* bt = a.block_table + (size_t)it.b * a.max_pages;
       const int seg = P < TILE_KEYS ? P : TILE_KEYS;
-      // unreadable pages of a tile (same rule as the producers: segments holding a key
-      // some row of the item may see, with a page id outside the pool)
+      // Does some page holding a key of the item lie outside the pool?  (Checked once per
+      // item; only then are per-tile masks of unreadable keys built.)
+      bool item_bad = false;
+      {
+        const int p0 = it.lo_min >> a.log2_page, p1 = it.k_hi >> a.log2_page;
+#pragma unroll 1
+        for (int pi = p0 + lane; pi <= p1; pi += 32) {
+          const int page = __ldg(bt + pi);
+          item_bad |= page < 0 || page >= a.num_pages;
+        }
+        item_bad = __any_sync(0xffffffffu, item_bad);
+      }
+      // unreadable keys of a tile (same rule as the producers: segments holding a key some
+      // row of the item may see, with a page id outside the pool)
       auto tile_bad = [&](int k0) {
         uint64_t bad = 0;
+#pragma unroll 1
         for (int sg = 0; sg < TILE_KEYS / seg; ++sg) {
           const int ks = k0 + sg * seg;
           if (ks > it.k_hi || ks + seg - 1 < it.lo_min) continue;
@@ -491,13 +546,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         return bad;
       };
       const int g0 = g;
+      // running max (natural units) and sum of this warpgroup's tiles
       float m = -INFINITY, l = 0.f;
       bool fresh = true;  // no tile of this item seen yet by this warpgroup
+      const float* bslot = reinterpret_cast<const float*>(smem + L_::bias + (size_t)wg * S::BIAS_SLOT);
       for (int j = 0; j < it.ntile; ++j, ++g) {
         const int k0 = (it.kt0 + j) * TILE_KEYS;
         const bool needs = tile_needs_bias(it.pos0, k0, a.E);
         if ((g & 1) != wg) continue;  // the other warpgroup's tile
-        uint64_t bad = tile_bad(k0);
+        uint64_t bad = item_bad ? tile_bad(k0) : 0ull;
         bool ok = wait_flag(&s_full[g & 1], (uint32_t)(g >> 1) & 1u, abort_flag, a.err);
         tc_fence_after();
         uint32_t sr[64];
@@ -512,37 +569,47 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[g & 1]);
         if (!ok) bad = ~0ull;
+        // visible columns of this row: [kmin - k0, kmax - k0] less unreadable keys
         int kmin, kmax;
         row_tile_keys(a, it, pr, k0, kmin, kmax);
-        if (!rv) kmax = kmin - 1;
-        const int dmin = pr - (k0 + TILE_KEYS - 1);   // distance of key c is dmin + 63 - c
-        const float* brow = nullptr;
+        uint64_t vis = 0;
+        if (rv && kmax >= kmin) vis = (~0ull >> (TILE_KEYS - 1 - (kmax - k0))) & (~0ull << (kmin - k0));
+        vis &= ~bad;
+        // key c sits at distance dmin + 63 - c; columns c <= cc read bucket E - 1
+        const int dmin = pr - (k0 + TILE_KEYS - 1);
+        const int cc = dmin + TILE_KEYS - a.E;
+        // bucket of key c at brow[-c] (group_base + i*100 + (d - x_g)); any address in the
+        // slot when the tile reads no bucket from it
+        const float* brow = bslot + (TILE_KEYS - 1);
         if (needs) {
-          const int slot = wg;
-          (void)wait_flag(&b_full[slot], (uint32_t)buse & 1u, abort_flag, a.err);
-          // bucket of key c is d = dmin + 63 - c, stored at group_base + i*100 + (d - x_g)
+          (void)wait_flag(&b_full[wg], (uint32_t)buse & 1u, abort_flag, a.err);
           const int gr = r >> 3;
-          brow = reinterpret_cast<const float*>(smem + L_::bias + (size_t)slot * S::BIAS_SLOT) + gr * PT_BIAS_GROUP +
-                 (r & 7) * BIAS_BOX_COLS + (dmin - bias_group_x(dmin - r, gr)) + (TILE_KEYS - 1);
+          brow = bslot + gr * PT_BIAS_GROUP + (r & 7) * BIAS_BOX_COLS + (dmin - bias_group_x(dmin - r, gr)) +
+                 (TILE_KEYS - 1);
         }
-        // fast path: every key of the tile visible to every row of the warp, no clamping
-        const bool fast_row = kmin == k0 && kmax == k0 + TILE_KEYS - 1 && bad == 0 && dmin + TILE_KEYS - 1 < a.E - 1;
         float mxv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (__all_sync(0xffffffffu, fast_row)) {
+        const bool all_vis = vis == ~0ull;
+        if (__all_sync(0xffffffffu, all_vis && cc < 0)) {
+          // every key visible, every bucket from the tile's bias rows
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
-            const float sv = fmaf(__uint_as_float(sr[c]), a.scale_log2, brow[-c] * LOG2E);
+            const float sv = fmaf(__uint_as_float(sr[c]), a.sm_scale, brow[-c]);
+            sr[c] = __float_as_uint(sv);
+            mxv[c & 3] = fmaxf(mxv[c & 3], sv);
+          }
+        } else if (__all_sync(0xffffffffu, all_vis && cc >= TILE_KEYS - 1)) {
+          // every key visible at distance >= E - 1
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const float sv = fmaf(__uint_as_float(sr[c]), a.sm_scale, clampv);
             sr[c] = __float_as_uint(sv);
             mxv[c & 3] = fmaxf(mxv[c & 3], sv);
           }
         } else {
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
-            const int k = k0 + c;
-            const bool v = k >= kmin && k <= kmax && !((bad >> c) & 1ull);
-            const bool clamped = dmin + (TILE_KEYS - 1) - c >= a.E - 1;
-            const float bsv = (needs && !clamped) ? brow[-c] * LOG2E : clampv;
-            const float sv = v ? fmaf(__uint_as_float(sr[c]), a.scale_log2, bsv) : -INFINITY;
+            const float bsv = c <= cc ? clampv : brow[-c];
+            const float sv = ((vis >> c) & 1ull) ? fmaf(__uint_as_float(sr[c]), a.sm_scale, bsv) : -INFINITY;
             sr[c] = __float_as_uint(sv);
             mxv[c & 3] = fmaxf(mxv[c & 3], sv);
           }
@@ -559,33 +626,34 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         if (fresh) {
           m = m_new;
         } else {
-          const bool mine = m_new > m + RESCALE_LOG2;
+          const bool mine = m_new > m + RESCALE_NAT;
           if (__any_sync(0xffffffffu, mine)) {
             // this warpgroup's O must be stable: its previous P V product (tile g - 2) is done
             (void)wait_flag(&o_done[g & 1], (uint32_t)((g - 2) >> 1) & 1u, abort_flag, a.err);
             tc_fence_after();
-            const float f = mine ? fast_exp2(m - m_new) : 1.f;
+            const float f = mine ? fast_exp2((m - m_new) * LOG2E) : 1.f;
 #pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc2 = 0; cc2 < D / 32; ++cc2) {
               uint32_t ov[32];
-              tmem_ld32(tm_o + cc * 32, ov);
+              tmem_ld32(tm_o + cc2 * 32, ov);
               tmem_wait_ld();
 #pragma unroll
               for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * f);
-              tmem_st32(tm_o + cc * 32, ov);
+              tmem_st32(tm_o + cc2 * 32, ov);
             }
             tmem_wait_st();
             l *= f;
             if (mine) m = m_new;
           }
         }
-        const float mu = m == -INFINITY ? 0.f : m;
+        // p = 2^(s log2(e) - m log2(e)); masked keys (s = -inf) give exactly 0
+        const float mb = m == -INFINITY ? 0.f : m * LOG2E;
         uint32_t pk[32];
         float lsv[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float p0 = fast_exp2(__uint_as_float(sr[2 * c]) - mu);
-          const float p1 = fast_exp2(__uint_as_float(sr[2 * c + 1]) - mu);
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * c]), LOG2E, -mb));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * c + 1]), LOG2E, -mb));
           lsv[c & 3] += p0 + p1;
           pk[c] = pack_bf16(p0, p1);
         }
@@ -623,8 +691,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         const float M = fmaxf(m, o1.x);
         const float Mu = M == -INFINITY ? 0.f : M;
         const bool has0 = l > 0.f, has1 = o1.y > 0.f;   // a warpgroup without tiles holds stale O
-        const float f0 = has0 ? fast_exp2(m - Mu) : 0.f;
-        const float f1 = has1 ? fast_exp2(o1.x - Mu) : 0.f;
+        const float f0 = has0 ? fast_exp2((m - Mu) * LOG2E) : 0.f;
+        const float f1 = has1 ? fast_exp2((o1.x - Mu) * LOG2E) : 0.f;
         const float Lt = l * f0 + o1.y * f1;
         const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
         const float c0 = f0 * inv, c1 = f1 * inv;
