@@ -58,13 +58,13 @@ cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& a, int head_
 // TMA descriptors of one prefill call: K/V pools as for decode (min(P, 64)-row boxes) and
 // q viewed as [total_q rows, Hq*D] with 128-row boxes (rows past total_q read as zero).
 // bias: rel_logits viewed as [E, Hq, total_q] fp32 (innermost first) with boxes of
-// 100 buckets x 1 head x 8 tokens (only built when rows of rel are 16-byte aligned).
+// 84 buckets x 1 head x 16 tokens (only built when rows of rel are 16-byte aligned).
 struct PrefillMaps {
   CUtensorMap k, v, q, bias;
 };
 
-constexpr int BIAS_BOX_COLS = 100;  // buckets per bias box row
-constexpr int BIAS_BOX_ROWS = 8;    // tokens per bias box
+constexpr int BIAS_BOX_COLS = 84;   // buckets per bias box row
+constexpr int BIAS_BOX_ROWS = 16;   // tokens per bias box
 
 cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int head_dim,
                               cudaStream_t stream);

@@ -13,21 +13,20 @@
 //           and of 64-key K tiles (warp 0) and V tiles (warp 3) into separate rings (K is
 //           freed when S = Q K^T is done, V when O += P V is done; 128-byte swizzle);
 //           block-table entries are held 32 at a time in lanes and looked up by shuffle.
-//   warp 1  MMA: one lane issues S = Q K^T (M 128, N 64, fp32 in TMEM, double-buffered)
-//           and O[g % 2] += P V (P bf16 from TMEM, V from shared memory, fp32 O in TMEM).  Its
-//           lanes zero the V rows of keys no row of the item may see (edges of the
-//           window, the sequence end, unreadable pages) before P V reads them, so any
-//           bit pattern there is harmless.
-//   warp 2  bias: one 3-D TMA box (100 buckets x 8 tokens) per group of 8 rows, skewed
-//           so the row-per-thread reads are free of bank conflicts (4-byte cp.async when
-//           rows of rel are not 16-byte aligned)
-//           into a skewed fp32 ring that a row-per-thread read sees without bank
-//           conflicts; keys at distance >= E - 1 use the row's bucket E - 1 instead.
+//   warp 1  S issuer: S = Q K^T (M 128, N 64, fp32 in TMEM, double-buffered), issued by
+//           one elected lane of the converged warp.
+//   warp 2  bias: one 3-D TMA box (84 buckets x 16 tokens) per group of 16 rows that
+//           reads any bucket below E - 1, into a 3-slot ring shared by both softmax
+//           warpgroups in tile order (4-byte cp.async when rows of rel are not 16-byte
+//           aligned); keys at distance >= E - 1 use the row's bucket E - 1 instead.
 //   warps 4-11  softmax, two warpgroups taking alternate key tiles: thread r of a
 //           warpgroup owns row r (TMEM lane r): reads its 64 scores, adds bias, masks,
-//           keeps the running max/sum in base 2 and writes P (bf16) back to TMEM; each
-//           warpgroup accumulates into its own O, rescaled in TMEM only when a row's max
-//           grows by more than 2^8.  Epilogue: the two partial results are merged,
+//           keeps the running max/sum and writes P (bf16) back to TMEM; then the
+//           warpgroup's first warp issues O[wg] += P V (P from TMEM, V from shared
+//           memory, fp32 O in TMEM), after zeroing the V rows of keys no row of the item
+//           may see (edges of the window, the sequence end, unreadable pages), so any bit
+//           pattern there is harmless.  O is rescaled in TMEM only when a row's max grows
+//           by more than 2^8.  Epilogue: the two partial results are merged,
 //           O / l -> bf16 -> out.
 #include <algorithm>
 
@@ -40,15 +39,17 @@ namespace {
 
 constexpr int PT_ROWS = 128;
 constexpr int PT_THREADS = 384;
-constexpr int PT_BIAS_SLOTS = 2;
-// Bias slot: 16 groups of 8 rows (tokens); group g at float 800 g, row i of it at +100 i.
-// A group holds buckets [x_g, x_g + 100) of its 8 rows, x_g = 4*floor((dmin0 + 8g)/4)
-// - 8*(g mod 4), where dmin0 = pos0 - (k0 + 63) is row 0's smallest distance in the tile.
-// Row r = 8g + i then finds the bucket of key k0 + c at offset boff + 63 - c with
-// boff = (dmin0 mod 4) + i + 8*(g mod 4) <= 34, so 98 columns suffice, and a
-// row-per-thread read of one c touches 32 different banks.
+constexpr int PT_BIAS_SLOTS = 3;      // bias ring, shared by both warpgroups in tile order
+// Bias slot: 8 groups of 16 rows (tokens); group g at float 1344 g, row i of it at
+// +84 i.  A group holds buckets [x_g, x_g + 84) of its 16 rows, x_g = 4*floor((dmin0 +
+// 16g)/4), where dmin0 = pos0 - (k0 + 63) is row 0's smallest distance in the tile (x_g
+// is a multiple of 4: TMA wants 16-byte aligned starts).  Row r = 16g + i then finds
+// the bucket of key k0 + c at offset boff + 63 - c with boff = (dmin0 mod 4) + i <= 18,
+// so 82 columns suffice; a row-per-thread read of one c touches every bank at most
+// twice (the row pitch 84 + 1 is odd mod 32, so the 16 rows of a group hit 16 banks).
 constexpr int PT_BIAS_GROUP = BIAS_BOX_ROWS * BIAS_BOX_COLS;   // floats per group
-constexpr int PT_BIAS_SLOT_FLOATS = 16 * PT_BIAS_GROUP;
+constexpr int PT_BIAS_NGROUP = PT_ROWS / BIAS_BOX_ROWS;         // groups per tile
+constexpr int PT_BIAS_SLOT_FLOATS = PT_BIAS_NGROUP * PT_BIAS_GROUP;
 constexpr uint32_t TM_S = 0;     // S[2]: 64 fp32 columns each
 constexpr uint32_t TM_P = 128;   // P[2]: 32 columns (64 bf16) each
 constexpr uint32_t TM_O = 256;   // O[2]: D fp32 columns each (one per softmax warpgroup)
@@ -62,7 +63,7 @@ struct PtShape {
   static constexpr int Q_BYTES = CB * Q_SUB;
   static constexpr int KV_SUB = TILE_KEYS * 128;
   static constexpr int KV_TILE = CB * KV_SUB;   // one K or one V tile
-  static constexpr int NK = D == 128 ? 3 : 4;    // K ring: freed once S = Q K^T is done
+  static constexpr int NK = D == 128 ? 2 : 4;    // K ring: freed once S = Q K^T is done
   static constexpr int NV = D == 128 ? 2 : 4;    // V ring: freed once O += P V is done
   static constexpr int BIAS_SLOT = PT_BIAS_SLOT_FLOATS * 4;
 };
@@ -76,8 +77,8 @@ struct PtSmem {
   static constexpr size_t bias = vst + (size_t)S::NV * S::KV_TILE;
   static constexpr size_t bars = bias + (size_t)PT_BIAS_SLOTS * S::BIAS_SLOT;
   // q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2],
-  // s_empty[2], p_full[2], o_done[2], o_free, b_full[NB], b_empty[NB], ml_full, ml_free
-  static constexpr int NBAR = 2 + 2 * S::NK + 2 * S::NV + 2 + 2 + 2 + 2 + 1 + 2 * PT_BIAS_SLOTS + 2;
+  // s_empty[2], o_done[2], o_free, b_full[NB], b_empty[NB], ml_full, ml_free
+  static constexpr int NBAR = 2 + 2 * S::NK + 2 * S::NV + 2 + 2 + 2 + 1 + 2 * PT_BIAS_SLOTS + 2;
   static constexpr size_t vbad = bars + NBAR * 8;
   static constexpr size_t ml1 = vbad + S::NV * 8;          // float2 [128]
   static constexpr size_t misc = ml1 + PT_ROWS * 8;
@@ -132,7 +133,7 @@ __device__ int cta_tiles(const PrefillArgs& a, int total_items) {
 
 // First bucket held by bias group g of a tile (may be negative or past E: read as 0).
 __device__ __forceinline__ int bias_group_x(int dmin0, int g) {
-  return ((dmin0 + 8 * g) & ~3) - 8 * (g & 3);
+  return (dmin0 + BIAS_BOX_ROWS * g) & ~3;
 }
 
 // Visible keys of row position pr within tile k0 (kmin > kmax: none).
@@ -143,13 +144,29 @@ __device__ __forceinline__ void row_tile_keys(const PrefillArgs& a, const PItem&
   kmax = min(min(k0 + TILE_KEYS - 1, pr), it.k_hi);
 }
 
+// Does bias group gr (rows 16 gr .. 16 gr + 15 of the item) read any bucket below E - 1 in
+// tile k0?  The union of the group's visible ranges is [window start of its first row,
+// its last row].
+__device__ __forceinline__ bool bias_group_needed(const PrefillArgs& a, const PItem& it, int k0, int gr) {
+  const int r0 = BIAS_BOX_ROWS * gr;
+  if (r0 >= it.rows) return false;
+  const int p_lo = it.pos0 + r0, p_hi = it.pos0 + min(r0 + BIAS_BOX_ROWS - 1, it.rows - 1);
+  const int lo_lo = a.W > 0 ? max(0, p_lo - a.W + 1) : 0;
+  const bool any_key = p_hi >= k0 && lo_lo <= min(k0 + TILE_KEYS - 1, it.k_hi);
+  const bool all_clamped = p_lo - (k0 + TILE_KEYS - 1) >= a.E - 1;
+  return any_key && !all_clamped;
+}
+
 // Every visible (row, key) pair of tile k0 lies at distance >= E - 1 (row 0 has the
 // smallest position, key k0 + 63 the largest index): the whole tile reads bucket E - 1.
 __device__ __forceinline__ bool tile_needs_bias(int pos0, int k0, int E) {
   return pos0 - (k0 + TILE_KEYS - 1) < E - 1;
 }
 
+// A completed phase returns at once; otherwise give up at once if another warp of the
+// CTA has timed out, else wait (bounded) and on a timeout record it and tell the others.
 __device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
   if (*abort_flag) return false;
   if (mbar_wait_bounded(bar, parity)) return true;
   record_error(err, INK_DEVERR_WAIT_TIMEOUT);
@@ -180,8 +197,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   uint64_t* v_empty = v_full + NV;
   uint64_t* s_full = v_empty + NV;
   uint64_t* s_empty = s_full + 2;
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* o_done = p_full + 2;
+  uint64_t* o_done = s_empty + 2;
   uint64_t* o_free = o_done + 2;
   uint64_t* b_full = o_free + 1;
   uint64_t* b_empty = b_full + PT_BIAS_SLOTS;
@@ -210,7 +226,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
       mbar_init(&s_empty[x], 4);
-      mbar_init(&p_full[x], 4);
       mbar_init(&o_done[x], 1);
     }
     mbar_init(o_free, 4);
@@ -287,54 +302,48 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         const bool load = want && !bad_seg;
         const uint32_t lmask = __ballot_sync(0xffffffffu, load);
         const uint32_t bmask = __ballot_sync(0xffffffffu, bad_seg);
-        if (lane == 0) {
-          if (bmask && is_k) record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
-          if (!is_k) {
+        if (bmask) {  // error path: record it, and tell the MMA warp which V rows to zero
+          if (lane == 0) {
+            if (is_k) record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
             uint64_t bad = 0;
 #pragma unroll 1
             for (uint32_t mm = bmask; mm; mm &= mm - 1)
               bad |= seg == 64 ? ~0ull : (((1ull << seg) - 1) << ((__ffs(mm) - 1) * seg));
-            vbad[st] = bad;
+            if (!is_k) vbad[st] = bad;
           }
-          mbar_arrive_expect_tx(&full[st], (uint32_t)__popc(lmask) * (uint32_t)(seg * D * 2));
+        } else if (!is_k && lane == 0) {
+          vbad[st] = 0;
         }
         __syncwarp();
-        if (load) {
-          const int row = ((page * a.Hkv + it.kvh) << a.log2_page) + (ks & (P - 1));
-          uint8_t* dst = ring + (size_t)st * S::KV_TILE + lane * seg * 128;
+        mbar_arrive_expect_tx_warp(&full[st], (uint32_t)__popc(lmask) * (uint32_t)(seg * D * 2));
+        const int my_row = ((page * a.Hkv + it.kvh) << a.log2_page) + (ks & (P - 1));
+#pragma unroll 1
+        for (uint32_t mm = lmask; mm; mm &= mm - 1) {
+          const int sg = __ffs(mm) - 1;
+          const int row = __shfl_sync(0xffffffffu, my_row, sg);
+          uint8_t* dst = ring + (size_t)st * S::KV_TILE + sg * seg * 128;
 #pragma unroll
-          for (int cb = 0; cb < S::CB; ++cb) tma_load_2d(dst + cb * S::KV_SUB, tm, cb * 64, row, &full[st]);
+          for (int cb = 0; cb < S::CB; ++cb) tma_load_2d_warp(dst + cb * S::KV_SUB, tm, cb * 64, row, &full[st]);
         }
-        __syncwarp();
       }
       ++icount;
     }
   } else if (warp == 1) {
-    // -------------------------------------------------------------- MMA issuer
-    // Static order over this CTA's tiles g (all items, in sequence): step g issues
-    // S(g) = Q K(g)^T, then O[(g-2) % 2] += P(g-2) V(g-2).  S(g) reuses the S buffer
-    // of tile g - 2, which its warpgroup empties as soon as it starts that tile, so each
-    // warpgroup finds its next S already computed when it finishes a P.  Every wait of
-    // step g depends only on earlier steps.  At the first tile of an item the product
-    // P V of step g goes first: S(g) waits for the item's query tile, which is loaded
-    // only once every S of the previous item is done.
-    const int total = cta_tiles(a, total_items);
-    PItem its{}, itp{};
-    int is = blockIdx.x - (int)gridDim.x, ip = is;
-    int js = 0, jp = 0, ics = -1, icp = -1;   // tile within item, items started
-    int ns = 0, np = 0;                        // tiles of the current S / PV item
-    auto issue_s = [&](int g) {
-      if (js == ns) {  // next item with tiles
-        do { is += gridDim.x; } while (!(get_item(a, is, its) && its.ntile > 0));
-        js = 0;
-        ns = its.ntile;
-        ++ics;
-        (void)wait_flag(q_full, (uint32_t)ics & 1u, abort_flag, a.err);
-      }
-      const int ks_ = g % NK;
-      (void)wait_flag(&k_full[ks_], (uint32_t)(g / NK) & 1u, abort_flag, a.err);
-      if (g >= 2) (void)wait_flag(&s_empty[g & 1], (uint32_t)((g >> 1) - 1) & 1u, abort_flag, a.err);
-      if (lane == 0) {
+    // -------------------------------------------------------------- S issuer
+    // S(g) = Q K(g)^T into S buffer g % 2 as soon as K(g) is in and the warpgroup that
+    // owns tile g - 2 has read S(g - 2) out of TMEM, which it does first thing, so each
+    // warpgroup finds its next S computed when it finishes a P.  Q is freed after the
+    // item's last S.
+    int icount = 0, g = 0;
+    for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
+      PItem it;
+      if (!get_item(a, i, it) || it.ntile == 0) continue;
+      (void)wait_flag(q_full, (uint32_t)icount & 1u, abort_flag, a.err);
+#pragma unroll 1
+      for (int j = 0; j < it.ntile; ++j, ++g) {
+        const int ks_ = g % NK;
+        (void)wait_flag(&k_full[ks_], (uint32_t)(g / NK) & 1u, abort_flag, a.err);
+        if (g >= 2) (void)wait_flag(&s_empty[g & 1], (uint32_t)((g >> 1) - 1) & 1u, abort_flag, a.err);
         tc_fence_after();
         const uint32_t qbase = smem_u32(smem + L_::q);
         const uint32_t kbase = smem_u32(smem + L_::kst + (size_t)ks_ * S::KV_TILE);
@@ -342,90 +351,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = umma_desc_sw128(qbase + (kk >> 2) * S::Q_SUB + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = umma_desc_sw128(kbase + (kk >> 2) * S::KV_SUB + (kk & 3) * 32, 16, 1024);
-          umma_ss(tmem + TM_S + (g & 1) * 64, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+          umma_ss_warp(tmem + TM_S + (g & 1) * 64, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[g & 1]);
-        umma_commit(&k_empty[ks_]);
-        if (js == ns - 1) umma_commit(q_empty);   // the item's last S: Q may be replaced
-      }
-      __syncwarp();
-      ++js;
-    };
-    // O[gg % 2] += P(gg) V(gg); the two warpgroups' first tiles of an item (jp 0 and 1)
-    // start their accumulators from zero
-    auto issue_pv = [&](int gg) {
-      if (jp == np) {
-        do { ip += gridDim.x; } while (!(get_item(a, ip, itp) && itp.ntile > 0));
-        jp = 0;
-        np = itp.ntile;
-        ++icp;
-      }
-      const int vs = gg % NV;
-      bool ok = wait_flag(&v_full[vs], (uint32_t)(gg / NV) & 1u, abort_flag, a.err);
-      // zero the V rows of keys that no row of this item may read
-      const int k0 = (itp.kt0 + jp) * TILE_KEYS;
-      const uint64_t bad = ok ? vbad[vs] : ~0ull;
-      uint8_t* vt = smem + L_::vst + (size_t)vs * S::KV_TILE;
-      if (k0 < itp.lo_min || k0 + TILE_KEYS - 1 > itp.k_hi || bad) {
-#pragma unroll 1
-        for (int rr = lane; rr < TILE_KEYS; rr += 32) {
-          const int k = k0 + rr;
-          if (k < itp.lo_min || k > itp.k_hi || ((bad >> rr) & 1ull)) {
-#pragma unroll 1
-            for (int cb = 0; cb < S::CB; ++cb) {
-              uint4* row = reinterpret_cast<uint4*>(vt + cb * S::KV_SUB + rr * 128);
-#pragma unroll
-              for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
-            }
-          }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        umma_commit_warp(&s_full[g & 1]);
+        umma_commit_warp(&k_empty[ks_]);
+        if (j == it.ntile - 1) umma_commit_warp(q_empty);   // the item's last S: Q may be replaced
         __syncwarp();
       }
-      ok = wait_flag(&p_full[gg & 1], (uint32_t)(gg >> 1) & 1u, abort_flag, a.err) && ok;
-      // the previous item's epilogue has read both O accumulators
-      if (ok && jp == 0 && icp > 0) ok = wait_flag(o_free, (uint32_t)(icp - 1) & 1u, abort_flag, a.err);
-      if (lane == 0) {
-        tc_fence_after();
-        const uint32_t vbase = smem_u32(vt);
-        if (ok) {
-#pragma unroll
-          for (int ks = 0; ks < TILE_KEYS / 16; ++ks) {
-            const uint64_t bdesc = umma_desc_sw128(vbase + ks * 16 * 128, S::KV_SUB, 1024);
-            umma_ts(tmem + TM_O + (uint32_t)((gg & 1) * D), tmem + TM_P + (gg & 1) * 32 + ks * 8, bdesc,
-                    IDESC_PV, (jp < 2 && ks == 0) ? 0u : 1u);
-          }
-        }
-        umma_commit(&v_empty[vs]);
-        umma_commit(&o_done[gg & 1]);
-      }
-      __syncwarp();
-      ++jp;
-    };
-#pragma unroll 1
-    for (int g = 0; g < total + 2 && !*abort_flag; ++g) {
-      const bool do_s = g < total, do_pv = g >= 2;
-      const bool pv_first = do_pv && do_s && js == ns;   // S(g) opens a new item
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        if ((half == 0) == pv_first) {
-          if (do_pv) issue_pv(g - 2);
-        } else if (do_s) {
-          issue_s(g);
-        }
-      }
+      ++icount;
     }
   } else if (warp == 2) {
     // -------------------------------------------------------------- bias loader
-    // Fast path (rows of rel 16-byte aligned): one lane issues one 3-D TMA box per group
-    // of 8 tokens (100 buckets x 8 rows, skewed start so the softmax reads are free of
-    // bank conflicts); out-of-range buckets arrive as zeros and are never used.
-    // Otherwise the warp copies the visible buckets with 4-byte cp.async into the same
-    // layout.  Buckets at distance >= E - 1 are never read: the softmax uses the row's
-    // bucket E - 1 for those keys.
-    // Slot s serves the tiles of softmax warpgroup s (tiles g with g % 2 == s), so each
-    // slot has one consumer that takes its tiles in order.
-    int bcnt[PT_BIAS_SLOTS] = {0, 0};
+    // Fast path (rows of rel 16-byte aligned): one 3-D TMA box per group of 16 tokens
+    // (84 buckets x 16 rows, laid out so the softmax reads see at most 2-way bank
+    // conflicts); out-of-range buckets arrive as zeros and are never used.  Otherwise the
+    // warp copies the visible buckets with 4-byte cp.async into the same layout.
+    // Buckets at distance >= E - 1 are never read: the softmax uses the row's bucket
+    // E - 1 for those keys.
+    // The n-th tile that reads bias goes to slot n % 3 whichever warpgroup owns it.  A
+    // wait on slot s for its use u cannot see the phase of use u - 2: the loader fills
+    // use u - 1 only after use u - 2 was consumed, and a warpgroup at tile g has its
+    // S(g) only after the other warpgroup finished tile g - 3 (the MMA issue order), so
+    // no bias tile three or more slots back is still unconsumed.
+    int bidx = 0;   // bias tiles loaded so far; tile n goes to slot n % PT_BIAS_SLOTS
     int g = 0;
     if (lane == 0) prefetch_tensormap(&tmB);
     for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
@@ -434,31 +382,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       for (int j = 0; j < it.ntile; ++j, ++g) {
         const int k0 = (it.kt0 + j) * TILE_KEYS;
         if (!tile_needs_bias(it.pos0, k0, a.E)) continue;
-        const int slot = g & 1;
-        const int use = bcnt[slot]++;
+        const int slot = bidx % PT_BIAS_SLOTS, use = bidx / PT_BIAS_SLOTS;
+        ++bidx;
         if (use >= 1) (void)wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err);
         float* sb = reinterpret_cast<float*>(smem + L_::bias + (size_t)slot * S::BIAS_SLOT);
         const int dmin0 = it.pos0 - (k0 + TILE_KEYS - 1);
         if (a.bias_bulk) {
-          if (lane == 0) {
-            uint32_t need = 0;
+          // lane gr < PT_BIAS_NGROUP decides whether group gr of this tile is read; the
+          // warp loads those
+          const uint32_t nm =
+              __ballot_sync(0xffffffffu, lane < PT_BIAS_NGROUP && bias_group_needed(a, it, k0, lane));
+          mbar_arrive_expect_tx_warp(&b_full[slot], (uint32_t)__popc(nm) * (uint32_t)(PT_BIAS_GROUP * 4));
 #pragma unroll 1
-            for (int gr = 0; gr < 16; ++gr) {
-              const int r0 = 8 * gr;
-              if (r0 >= it.rows) break;
-              const int p_lo = it.pos0 + r0, p_hi = it.pos0 + min(r0 + 7, it.rows - 1);
-              // union of the group's visible ranges is [window start of p_lo, p_hi]
-              const int lo_lo = a.W > 0 ? max(0, p_lo - a.W + 1) : 0;
-              const bool any_key = p_hi >= k0 && lo_lo <= min(k0 + TILE_KEYS - 1, it.k_hi);
-              const bool all_clamped = p_lo - (k0 + TILE_KEYS - 1) >= a.E - 1;
-              if (any_key && !all_clamped) need |= 1u << gr;
-            }
-            mbar_arrive_expect_tx(&b_full[slot], (uint32_t)__popc(need) * (uint32_t)(PT_BIAS_GROUP * 4));
-#pragma unroll 1
-            for (int gr = 0; gr < 16; ++gr)
-              if ((need >> gr) & 1u)
-                tma_load_3d(sb + gr * PT_BIAS_GROUP, &tmB, bias_group_x(dmin0, gr), it.h, it.t0 + 8 * gr,
-                            &b_full[slot]);
+          for (uint32_t mm = nm; mm; mm &= mm - 1) {
+            const int gr = __ffs(mm) - 1;
+            tma_load_3d_warp(sb + gr * PT_BIAS_GROUP, &tmB, bias_group_x(dmin0, gr), it.h, it.t0 + BIAS_BOX_ROWS * gr,
+                             &b_full[slot]);
           }
         } else {
 #pragma unroll 1
@@ -467,7 +406,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             int kmin, kmax;
             row_tile_keys(a, it, pr, k0, kmin, kmax);
             const float* srcr = a.rel + ((size_t)(it.t0 + r) * a.Hq + it.h) * a.E;
-            const int gr = r >> 3, ii = r & 7;
+            const int gr = r / BIAS_BOX_ROWS, ii = r % BIAS_BOX_ROWS;
             const int xg = bias_group_x(dmin0, gr);
             // bucket d sits at group_base + ii*100 + (d - x_g); visible keys give d >= x_g
             const uint32_t rb = smem_u32(sb + gr * PT_BIAS_GROUP + ii * BIAS_BOX_COLS);
@@ -496,7 +435,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const uint32_t tlane = tmem + ((uint32_t)(sw * 32) << 16);
     const uint32_t tm_o = tlane + TM_O + (uint32_t)(wg * D);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-    int icount = 0, g = 0, buse = 0;  // buse: bias tiles this warpgroup has consumed
+    // bidx counts the bias tiles of both warpgroups, in tile order, as the loader does
+    int icount = 0, g = 0, bidx = 0;
     for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
       PItem it;
       if (!get_item(a, i, it)) continue;
@@ -549,11 +489,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       // running max (natural units) and sum of this warpgroup's tiles
       float m = -INFINITY, l = 0.f;
       bool fresh = true;  // no tile of this item seen yet by this warpgroup
-      const float* bslot = reinterpret_cast<const float*>(smem + L_::bias + (size_t)wg * S::BIAS_SLOT);
       for (int j = 0; j < it.ntile; ++j, ++g) {
         const int k0 = (it.kt0 + j) * TILE_KEYS;
         const bool needs = tile_needs_bias(it.pos0, k0, a.E);
+        const int bslot_i = bidx % PT_BIAS_SLOTS, buse = bidx / PT_BIAS_SLOTS;
+        if (needs) ++bidx;
         if ((g & 1) != wg) continue;  // the other warpgroup's tile
+        const float* bslot = reinterpret_cast<const float*>(smem + L_::bias + (size_t)bslot_i * S::BIAS_SLOT);
         uint64_t bad = item_bad ? tile_bad(k0) : 0ull;
         bool ok = wait_flag(&s_full[g & 1], (uint32_t)(g >> 1) & 1u, abort_flag, a.err);
         tc_fence_after();
@@ -582,9 +524,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         // slot when the tile reads no bucket from it
         const float* brow = bslot + (TILE_KEYS - 1);
         if (needs) {
-          (void)wait_flag(&b_full[wg], (uint32_t)buse & 1u, abort_flag, a.err);
-          const int gr = r >> 3;
-          brow = bslot + gr * PT_BIAS_GROUP + (r & 7) * BIAS_BOX_COLS + (dmin - bias_group_x(dmin - r, gr)) +
+          (void)wait_flag(&b_full[bslot_i], (uint32_t)buse & 1u, abort_flag, a.err);
+          const int gr = r / BIAS_BOX_ROWS;
+          brow = bslot + gr * PT_BIAS_GROUP + (r % BIAS_BOX_ROWS) * BIAS_BOX_COLS + (dmin - bias_group_x(dmin - r, gr)) +
                  (TILE_KEYS - 1);
         }
         float mxv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -619,8 +561,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
           // every bias value this thread read is consumed (mx depends on all of them)
           asm volatile("" ::"f"(mx) : "memory");
           __syncwarp();
-          if (lane == 0) mbar_arrive(&b_empty[wg]);
-          ++buse;
+          if (lane == 0) mbar_arrive(&b_empty[bslot_i]);
         }
         const float m_new = fmaxf(m, mx);
         if (fresh) {
@@ -663,8 +604,48 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         tmem_st32(tlane + TM_P + (g & 1) * 32, pk);
         tmem_wait_st();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[g & 1]);
+        named_barrier_sync(1 + wg, 128);   // all 128 rows of P(g) are in TMEM
+        if (sw == 0) {
+          // O[wg] += P(g) V(g), issued by this warpgroup's first warp
+          const int vs = g % NV;
+          bool pv_ok = wait_flag(&v_full[vs], (uint32_t)(g / NV) & 1u, abort_flag, a.err);
+          // warpgroup 1's first product of an item overwrites O[1], which the previous
+          // item's epilogue (warpgroup 0) reads: wait until it has
+          if (fresh && wg == 1 && icount > 0) pv_ok = wait_flag(o_free, (uint32_t)(icount - 1) & 1u, abort_flag, a.err) && pv_ok;
+          // zero the V rows of keys that no row of this item may read
+          const uint64_t vb = pv_ok ? vbad[vs] : ~0ull;
+          uint8_t* vt = smem + L_::vst + (size_t)vs * S::KV_TILE;
+          if (k0 < it.lo_min || k0 + TILE_KEYS - 1 > it.k_hi || vb) {
+#pragma unroll 1
+            for (int rr = lane; rr < TILE_KEYS; rr += 32) {
+              const int k = k0 + rr;
+              if (k < it.lo_min || k > it.k_hi || ((vb >> rr) & 1ull)) {
+#pragma unroll 1
+                for (int cb = 0; cb < S::CB; ++cb) {
+                  uint4* row = reinterpret_cast<uint4*>(vt + cb * S::KV_SUB + rr * 128);
+#pragma unroll
+                  for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
+              }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+          }
+          pv_ok = __all_sync(0xffffffffu, pv_ok);
+          tc_fence_after();
+          if (pv_ok) {
+            const uint32_t vbase = smem_u32(vt);
+#pragma unroll
+            for (int ks = 0; ks < TILE_KEYS / 16; ++ks) {
+              const uint64_t bdesc = umma_desc_sw128(vbase + ks * 16 * 128, S::KV_SUB, 1024);
+              umma_ts_warp(tmem + TM_O + (uint32_t)(wg * D), tmem + TM_P + (g & 1) * 32 + ks * 8, bdesc, IDESC_PV,
+                           (fresh && ks == 0) ? 0u : 1u);
+            }
+          }
+          umma_commit_warp(&v_empty[vs]);
+          umma_commit_warp(&o_done[g & 1]);
+          __syncwarp();
+        }
         fresh = false;
       }
       // ---- item epilogue
