@@ -16,9 +16,9 @@
 //   warp 1  S issuer: S = Q K^T (M 128, N 64, fp32 in TMEM, double-buffered), issued by
 //           one elected lane of the converged warp.
 //   warp 2  bias: one 3-D TMA box (84 buckets x 16 tokens) per group of 16 rows that
-//           reads any bucket below E - 1, into a 3-slot ring shared by both softmax
-//           warpgroups in tile order (4-byte cp.async when rows of rel are not 16-byte
-//           aligned); keys at distance >= E - 1 use the row's bucket E - 1 instead.
+//           reads any bucket below E - 1, into the slot of the softmax warpgroup that
+//           owns the tile (4-byte cp.async when rows of rel are not 16-byte aligned);
+//           keys at distance >= E - 1 use the row's bucket E - 1 instead.
 //   warps 4-11  softmax, two warpgroups taking alternate key tiles: thread r of a
 //           warpgroup owns row r (TMEM lane r): reads its 64 scores, adds bias, masks,
 //           keeps the running max/sum and writes P (bf16) back to TMEM; then the
@@ -39,7 +39,7 @@ namespace {
 
 constexpr int PT_ROWS = 128;
 constexpr int PT_THREADS = 384;
-constexpr int PT_BIAS_SLOTS = 3;      // bias ring, shared by both warpgroups in tile order
+constexpr int PT_BIAS_SLOTS = 2;      // one bias slot per softmax warpgroup
 // Bias slot: 8 groups of 16 rows (tokens); group g at float 1344 g, row i of it at
 // +84 i.  A group holds buckets [x_g, x_g + 84) of its 16 rows, x_g = 4*floor((dmin0 +
 // 16g)/4), where dmin0 = pos0 - (k0 + 63) is row 0's smallest distance in the tile (x_g
@@ -63,8 +63,8 @@ struct PtShape {
   static constexpr int Q_BYTES = CB * Q_SUB;
   static constexpr int KV_SUB = TILE_KEYS * 128;
   static constexpr int KV_TILE = CB * KV_SUB;   // one K or one V tile
-  static constexpr int NK = D == 128 ? 2 : 4;    // K ring: freed once S = Q K^T is done
-  static constexpr int NV = D == 128 ? 2 : 4;    // V ring: freed once O += P V is done
+  static constexpr int NK = D == 128 ? 3 : 4;    // K ring: freed once S = Q K^T is done
+  static constexpr int NV = D == 128 ? 2 : 4;    // V ring (even: slot g % NV serves warpgroup g % 2)
   static constexpr int BIAS_SLOT = PT_BIAS_SLOT_FLOATS * 4;
 };
 
@@ -368,12 +368,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     // warp copies the visible buckets with 4-byte cp.async into the same layout.
     // Buckets at distance >= E - 1 are never read: the softmax uses the row's bucket
     // E - 1 for those keys.
-    // The n-th tile that reads bias goes to slot n % 3 whichever warpgroup owns it.  A
-    // wait on slot s for its use u cannot see the phase of use u - 2: the loader fills
-    // use u - 1 only after use u - 2 was consumed, and a warpgroup at tile g has its
-    // S(g) only after the other warpgroup finished tile g - 3 (the MMA issue order), so
-    // no bias tile three or more slots back is still unconsumed.
-    int bidx = 0;   // bias tiles loaded so far; tile n goes to slot n % PT_BIAS_SLOTS
+    // Slot s serves the tiles of softmax warpgroup s (tiles g with g % 2 == s): each
+    // slot has one consumer that takes its fills in order, so a parity wait never sees
+    // a phase two behind.  (V slots follow the same rule: NV is even.)
+    int bcnt[PT_BIAS_SLOTS] = {0, 0};
     int g = 0;
     if (lane == 0) prefetch_tensormap(&tmB);
     for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
@@ -382,8 +380,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       for (int j = 0; j < it.ntile; ++j, ++g) {
         const int k0 = (it.kt0 + j) * TILE_KEYS;
         if (!tile_needs_bias(it.pos0, k0, a.E)) continue;
-        const int slot = bidx % PT_BIAS_SLOTS, use = bidx / PT_BIAS_SLOTS;
-        ++bidx;
+        const int slot = g & 1;
+        const int use = bcnt[slot]++;
         if (use >= 1) (void)wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err);
         float* sb = reinterpret_cast<float*>(smem + L_::bias + (size_t)slot * S::BIAS_SLOT);
         const int dmin0 = it.pos0 - (k0 + TILE_KEYS - 1);
@@ -435,8 +433,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const uint32_t tlane = tmem + ((uint32_t)(sw * 32) << 16);
     const uint32_t tm_o = tlane + TM_O + (uint32_t)(wg * D);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-    // bidx counts the bias tiles of both warpgroups, in tile order, as the loader does
-    int icount = 0, g = 0, bidx = 0;
+    int icount = 0, g = 0, buse = 0;  // buse: bias tiles this warpgroup has consumed
     for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
       PItem it;
       if (!get_item(a, i, it)) continue;
@@ -492,10 +489,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       for (int j = 0; j < it.ntile; ++j, ++g) {
         const int k0 = (it.kt0 + j) * TILE_KEYS;
         const bool needs = tile_needs_bias(it.pos0, k0, a.E);
-        const int bslot_i = bidx % PT_BIAS_SLOTS, buse = bidx / PT_BIAS_SLOTS;
-        if (needs) ++bidx;
         if ((g & 1) != wg) continue;  // the other warpgroup's tile
-        const float* bslot = reinterpret_cast<const float*>(smem + L_::bias + (size_t)bslot_i * S::BIAS_SLOT);
+        const float* bslot = reinterpret_cast<const float*>(smem + L_::bias + (size_t)wg * S::BIAS_SLOT);
         uint64_t bad = item_bad ? tile_bad(k0) : 0ull;
         bool ok = wait_flag(&s_full[g & 1], (uint32_t)(g >> 1) & 1u, abort_flag, a.err);
         tc_fence_after();
@@ -524,7 +519,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         // slot when the tile reads no bucket from it
         const float* brow = bslot + (TILE_KEYS - 1);
         if (needs) {
-          (void)wait_flag(&b_full[bslot_i], (uint32_t)buse & 1u, abort_flag, a.err);
+          (void)wait_flag(&b_full[wg], (uint32_t)buse & 1u, abort_flag, a.err);
           const int gr = r / BIAS_BOX_ROWS;
           brow = bslot + gr * PT_BIAS_GROUP + (r % BIAS_BOX_ROWS) * BIAS_BOX_COLS + (dmin - bias_group_x(dmin - r, gr)) +
                  (TILE_KEYS - 1);
@@ -561,7 +556,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
           // every bias value this thread read is consumed (mx depends on all of them)
           asm volatile("" ::"f"(mx) : "memory");
           __syncwarp();
-          if (lane == 0) mbar_arrive(&b_empty[bslot_i]);
+          if (lane == 0) mbar_arrive(&b_empty[wg]);
+          ++buse;
         }
         const float m_new = fmaxf(m, mx);
         if (fresh) {
@@ -607,7 +603,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         named_barrier_sync(1 + wg, 128);   // all 128 rows of P(g) are in TMEM
         if (sw == 0) {
           // O[wg] += P(g) V(g), issued by this warpgroup's first warp
-          const int vs = g % NV;
+          const int vs = g % NV;   // NV is even: this warpgroup's own V slots
           bool pv_ok = wait_flag(&v_full[vs], (uint32_t)(g / NV) & 1u, abort_flag, a.err);
           // warpgroup 1's first product of an item overwrites O[1], which the previous
           // item's epilogue (warpgroup 0) reads: wait until it has
@@ -731,6 +727,7 @@ template <int D>
 cudaError_t launch_prefill_tc_t(const PrefillMaps& m, const PrefillArgs& a, cudaStream_t stream) {
   constexpr size_t smem = PtSmem<D>::alloc;
   static_assert(smem <= 227 * 1024, "shared memory budget");
+  static_assert(PtShape<D>::NV % 2 == 0, "each V slot must serve one softmax warpgroup");
   cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long items = (long long)a.num_q_tiles * a.B * a.Hq;
