@@ -129,6 +129,39 @@ bool make_rows_map(CUtensorMap* map, const void* base, uint64_t rows, int cols, 
   return r == CUDA_SUCCESS;
 }
 
+// The same bf16 rows as a 3-D tensor {64 columns, rows, column blocks} (row pitch
+// `pitch` elements, blocks 128 bytes apart): one box of box_rows rows x `blocks` column
+// blocks lands in shared memory as the 128-byte-swizzled sub-tiles [block][row][64] that
+// separate 2-D boxes would give, block stride box_rows * 128 bytes.
+bool make_rows_map3(CUtensorMap* map, const void* base, uint64_t rows, uint64_t pitch, int blocks, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(pitch / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)pitch * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)blocks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// A K or V pool of `rows` rows (a multiple of 16) as a 4-D tensor {64 columns, 16 rows,
+// column blocks, 16-row groups}: one box of `groups` groups lands in shared memory as
+// [group][block][16 rows][64], 2 KB blocks with the 128-byte swizzle.
+bool make_group_map(CUtensorMap* map, const void* base, uint64_t rows, int D, int groups) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {64, 16, (cuuint64_t)(D / 64), (cuuint64_t)(rows / 16)};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, 128, (cuuint64_t)D * 2 * 16};
+  cuuint32_t box[4] = {64, 16, (cuuint32_t)(D / 64), (cuuint32_t)groups};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 uint64_t pool_rows(const ink_attn_params_t* p) {
   return (uint64_t)p->num_pages * p->num_kv_heads * p->page_size;
 }
@@ -224,12 +257,22 @@ ink_status_t inkling_attn_decode(const ink_attn_params_t* params, const void* q,
   if (workspace_bytes < lay.total) return INK_ERR_WORKSPACE;
   if (params->num_seqs == 0) return INK_OK;
   ink::DecodeMaps maps;
-  if (!make_pool_map(&maps.k, k_cache, params, ink::TILE_KEYS) ||
-      !make_pool_map(&maps.v, v_cache, params, ink::TILE_KEYS) ||
-      !make_pool_map(&maps.k_seg, k_cache, params, 16) ||
+  const int cblocks = params->head_dim / 64;
+  if (!make_pool_map(&maps.k_seg, k_cache, params, 16) ||
       !make_pool_map(&maps.v_seg, v_cache, params, 16) ||
-      !make_rows_map(&maps.q, q, (uint64_t)params->num_seqs * params->num_q_heads,
-                     params->head_dim, 16))
+      !make_rows_map3(&maps.q3, q, (uint64_t)params->num_seqs * params->num_q_heads, params->head_dim, cblocks, 16))
+    return INK_ERR_CUDA;
+  std::memset(&maps.k_tile, 0, sizeof maps.k_tile);
+  std::memset(&maps.v_tile, 0, sizeof maps.v_tile);
+  std::memset(&maps.k_grp, 0, sizeof maps.k_grp);
+  std::memset(&maps.v_grp, 0, sizeof maps.v_grp);
+  if (params->page_size >= 16 &&
+      (!make_group_map(&maps.k_grp, k_cache, pool_rows(params), params->head_dim, 1) ||
+       !make_group_map(&maps.v_grp, v_cache, pool_rows(params), params->head_dim, 1)))
+    return INK_ERR_CUDA;
+  if (params->page_size >= ink::TILE_KEYS &&
+      (!make_group_map(&maps.k_tile, k_cache, pool_rows(params), params->head_dim, ink::TILE_KEYS / 16) ||
+       !make_group_map(&maps.v_tile, v_cache, pool_rows(params), params->head_dim, ink::TILE_KEYS / 16)))
     return INK_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodeArgs a;
@@ -282,9 +325,16 @@ ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q
   const int num_q_tiles = (max_q_len + 63) / 64;
   if (num_q_tiles > 65535 || params->num_seqs > 65535) return INK_ERR_TOO_LARGE;
   ink::PrefillMaps maps;
+  const int cblocks = params->head_dim / 64;
+  std::memset(&maps.k3, 0, sizeof maps.k3);
+  std::memset(&maps.v3, 0, sizeof maps.v3);
+  if (params->page_size >= ink::TILE_KEYS &&
+      (!make_rows_map3(&maps.k3, k_cache, pool_rows(params), params->head_dim, cblocks, ink::TILE_KEYS) ||
+       !make_rows_map3(&maps.v3, v_cache, pool_rows(params), params->head_dim, cblocks, ink::TILE_KEYS)))
+    return INK_ERR_CUDA;
   if (!make_pool_map(&maps.k, k_cache, params, ink::TILE_KEYS) ||
       !make_pool_map(&maps.v, v_cache, params, ink::TILE_KEYS) ||
-      !make_rows_map(&maps.q, q, (uint64_t)total_q, params->num_q_heads * params->head_dim, 128))
+      !make_rows_map3(&maps.q3, q, (uint64_t)total_q, (uint64_t)params->num_q_heads * params->head_dim, cblocks, 128))
     return INK_ERR_CUDA;
   PrefillArgs a;
   a.q = q;

@@ -103,6 +103,16 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int c
                : "memory");
 }
 
+// 4-D tiled bulk tensor load global -> shared (innermost coordinate c0 as above).
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Warp-collective forms of the copies above: every lane of a converged warp executes
 // them with warp-uniform operands and one elected lane issues (no per-lane serialisation).
 __device__ __forceinline__ void tma_load_2d_warp(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {

@@ -51,8 +51,11 @@ constexpr int PTAB = 576;       // staged block-table entries per unit (>= 64 ti
 template <int D>
 struct DecShape {
   static constexpr int COL_BLOCKS = D / 64;             // 128-byte column blocks
-  static constexpr int SUB_BYTES = TILE_KEYS * 128;     // one column block of a 64-key tile
-  static constexpr int TILE_BYTES = COL_BLOCKS * SUB_BYTES;
+  // K and V tiles are staged group-major: [16-key group][column block][16 rows x 128 B],
+  // 2 KB blocks with the 128-byte swizzle; consumer warp w reads group w.
+  static constexpr int BLOCK_BYTES = 16 * 128;
+  static constexpr int GROUP_BYTES = COL_BLOCKS * BLOCK_BYTES;
+  static constexpr int TILE_BYTES = (TILE_KEYS / 16) * GROUP_BYTES;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // K tile + V tile
   static constexpr int QSUB_BYTES = QROWS * 128;        // one column block of the query rows
   static constexpr int QSLOT_BYTES = COL_BLOCKS * QSUB_BYTES;
@@ -131,34 +134,6 @@ __device__ __forceinline__ void unit_page_span(const DecodeArgs& a, const Unit& 
 // that hold at least one visible key.  rows[sg] is the pool row of segment sg, or -1
 // (nothing to fetch), or -2 (unreadable page: its keys are masked).  Page ids come from
 // the unit's slice of the block table, staged in shared memory (ptab[j] = entry first+j).
-struct TilePlan {
-  bool whole;
-  int sk, nseg;
-  int rows[TILE_KEYS / 8];
-};
-
-__device__ __forceinline__ void plan_tile(const DecodeArgs& a, const Unit& w, int i, const int* ptab,
-                                          int pfirst, TilePlan& t) {
-  const int P = 1 << a.log2_page;
-  const int seg = P < SEG_ROWS ? P : SEG_ROWS;
-  const int k0 = (w.tb + i) * TILE_KEYS;
-  const int kfirst = max(k0, w.lo), klast = min(k0 + TILE_KEYS - 1, w.p);
-  t.whole = kfirst == k0 && klast == k0 + TILE_KEYS - 1 && P >= TILE_KEYS;
-  t.sk = t.whole ? TILE_KEYS : seg;
-  t.nseg = TILE_KEYS / t.sk;
-  for (int sg = 0; sg < t.nseg; ++sg) {
-    const int ks = k0 + sg * t.sk;
-    t.rows[sg] = -1;
-    if (ks > klast || ks + t.sk - 1 < kfirst) continue;
-    const int page = ptab[(ks >> a.log2_page) - pfirst];
-    if (page < 0 || page >= a.num_pages) {
-      t.rows[sg] = -2;
-      continue;
-    }
-    t.rows[sg] = ((page * a.Hkv + w.kvh) << a.log2_page) + (ks & (P - 1));
-  }
-}
-
 // Does tile k0 of unit w need its own bias values?  Not when every visible key of the
 // tile is at distance >= E - 1: those all read the clamped bucket E - 1.
 __device__ __forceinline__ bool tile_needs_bias(const Unit& w, int k0, int E) {
@@ -182,9 +157,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 
 template <int D, int NSTAGE, int HB>
 __global__ void __launch_bounds__(DEC_THREADS, dec_ctas_per_sm<HB>())
-decode_persistent_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                         const __grid_constant__ CUtensorMap tmKs, const __grid_constant__ CUtensorMap tmVs,
-                         const __grid_constant__ CUtensorMap tmQ, const DecodeArgs a) {
+decode_persistent_kernel(const __grid_constant__ CUtensorMap tmKs, const __grid_constant__ CUtensorMap tmVs,
+                         const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt,
+                         const __grid_constant__ CUtensorMap tmKg, const __grid_constant__ CUtensorMap tmVg,
+                         const __grid_constant__ CUtensorMap tmQ3, const DecodeArgs a) {
   using S = DecShape<D>;
   using L_ = DecSmem<D, NSTAGE, HB>;
   constexpr int KSTEPS = D / 16;
@@ -230,11 +206,18 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_c
     // a short path (one page lookup, four TMA copies for D = 128).
     int* ptab = reinterpret_cast<int*>(smem + L_::ptab);
     if (lane == 0) {
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
-      prefetch_tensormap(&tmKs);
-      prefetch_tensormap(&tmVs);
-      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmQ3);
+      if (P >= TILE_KEYS) {
+        prefetch_tensormap(&tmKt);
+        prefetch_tensormap(&tmVt);
+      }
+      if (P >= 16) {
+        prefetch_tensormap(&tmKg);
+        prefetch_tensormap(&tmVg);
+      } else {
+        prefetch_tensormap(&tmKs);
+        prefetch_tensormap(&tmVs);
+      }
     }
     const int per_b = a.Hkv * a.head_chunks, per_s = a.B * per_b;
     auto next_active = [&](int u, Unit& w) -> int {
@@ -298,44 +281,52 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_c
             if (!okp) record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
             mbar_arrive_expect_tx(&full[st], (okp ? WHOLE_BYTES : 0u) + qbytes);
             if (okp) {
+              // one box per tensor: the tile's 4 groups x every column block
               const int row = page * hkvp + row_kv + (k0 & (P - 1));
-#pragma unroll
-              for (int cb = 0; cb < S::COL_BLOCKS; ++cb) {
-                tma_load_2d(kdst + cb * S::SUB_BYTES, &tmK, cb * 64, row, &full[st]);
-                tma_load_2d(vdst + cb * S::SUB_BYTES, &tmV, cb * 64, row, &full[st]);
-              }
+              tma_load_4d(kdst, &tmKt, 0, 0, 0, row >> 4, &full[st]);
+              tma_load_4d(vdst, &tmVt, 0, 0, 0, row >> 4, &full[st]);
             }
           } else {
-            TilePlan t;
-            plan_tile(a, cur, i, tab, pfirst, t);
+            // the tile's copies of seg keys (one 16-key group, or an 8-key page) that hold
+            // a visible key; pages outside the pool are skipped and their keys masked
+            const int seg = P < 16 ? P : 16;
+            const int kfirst = max(k0, cur.lo), klast = min(k0 + TILE_KEYS - 1, cur.p);
             uint64_t bad = 0;
             uint32_t bytes = qbytes;
-            for (int sg = 0; sg < t.nseg; ++sg) {
-              if (t.rows[sg] == -2) {
-                bad |= (t.sk == 64 ? ~0ull : (((1ull << t.sk) - 1) << (sg * t.sk)));
+            for (int ks = k0; ks < k0 + TILE_KEYS; ks += seg) {
+              if (ks > klast || ks + seg - 1 < kfirst) continue;
+              const int page = tab[(ks >> a.log2_page) - pfirst];
+              if (page < 0 || page >= a.num_pages) {
+                bad |= ((1ull << seg) - 1) << (ks - k0);
                 record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
-              } else if (t.rows[sg] >= 0) {
-                bytes += 2u * t.sk * D * 2u;
+              } else {
+                bytes += 2u * seg * D * 2u;
               }
             }
             badmask[st] = bad;
             mbar_arrive_expect_tx(&full[st], bytes);
-            for (int sg = 0; sg < t.nseg; ++sg) {
-              if (t.rows[sg] < 0) continue;
+            for (int ks = k0; ks < k0 + TILE_KEYS; ks += seg) {
+              if (ks > klast || ks + seg - 1 < kfirst) continue;
+              const int page = tab[(ks >> a.log2_page) - pfirst];
+              if (page < 0 || page >= a.num_pages) continue;
+              const int row = page * hkvp + row_kv + (ks & (P - 1));
+              const int off = ((ks - k0) >> 4) * S::GROUP_BYTES;
+              if (seg == 16) {
+                tma_load_4d(kdst + off, &tmKg, 0, 0, 0, row >> 4, &full[st]);
+                tma_load_4d(vdst + off, &tmVg, 0, 0, 0, row >> 4, &full[st]);
+              } else {
+                const int r16 = ((ks - k0) & 15) * 128;
 #pragma unroll
-              for (int cb = 0; cb < S::COL_BLOCKS; ++cb) {
-                tma_load_2d(kdst + cb * S::SUB_BYTES + sg * t.sk * 128, t.whole ? &tmK : &tmKs, cb * 64,
-                            t.rows[sg], &full[st]);
-                tma_load_2d(vdst + cb * S::SUB_BYTES + sg * t.sk * 128, t.whole ? &tmV : &tmVs, cb * 64,
-                            t.rows[sg], &full[st]);
+                for (int cb = 0; cb < S::COL_BLOCKS; ++cb) {
+                  tma_load_2d(kdst + off + cb * S::BLOCK_BYTES + r16, &tmKs, cb * 64, row, &full[st]);
+                  tma_load_2d(vdst + off + cb * S::BLOCK_BYTES + r16, &tmVs, cb * 64, row, &full[st]);
+                }
               }
             }
           }
           if (i == 0) {
             uint8_t* qdst = smem + L_::q + slot * S::QSLOT_BYTES;
-#pragma unroll
-            for (int cb = 0; cb < S::COL_BLOCKS; ++cb)
-              tma_load_2d(qdst + cb * S::QSUB_BYTES, &tmQ, cb * 64, cur.b * a.Hq + cur.h0, &full[st]);
+            tma_load_3d(qdst, &tmQ3, 0, cur.b * a.Hq + cur.h0, 0, &full[st]);
           }
         }
       }
@@ -481,7 +472,8 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_c
           const int krow = 16 * warp + (mi & 1) * 8 + (lane & 7);
           const int chunk = 2 * kk + (mi >> 1);
           uint32_t ka[4];
-          ldmatrix_x4(kbase + (chunk >> 3) * S::SUB_BYTES + swz128(krow, chunk & 7), ka[0], ka[1], ka[2], ka[3]);
+          ldmatrix_x4(kbase + warp * S::GROUP_BYTES + (chunk >> 3) * S::BLOCK_BYTES + swz128(krow & 15, chunk & 7),
+                      ka[0], ka[1], ka[2], ka[3]);
 #pragma unroll
           for (int j = 0; j < NB; ++j) mma_bf16_16816(acc[j], ka, qb[j][kk][0], qb[j][kk][1]);
         }
@@ -495,7 +487,8 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_c
         for (int dn = 0; dn < D / 16; ++dn) {
           const int vrow = 16 * warp + (mi >> 1) * 8 + (lane & 7);
           const int chunk = 2 * dn + (mi & 1);
-          ldmatrix_x4_trans(vbase + (chunk >> 3) * S::SUB_BYTES + swz128(vrow, chunk & 7), va[dn][0], va[dn][1],
+          ldmatrix_x4_trans(vbase + warp * S::GROUP_BYTES + (chunk >> 3) * S::BLOCK_BYTES + swz128(vrow & 15, chunk & 7),
+                            va[dn][0], va[dn][1],
                             va[dn][2], va[dn][3]);
           if (!all_valid) { va[dn][0] &= mlo; va[dn][1] &= mlo; va[dn][2] &= mhi; va[dn][3] &= mhi; }
         }
@@ -689,8 +682,8 @@ cudaError_t launch_decode_t(const DecodeMaps& m, const DecodeArgs& a, cudaStream
   if (e != cudaSuccess) return e;
   const long long units = (long long)a.num_splits * a.B * a.Hkv * a.head_chunks;
   const int grid = (int)std::min<long long>(units, (long long)dec_ctas_per_sm<HB>() * num_sms());
-  decode_persistent_kernel<D, NSTAGE, HB><<<grid, DEC_THREADS, smem, stream>>>(m.k, m.v, m.k_seg, m.v_seg,
-                                                                              m.q, a);
+  decode_persistent_kernel<D, NSTAGE, HB><<<grid, DEC_THREADS, smem, stream>>>(
+      m.k_seg, m.v_seg, m.k_tile, m.v_tile, m.k_grp, m.v_grp, m.q3, a);
   return cudaGetLastError();
 }
 

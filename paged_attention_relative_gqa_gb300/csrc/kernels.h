@@ -50,7 +50,10 @@ struct PrefillArgs {
 // with 64-row boxes (whole tiles) and 16-row boxes (tiles cut by the window start or
 // the sequence end), and q viewed as [B*Hq rows, D] with 16-row boxes.
 struct DecodeMaps {
-  CUtensorMap k, v, k_seg, v_seg, q;
+  CUtensorMap k_seg, v_seg;   // 2-D, boxes of min(P, 16) rows x 64 columns (pages of 8 keys)
+  CUtensorMap k_tile, v_tile; // 4-D group view, one box = 4 groups (a whole 64-key tile; P >= 64)
+  CUtensorMap k_grp, v_grp;   // 4-D group view, one box = 1 group of 16 keys (P >= 16)
+  CUtensorMap q3;             // 16 query rows, all column blocks in one box
 };
 
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& a, int head_dim,
@@ -60,7 +63,9 @@ cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& a, int head_
 // bias: rel_logits viewed as [E, Hq, total_q] fp32 (innermost first) with boxes of
 // 84 buckets x 1 head x 16 tokens (only built when rows of rel are 16-byte aligned).
 struct PrefillMaps {
-  CUtensorMap k, v, q, bias;
+  CUtensorMap k, v, bias;
+  CUtensorMap k3, v3;   // whole 64-key tiles, all column blocks in one box (P >= 64 only)
+  CUtensorMap q3;       // 128 query rows of one head, all column blocks in one box
 };
 
 constexpr int BIAS_BOX_COLS = 84;   // buckets per bias box row

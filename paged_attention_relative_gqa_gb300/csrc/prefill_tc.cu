@@ -177,7 +177,8 @@ __device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, volati
 template <int D>
 __global__ void __launch_bounds__(PT_THREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmK3, const __grid_constant__ CUtensorMap tmV3,
+                  const __grid_constant__ CUtensorMap tmQ3, const __grid_constant__ CUtensorMap tmB,
                   const PrefillArgs a) {
   using S = PtShape<D>;
   using L_ = PtSmem<D>;
@@ -257,10 +258,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     uint64_t* full = is_k ? k_full : v_full;
     uint64_t* empty = is_k ? k_empty : v_empty;
     const CUtensorMap* tm = is_k ? &tmK : &tmV;
+    const CUtensorMap* tm3 = is_k ? &tmK3 : &tmV3;   // whole tiles, P >= 64
     uint8_t* ring = smem + (is_k ? L_::kst : L_::vst);
     if (lane == 0) {
       prefetch_tensormap(tm);
-      if (is_k) prefetch_tensormap(&tmQ);
+      if (P >= TILE_KEYS) prefetch_tensormap(tm3);
+      if (is_k) prefetch_tensormap(&tmQ3);
     }
     int icount = 0, g = 0;
     int chunk_b = -1, chunk_base = 0, chunk_val = -1;
@@ -273,9 +276,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         bool ok = icount == 0 || wait_flag(q_empty, (uint32_t)(icount - 1) & 1u, abort_flag, a.err);
         if (ok) {
           mbar_arrive_expect_tx(q_full, (uint32_t)S::Q_BYTES);
-#pragma unroll
-          for (int cb = 0; cb < S::CB; ++cb)
-            tma_load_2d(smem + L_::q + cb * S::Q_SUB, &tmQ, it.h * D + cb * 64, it.t0, q_full);
+          tma_load_3d(smem + L_::q, &tmQ3, 0, it.t0, it.h * S::CB, q_full);   // 128 rows x all column blocks
         }
       }
       const int32_t* bt = a.block_table + (size_t)it.b * a.max_pages;
@@ -322,8 +323,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
           const int sg = __ffs(mm) - 1;
           const int row = __shfl_sync(0xffffffffu, my_row, sg);
           uint8_t* dst = ring + (size_t)st * S::KV_TILE + sg * seg * 128;
+          if (seg == TILE_KEYS) {
+            tma_load_3d_warp(dst, tm3, 0, row, 0, &full[st]);   // whole tile: one box
+          } else {
 #pragma unroll
-          for (int cb = 0; cb < S::CB; ++cb) tma_load_2d_warp(dst + cb * S::KV_SUB, tm, cb * 64, row, &full[st]);
+            for (int cb = 0; cb < S::CB; ++cb) tma_load_2d_warp(dst + cb * S::KV_SUB, tm, cb * 64, row, &full[st]);
+          }
         }
       }
       ++icount;
@@ -732,7 +737,7 @@ cudaError_t launch_prefill_tc_t(const PrefillMaps& m, const PrefillArgs& a, cuda
   if (e != cudaSuccess) return e;
   const long long items = (long long)a.num_q_tiles * a.B * a.Hq;
   const int grid = (int)std::min<long long>(items, num_sms_pf());
-  prefill_tc_kernel<D><<<grid, PT_THREADS, smem, stream>>>(m.k, m.v, m.q, m.bias, a);
+  prefill_tc_kernel<D><<<grid, PT_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.q3, m.bias, a);
   return cudaGetLastError();
 }
 
