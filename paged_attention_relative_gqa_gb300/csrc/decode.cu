@@ -415,7 +415,9 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmKs, const __grid_
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int h = 8 * j + 2 * cq + e;
-        clampv[j][e] = h < cur.nh ? __ldg(a.rel + ((size_t)cur.b * a.Hq + cur.h0 + h) * a.E + a.E - 1) : 0.f;
+        // heads past the unit's last read head h0's bucket instead: never outside rel
+        const float ld = __ldg(a.rel + ((size_t)cur.b * a.Hq + cur.h0 + (h < cur.nh ? h : 0)) * a.E + a.E - 1);
+        clampv[j][e] = h < cur.nh ? ld : 0.f;
       }
     const int qslot = uc & 1;
     uint32_t qb[NB][KSTEPS][2];  // B fragments of Q^T

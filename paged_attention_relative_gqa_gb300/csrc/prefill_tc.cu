@@ -294,7 +294,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
           chunk_b = it.b;
           chunk_base = pfirst;
           const int idx = chunk_base + lane;
-          chunk_val = idx <= last_idx ? __ldg(bt + idx) : -1;
+          const int v = __ldg(bt + min(idx, last_idx));   // in bounds even past the last entry
+          chunk_val = idx <= last_idx ? v : -1;
         }
         const int ks = k0 + lane * seg;
         const bool want = lane < nseg && ks <= it.k_hi && ks + seg - 1 >= it.lo_min;
@@ -458,8 +459,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         continue;
       }
       const int pr = it.pos0 + r;
-      const float* relrow = a.rel + ((size_t)(it.t0 + r) * a.Hq + it.h) * a.E;
-      const float clampv = rv ? __ldg(relrow + a.E - 1) : 0.f;   // bucket of distances >= E - 1
+      // (rows past the item's last use its last row's address: never outside rel)
+      const float* relrow = a.rel + ((size_t)(it.t0 + (rv ? r : it.rows - 1)) * a.Hq + it.h) * a.E;
+      const float clamp_ld = __ldg(relrow + a.E - 1);
+      const float clampv = rv ? clamp_ld : 0.f;   // bucket of distances >= E - 1
       const int32_t* bt = a.block_table + (size_t)it.b * a.max_pages;
       const int seg = P < TILE_KEYS ? P : TILE_KEYS;
       // Does some page holding a key of the item lie outside the pool?  (Checked once per
@@ -482,7 +485,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         for (int sg = 0; sg < TILE_KEYS / seg; ++sg) {
           const int ks = k0 + sg * seg;
           if (ks > it.k_hi || ks + seg - 1 < it.lo_min) continue;
-          const int page = __ldg(bt + (ks >> a.log2_page));
+          const int page = __ldg(bt + min(ks >> a.log2_page, it.k_hi >> a.log2_page));
           if (page < 0 || page >= a.num_pages) bad |= (seg == 64 ? ~0ull : (((1ull << seg) - 1) << (sg * seg)));
         }
         return bad;
