@@ -69,7 +69,7 @@ def prefill_work(prob):
     for (pos, lo) in visible_ranges(prob):
         vis = pos - lo + 1
         flops += int(vis.sum()) * 4 * D * Hq
-        bias += int(np.minimum(vis, E).sum()) * Hq * 4
+        bias += int(np.minimum(vis, E).sum()) * Hq * prob.rel_logits.element_size()
     kv = sum(prob.seq_lens_list) * Hkv * D * 2 * 2
     qo = prob.total_q * Hq * D * 2 * 2
     return flops, bias + kv + qo
@@ -249,6 +249,9 @@ WORKLOAD_DESC = {
                         "window 512, page 16, bias [1024,8,512] fp32",
     "global_prefill": "global_prefill: 4 x 8192 tokens, 64 q heads / 8 kv heads, head_dim 128, "
                       "full causal, page 64, bias [32768,64,4096] fp32 (clamped)",
+    "global_prefill_bf16bias": "global_prefill with the bias in bf16 (inkling_attn_prefill_bf16bias): "
+                               "4 x 8192 tokens, 64 q heads / 8 kv heads, head_dim 128, full causal, "
+                               "page 64, bias [32768,64,4096] bf16 (clamped)",
     "global_prefill_small": "global_prefill_small (profiling size): 1 x 2048 tokens, 64 q heads / "
                             "8 kv heads, head_dim 128, full causal, page 64, bias [2048,64,4096] fp32",
     "mixed": "mixed serving step: 5 SWA + 1 global layer, each one prefill call (8 x 2048 tokens) "
@@ -267,6 +270,8 @@ def workload_instances(name, dev):
         return [W.swa_prefill_tiny(dev, seed=s) for s in range(8)]  # 8 x 17 MB > L2
     if name == "global_prefill":
         return [W.global_prefill(dev, seed=4)]                       # 36 GB > L2
+    if name == "global_prefill_bf16bias":
+        return [W.global_prefill(dev, seed=4, bias_dtype=torch.bfloat16)]   # 19 GB > L2
     if name == "global_prefill_small":
         return [W.global_prefill(dev, seed=4, batch=1, tokens=2048)]  # 2.2 GB > L2
     raise ValueError(name)
@@ -399,7 +404,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_extra:
         wl = {}
         steps_x = max(5, args.steps // 4)
-        for other in ("global_decode", "swa_prefill_tiny", "global_prefill", "mixed"):
+        for other in ("global_decode", "swa_prefill_tiny", "global_prefill", "global_prefill_bf16bias", "mixed"):
             if other == name:
                 continue
             st = steps_x if other in ("global_decode", "swa_prefill_tiny") else max(3, steps_x // 2)

@@ -124,6 +124,24 @@ ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q
                                   size_t workspace_bytes, void* stream);
 
 /*
+ * inkling_attn_prefill with the bias in bf16: rel_logits_bf16 is bf16 [total_q, Hq, E]
+ * (same layout as rel_logits), every other argument and result as for
+ * inkling_attn_prefill.  The review of _build_rel_logits in "Support Inkling-NVFP4 model"
+ * (TensorRT-LLM PR #17062) proposes emitting the bias in bf16 when the kernel accepts
+ * it: on long prompts the fp32 bias is the largest input of the call, and bf16 halves it.
+ * The bias enters the scores as exactly the bf16 values given (widened to fp32); the
+ * rest of the arithmetic is unchanged.
+ *   Requirements beyond inkling_attn_prefill: E a multiple of 8 (else INK_ERR_BAD_SHAPE)
+ *   and rel_logits_bf16 16-byte aligned (else INK_ERR_ALIGNMENT).
+ */
+ink_status_t inkling_attn_prefill_bf16bias(const ink_attn_params_t* params, const void* q,
+                                           const int32_t* cu_q_lens, int32_t max_q_len, int32_t total_q,
+                                           const void* k_cache, const void* v_cache,
+                                           const int32_t* block_table, const int32_t* seq_lens,
+                                           const void* rel_logits_bf16, void* out, void* workspace,
+                                           size_t workspace_bytes, void* stream);
+
+/*
  * Paged decode: one new token per sequence (row b of q is sequence b, at p = L_b - 1).
  *   q          device, bf16 [B, Hq, D]
  *   rel_logits device, fp32 [B, Hq, E]

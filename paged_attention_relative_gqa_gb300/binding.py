@@ -27,7 +27,8 @@ DEVERR_WAIT_TIMEOUT = 0x4
 DEVERR_QLEN_EXCEEDS_MAX = 0x8
 
 EXPORTED_SYMBOLS = ("inkling_attn_workspace_bytes", "inkling_attn_workspace_init",
-                    "inkling_attn_prefill", "inkling_attn_decode", "inkling_attn_decode_noalloc",
+                    "inkling_attn_prefill", "inkling_attn_prefill_bf16bias", "inkling_attn_decode",
+                    "inkling_attn_decode_noalloc",
                     "inkling_attn_read_device_error", "inkling_attn_status_string",
                     "inkling_attn_version")
 
@@ -68,6 +69,8 @@ def load_library(path: Optional[str] = None):
     lib.inkling_attn_workspace_init.restype = ctypes.c_int
     lib.inkling_attn_prefill.argtypes = [PP, V, V, I32, I32, V, V, V, V, V, V, V, S, V]
     lib.inkling_attn_prefill.restype = ctypes.c_int
+    lib.inkling_attn_prefill_bf16bias.argtypes = [PP, V, V, I32, I32, V, V, V, V, V, V, V, S, V]
+    lib.inkling_attn_prefill_bf16bias.restype = ctypes.c_int
     lib.inkling_attn_decode.argtypes = [PP, V, V, V, V, V, V, V, V, S, V]
     lib.inkling_attn_decode.restype = ctypes.c_int
     lib.inkling_attn_decode_noalloc.argtypes = [PP, V, V, V, V, V, V, V, V]
@@ -150,15 +153,19 @@ def alloc_workspace(params: ink_attn_params_t, is_decode: bool = True, device="c
 
 def inkling_attn_prefill(params, q, cu_q_lens, max_q_len, k_cache, v_cache, block_table,
                          seq_lens, rel_logits, out, workspace, stream=None):
+    """Paged prefill; a bf16 ``rel_logits`` goes to inkling_attn_prefill_bf16bias."""
     lib = load_library()
-    code = lib.inkling_attn_prefill(
+    bf16 = isinstance(rel_logits, torch.Tensor) and rel_logits.dtype == torch.bfloat16
+    fn = lib.inkling_attn_prefill_bf16bias if bf16 else lib.inkling_attn_prefill
+    code = fn(
         ctypes.byref(params), _dev(q, "q", torch.bfloat16), _dev(cu_q_lens, "cu_q_lens", torch.int32),
         int(max_q_len), int(q.shape[0]), _dev(k_cache, "k_cache", torch.bfloat16),
         _dev(v_cache, "v_cache", torch.bfloat16),
         _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
-        _dev(rel_logits, "rel_logits", torch.float32), _dev(out, "out", torch.bfloat16),
+        _dev(rel_logits, "rel_logits", torch.bfloat16 if bf16 else torch.float32),
+        _dev(out, "out", torch.bfloat16),
         _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream_handle(stream))
-    _check(code, "inkling_attn_prefill")
+    _check(code, "inkling_attn_prefill_bf16bias" if bf16 else "inkling_attn_prefill")
     return out
 
 

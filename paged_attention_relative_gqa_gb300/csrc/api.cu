@@ -176,14 +176,17 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 // rel_logits [total_q, Hq, E] fp32 as a 3-D tensor {E, Hq, total_q}; boxes of
 // BIAS_BOX_COLS buckets x 1 head x BIAS_BOX_ROWS tokens, out-of-range elements read as 0.
-bool make_bias_map(CUtensorMap* map, const float* rel, const ink_attn_params_t* p, int total_q) {
+bool make_bias_map(CUtensorMap* map, const void* rel, bool bf16, const ink_attn_params_t* p, int total_q) {
   auto fn = encode_fn();
   if (!fn) return false;
+  const cuuint64_t es = bf16 ? 2 : 4;
   cuuint64_t dims[3] = {(cuuint64_t)p->rel_extent, (cuuint64_t)p->num_q_heads, (cuuint64_t)total_q};
-  cuuint64_t strides[2] = {(cuuint64_t)p->rel_extent * 4, (cuuint64_t)p->rel_extent * 4 * p->num_q_heads};
-  cuuint32_t box[3] = {(cuuint32_t)ink::BIAS_BOX_COLS, 1, (cuuint32_t)ink::BIAS_BOX_ROWS};
+  cuuint64_t strides[2] = {(cuuint64_t)p->rel_extent * es, (cuuint64_t)p->rel_extent * es * p->num_q_heads};
+  cuuint32_t box[3] = {(cuuint32_t)(bf16 ? ink::BIAS_BOX_COLS_BF16 : ink::BIAS_BOX_COLS), 1,
+                       (cuuint32_t)ink::BIAS_BOX_ROWS};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(rel), dims, strides, box, estr,
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                  const_cast<void*>(rel), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -303,12 +306,15 @@ ink_status_t inkling_attn_decode(const ink_attn_params_t* params, const void* q,
   return INK_OK;
 }
 
-ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q,
-                                  const int32_t* cu_q_lens, int32_t max_q_len, int32_t total_q,
-                                  const void* k_cache,
-                                  const void* v_cache, const int32_t* block_table,
-                                  const int32_t* seq_lens, const float* rel_logits, void* out,
-                                  void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by the fp32-bias and bf16-bias prefill entry points.
+ink_status_t prefill_impl(const ink_attn_params_t* params, const void* q, const int32_t* cu_q_lens,
+                          int32_t max_q_len, int32_t total_q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_table, const int32_t* seq_lens, const void* rel_logits,
+                          bool bias_bf16, void* out, void* workspace, size_t workspace_bytes, void* stream) {
   ink_status_t st = validate(params);
   if (st != INK_OK) return st;
   if (!q || !cu_q_lens || !k_cache || !v_cache || !block_table || !seq_lens || !rel_logits ||
@@ -318,11 +324,12 @@ ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q
   if ((long long)total_q * params->num_q_heads >= (1ll << 31)) return INK_ERR_TOO_LARGE;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(cu_q_lens, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
-      !aligned(rel_logits, 4) || !aligned(workspace, 256))
+      !aligned(rel_logits, bias_bf16 ? 16 : 4) || !aligned(workspace, 256))
     return INK_ERR_ALIGNMENT;
+  if (bias_bf16 && params->rel_extent % 8 != 0) return INK_ERR_BAD_SHAPE;   // 16-byte bias rows
   if (workspace_bytes < kHeaderBytes) return INK_ERR_WORKSPACE;
   if (params->num_seqs == 0 || max_q_len == 0 || total_q == 0) return INK_OK;
-  const int num_q_tiles = (max_q_len + 63) / 64;
+  const int num_q_tiles = (max_q_len + ink::PREFILL_ROWS - 1) / ink::PREFILL_ROWS;
   if (num_q_tiles > 65535 || params->num_seqs > 65535) return INK_ERR_TOO_LARGE;
   ink::PrefillMaps maps;
   const int cblocks = params->head_dim / 64;
@@ -357,12 +364,37 @@ ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q
   a.sm_scale = params->sm_scale;
   a.max_q_len = max_q_len;
   a.num_q_tiles = num_q_tiles;
-  a.bias_bulk = (params->rel_extent % 4 == 0) && aligned(rel_logits, 16);
+  a.bias_bf16 = bias_bf16 ? 1 : 0;
+  a.bias_bulk = bias_bf16 || ((params->rel_extent % 4 == 0) && aligned(rel_logits, 16));
   std::memset(&maps.bias, 0, sizeof maps.bias);
-  if (a.bias_bulk && !make_bias_map(&maps.bias, rel_logits, params, total_q)) return INK_ERR_CUDA;
+  if (a.bias_bulk && !make_bias_map(&maps.bias, rel_logits, bias_bf16, params, total_q)) return INK_ERR_CUDA;
   if (ink::launch_prefill_tc(maps, a, params->head_dim, (cudaStream_t)stream) != cudaSuccess)
     return INK_ERR_CUDA;
   return INK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q,
+                                  const int32_t* cu_q_lens, int32_t max_q_len, int32_t total_q,
+                                  const void* k_cache,
+                                  const void* v_cache, const int32_t* block_table,
+                                  const int32_t* seq_lens, const float* rel_logits, void* out,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  return prefill_impl(params, q, cu_q_lens, max_q_len, total_q, k_cache, v_cache, block_table, seq_lens,
+                      rel_logits, false, out, workspace, workspace_bytes, stream);
+}
+
+ink_status_t inkling_attn_prefill_bf16bias(const ink_attn_params_t* params, const void* q,
+                                           const int32_t* cu_q_lens, int32_t max_q_len, int32_t total_q,
+                                           const void* k_cache, const void* v_cache,
+                                           const int32_t* block_table, const int32_t* seq_lens,
+                                           const void* rel_logits_bf16, void* out, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  return prefill_impl(params, q, cu_q_lens, max_q_len, total_q, k_cache, v_cache, block_table, seq_lens,
+                      rel_logits_bf16, true, out, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -35,7 +35,7 @@ struct PrefillArgs {
   const int32_t* cu_q;        // [B+1]
   const int32_t* block_table; // [B, max_pages]
   const int32_t* seq_lens;    // [B]
-  const float* rel;           // fp32 [total_q, Hq, E]
+  const void* rel;            // [total_q, Hq, E], fp32, or bf16 when bias_bf16
   void* out;                  // bf16 [total_q, Hq, D]
   uint32_t* err;
   int B, Hq, Hkv, G;
@@ -43,7 +43,8 @@ struct PrefillArgs {
   float scale_log2;
   float sm_scale;             // multiplies q.k (the bias is added unscaled)
   int max_q_len, num_q_tiles;
-  int bias_bulk;              // rows of rel are 16-byte aligned (E % 4 == 0, aligned base)
+  int bias_bulk;              // rows of rel are 16-byte aligned (E a multiple of 16 bytes, aligned base)
+  int bias_bf16;              // rel holds bf16 values (always with bias_bulk)
 };
 
 // TMA descriptors of one decode call: K/V pools viewed as [num_pages*Hkv*P rows, D]
@@ -70,6 +71,8 @@ struct PrefillMaps {
 
 constexpr int BIAS_BOX_COLS = 84;   // buckets per bias box row
 constexpr int BIAS_BOX_ROWS = 16;   // tokens per bias box
+constexpr int BIAS_BOX_COLS_BF16 = 88;   // buckets per bias box row, bf16 bias
+constexpr int PREFILL_ROWS = 128;        // new tokens per prefill work item
 
 cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int head_dim,
                               cudaStream_t stream);

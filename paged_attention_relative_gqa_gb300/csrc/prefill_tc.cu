@@ -29,6 +29,7 @@
 //           by more than 2^8.  Epilogue: the two partial results are merged,
 //           O / l -> bf16 -> out.
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -37,48 +38,66 @@ namespace ink {
 
 namespace {
 
-constexpr int PT_ROWS = 128;
+constexpr int PT_ROWS = PREFILL_ROWS;
 constexpr int PT_THREADS = 384;
-constexpr int PT_BIAS_SLOTS = 2;      // one bias slot per softmax warpgroup
-// Bias slot: 8 groups of 16 rows (tokens); group g at float 1344 g, row i of it at
-// +84 i.  A group holds buckets [x_g, x_g + 84) of its 16 rows, x_g = 4*floor((dmin0 +
-// 16g)/4), where dmin0 = pos0 - (k0 + 63) is row 0's smallest distance in the tile (x_g
-// is a multiple of 4: TMA wants 16-byte aligned starts).  Row r = 16g + i then finds
-// the bucket of key k0 + c at offset boff + 63 - c with boff = (dmin0 mod 4) + i <= 18,
-// so 82 columns suffice; a row-per-thread read of one c touches every bank at most
-// twice (the row pitch 84 + 1 is odd mod 32, so the 16 rows of a group hit 16 banks).
-constexpr int PT_BIAS_GROUP = BIAS_BOX_ROWS * BIAS_BOX_COLS;   // floats per group
-constexpr int PT_BIAS_NGROUP = PT_ROWS / BIAS_BOX_ROWS;         // groups per tile
-constexpr int PT_BIAS_SLOT_FLOATS = PT_BIAS_NGROUP * PT_BIAS_GROUP;
+// Bias slot: 8 groups of 16 rows (tokens); group g holds buckets [x_g, x_g + COLS) of its
+// rows, row i of it at +COLS i, x_g = ALIGN*floor((dmin0 + 16g)/ALIGN), where
+// dmin0 = pos0 - (k0 + 63) is row 0's smallest distance in the tile (x_g is 16-byte
+// aligned, as TMA wants).  Row r = 16g + i then finds the bucket of key k0 + c at offset
+// boff + 63 - c with boff = (dmin0 mod ALIGN) + i, so 64 + 15 + ALIGN - 1 columns suffice.
+// fp32: COLS 84 (the row pitch 85 is odd mod 32, so a row-per-thread read of one c hits
+// each bank at most twice); bf16: COLS 88 (also at most two rows per bank word).
+// Each softmax warpgroup owns PER_WG slots that it fills in turn; every slot then has one
+// consumer taking its fills in order, so a parity wait never matches a phase two behind.
+template <bool BF>
+struct BiasShape {
+  using T = typename std::conditional<BF, __nv_bfloat16, float>::type;
+  static constexpr int COLS = BF ? BIAS_BOX_COLS_BF16 : BIAS_BOX_COLS;
+  static constexpr int ALIGN = 16 / (int)sizeof(T);          // elements per 16 bytes
+  static constexpr int GROUP = BIAS_BOX_ROWS * COLS;          // elements per group
+  static constexpr int NGROUP = PT_ROWS / BIAS_BOX_ROWS;      // groups per tile
+  static constexpr int SLOT_BYTES = NGROUP * GROUP * (int)sizeof(T);
+  static constexpr int PER_WG = 1;                            // slots per softmax warpgroup
+  static constexpr int SLOTS = 2 * PER_WG;
+  static_assert(COLS >= TILE_KEYS + BIAS_BOX_ROWS - 1 + ALIGN - 1, "bias box too narrow");
+  static_assert((COLS * (int)sizeof(T)) % 16 == 0 && (GROUP * (int)sizeof(T)) % 128 == 0, "TMA alignment");
+};
+
+__device__ __forceinline__ float to_float(float x) { return x; }
+__device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+
 constexpr uint32_t TM_S = 0;     // S[2]: 64 fp32 columns each
 constexpr uint32_t TM_P = 128;   // P[2]: 32 columns (64 bf16) each
 constexpr uint32_t TM_O = 256;   // O[2]: D fp32 columns each (one per softmax warpgroup)
 constexpr uint32_t TM_COLS = 512;
 constexpr float RESCALE_NAT = 5.545177444479562f;   // rescale O when a max grows by > 2^8
 
-template <int D>
+// Ring depths (D = 128): V gets two slots per softmax warpgroup (a V tile waits for the P V
+// product two tiles back, so one slot each left the P V issue waiting for V); K gets three
+// stages when the smaller bf16 bias slots leave room, two with the fp32 bias.
+template <int D, bool BF>
 struct PtShape {
   static constexpr int CB = D / 64;
   static constexpr int Q_SUB = PT_ROWS * 128;
   static constexpr int Q_BYTES = CB * Q_SUB;
   static constexpr int KV_SUB = TILE_KEYS * 128;
   static constexpr int KV_TILE = CB * KV_SUB;   // one K or one V tile
-  static constexpr int NK = D == 128 ? 3 : 4;    // K ring: freed once S = Q K^T is done
-  static constexpr int NV = D == 128 ? 2 : 4;    // V ring (even: slot g % NV serves warpgroup g % 2)
-  static constexpr int BIAS_SLOT = PT_BIAS_SLOT_FLOATS * 4;
+  static constexpr int NK = D == 128 ? (BF ? 3 : 2) : 4;   // K ring: freed once S = Q K^T is done
+  static constexpr int NV = 4;   // V ring (even: slot g % NV serves warpgroup g % 2)
 };
 
-template <int D>
+template <int D, bool BF>
 struct PtSmem {
-  using S = PtShape<D>;
+  using S = PtShape<D, BF>;
+  using BS = BiasShape<BF>;
   static constexpr size_t q = 0;
   static constexpr size_t kst = q + S::Q_BYTES;
   static constexpr size_t vst = kst + (size_t)S::NK * S::KV_TILE;
   static constexpr size_t bias = vst + (size_t)S::NV * S::KV_TILE;
-  static constexpr size_t bars = bias + (size_t)PT_BIAS_SLOTS * S::BIAS_SLOT;
+  static constexpr size_t bars = bias + (size_t)BS::SLOTS * BS::SLOT_BYTES;
   // q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2],
   // s_empty[2], o_done[2], o_free, b_full[NB], b_empty[NB], ml_full, ml_free
-  static constexpr int NBAR = 2 + 2 * S::NK + 2 * S::NV + 2 + 2 + 2 + 1 + 2 * PT_BIAS_SLOTS + 2;
+  static constexpr int NBAR = 2 + 2 * S::NK + 2 * S::NV + 2 + 2 + 2 + 1 + 2 * BS::SLOTS + 2;
   static constexpr size_t vbad = bars + NBAR * 8;
   static constexpr size_t ml1 = vbad + S::NV * 8;          // float2 [128]
   static constexpr size_t misc = ml1 + PT_ROWS * 8;
@@ -121,19 +140,9 @@ __device__ __forceinline__ bool get_item(const PrefillArgs& a, int i, PItem& it)
   return true;
 }
 
-// Key tiles of all items this CTA takes.
-__device__ int cta_tiles(const PrefillArgs& a, int total_items) {
-  int n = 0;
-  PItem it;
-#pragma unroll 1
-  for (int i = blockIdx.x; i < total_items; i += gridDim.x)
-    if (get_item(a, i, it)) n += it.ntile;
-  return n;
-}
-
-// First bucket held by bias group g of a tile (may be negative or past E: read as 0).
+template <int ALIGN>
 __device__ __forceinline__ int bias_group_x(int dmin0, int g) {
-  return (dmin0 + BIAS_BOX_ROWS * g) & ~3;
+  return (dmin0 + BIAS_BOX_ROWS * g) & ~(ALIGN - 1);
 }
 
 // Visible keys of row position pr within tile k0 (kmin > kmax: none).
@@ -174,14 +183,16 @@ __device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, volati
   return false;
 }
 
-template <int D>
+template <int D, bool BF>
 __global__ void __launch_bounds__(PT_THREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmK3, const __grid_constant__ CUtensorMap tmV3,
                   const __grid_constant__ CUtensorMap tmQ3, const __grid_constant__ CUtensorMap tmB,
                   const PrefillArgs a) {
-  using S = PtShape<D>;
-  using L_ = PtSmem<D>;
+  using S = PtShape<D, BF>;
+  using L_ = PtSmem<D, BF>;
+  using BS = BiasShape<BF>;
+  using BT = typename BS::T;
   constexpr int NK = S::NK, NV = S::NV;
   constexpr uint32_t IDESC_S = umma_idesc_bf16(PT_ROWS, TILE_KEYS, false, false);
   constexpr uint32_t IDESC_PV = umma_idesc_bf16(PT_ROWS, D, false, true);
@@ -201,8 +212,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   uint64_t* o_done = s_empty + 2;
   uint64_t* o_free = o_done + 2;
   uint64_t* b_full = o_free + 1;
-  uint64_t* b_empty = b_full + PT_BIAS_SLOTS;
-  uint64_t* ml_full = b_empty + PT_BIAS_SLOTS;
+  uint64_t* b_empty = b_full + BS::SLOTS;
+  uint64_t* ml_full = b_empty + BS::SLOTS;
   uint64_t* ml_free = ml_full + 1;
   float2* ml1 = reinterpret_cast<float2*>(smem + L_::ml1);
   uint64_t* vbad = reinterpret_cast<uint64_t*>(smem + L_::vbad);
@@ -232,7 +243,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     mbar_init(o_free, 4);
     mbar_init(ml_full, 4);
     mbar_init(ml_free, 4);
-    for (int x = 0; x < PT_BIAS_SLOTS; ++x) {
+    for (int x = 0; x < BS::SLOTS; ++x) {
       mbar_init(&b_full[x], a.bias_bulk ? 1 : 32);
       mbar_init(&b_empty[x], 4);
     }
@@ -374,10 +385,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     // warp copies the visible buckets with 4-byte cp.async into the same layout.
     // Buckets at distance >= E - 1 are never read: the softmax uses the row's bucket
     // E - 1 for those keys.
-    // Slot s serves the tiles of softmax warpgroup s (tiles g with g % 2 == s): each
-    // slot has one consumer that takes its fills in order, so a parity wait never sees
-    // a phase two behind.  (V slots follow the same rule: NV is even.)
-    int bcnt[PT_BIAS_SLOTS] = {0, 0};
+    // Warpgroup w's tiles (g % 2 == w) fill its PER_WG slots in turn: each slot has one
+    // consumer that takes its fills in order, so a parity wait never sees a phase two
+    // behind.  (V slots follow the same rule: NV is even.)
+    int bcnt[2] = {0, 0};   // bias tiles loaded per warpgroup
     int g = 0;
     if (lane == 0) prefetch_tensormap(&tmB);
     for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
@@ -386,34 +397,33 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       for (int j = 0; j < it.ntile; ++j, ++g) {
         const int k0 = (it.kt0 + j) * TILE_KEYS;
         if (!tile_needs_bias(it.pos0, k0, a.E)) continue;
-        const int slot = g & 1;
-        const int use = bcnt[slot]++;
+        const int u = bcnt[g & 1]++;
+        const int slot = (g & 1) * BS::PER_WG + u % BS::PER_WG, use = u / BS::PER_WG;
         if (use >= 1) (void)wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err);
-        float* sb = reinterpret_cast<float*>(smem + L_::bias + (size_t)slot * S::BIAS_SLOT);
+        BT* sb = reinterpret_cast<BT*>(smem + L_::bias + (size_t)slot * BS::SLOT_BYTES);
         const int dmin0 = it.pos0 - (k0 + TILE_KEYS - 1);
         if (a.bias_bulk) {
-          // lane gr < PT_BIAS_NGROUP decides whether group gr of this tile is read; the
-          // warp loads those
+          // lane gr < NGROUP decides whether group gr of this tile is read; the warp loads those
           const uint32_t nm =
-              __ballot_sync(0xffffffffu, lane < PT_BIAS_NGROUP && bias_group_needed(a, it, k0, lane));
-          mbar_arrive_expect_tx_warp(&b_full[slot], (uint32_t)__popc(nm) * (uint32_t)(PT_BIAS_GROUP * 4));
+              __ballot_sync(0xffffffffu, lane < BS::NGROUP && bias_group_needed(a, it, k0, lane));
+          mbar_arrive_expect_tx_warp(&b_full[slot], (uint32_t)__popc(nm) * (uint32_t)(BS::GROUP * sizeof(BT)));
 #pragma unroll 1
           for (uint32_t mm = nm; mm; mm &= mm - 1) {
             const int gr = __ffs(mm) - 1;
-            tma_load_3d_warp(sb + gr * PT_BIAS_GROUP, &tmB, bias_group_x(dmin0, gr), it.h, it.t0 + BIAS_BOX_ROWS * gr,
-                             &b_full[slot]);
+            tma_load_3d_warp(sb + gr * BS::GROUP, &tmB, bias_group_x<BS::ALIGN>(dmin0, gr), it.h,
+                             it.t0 + BIAS_BOX_ROWS * gr, &b_full[slot]);
           }
-        } else {
+        } else if constexpr (!BF) {   // fp32 rows that are not 16-byte aligned (never bf16)
 #pragma unroll 1
           for (int r = 0; r < it.rows; ++r) {
             const int pr = it.pos0 + r;
             int kmin, kmax;
             row_tile_keys(a, it, pr, k0, kmin, kmax);
-            const float* srcr = a.rel + ((size_t)(it.t0 + r) * a.Hq + it.h) * a.E;
+            const float* srcr = static_cast<const float*>(a.rel) + ((size_t)(it.t0 + r) * a.Hq + it.h) * a.E;
             const int gr = r / BIAS_BOX_ROWS, ii = r % BIAS_BOX_ROWS;
-            const int xg = bias_group_x(dmin0, gr);
-            // bucket d sits at group_base + ii*100 + (d - x_g); visible keys give d >= x_g
-            const uint32_t rb = smem_u32(sb + gr * PT_BIAS_GROUP + ii * BIAS_BOX_COLS);
+            const int xg = bias_group_x<BS::ALIGN>(dmin0, gr);
+            // bucket d sits at group_base + ii*COLS + (d - x_g); visible keys give d >= x_g
+            const uint32_t rb = smem_u32(sb + gr * BS::GROUP + ii * BS::COLS);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               const int c = lane + 32 * half;
@@ -460,8 +470,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       }
       const int pr = it.pos0 + r;
       // (rows past the item's last use its last row's address: never outside rel)
-      const float* relrow = a.rel + ((size_t)(it.t0 + (rv ? r : it.rows - 1)) * a.Hq + it.h) * a.E;
-      const float clamp_ld = __ldg(relrow + a.E - 1);
+      const BT* relrow = static_cast<const BT*>(a.rel) + ((size_t)(it.t0 + (rv ? r : it.rows - 1)) * a.Hq + it.h) * a.E;
+      const float clamp_ld = to_float(__ldg(relrow + a.E - 1));
       const float clampv = rv ? clamp_ld : 0.f;   // bucket of distances >= E - 1
       const int32_t* bt = a.block_table + (size_t)it.b * a.max_pages;
       const int seg = P < TILE_KEYS ? P : TILE_KEYS;
@@ -498,7 +508,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         const int k0 = (it.kt0 + j) * TILE_KEYS;
         const bool needs = tile_needs_bias(it.pos0, k0, a.E);
         if ((g & 1) != wg) continue;  // the other warpgroup's tile
-        const float* bslot = reinterpret_cast<const float*>(smem + L_::bias + (size_t)wg * S::BIAS_SLOT);
+        const int bslot_i = wg * BS::PER_WG + buse % BS::PER_WG;   // this warpgroup's next fill
+        const BT* bslot = reinterpret_cast<const BT*>(smem + L_::bias + (size_t)bslot_i * BS::SLOT_BYTES);
         uint64_t bad = item_bad ? tile_bad(k0) : 0ull;
         bool ok = wait_flag(&s_full[g & 1], (uint32_t)(g >> 1) & 1u, abort_flag, a.err);
         tc_fence_after();
@@ -523,13 +534,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         // key c sits at distance dmin + 63 - c; columns c <= cc read bucket E - 1
         const int dmin = pr - (k0 + TILE_KEYS - 1);
         const int cc = dmin + TILE_KEYS - a.E;
-        // bucket of key c at brow[-c] (group_base + i*100 + (d - x_g)); any address in the
+        // bucket of key c at brow[-c] (group_base + i*COLS + (d - x_g)); any address in the
         // slot when the tile reads no bucket from it
-        const float* brow = bslot + (TILE_KEYS - 1);
+        const BT* brow = bslot + (TILE_KEYS - 1);
         if (needs) {
-          (void)wait_flag(&b_full[wg], (uint32_t)buse & 1u, abort_flag, a.err);
+          (void)wait_flag(&b_full[bslot_i], (uint32_t)(buse / BS::PER_WG) & 1u, abort_flag, a.err);
           const int gr = r / BIAS_BOX_ROWS;
-          brow = bslot + gr * PT_BIAS_GROUP + (r % BIAS_BOX_ROWS) * BIAS_BOX_COLS + (dmin - bias_group_x(dmin - r, gr)) +
+          brow = bslot + gr * BS::GROUP + (r % BIAS_BOX_ROWS) * BS::COLS + (dmin - bias_group_x<BS::ALIGN>(dmin - r, gr)) +
                  (TILE_KEYS - 1);
         }
         float mxv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -538,7 +549,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
           // every key visible, every bucket from the tile's bias rows
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
-            const float sv = fmaf(__uint_as_float(sr[c]), a.sm_scale, brow[-c]);
+            const float sv = fmaf(__uint_as_float(sr[c]), a.sm_scale, to_float(brow[-c]));
             sr[c] = __float_as_uint(sv);
             mxv[c & 3] = fmaxf(mxv[c & 3], sv);
           }
@@ -553,7 +564,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         } else {
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
-            const float bsv = c <= cc ? clampv : brow[-c];
+            const float bsv = c <= cc ? clampv : to_float(brow[-c]);
             const float sv = ((vis >> c) & 1ull) ? fmaf(__uint_as_float(sr[c]), a.sm_scale, bsv) : -INFINITY;
             sr[c] = __float_as_uint(sv);
             mxv[c & 3] = fmaxf(mxv[c & 3], sv);
@@ -564,7 +575,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
           // every bias value this thread read is consumed (mx depends on all of them)
           asm volatile("" ::"f"(mx) : "memory");
           __syncwarp();
-          if (lane == 0) mbar_arrive(&b_empty[wg]);
+          if (lane == 0) mbar_arrive(&b_empty[bslot_i]);
           ++buse;
         }
         const float m_new = fmaxf(m, mx);
@@ -731,24 +742,25 @@ int num_sms_pf() {
   return n;
 }
 
-template <int D>
+template <int D, bool BF>
 cudaError_t launch_prefill_tc_t(const PrefillMaps& m, const PrefillArgs& a, cudaStream_t stream) {
-  constexpr size_t smem = PtSmem<D>::alloc;
+  constexpr size_t smem = PtSmem<D, BF>::alloc;
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  static_assert(PtShape<D>::NV % 2 == 0, "each V slot must serve one softmax warpgroup");
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static_assert(PtShape<D, BF>::NV % 2 == 0, "each V slot must serve one softmax warpgroup");
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long items = (long long)a.num_q_tiles * a.B * a.Hq;
   const int grid = (int)std::min<long long>(items, num_sms_pf());
-  prefill_tc_kernel<D><<<grid, PT_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.q3, m.bias, a);
+  prefill_tc_kernel<D, BF><<<grid, PT_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.q3, m.bias, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PrefillMaps& m, const PrefillArgs& a, int head_dim, cudaStream_t stream) {
-  if (head_dim == 128) return launch_prefill_tc_t<128>(m, a, stream);
-  return launch_prefill_tc_t<64>(m, a, stream);
+  if (a.bias_bf16)
+    return head_dim == 128 ? launch_prefill_tc_t<128, true>(m, a, stream) : launch_prefill_tc_t<64, true>(m, a, stream);
+  return head_dim == 128 ? launch_prefill_tc_t<128, false>(m, a, stream) : launch_prefill_tc_t<64, false>(m, a, stream);
 }
 
 }  // namespace ink

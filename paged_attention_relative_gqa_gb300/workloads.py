@@ -108,7 +108,7 @@ class Problem:
                     cu_q=self.cu_q_lens.cpu().numpy(), seq_lens=self.seq_lens.cpu().numpy(),
                     q_bits=bits(self.q), k_bits=bits(self.k_cache), v_bits=bits(self.v_cache),
                     block_table=self.block_table.cpu().numpy(),
-                    rel=self.rel_logits.detach().cpu().numpy())
+                    rel=self.rel_logits.detach().float().cpu().numpy())
 
 
 def _randn(shape, gen, device, dtype, std=1.0):
@@ -122,8 +122,12 @@ def make_problem(*, num_q_heads: int, num_kv_heads: int, head_dim: int, page_siz
                  rel_extent: int, window: int, q_lens: List[int], seq_lens: List[int],
                  seed: int, device="cpu", sm_scale: Optional[float] = None,
                  extra_page_frac: float = 0.1, max_pages: Optional[int] = None,
-                 rel_std: float = 0.5, nan_spare_pages: bool = True) -> Problem:
-    """Build a seeded problem.  ``q_lens[b]`` new tokens are the last of ``seq_lens[b]``."""
+                 rel_std: float = 0.5, nan_spare_pages: bool = True,
+                 bias_dtype=torch.float32) -> Problem:
+    """Build a seeded problem.  ``q_lens[b]`` new tokens are the last of ``seq_lens[b]``.
+
+    ``bias_dtype=torch.bfloat16`` rounds the same seeded bias to bf16 (the input of the
+    bf16-bias prefill); the oracle then reads those rounded values."""
     assert len(q_lens) == len(seq_lens)
     for n, L in zip(q_lens, seq_lens):
         assert 0 <= n <= L or (L == 0 and n == 0)
@@ -155,7 +159,7 @@ def make_problem(*, num_q_heads: int, num_kv_heads: int, head_dim: int, page_siz
         v_cache[idx] = float("nan")
     total_q = int(sum(q_lens))
     q = _randn((total_q, num_q_heads, head_dim), gen, device, torch.bfloat16)
-    rel = _randn((total_q, num_q_heads, rel_extent), gen, device, torch.float32, std=rel_std)
+    rel = _randn((total_q, num_q_heads, rel_extent), gen, device, bias_dtype, std=rel_std)
     cu = torch.zeros(B + 1, dtype=torch.int32)
     cu[1:] = torch.cumsum(torch.tensor(q_lens, dtype=torch.int64), 0).to(torch.int32)
     return Problem(num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
@@ -206,10 +210,10 @@ def global_decode(device="cpu", seed=3, batch=32) -> Problem:
                         seed=seed, device=device)
 
 
-def global_prefill(device="cpu", seed=4, batch=4, tokens=8192) -> Problem:
+def global_prefill(device="cpu", seed=4, batch=4, tokens=8192, bias_dtype=torch.float32) -> Problem:
     """Global-layer prefill: 4 x 8192 tokens, full causal, E 4096, page 64."""
     return make_problem(**GLOBAL_LAYER, page_size=64, q_lens=[tokens] * batch,
-                        seq_lens=[tokens] * batch, seed=seed, device=device)
+                        seq_lens=[tokens] * batch, seed=seed, device=device, bias_dtype=bias_dtype)
 
 
 def mixed_layer(kind: str, layer: int, device="cpu", seed=5,

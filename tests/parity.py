@@ -40,7 +40,7 @@ def oracle_rows(prob, rows: np.ndarray) -> np.ndarray:
     t = torch.from_numpy(rows[:, 0].astype(np.int64)).to(dev)
     h = torch.from_numpy(rows[:, 1].astype(np.int64)).to(dev)
     q_rows = bits(prob.q[t, h])
-    rel_rows = prob.rel_logits[t, h].cpu().numpy()
+    rel_rows = prob.rel_logits[t, h].float().cpu().numpy()
     return oracle.attention_rows(
         num_q_heads=prob.num_q_heads, num_kv_heads=prob.num_kv_heads, head_dim=prob.head_dim,
         page_size=prob.page_size, rel_extent=prob.rel_extent, window=prob.window,

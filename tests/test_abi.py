@@ -83,6 +83,24 @@ def test_invalid_params_are_rejected_without_launch(lib, bad, code):
     r = lib.inkling_attn_prefill(ctypes.byref(params), fake, fake, 16, 64, fake, fake, fake, fake, fake,
                                  fake, fake, 1 << 30, None)
     assert r == code
+    r = lib.inkling_attn_prefill_bf16bias(ctypes.byref(params), fake, fake, 16, 64, fake, fake, fake, fake,
+                                          fake, fake, fake, 1 << 30, None)
+    assert r == code
+
+
+def test_bf16_bias_prefill_needs_16_byte_bias_rows(lib):
+    ok = ctypes.c_void_p(1 << 20)
+    # E a multiple of 4 but not of 8: bf16 rows are not 16-byte multiples
+    params = good_params(rel_extent=4092)
+    r = lib.inkling_attn_prefill_bf16bias(ctypes.byref(params), ok, ok, 16, 64, ok, ok, ok, ok, ok,
+                                          ok, ok, 1 << 30, None)
+    assert r == 2
+    # bias base 8-byte but not 16-byte aligned (the fp32 entry only needs 4 bytes)
+    params = good_params()
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    r = lib.inkling_attn_prefill_bf16bias(ctypes.byref(params), ok, ok, 16, 64, ok, ok, ok, ok, odd,
+                                          ok, ok, 1 << 30, None)
+    assert r == 5
 
 
 def test_null_and_misaligned_pointers_are_rejected(lib):
