@@ -127,7 +127,7 @@ ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q
  * inkling_attn_prefill with the bias in bf16: rel_logits_bf16 is bf16 [total_q, Hq, E]
  * (same layout as rel_logits), every other argument and result as for
  * inkling_attn_prefill.  The review of _build_rel_logits in "Support Inkling-NVFP4 model"
- * (TensorRT-LLM PR #17062) proposes emitting the bias in bf16 when the kernel accepts
+ * (TensorRT-LLM PR #17062) suggests producing the bias in bf16 where the kernel can take
  * it: on long prompts the fp32 bias is the largest input of the call, and bf16 halves it.
  * The bias enters the scores as exactly the bf16 values given (widened to fp32); the
  * rest of the arithmetic is unchanged.
