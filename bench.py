@@ -256,6 +256,9 @@ WORKLOAD_DESC = {
                             "8 kv heads, head_dim 128, full causal, page 64, bias [2048,64,4096] fp32",
     "mixed": "mixed serving step: 5 SWA + 1 global layer, each one prefill call (8 x 2048 tokens) "
              "and one decode call (128 requests, contexts log-uniform 512..16384)",
+    "mixed_graph": "mixed serving step replayed from one CUDA graph (its 12 calls captured once): 5 SWA + "
+                   "1 global layer, each one prefill call (8 x 2048 tokens) and one decode call (128 "
+                   "requests, contexts log-uniform 512..16384)",
 }
 
 
@@ -279,7 +282,7 @@ def workload_instances(name, dev):
 
 def measure(binding, name, dev, steps, warmup, stream, hbm_peak, bf16_peak):
     """Time one workload; returns a dict of its numbers (value in its own unit)."""
-    if name == "mixed":
+    if name in ("mixed", "mixed_graph"):
         layers = [W.mixed_layer(k, i, dev) for i, k in enumerate(W.MIXED_STACK)]
         calls, keep = [], []
         for pre, dec in layers:
@@ -294,14 +297,24 @@ def measure(binding, name, dev, steps, warmup, stream, hbm_peak, bf16_peak):
             for c in calls:
                 c()
 
-        m = time_steps([mixed_step], steps, warmup, stream)
+        if name == "mixed_graph":
+            with torch.cuda.stream(stream):
+                mixed_step()               # eager once: one-time per-device setup
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                mixed_step()
+            m = time_steps([graph.replay], steps, warmup, stream)
+            del graph
+        else:
+            m = time_steps([mixed_step], steps, warmup, stream)
         per_call = [round(time_steps([c], 3, 1, stream), 4) for c in calls]
         for ws, _ in keep:
             assert binding.inkling_attn_read_device_error(ws) == 0
         # every token of the step passes through all 6 layers once
         ntok = layers[0][0].total_q + layers[0][1].total_q
         return {"ms": m, "value": ntok / m * 1e3, "unit": "tok/s", "tok_s": ntok / m * 1e3,
-                "tokens_per_step": ntok, "launches_per_step": len(calls),
+                "tokens_per_step": ntok, "launches_per_step": len(calls), "graph": name == "mixed_graph",
                 "per_call_ms(prefill,decode)xlayer": per_call}
     probs = workload_instances(name, dev)
     m = bench_workload(binding, probs, steps, warmup, stream)
@@ -364,7 +377,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": args.steps * r["launches_per_step"],
         "clocks": clk,
     }
-    if name != "mixed":
+    if name not in ("mixed", "mixed_graph"):
         decode = "flops" not in r
         src, kernel = ("decode.cu", "decode_persistent_kernel") if decode else ("prefill_tc.cu", "prefill_tc_kernel")
         if r["bound"] == "hbm":
@@ -397,14 +410,15 @@ def run_ours(args, rank, world, local_rank):
         del probs
     else:
         line["e2e"] = None
-        line["mixed"] = {k: v for k, v in r.items() if k not in ("value", "unit")}
+        line[name] = {k: v for k, v in r.items() if k not in ("value", "unit")}
     torch.cuda.empty_cache()
 
     # ---- the other workloads, reported beside the headline
     if not args.no_extra:
         wl = {}
         steps_x = max(5, args.steps // 4)
-        for other in ("global_decode", "swa_prefill_tiny", "global_prefill", "global_prefill_bf16bias", "mixed"):
+        for other in ("global_decode", "swa_prefill_tiny", "global_prefill", "global_prefill_bf16bias", "mixed",
+                      "mixed_graph"):
             if other == name:
                 continue
             st = steps_x if other in ("global_decode", "swa_prefill_tiny") else max(3, steps_x // 2)

@@ -662,16 +662,27 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmKs, const __grid_
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-int num_sms() {
-  static int cached[64] = {};
+}  // namespace
+
+int current_device_sms(int* dev_out) {
+  static std::atomic<int> cached[64] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!cached[dev]) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cached[dev] = n;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  *dev_out = dev;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
+}
+
+namespace {
+
+int num_sms() {
+  int dev = 0;
+  const int n = current_device_sms(&dev);
+  return n > 0 ? n : 148;
 }
 
 template <int D, int NSTAGE, int HB>
@@ -679,8 +690,8 @@ cudaError_t launch_decode_t(const DecodeMaps& m, const DecodeArgs& a, cudaStream
   constexpr size_t smem = DecSmem<D, NSTAGE, HB>::alloc;
   constexpr int ctas = dec_ctas_per_sm<HB>();
   static_assert(smem * ctas <= 228 * 1024 - ctas * 1024, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(decode_persistent_kernel<D, NSTAGE, HB>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<unsigned long long> opted{0};
+  cudaError_t e = smem_opt_in_once(decode_persistent_kernel<D, NSTAGE, HB>, (int)smem, opted);
   if (e != cudaSuccess) return e;
   const long long units = (long long)a.num_splits * a.B * a.Hkv * a.head_chunks;
   const int grid = (int)std::min<long long>(units, (long long)dec_ctas_per_sm<HB>() * num_sms());

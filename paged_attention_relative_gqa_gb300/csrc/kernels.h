@@ -2,6 +2,7 @@
 // and the kernel translation units.
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -56,6 +57,23 @@ struct DecodeMaps {
   CUtensorMap k_grp, v_grp;   // 4-D group view, one box = 1 group of 16 keys (P >= 16)
   CUtensorMap q3;             // 16 query rows, all column blocks in one box
 };
+
+// The current device's id and SM count, looked up once per device (host-only afterwards,
+// so launches stay legal inside CUDA-graph stream capture).
+int current_device_sms(int* dev_out);
+
+// Opt a kernel into `bytes` of dynamic shared memory on the current device, once per
+// device and kernel (the setting persists; repeating it inside stream capture is avoided).
+template <typename Kernel>
+inline cudaError_t smem_opt_in_once(Kernel kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  if (current_device_sms(&dev) <= 0 || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const unsigned long long bit = 1ull << dev;
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& a, int head_dim,
                           cudaStream_t stream);

@@ -736,10 +736,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 }
 
 int num_sms_pf() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
-  return n;
+  int dev = 0;
+  const int n = current_device_sms(&dev);
+  return n > 0 ? n : 148;
 }
 
 template <int D, bool BF>
@@ -747,7 +746,8 @@ cudaError_t launch_prefill_tc_t(const PrefillMaps& m, const PrefillArgs& a, cuda
   constexpr size_t smem = PtSmem<D, BF>::alloc;
   static_assert(smem <= 227 * 1024, "shared memory budget");
   static_assert(PtShape<D, BF>::NV % 2 == 0, "each V slot must serve one softmax warpgroup");
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<unsigned long long> opted{0};
+  cudaError_t e = smem_opt_in_once(prefill_tc_kernel<D, BF>, (int)smem, opted);
   if (e != cudaSuccess) return e;
   const long long items = (long long)a.num_q_tiles * a.B * a.Hq;
   const int grid = (int)std::min<long long>(items, num_sms_pf());
