@@ -75,6 +75,22 @@ def prefill_work(prob):
     return flops, bias + kv + qo
 
 
+def kv_write_bytes(step) -> int:
+    """K/V write: new K and V rows read, the same number of cache rows written, the
+    carried state read and written, the filters, lengths, offsets and the table entries
+    of the pages written."""
+    row = step.num_kv_heads * step.head_dim * 2
+    ks, B, P = step.kernel_size, step.num_seqs, step.page_size
+    total = 2 * step.total_q * row * 2
+    total += 2 * 2 * B * (ks - 1) * row
+    total += 2 * step.num_kv_heads * step.head_dim * ks * 4
+    total += (2 * B + 1) * 4
+    for n, L in zip(step.q_lens, step.seq_lens_list):
+        if n:
+            total += ((L - 1) // P - (L - n) // P + 1) * 4
+    return total
+
+
 # ---------------------------------------------------------------- GPU timing helpers
 
 class Clocks:
@@ -140,6 +156,25 @@ def time_steps(fns, steps, warmup, stream):
         end.record(stream)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / steps
+
+
+def time_flushed(fn, steps, warmup, stream, flush):
+    """Per-call CUDA-event time of `fn` with L2 flushed (a write of `flush`, larger than
+    L2) before every call; returns the mean ms of the calls alone."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.zero_()
+            fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / steps
 
 
 def peaks():
@@ -254,6 +289,10 @@ WORKLOAD_DESC = {
                                "page 64, bias [32768,64,4096] bf16 (clamped)",
     "global_prefill_small": "global_prefill_small (profiling size): 1 x 2048 tokens, 64 q heads / "
                             "8 kv heads, head_dim 128, full causal, page 64, bias [2048,64,4096] fp32",
+    "kv_prefill_global": "K/V short convolution (ks 4) + paged write of a global-layer prefill step: "
+                         "4 fresh prompts x 8192 tokens, 8 kv heads, head_dim 128, page 64",
+    "kv_decode_swa": "K/V short convolution (ks 4) + paged write of an SWA-layer decode step: 64 requests, "
+                     "16 kv heads, head_dim 128, contexts U{1024..8192}, page 64 (L2 flushed before each call)",
     "mixed": "mixed serving step: 5 SWA + 1 global layer, each one prefill call (8 x 2048 tokens) "
              "and one decode call (128 requests, contexts log-uniform 512..16384)",
     "mixed_graph": "mixed serving step replayed from one CUDA graph (its 12 calls captured once): 5 SWA + "
@@ -280,8 +319,43 @@ def workload_instances(name, dev):
     raise ValueError(name)
 
 
+def kv_call(binding, step, dev):
+    """A K/V-write call over `step` into copies of its pools; returns (fn, workspace)."""
+    params = binding.make_params(num_seqs=step.num_seqs, num_q_heads=step.num_kv_heads,
+                                 num_kv_heads=step.num_kv_heads, head_dim=step.head_dim,
+                                 page_size=step.page_size, max_pages_per_seq=step.max_pages,
+                                 num_pages=step.num_pages, rel_extent=1, window=-1, sm_scale=1.0)
+    ws = binding.alloc_workspace(params, False, dev)
+    sk, sv = torch.empty_like(step.state_k), torch.empty_like(step.state_v)
+
+    def fn():
+        binding.inkling_attn_kv_conv_write(params, step.k_new, step.v_new, step.cu_q_lens, step.seq_lens,
+                                           step.block_table, step.w_k, step.w_v, step.state_k, step.state_v,
+                                           sk, sv, step.k_cache, step.v_cache, ws)
+    return fn, ws
+
+
+def measure_kv(binding, name, dev, steps, warmup, stream, hbm_peak):
+    step = W.kv_prefill_global(dev) if name == "kv_prefill_global" else W.kv_decode_swa(dev)
+    fn, ws = kv_call(binding, step, dev)
+    if name == "kv_prefill_global":
+        m = time_steps([fn], steps, warmup, stream)          # 268 MB read + 268 MB written per call > L2
+    else:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        m = time_flushed(fn, steps, warmup, stream, flush)
+        del flush
+    assert binding.inkling_attn_read_device_error(ws) == 0
+    nbytes = kv_write_bytes(step)
+    gbs = nbytes / m / 1e6
+    return {"ms": m, "value": gbs, "unit": "GB/s", "GB/s": gbs, "hbm_frac": gbs / hbm_peak,
+            "tok_s": step.total_q / m * 1e3, "bytes": nbytes, "launches_per_step": 1, "bound": "hbm",
+            "kv_step": step}
+
+
 def measure(binding, name, dev, steps, warmup, stream, hbm_peak, bf16_peak):
     """Time one workload; returns a dict of its numbers (value in its own unit)."""
+    if name.startswith("kv_"):
+        return measure_kv(binding, name, dev, steps, warmup, stream, hbm_peak)
     if name in ("mixed", "mixed_graph"):
         layers = [W.mixed_layer(k, i, dev) for i, k in enumerate(W.MIXED_STACK)]
         calls, keep = [], []
@@ -377,7 +451,17 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": args.steps * r["launches_per_step"],
         "clocks": clk,
     }
-    if name not in ("mixed", "mixed_graph"):
+    if name.startswith("kv_"):
+        step = r.pop("kv_step")
+        line["roofline"] = {"bound": "hbm", "achieved": round(r["GB/s"], 2), "peak": hbm_peak, "unit": "GB/s",
+                            "frac": round(r["GB/s"] / hbm_peak, 4), "peak_source": peak_src,
+                            "traffic": profiled_traffic("kv_conv.cu", name), "algorithmic_bytes": r["bytes"],
+                            "kernel": "kv_conv_write_kernel"}
+        e2e_ms, h2d, d2h = e2e_kv(binding, step, max(5, args.steps // 4), args.warmup, stream)
+        line["e2e"] = {"value": round(r["bytes"] / e2e_ms / 1e6 * world, 2), "unit": "GB/s",
+                       "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del step
+    elif name not in ("mixed", "mixed_graph"):
         decode = "flops" not in r
         src, kernel = ("decode.cu", "decode_persistent_kernel") if decode else ("prefill_tc.cu", "prefill_tc_kernel")
         if r["bound"] == "hbm":
@@ -418,12 +502,14 @@ def run_ours(args, rank, world, local_rank):
         wl = {}
         steps_x = max(5, args.steps // 4)
         for other in ("global_decode", "swa_prefill_tiny", "global_prefill", "global_prefill_bf16bias", "mixed",
-                      "mixed_graph"):
+                      "mixed_graph", "kv_prefill_global", "kv_decode_swa"):
             if other == name:
                 continue
-            st = steps_x if other in ("global_decode", "swa_prefill_tiny") else max(3, steps_x // 2)
+            st = steps_x if other in ("global_decode", "swa_prefill_tiny", "kv_prefill_global",
+                                      "kv_decode_swa") else max(3, steps_x // 2)
             o = measure(binding, other, dev, st, min(args.warmup, 3), stream, hbm_peak, bf16_peak)
             o.pop("probs", None)
+            o.pop("kv_step", None)
             wl[other] = {k: (round(v, 5) if isinstance(v, float) else v) for k, v in o.items()
                          if k not in ("value", "unit", "bound", "launches_per_step")}
             torch.cuda.empty_cache()
@@ -463,6 +549,39 @@ def e2e_prefill(binding, prob, steps, warmup, stream):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size()
     del host, dbuf
+    return ms, h2d, d2h
+
+
+def e2e_kv(binding, step, steps, warmup, stream):
+    """K/V write through the C ABI with host buffers: the step's new K/V rows, state,
+    lengths, offsets and table copied in from pinned memory each step, the new state
+    copied back; the pools are the resident caches."""
+    dev = step.k_new.device
+    keys = ("k_new", "v_new", "state_k", "state_v", "block_table", "seq_lens", "cu_q_lens")
+    host = {k: getattr(step, k).cpu().pin_memory() for k in keys}
+    dbuf = {k: torch.empty_like(getattr(step, k)) for k in keys}
+    params = binding.make_params(num_seqs=step.num_seqs, num_q_heads=step.num_kv_heads,
+                                 num_kv_heads=step.num_kv_heads, head_dim=step.head_dim,
+                                 page_size=step.page_size, max_pages_per_seq=step.max_pages,
+                                 num_pages=step.num_pages, rel_extent=1, window=-1, sm_scale=1.0)
+    ws = binding.alloc_workspace(params, False, dev)
+    sk, sv = torch.empty_like(step.state_k), torch.empty_like(step.state_v)
+    sk_h = torch.empty(sk.shape, dtype=sk.dtype).pin_memory()
+    sv_h = torch.empty(sv.shape, dtype=sv.dtype).pin_memory()
+
+    def one():
+        for k in keys:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        binding.inkling_attn_kv_conv_write(params, dbuf["k_new"], dbuf["v_new"], dbuf["cu_q_lens"],
+                                           dbuf["seq_lens"], dbuf["block_table"], step.w_k, step.w_v,
+                                           dbuf["state_k"], dbuf["state_v"], sk, sv, step.k_cache,
+                                           step.v_cache, ws)
+        sk_h.copy_(sk, non_blocking=True)
+        sv_h.copy_(sv, non_blocking=True)
+
+    ms = time_steps([one], steps, warmup, stream)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = 2 * sk_h.numel() * sk_h.element_size()
     return ms, h2d, d2h
 
 

@@ -71,6 +71,7 @@ typedef enum {
 #define INK_DEVERR_QLEN_EXCEEDS_KV   0x2u  /* cu_q_lens gives more new tokens than seq_lens */
 #define INK_DEVERR_WAIT_TIMEOUT      0x4u  /* a bounded wait on a copy ran out */
 #define INK_DEVERR_QLEN_EXCEEDS_MAX  0x8u  /* a sequence has more new tokens than max_q_len */
+#define INK_DEVERR_BAD_ROWS          0x10u /* cu_q_lens names rows outside [0, total_q) */
 
 /* Per-call shape and layer scalars.  All sizes are element counts. */
 typedef struct {
@@ -185,6 +186,51 @@ ink_status_t inkling_attn_decode_noalloc(const ink_attn_params_t* params, const 
                                          const void* k_cache, const void* v_cache,
                                          const int32_t* block_table, const int32_t* seq_lens,
                                          const float* rel_logits, void* out, void* stream);
+
+/*
+ * The step's K/V write: causal short convolution of the new K and V rows, written into
+ * the paged caches, and the convolution state carried to the next step.
+ * "Support Inkling-NVFP4 model" (TensorRT-LLM PR #17062), section "Architecture": every
+ * attention layer runs a causal short convolution over K and over V, with per-request
+ * state between steps.  "Inkling attn backend cleanup fake registry" (TensorRT-LLM PR
+ * #17860): the state is a window of kernel_size - 1 past inputs per request, carried with
+ * the request; the backend itself writes the step's K/V into the paged cache through the
+ * block table.  Neither page gives the kernel size, a bias or an activation: the
+ * convolution here is depthwise (one filter per channel), without bias or activation.
+ * For request b with n_b = cu_q_lens[b+1] - cu_q_lens[b] new rows and L_b = seq_lens[b]
+ * (history including them), new row i sits at position p = L_b - n_b + i, and for each
+ * channel c = (g, d) of K (and likewise of V)
+ *     y[p, c] = sum_{j=0}^{ks-1} w_k[g, d, j] * x[p - (ks-1) + j, c]
+ * where x at the ks - 1 positions before the first new row is state_k_in[b] (oldest
+ * first).  y is computed in fp32 and stored rounded to bf16 (nearest even) at
+ * k_cache[block_table[b][p / P], g, p % P, :].  state_k_out[b] receives the last ks - 1
+ * rows of (state_k_in[b], new rows of b), unconvolved.
+ *   k_new, v_new          device, bf16 [total_q, Hkv, D], rows packed by request
+ *   cu_q_lens             device, int32 [B+1], cu_q_lens[0] = 0, cu_q_lens[B] = total_q
+ *   seq_lens, block_table device, as for inkling_attn_prefill
+ *   w_k, w_v              device, fp32 [Hkv, D, kernel_size] (a depthwise Conv1d weight over
+ *                         the Hkv*D channels), 16-byte aligned
+ *   kernel_size           1..8 (else INK_ERR_BAD_SHAPE); 1 stores x * w unshifted
+ *   state_*_in/out        device, bf16 [B, kernel_size - 1, Hkv, D]; unused (may be NULL)
+ *                         when kernel_size == 1.  Outputs must not overlap inputs; a fresh
+ *                         request passes zero rows.
+ *   k_cache, v_cache      device, bf16 [num_pages, Hkv, P, D]; only the slots of the step's
+ *                         positions are written
+ *   workspace             device, >= inkling_attn_workspace_bytes(params, 0) (error word)
+ * Only num_seqs, num_kv_heads, head_dim, page_size, max_pages_per_seq and num_pages of
+ * params are used; the rest must still be valid.  Device-side checks: a request with
+ * n_b > L_b (INK_DEVERR_QLEN_EXCEEDS_KV) or a page id outside [0, num_pages)
+ * (INK_DEVERR_PAGE_OUT_OF_RANGE) has those rows skipped; rows named outside [0, total_q)
+ * set INK_DEVERR_BAD_ROWS.  Stream-ordered, no allocation: capturable in a CUDA graph.
+ */
+ink_status_t inkling_attn_kv_conv_write(const ink_attn_params_t* params, const void* k_new,
+                                        const void* v_new, const int32_t* cu_q_lens, int32_t total_q,
+                                        const int32_t* seq_lens, const int32_t* block_table,
+                                        const float* w_k, const float* w_v, int32_t kernel_size,
+                                        const void* state_k_in, const void* state_v_in,
+                                        void* state_k_out, void* state_v_out, void* k_cache,
+                                        void* v_cache, void* workspace, size_t workspace_bytes,
+                                        void* stream);
 
 /*
  * Synchronise `stream`, copy the sticky device error word (INK_DEVERR_* bits) to

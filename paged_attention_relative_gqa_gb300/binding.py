@@ -25,10 +25,11 @@ DEVERR_PAGE_OUT_OF_RANGE = 0x1
 DEVERR_QLEN_EXCEEDS_KV = 0x2
 DEVERR_WAIT_TIMEOUT = 0x4
 DEVERR_QLEN_EXCEEDS_MAX = 0x8
+DEVERR_BAD_ROWS = 0x10
 
 EXPORTED_SYMBOLS = ("inkling_attn_workspace_bytes", "inkling_attn_workspace_init",
                     "inkling_attn_prefill", "inkling_attn_prefill_bf16bias", "inkling_attn_decode",
-                    "inkling_attn_decode_noalloc",
+                    "inkling_attn_decode_noalloc", "inkling_attn_kv_conv_write",
                     "inkling_attn_read_device_error", "inkling_attn_status_string",
                     "inkling_attn_version")
 
@@ -75,6 +76,8 @@ def load_library(path: Optional[str] = None):
     lib.inkling_attn_decode.restype = ctypes.c_int
     lib.inkling_attn_decode_noalloc.argtypes = [PP, V, V, V, V, V, V, V, V]
     lib.inkling_attn_decode_noalloc.restype = ctypes.c_int
+    lib.inkling_attn_kv_conv_write.argtypes = [PP, V, V, V, I32, V, V, V, V, I32, V, V, V, V, V, V, V, S, V]
+    lib.inkling_attn_kv_conv_write.restype = ctypes.c_int
     lib.inkling_attn_read_device_error.argtypes = [V, S, V, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
     lib.inkling_attn_read_device_error.restype = ctypes.c_int
     lib.inkling_attn_status_string.argtypes = [ctypes.c_int]
@@ -193,6 +196,33 @@ def inkling_attn_decode_noalloc(params, q, k_cache, v_cache, block_table, seq_le
         _dev(out, "out", torch.bfloat16), _stream_handle(stream))
     _check(code, "inkling_attn_decode_noalloc")
     return out
+
+
+def inkling_attn_kv_conv_write(params, k_new, v_new, cu_q_lens, seq_lens, block_table, w_k, w_v,
+                               state_k_in, state_v_in, state_k_out, state_v_out, k_cache, v_cache,
+                               workspace, stream=None):
+    """Causal short convolution of the step's K/V rows into the paged caches, and the
+    carried state; ``kernel_size`` is the last dimension of ``w_k``.  With kernel size 1
+    the state tensors may be None."""
+    lib = load_library()
+    ks = int(w_k.shape[-1])
+    if tuple(w_v.shape) != tuple(w_k.shape):
+        raise ValueError("w_k and w_v must have the same shape")
+
+    def opt(t, name):
+        return None if t is None else _dev(t, name, torch.bfloat16)
+
+    code = lib.inkling_attn_kv_conv_write(
+        ctypes.byref(params), _dev(k_new, "k_new", torch.bfloat16), _dev(v_new, "v_new", torch.bfloat16),
+        _dev(cu_q_lens, "cu_q_lens", torch.int32), int(k_new.shape[0]),
+        _dev(seq_lens, "seq_lens", torch.int32), _dev(block_table, "block_table", torch.int32),
+        _dev(w_k, "w_k", torch.float32), _dev(w_v, "w_v", torch.float32), ks,
+        opt(state_k_in, "state_k_in"), opt(state_v_in, "state_v_in"),
+        opt(state_k_out, "state_k_out"), opt(state_v_out, "state_v_out"),
+        _dev(k_cache, "k_cache", torch.bfloat16), _dev(v_cache, "v_cache", torch.bfloat16),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream_handle(stream))
+    _check(code, "inkling_attn_kv_conv_write")
+    return k_cache, v_cache
 
 
 def inkling_attn_read_device_error(workspace: torch.Tensor, stream=None, clear: bool = True) -> int:

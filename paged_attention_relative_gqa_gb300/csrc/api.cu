@@ -397,4 +397,62 @@ ink_status_t inkling_attn_prefill_bf16bias(const ink_attn_params_t* params, cons
                       rel_logits_bf16, true, out, workspace, workspace_bytes, stream);
 }
 
+ink_status_t inkling_attn_kv_conv_write(const ink_attn_params_t* params, const void* k_new,
+                                        const void* v_new, const int32_t* cu_q_lens, int32_t total_q,
+                                        const int32_t* seq_lens, const int32_t* block_table,
+                                        const float* w_k, const float* w_v, int32_t kernel_size,
+                                        const void* state_k_in, const void* state_v_in,
+                                        void* state_k_out, void* state_v_out, void* k_cache,
+                                        void* v_cache, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  ink_status_t st = validate(params);
+  if (st != INK_OK) return st;
+  if (kernel_size < 1 || kernel_size > 8 || total_q < 0) return INK_ERR_BAD_SHAPE;
+  const bool has_state = kernel_size > 1;
+  if (!k_new || !v_new || !cu_q_lens || !seq_lens || !block_table || !w_k || !w_v || !k_cache ||
+      !v_cache || !workspace)
+    return INK_ERR_NULL_PTR;
+  if (has_state && (!state_k_in || !state_v_in || !state_k_out || !state_v_out)) return INK_ERR_NULL_PTR;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(w_k, 16) || !aligned(w_v, 16) || !aligned(cu_q_lens, 4) || !aligned(seq_lens, 4) ||
+      !aligned(block_table, 4) || !aligned(workspace, 256))
+    return INK_ERR_ALIGNMENT;
+  if (has_state && (!aligned(state_k_in, 16) || !aligned(state_v_in, 16) || !aligned(state_k_out, 16) ||
+                    !aligned(state_v_out, 16)))
+    return INK_ERR_ALIGNMENT;
+  if (workspace_bytes < kHeaderBytes) return INK_ERR_WORKSPACE;
+  const int nvec = params->num_kv_heads * params->head_dim / 8;
+  if ((long long)total_q * nvec * 8 >= (1ll << 40)) return INK_ERR_TOO_LARGE;
+  ink::KvConvArgs a;
+  a.x[0] = static_cast<const uint16_t*>(k_new);
+  a.x[1] = static_cast<const uint16_t*>(v_new);
+  a.w[0] = w_k;
+  a.w[1] = w_v;
+  a.st_in[0] = static_cast<const uint16_t*>(state_k_in);
+  a.st_in[1] = static_cast<const uint16_t*>(state_v_in);
+  a.st_out[0] = static_cast<uint16_t*>(state_k_out);
+  a.st_out[1] = static_cast<uint16_t*>(state_v_out);
+  a.cache[0] = static_cast<uint16_t*>(k_cache);
+  a.cache[1] = static_cast<uint16_t*>(v_cache);
+  a.cu_q = cu_q_lens;
+  a.seq_lens = seq_lens;
+  a.block_table = block_table;
+  a.err = reinterpret_cast<uint32_t*>(workspace);
+  a.B = params->num_seqs;
+  a.T = total_q;
+  a.Hkv = params->num_kv_heads;
+  a.D = params->head_dim;
+  a.log2_page = ilog2(params->page_size);
+  a.max_pages = params->max_pages_per_seq;
+  a.num_pages = params->num_pages;
+  a.nvec = nvec;
+  a.tok = ink::kv_conv_tokens_per_thread(total_q, nvec);
+  a.nchunks = (total_q + a.tok - 1) / a.tok;
+  a.conv_items = 2ll * a.nchunks * nvec;
+  a.state_items = has_state ? 2ll * a.B * (kernel_size - 1) * nvec : 0;
+  if ((a.conv_items + a.state_items + 255) / 256 >= (1ll << 31)) return INK_ERR_TOO_LARGE;
+  if (ink::launch_kv_conv(a, kernel_size, (cudaStream_t)stream) != cudaSuccess) return INK_ERR_CUDA;
+  return INK_OK;
+}
+
 }  // extern "C"

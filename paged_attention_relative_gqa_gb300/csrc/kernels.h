@@ -95,4 +95,27 @@ constexpr int PREFILL_ROWS = 128;        // new tokens per prefill work item
 cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int head_dim,
                               cudaStream_t stream);
 
+// One call of the K/V short convolution and paged write (kv_conv.cu).  Rows of the
+// step's K/V and of the carried state are Hkv*D bf16 (nvec 16-byte vectors).
+struct KvConvArgs {
+  const uint16_t* x[2];        // k_new, v_new: bf16 [T, Hkv, D]
+  const float* w[2];           // taps: fp32 [Hkv, D, ks]
+  const uint16_t* st_in[2];    // bf16 [B, ks-1, Hkv, D], oldest row first
+  uint16_t* st_out[2];         // same layout, never overlapping st_in
+  uint16_t* cache[2];          // bf16 [num_pages, Hkv, P, D]
+  const int32_t* cu_q;         // [B+1]
+  const int32_t* seq_lens;     // [B]
+  const int32_t* block_table;  // [B, max_pages]
+  uint32_t* err;
+  int B, T, Hkv, D, log2_page, max_pages, num_pages;
+  int nvec;                    // Hkv * D / 8
+  int tok;                     // tokens per thread (1 or 8)
+  int nchunks;                 // ceil(T / tok)
+  long long conv_items;        // 2 * nchunks * nvec threads of convolution
+  long long state_items;       // 2 * B * (ks-1) * nvec threads of state copy
+};
+
+int kv_conv_tokens_per_thread(long long total_q, int nvec);
+cudaError_t launch_kv_conv(const KvConvArgs& a, int kernel_size, cudaStream_t stream);
+
 }  // namespace ink

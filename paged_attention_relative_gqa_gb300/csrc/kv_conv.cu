@@ -1,0 +1,241 @@
+// kv_conv.cu -- the step before attention: the causal short convolution of the step's K
+// and V rows, written into the paged K/V cache, and the convolution state carried to the
+// next step.
+//
+// Operation ("Support Inkling-NVFP4 model", TensorRT-LLM PR #17062, section
+// "Architecture"; the state and the in-backend KV write from the commits of "Inkling attn
+// backend cleanup fake registry", TensorRT-LLM PR #17860): per channel (g, d) of each of K
+// and V, with x the raw projection rows of a request in position order,
+//     y[p] = sum_{j < ks} w[g, d, j] * x[p - (ks - 1) + j]
+// where the ks - 1 rows before the step's first new token come from the carried state.
+// y goes to cache[block_table[b][p / P], g, p % P, :] rounded to bf16; the new state is
+// the last ks - 1 raw rows of (state, new rows).
+//
+// The work is pure streaming: every input row is read once from HBM and every output row
+// written once, so the kernel is HBM-bound.  One thread owns one 16-byte vector (8
+// channels) of either K or V over a run of TOK consecutive tokens: it loads its TOK rows
+// up front (TOK independent 16-byte loads in flight), keeps the last ks - 1 rows of the
+// run in registers as a sliding window, and reloads the window only where a run starts or
+// crosses into the next request.  Consecutive threads take consecutive vectors of a row,
+// so every load and store of a warp is 512 contiguous bytes of one row (or 256 bytes per
+// KV head in the cache).  A second set of threads in the same launch copies the carried
+// state rows.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ink {
+namespace {
+
+constexpr int KV_CONV_THREADS = 256;
+
+__device__ __forceinline__ uint4 ld_row16(const uint16_t* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ void unpack8(const uint4 r, float (&f)[8]) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Index b of the request that owns packed token t: the last b with cu_q[b] <= t.
+// Returns -1 when t lies before cu_q[0] or at/after cu_q[B].
+__device__ __forceinline__ int find_seq(const int32_t* cu_q, int B, int t) {
+  if (B <= 0 || t < __ldg(cu_q) || t >= __ldg(cu_q + B)) return -1;
+  int lo = 0, hi = B;   // cu_q[lo] <= t < cu_q[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(cu_q + mid) <= t) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+template <int KS, int TOK>
+__global__ void __launch_bounds__(KV_CONV_THREADS, 2) kv_conv_write_kernel(const KvConvArgs a) {
+  const long long gid = (long long)blockIdx.x * KV_CONV_THREADS + threadIdx.x;
+  const int row_elems = a.nvec * 8;
+  if (gid < a.conv_items) {
+    // ---------------------------------------------------------------- convolution
+    const int v = (int)(gid % a.nvec);
+    const long long rest = gid / a.nvec;
+    const int chunk = (int)(rest % a.nchunks);
+    const int z = (int)(rest / a.nchunks);          // 0: K, 1: V
+    const uint16_t* __restrict__ x = a.x[z];
+    uint16_t* __restrict__ cache = a.cache[z];
+    const int col = v * 8;                           // element offset inside a row
+    const int g = col / a.D, d = col % a.D;
+    const int t0 = chunk * TOK;
+
+    // this run's raw rows, loaded first so that TOK loads are in flight together
+    uint4 raw[TOK];
+#pragma unroll
+    for (int k = 0; k < TOK; ++k) {
+      const int t = t0 + k;
+      raw[k] = t < a.T ? ld_row16(x + (size_t)t * row_elems + col) : make_uint4(0, 0, 0, 0);
+    }
+    // taps of these 8 channels: w[g, d + e, j] at ((g*D + d + e) * KS + j)
+    float w[KS][8];
+    {
+      const float4* wp = reinterpret_cast<const float4*>(a.w[z] + (size_t)(g * a.D + d) * KS);
+      float flat[8 * KS];
+#pragma unroll
+      for (int q = 0; q < 2 * KS; ++q) {
+        const float4 f = __ldg(wp + q);
+        flat[4 * q] = f.x; flat[4 * q + 1] = f.y; flat[4 * q + 2] = f.z; flat[4 * q + 3] = f.w;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+#pragma unroll
+        for (int j = 0; j < KS; ++j) w[j][e] = flat[e * KS + j];
+    }
+
+    float win[KS > 1 ? KS - 1 : 1][8];   // rows at positions p - (KS-1) .. p - 1
+    // The run is cut at request boundaries into segments [k, k_end); each segment loads
+    // its request's scalars and window once, then convolves its tokens.
+    int k = 0;
+    while (k < TOK && t0 + k < a.T) {
+      const int t = t0 + k;
+      const int b = find_seq(a.cu_q, a.B, t);
+      if (b < 0) {                                    // token outside every request
+        record_error(a.err, INK_DEVERR_BAD_ROWS);
+        ++k;
+        continue;
+      }
+      const int seq_start = __ldg(a.cu_q + b);
+      const int seq_end = __ldg(a.cu_q + b + 1);
+      const int k_end = min(TOK, seq_end - t0);
+      if (seq_start < 0) {                            // request rows named before row 0
+        record_error(a.err, INK_DEVERR_BAD_ROWS);
+        k = k_end;
+        continue;
+      }
+      const int n = seq_end - seq_start;
+      const int L = __ldg(a.seq_lens + b);
+      const bool seq_ok = n <= L;
+      if (!seq_ok) record_error(a.err, INK_DEVERR_QLEN_EXCEEDS_KV);
+      const int i0 = t - seq_start;                   // index of token t among the request's new rows
+#pragma unroll
+      for (int m = 0; m < KS - 1; ++m) {
+        const int r = i0 - (KS - 1) + m;              // row of the new rows, or of the state if < 0
+        const uint16_t* src = r >= 0 ? x + (size_t)(seq_start + r) * row_elems + col
+                                     : a.st_in[z] + ((size_t)b * (KS - 1) + (KS - 1 + r)) * row_elems + col;
+        unpack8(ld_row16(src), win[m]);
+      }
+      const int pos_t0 = L - n - seq_start + t0;      // position of run token 0 if it were in b
+      const int* bt_row = a.block_table + (size_t)b * a.max_pages;
+#pragma unroll
+      for (int kk = 0; kk < TOK; ++kk) {
+        if (kk < k || kk >= k_end) continue;
+        float cur[8];
+        unpack8(raw[kk], cur);
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float s = 0.f;
+#pragma unroll
+          for (int j = 0; j < KS - 1; ++j) s = fmaf(w[j][e], win[j][e], s);
+          y[e] = fmaf(w[KS - 1][e], cur[e], s);
+        }
+#pragma unroll
+        for (int m = 0; m + 1 < KS - 1; ++m)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) win[m][e] = win[m + 1][e];
+        if constexpr (KS > 1) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) win[KS - 2][e] = cur[e];
+        }
+        if (!seq_ok) continue;
+        const int p = pos_t0 + kk;
+        const int pidx = p >> a.log2_page;
+        const int page = pidx < a.max_pages ? __ldg(bt_row + pidx) : -1;
+        if (page < 0 || page >= a.num_pages) {
+          record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
+          continue;
+        }
+        const size_t slot = (((size_t)page * a.Hkv + g) << a.log2_page) + (p & ((1 << a.log2_page) - 1));
+        *reinterpret_cast<uint4*>(cache + slot * a.D + d) = pack8(y);
+      }
+      k = k_end;
+    }
+    return;
+  }
+  if constexpr (KS > 1) {
+    if (gid >= a.conv_items + a.state_items) return;
+    // ---------------------------------------------------------------- carried state
+    const long long sid = gid - a.conv_items;
+    const int v = (int)(sid % a.nvec);
+    long long rest = sid / a.nvec;
+    const int r = (int)(rest % (KS - 1));
+    rest /= (KS - 1);
+    const int b = (int)(rest % a.B);
+    const int z = (int)(rest / a.B);
+    const int col = v * 8;
+    const int seq_start = __ldg(a.cu_q + b);
+    const int n = max(__ldg(a.cu_q + b + 1) - seq_start, 0);
+    uint4 row = make_uint4(0, 0, 0, 0);
+    if (r + n < KS - 1) {
+      row = ld_row16(a.st_in[z] + ((size_t)b * (KS - 1) + (r + n)) * row_elems + col);
+    } else {
+      const int t = seq_start + r + n - (KS - 1);
+      if (t >= 0 && t < a.T) row = ld_row16(a.x[z] + (size_t)t * row_elems + col);
+      else record_error(a.err, INK_DEVERR_BAD_ROWS);
+    }
+    *reinterpret_cast<uint4*>(a.st_out[z] + ((size_t)b * (KS - 1) + r) * row_elems + col) = row;
+  }
+}
+
+template <int KS>
+cudaError_t launch_ks(const KvConvArgs& a, int tok, cudaStream_t stream) {
+  const long long items = a.conv_items + a.state_items;
+  const unsigned blocks = (unsigned)((items + KV_CONV_THREADS - 1) / KV_CONV_THREADS);
+  if (tok == 8) kv_conv_write_kernel<KS, 8><<<blocks, KV_CONV_THREADS, 0, stream>>>(a);
+  else kv_conv_write_kernel<KS, 1><<<blocks, KV_CONV_THREADS, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int kv_conv_tokens_per_thread(long long total_q, int nvec) {
+  // Runs of 8 tokens amortise the window reload and keep 8 loads in flight per thread,
+  // but leave few threads when the step has few tokens (decode: one token per request,
+  // where every token also starts a new request); there one token per thread keeps the
+  // GPU's threads busy instead.
+  const long long threads_at_8 = 2ll * nvec * ((total_q + 7) / 8);
+  return threads_at_8 >= 152ll * 1024 ? 8 : 1;
+}
+
+cudaError_t launch_kv_conv(const KvConvArgs& a, int kernel_size, cudaStream_t stream) {
+  const int tok = a.tok;
+  if (tok != 1 && tok != 8) return cudaErrorInvalidValue;
+  if (a.conv_items + a.state_items <= 0) return cudaSuccess;
+  switch (kernel_size) {
+    case 1: return launch_ks<1>(a, tok, stream);
+    case 2: return launch_ks<2>(a, tok, stream);
+    case 3: return launch_ks<3>(a, tok, stream);
+    case 4: return launch_ks<4>(a, tok, stream);
+    case 5: return launch_ks<5>(a, tok, stream);
+    case 6: return launch_ks<6>(a, tok, stream);
+    case 7: return launch_ks<7>(a, tok, stream);
+    case 8: return launch_ks<8>(a, tok, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ink

@@ -244,6 +244,130 @@ WORKLOADS = {
 }
 
 
+@dataclasses.dataclass
+class KvStep:
+    """One call of the K/V short convolution and paged write: the step's raw K/V rows,
+    the filters, the carried state, and the paged pools they are written into."""
+
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    kernel_size: int
+    q_lens: List[int]
+    seq_lens_list: List[int]
+    k_new: torch.Tensor        # [T, Hkv, D] bf16
+    v_new: torch.Tensor
+    w_k: torch.Tensor          # [Hkv, D, ks] fp32
+    w_v: torch.Tensor
+    state_k: torch.Tensor      # [B, ks-1, Hkv, D] bf16, oldest row first
+    state_v: torch.Tensor
+    k_cache: torch.Tensor      # [num_pages, Hkv, P, D] bf16
+    v_cache: torch.Tensor
+    block_table: torch.Tensor  # [B, max_pages] int32
+    seq_lens: torch.Tensor     # [B] int32
+    cu_q_lens: torch.Tensor    # [B + 1] int32
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.seq_lens_list)
+
+    @property
+    def total_q(self) -> int:
+        return int(sum(self.q_lens))
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_cache.shape[0])
+
+    @property
+    def max_pages(self) -> int:
+        return int(self.block_table.shape[1])
+
+    def oracle_kwargs(self) -> Dict:
+        def bits(t):
+            return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+        return dict(k_new_bits=bits(self.k_new), v_new_bits=bits(self.v_new),
+                    cu_q=self.cu_q_lens.cpu().numpy(), seq_lens=self.seq_lens.cpu().numpy(),
+                    block_table=self.block_table.cpu().numpy(), page_size=self.page_size,
+                    w_k=self.w_k.double().cpu().numpy(), w_v=self.w_v.double().cpu().numpy(),
+                    ks=self.kernel_size, state_k_bits=bits(self.state_k), state_v_bits=bits(self.state_v),
+                    k_cache_bits=bits(self.k_cache), v_cache_bits=bits(self.v_cache))
+
+
+def make_kv_step(*, num_kv_heads: int, head_dim: int, page_size: int, kernel_size: int,
+                 q_lens: List[int], seq_lens: List[int], seed: int, device="cpu",
+                 extra_page_frac: float = 0.1) -> KvStep:
+    """Seeded inputs of one K/V write.  Recipe: new K/V rows and the pools' old contents
+    bf16 N(0,1) (spare pages NaN, so a write to a page that is not the request's own
+    is visible); filters fp32 N(0, 1/ks); carried state bf16 N(0,1), except that a
+    request whose step holds its whole history (n_b == L_b) starts from zero rows;
+    pages placed at random, block-table tails num_pages + 7 as in ``make_problem``."""
+    assert len(q_lens) == len(seq_lens)
+    for n, L in zip(q_lens, seq_lens):
+        assert 0 <= n <= L
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    host_gen = torch.Generator()
+    host_gen.manual_seed(seed + 2_000_003)
+    B, Hkv, D, P, ks = len(seq_lens), num_kv_heads, head_dim, page_size, kernel_size
+    pages_per_seq = [(L + P - 1) // P for L in seq_lens]
+    used = sum(pages_per_seq)
+    num_pages = used + max(1, int(math.ceil(extra_page_frac * used)))
+    width = max(pages_per_seq + [1])
+    perm = torch.randperm(num_pages, generator=host_gen)
+    bt = torch.full((B, width), num_pages + TAIL_PAGE_OFFSET, dtype=torch.int32)
+    cur = 0
+    for b, npg in enumerate(pages_per_seq):
+        bt[b, :npg] = perm[cur:cur + npg].to(torch.int32)
+        cur += npg
+    spare_ids = perm[cur:].to(device)
+    pool = (num_pages, Hkv, P, D)
+    k_cache = _randn(pool, gen, device, torch.bfloat16)
+    v_cache = _randn(pool, gen, device, torch.bfloat16)
+    if spare_ids.numel():
+        k_cache[spare_ids] = float("nan")
+        v_cache[spare_ids] = float("nan")
+    T = int(sum(q_lens))
+    k_new = _randn((T, Hkv, D), gen, device, torch.bfloat16)
+    v_new = _randn((T, Hkv, D), gen, device, torch.bfloat16)
+    w_k = _randn((Hkv, D, ks), gen, device, torch.float32, std=1.0 / math.sqrt(ks))
+    w_v = _randn((Hkv, D, ks), gen, device, torch.float32, std=1.0 / math.sqrt(ks))
+    state_k = _randn((B, ks - 1, Hkv, D), gen, device, torch.bfloat16)
+    state_v = _randn((B, ks - 1, Hkv, D), gen, device, torch.bfloat16)
+    fresh = [b for b, (n, L) in enumerate(zip(q_lens, seq_lens)) if n == L]
+    if fresh and ks > 1:
+        idx = torch.tensor(fresh, device=device)
+        state_k[idx] = 0
+        state_v[idx] = 0
+    cu = torch.zeros(B + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(q_lens, dtype=torch.int64), 0).to(torch.int32)
+    return KvStep(num_kv_heads=Hkv, head_dim=D, page_size=P, kernel_size=ks, q_lens=list(q_lens),
+                  seq_lens_list=list(seq_lens), k_new=k_new, v_new=v_new, w_k=w_k, w_v=w_v,
+                  state_k=state_k, state_v=state_v, k_cache=k_cache, v_cache=v_cache,
+                  block_table=bt.to(device), seq_lens=torch.tensor(seq_lens, dtype=torch.int32, device=device),
+                  cu_q_lens=cu.to(device))
+
+
+# Short-convolution kernel size of the K/V write workloads: the pages give none; 4 is the
+# usual width of a causal short convolution in hybrid models.
+KV_CONV_KERNEL = 4
+
+
+def kv_prefill_global(device="cpu", seed=6, batch=4, tokens=8192) -> KvStep:
+    """K/V write of a global-layer prefill: 4 fresh prompts of 8192 tokens, 8 KV heads."""
+    return make_kv_step(num_kv_heads=GLOBAL_LAYER["num_kv_heads"], head_dim=128, page_size=64,
+                        kernel_size=KV_CONV_KERNEL, q_lens=[tokens] * batch, seq_lens=[tokens] * batch,
+                        seed=seed, device=device)
+
+
+def kv_decode_swa(device="cpu", seed=7, batch=64) -> KvStep:
+    """K/V write of an SWA-layer decode step: 64 requests, contexts U{1024..8192}."""
+    L = _uniform_lengths(batch, 1024, 8192, seed)
+    return make_kv_step(num_kv_heads=SWA_LAYER["num_kv_heads"], head_dim=128, page_size=64,
+                        kernel_size=KV_CONV_KERNEL, q_lens=[1] * batch, seq_lens=L, seed=seed, device=device)
+
+
 def sample_rows(prob: Problem, per_seq: int, seed: int) -> np.ndarray:
     """A seeded sample of (packed row, head) pairs for oracle checks on big problems.
 

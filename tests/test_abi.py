@@ -132,3 +132,34 @@ def test_binding_refuses_cpu_tensors(lib):
         binding.inkling_attn_decode(binding.params_of(prob), prob.q, prob.k_cache, prob.v_cache,
                                     prob.block_table, prob.seq_lens, prob.rel_logits,
                                     torch.empty_like(prob.q), torch.empty(256, dtype=torch.uint8))
+
+
+def _kv_call(lib, params, ks=4, *, k_new=None, w=None, st=None, ws_bytes=1 << 30, total_q=64):
+    ok = ctypes.c_void_p(1 << 20)
+    k_new = ok if k_new is None else k_new
+    w = ok if w is None else w
+    st = ok if st is None else st
+    return lib.inkling_attn_kv_conv_write(ctypes.byref(params), k_new, ok, ok, total_q, ok, ok, w, ok, ks,
+                                          st, ok, ok, ok, ok, ok, ok, ws_bytes, None)
+
+
+def test_kv_conv_write_rejects_bad_arguments_without_launch(lib):
+    params = good_params()
+    assert _kv_call(lib, params, ks=0) == 2                      # kernel size below 1
+    assert _kv_call(lib, params, ks=9) == 2                      # kernel size above 8
+    assert _kv_call(lib, params, total_q=-1) == 2
+    assert _kv_call(lib, params, k_new=ctypes.c_void_p(0)) == 1  # NULL input rows
+    assert _kv_call(lib, params, st=ctypes.c_void_p(0)) == 1     # NULL state with ks > 1
+    assert _kv_call(lib, params, k_new=ctypes.c_void_p((1 << 20) + 2)) == 5
+    assert _kv_call(lib, params, w=ctypes.c_void_p((1 << 20) + 4)) == 5    # filters need 16 bytes
+    assert _kv_call(lib, params, st=ctypes.c_void_p((1 << 20) + 8)) == 5
+    assert _kv_call(lib, params, ws_bytes=16) == 4
+    assert _kv_call(lib, good_params(head_dim=96)) == 2
+    assert _kv_call(lib, good_params(page_size=12)) == 3
+
+
+def test_kv_conv_write_kernel_size_one_needs_no_state(lib):
+    """ks == 1 has no state: NULL state pointers pass validation; total_q == 0 launches
+    nothing (B = 0 rows of state are also nothing), so the call returns without a GPU."""
+    params = good_params(num_seqs=0)
+    assert _kv_call(lib, params, ks=1, st=ctypes.c_void_p(0), total_q=0) == 0
