@@ -54,40 +54,66 @@ def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def kv_conv_rows(*, x_bits, cu_q, seq_lens, block_table, page_size, w, ks, state_bits):
+    """The convolution of one of K or V, row by row, before any rounding.
+
+    Returns (y, mag, page, slot, state_out): y[t] the fp64 value of new row t
+    ([T, Hkv, D]); mag[t] = sum_j |w[., ., j] * x_j| of its terms (the scale of the
+    rounding error of any finite-precision sum of them); page[t], slot[t] the cache slot it
+    goes to (page -1 for rows of no request); state_out the carried state [B, ks - 1, Hkv, D]
+    (bf16 bits).
+    """
+    T, Hkv, D = x_bits.shape
+    B = len(seq_lens)
+    w = np.asarray(w, np.float64)
+    y_all = np.zeros((T, Hkv, D), np.float64)
+    mag_all = np.zeros((T, Hkv, D), np.float64)
+    page_of = np.full(T, -1, np.int64)
+    slot_of = np.full(T, -1, np.int64)
+    st_out = np.zeros((B, max(ks - 1, 0), Hkv, D), np.uint16)
+    for b in range(B):
+        t0, t1 = int(cu_q[b]), int(cu_q[b + 1])
+        n, L = t1 - t0, int(seq_lens[b])
+        x_new = bf16_bits_to_f64(x_bits[t0:t1])                       # [n, Hkv, D]
+        st_bits = state_bits
+        prev = bf16_bits_to_f64(st_bits[b]) if ks > 1 else np.zeros((0, Hkv, D))
+        hist = np.concatenate([prev, x_new], axis=0)                  # [ks - 1 + n, Hkv, D]
+        for i in range(n):
+            p = L - n + i
+            # window rows hist[i .. i + ks - 1] are positions p - (ks - 1) .. p
+            y = np.zeros((Hkv, D), np.float64)
+            mag = np.zeros((Hkv, D), np.float64)
+            for j in range(ks):
+                y += w[:, :, j] * hist[i + j]
+                mag += np.abs(w[:, :, j] * hist[i + j])
+            y_all[t0 + i], mag_all[t0 + i] = y, mag
+            page_of[t0 + i] = int(block_table[b][p // page_size])
+            slot_of[t0 + i] = p % page_size
+        if ks > 1:
+            st_out[b] = np.concatenate([np.asarray(st_bits[b], np.uint16), np.asarray(x_bits[t0:t1], np.uint16)],
+                                       axis=0)[n:]
+    return y_all, mag_all, page_of, slot_of, st_out
+
+
 def kv_conv_write(*, k_new_bits, v_new_bits, cu_q, seq_lens, block_table, page_size,
                   w_k, w_v, ks, state_k_bits, state_v_bits, k_cache_bits, v_cache_bits):
-    """The step's convolution and paged write, in fp64.
+    """The step's convolution and paged write, in fp64, rounded to bf16 when stored.
 
     Shapes: k_new/v_new bf16 bits [T, Hkv, D]; w_k/w_v float [Hkv, D, ks];
     state_k/state_v bf16 bits [B, ks - 1, Hkv, D] (oldest first); caches bf16 bits
     [num_pages, Hkv, P, D].  Returns (k_cache, v_cache, state_k_out, state_v_out) as bf16
     bits; slots the step does not write keep their input bits.
     """
-    k_cache = np.array(k_cache_bits, dtype=np.uint16, copy=True)
-    v_cache = np.array(v_cache_bits, dtype=np.uint16, copy=True)
-    B = len(seq_lens)
-    Hkv, D = k_new_bits.shape[1], k_new_bits.shape[2]
-    st_k_out = np.zeros((B, max(ks - 1, 0), Hkv, D), np.uint16)
-    st_v_out = np.zeros_like(st_k_out)
-    wk = np.asarray(w_k, np.float64)
-    wv = np.asarray(w_v, np.float64)
-    for b in range(B):
-        t0, t1 = int(cu_q[b]), int(cu_q[b + 1])
-        n, L = t1 - t0, int(seq_lens[b])
-        for name, x_bits, st_bits, w, cache, st_out in (("k", k_new_bits, state_k_bits, wk, k_cache, st_k_out),
-                                                        ("v", v_new_bits, state_v_bits, wv, v_cache, st_v_out)):
-            x_new = bf16_bits_to_f64(x_bits[t0:t1])                       # [n, Hkv, D]
-            prev = bf16_bits_to_f64(st_bits[b]) if ks > 1 else np.zeros((0, Hkv, D))
-            hist = np.concatenate([prev, x_new], axis=0)                  # [ks - 1 + n, Hkv, D]
-            for i in range(n):
-                p = L - n + i
-                # window rows hist[i .. i + ks - 1] are positions p - (ks - 1) .. p
-                y = np.zeros((Hkv, D), np.float64)
-                for j in range(ks):
-                    y += w[:, :, j] * hist[i + j]
-                page = int(block_table[b][p // page_size])
-                cache[page, :, p % page_size, :] = f64_to_bf16_bits(y)
-            if ks > 1:
-                st_out[b] = np.concatenate([np.asarray(st_bits[b], np.uint16), np.asarray(x_bits[t0:t1], np.uint16)],
-                                           axis=0)[n:]
-    return k_cache, v_cache, st_k_out, st_v_out
+    out = []
+    states = []
+    for x_bits, st_bits, w, cache_bits in ((k_new_bits, state_k_bits, w_k, k_cache_bits),
+                                           (v_new_bits, state_v_bits, w_v, v_cache_bits)):
+        cache = np.array(cache_bits, dtype=np.uint16, copy=True)
+        y, _, page, slot, st_out = kv_conv_rows(x_bits=x_bits, cu_q=cu_q, seq_lens=seq_lens,
+                                                block_table=block_table, page_size=page_size, w=w, ks=ks,
+                                                state_bits=st_bits)
+        rows = page >= 0
+        cache[page[rows], :, slot[rows], :] = f64_to_bf16_bits(y[rows])
+        out.append(cache)
+        states.append(st_out)
+    return out[0], out[1], states[0], states[1]

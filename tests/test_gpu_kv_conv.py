@@ -1,10 +1,14 @@
 """GPU parity of the K/V short convolution and paged write (inkling_attn_kv_conv_write)
 against the fp64 oracle ``oracle/kv_conv.py``, through the C ABI.
 
-Bar: every slot the step writes holds the oracle's value rounded to bf16 within one bf16
-ulp (the kernel sums in fp32, the oracle in fp64; the two roundings can differ only where
-the fp32 sum lands next to a bf16 rounding boundary), every other slot of the pools keeps
-its bits (NaN pages included), and the carried state is bit-exact (it is a copy).
+Bar: every slot the step writes holds a value within  ulp_bf16(|y|) + ks * 2^-24 * mag
+of the oracle's exact fp64 value y, where mag = sum_j |w_j x_j|: the kernel sums the ks
+products in fp32 (at most ks roundings, each below 2^-24 of a partial sum bounded by mag)
+and rounds once to bf16 (half an ulp of a value at most one binade above |y|).  Every
+other slot of the pools keeps its bits (NaN pages included), and the carried state is
+bit-exact (it is a copy).  Most slots also equal the oracle's own bf16 rounding; where
+the products cancel, the fp32 error can move the result by more than one bf16 ulp of the
+small result.
 """
 import numpy as np
 import pytest
@@ -63,30 +67,38 @@ def written_mask(step, only=None):
     return np.broadcast_to(m[:, None, :], (step.num_pages, step.num_kv_heads, P))
 
 
-def ulp_distance(a, b):
-    """Distance in bf16 steps between bit patterns (monotone integer map of the floats)."""
-    def key(u):
-        u = u.astype(np.int32)
-        return np.where(u & 0x8000, 0x8000 - (u & 0x7FFF), 0x8000 + u)
-    return np.abs(key(a) - key(b))
+def bf16_ulp(y):
+    e = np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -133)))
+    return 2.0 ** (e - 7)
 
 
 def check(step, got, label):
     kc, vc, sk, sv, err = got
     assert err == 0, f"{label}: device error {err:#x}"
-    ref = okc.kv_conv_write(**step.oracle_kwargs())
+    kw = step.oracle_kwargs()
+    ref = okc.kv_conv_write(**kw)
     mask = written_mask(step)
-    for name, ours, want, before in (("k", bits(kc), ref[0], bits(step.k_cache)),
-                                     ("v", bits(vc), ref[1], bits(step.v_cache))):
+    ks = step.kernel_size
+    for name, ours_t, before, x, st, w, st_ours, st_ref in (
+            ("k", kc, kw["k_cache_bits"], kw["k_new_bits"], kw["state_k_bits"], kw["w_k"], sk, ref[2]),
+            ("v", vc, kw["v_cache_bits"], kw["v_new_bits"], kw["state_v_bits"], kw["w_v"], sv, ref[3])):
+        ours = bits(ours_t)
         # untouched slots: exactly the old bits
         assert np.array_equal(ours[~mask], before[~mask]), f"{label} {name}: stray write"
-        sel = mask
-        d = ulp_distance(ours[sel], want[sel])
-        assert np.isfinite(okc.bf16_bits_to_f64(ours[sel])).all(), f"{label} {name}: non-finite output"
-        assert d.max(initial=0) <= 1, f"{label} {name}: {int((d > 1).sum())} slots beyond 1 ulp (max {d.max()})"
-    if step.kernel_size > 1:
-        assert np.array_equal(bits(sk), ref[2]), f"{label}: state_k differs"
-        assert np.array_equal(bits(sv), ref[3]), f"{label}: state_v differs"
+        y, mag, page, slot, _ = okc.kv_conv_rows(x_bits=x, cu_q=kw["cu_q"], seq_lens=kw["seq_lens"],
+                                                 block_table=kw["block_table"], page_size=kw["page_size"],
+                                                 w=w, ks=ks, state_bits=st)
+        rows = page >= 0
+        got_v = okc.bf16_bits_to_f64(ours[page[rows], :, slot[rows], :])
+        tol = bf16_ulp(y[rows]) + ks * 2.0 ** -24 * mag[rows]
+        bad = ~(np.abs(got_v - y[rows]) <= tol)
+        assert not bad.any(), (f"{label} {name}: {int(bad.sum())} slots outside the fp32 bound; worst excess "
+                               f"{np.nanmax(np.abs(got_v - y[rows]) - tol):.3e}")
+        want_bits = ref[0] if name == "k" else ref[1]
+        same = (ours[mask] == want_bits[mask]).mean() if mask.any() else 1.0
+        assert same > 0.99, f"{label} {name}: only {same:.4f} of slots equal the oracle's bf16 rounding"
+        if ks > 1:
+            assert np.array_equal(bits(st_ours), st_ref), f"{label}: state_{name} differs"
 
 
 # (Hkv, D, P, ks, q_lens, seq_lens)

@@ -161,6 +161,26 @@ def check_two_steps(kc):
     assert np.array_equal(sk2, sk_w) and np.array_equal(sv2, sv_w)
 
 
+def test_magnitude_bounds_the_value_and_is_tight_without_cancellation():
+    """mag = sum_j |w_j x_j| is >= |y| always, and == |y| when every term has one sign."""
+    rng = np.random.default_rng(21)
+    case = make_case(rng, ks=4)
+    y, mag, page, slot, _ = kc.kv_conv_rows(x_bits=case["k_new_bits"], cu_q=case["cu_q"],
+                                            seq_lens=case["seq_lens"], block_table=case["block_table"],
+                                            page_size=case["page_size"], w=case["w_k"], ks=4,
+                                            state_bits=case["state_k_bits"])
+    assert (mag >= np.abs(y) - 1e-12).all() and (mag > 0).any()
+    pos = dict(case)
+    pos["k_new_bits"] = to_bits(np.abs(kc.bf16_bits_to_f64(case["k_new_bits"])))
+    pos["state_k_bits"] = to_bits(np.abs(kc.bf16_bits_to_f64(case["state_k_bits"])))
+    y2, mag2, *_ = kc.kv_conv_rows(x_bits=pos["k_new_bits"], cu_q=case["cu_q"], seq_lens=case["seq_lens"],
+                                   block_table=case["block_table"], page_size=case["page_size"],
+                                   w=np.abs(case["w_k"]), ks=4, state_bits=pos["state_k_bits"])
+    assert np.allclose(mag2, y2, rtol=1e-15, atol=0)
+    # rows map to the slots of their positions; rows of no request (none here) would be -1
+    assert (page >= 0).all() and ((0 <= slot) & (slot < case["page_size"])).all()
+
+
 def test_mutants_fail_the_pins():
     """Plausible mistakes planted in copies of the oracle must each fail a pin."""
     import importlib.util, pathlib
@@ -169,7 +189,7 @@ def test_mutants_fail_the_pins():
         "reversed taps": ("y += w[:, :, j] * hist[i + j]", "y += w[:, :, ks - 1 - j] * hist[i + j]"),
         "state ignored": ("prev = bf16_bits_to_f64(st_bits[b]) if ks > 1 else np.zeros((0, Hkv, D))",
                           "prev = np.zeros((ks - 1, Hkv, D))"),
-        "off-by-one position": ("p = L - n + i", "p = L - n + i - 1"),
+        "off-by-one position": ("p = L - n + i\n", "p = L - n + i - 1\n"),
         "stale state": ("axis=0)[n:]", "axis=0)[:ks - 1]"),
     }
     for name, (a, b) in mutants.items():
