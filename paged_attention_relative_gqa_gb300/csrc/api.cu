@@ -446,9 +446,11 @@ ink_status_t inkling_attn_kv_conv_write(const ink_attn_params_t* params, const v
   a.max_pages = params->max_pages_per_seq;
   a.num_pages = params->num_pages;
   a.nvec = nvec;
-  a.tok = ink::kv_conv_tokens_per_thread(total_q, nvec);
-  a.nchunks = (total_q + a.tok - 1) / a.tok;
-  a.conv_items = 2ll * a.nchunks * nvec;
+  if (total_q == 0 && (params->num_seqs == 0 || !has_state)) return INK_OK;   // nothing to write
+  int dev = 0;
+  const int sms = ink::current_device_sms(&dev);
+  if (sms <= 0) return INK_ERR_CUDA;
+  ink::kv_conv_plan(a, kernel_size, sms);
   a.state_items = has_state ? 2ll * a.B * (kernel_size - 1) * nvec : 0;
   if ((a.conv_items + a.state_items + 255) / 256 >= (1ll << 31)) return INK_ERR_TOO_LARGE;
   if (ink::launch_kv_conv(a, kernel_size, (cudaStream_t)stream) != cudaSuccess) return INK_ERR_CUDA;

@@ -113,9 +113,17 @@ struct KvConvArgs {
   int nchunks;                 // ceil(T / tok)
   long long conv_items;        // 2 * nchunks * nvec threads of convolution
   long long state_items;       // 2 * B * (ks-1) * nvec threads of state copy
+  int tile_tokens;             // staged kernel: new rows per tile (<= 32)
+  int stages;                  // staged kernel: ring depth (0: use the per-thread kernel)
 };
 
+// Largest dynamic shared memory of the staged K/V kernel.
+constexpr size_t KV_STAGED_SMEM_MAX = 216 * 1024;
+
 int kv_conv_tokens_per_thread(long long total_q, int nvec);
+size_t kv_staged_smem_bytes(int tile_tokens, int kernel_size, int nvec, int stages);
+// Fill tile_tokens, stages, tok, nchunks and conv_items of `a` (T, nvec, B set).
+void kv_conv_plan(KvConvArgs& a, int kernel_size, int num_sms);
 cudaError_t launch_kv_conv(const KvConvArgs& a, int kernel_size, cudaStream_t stream);
 
 }  // namespace ink

@@ -24,6 +24,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -63,6 +65,17 @@ __device__ __forceinline__ int find_seq(const int32_t* cu_q, int B, int t) {
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (__ldg(cu_q + mid) <= t) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// find_seq over a copy of cu_q in shared memory.
+__device__ __forceinline__ int find_seq_shared(const int* cu_q, int B, int t) {
+  if (B <= 0 || t < cu_q[0] || t >= cu_q[B]) return -1;
+  int lo = 0, hi = B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cu_q[mid] <= t) lo = mid; else hi = mid;
   }
   return lo;
 }
@@ -201,8 +214,267 @@ __global__ void __launch_bounds__(KV_CONV_THREADS, 2) kv_conv_write_kernel(const
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// Staged kernel for steps with many new rows (prefill).  The step's rows of K (or V) are
+// one contiguous array in token order, so a tile of TT consecutive tokens plus the ks - 1
+// rows before it is one contiguous run of bytes: a single 1-D bulk async copy brings it
+// into shared memory.  One CTA per SM walks the tiles (K and V tiles interleaved) through
+// a ring of NS stages.  Each stage has its own producer warp, which issues the copy of a
+// tile and then computes the tile's per-token metadata (request, index inside the request,
+// destination slot) while the copy is in flight; the request offsets and lengths are held
+// in shared memory, so that chain is one block-table load.  Eight consumer warps convolve
+// from shared memory and store each 16-byte result straight to its cache slot.
+
+constexpr int KVS_CONSUMER_WARPS = 8;
+constexpr int KVS_CONSUMERS = KVS_CONSUMER_WARPS * 32;
+constexpr int KVS_MAX_TT = 32;
+constexpr int KVS_MAX_STAGES = 4;
+constexpr int KVS_THREADS = KVS_CONSUMERS + 32 * KVS_MAX_STAGES;   // one producer warp per stage
+constexpr int KVS_MAX_CACHED_SEQS = 2047;   // cu_q / seq_lens held in shared memory up to this B
+
+struct KvsMeta {
+  long long slot[KVS_MAX_TT];   // element offset of the token's cache row for head 0, or -1
+  int b[KVS_MAX_TT];            // request of the token (-1: none)
+  int i[KVS_MAX_TT];            // index of the token among its request's new rows
+};
+
+// Shared memory: barriers and flag (128 B), per-stage metadata, cached cu_q and seq_lens,
+// then the stages (128-byte aligned).
+constexpr size_t KVS_STAGE_OFFSET =
+    (128 + KVS_MAX_STAGES * sizeof(KvsMeta) + (2 * KVS_MAX_CACHED_SEQS + 1) * sizeof(int) + 127) / 128 * 128;
+
+template <int KS>
+__global__ void __launch_bounds__(KVS_THREADS, 1) kv_conv_staged_kernel(const KvConvArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);               // [NS]
+  uint64_t* empty = full + KVS_MAX_STAGES;                          // [NS]
+  int* abort_flag = reinterpret_cast<int*>(empty + KVS_MAX_STAGES);
+  KvsMeta* meta = reinterpret_cast<KvsMeta*>(smem + 128);           // [NS]
+  int* cu_s = reinterpret_cast<int*>(smem + 128 + KVS_MAX_STAGES * sizeof(KvsMeta));   // [B + 1]
+  int* len_s = cu_s + (KVS_MAX_CACHED_SEQS + 1);                                          // [B]
+  unsigned char* stage_base = smem + KVS_STAGE_OFFSET;
+  const bool cached = a.B <= KVS_MAX_CACHED_SEQS;
+  const int NS = a.stages, TT = a.tile_tokens;
+  const int row_elems = a.nvec * 8;
+  const size_t row_bytes = (size_t)row_elems * 2;
+  const size_t stage_bytes = (size_t)(TT + KS - 1) * row_bytes;
+  const int ntiles = (a.T + TT - 1) / TT;
+  const int units = 2 * ntiles;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 33);
+      mbar_init(&empty[s], KVS_CONSUMER_WARPS);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (cached) {
+    for (int j = threadIdx.x; j <= a.B; j += KVS_THREADS) {
+      cu_s[j] = __ldg(a.cu_q + j);
+      if (j < a.B) len_s[j] = __ldg(a.seq_lens + j);
+    }
+  }
+  __syncthreads();
+
+  if (warp >= KVS_CONSUMER_WARPS) {
+    // ------------------------------------------------------------ producer warps
+    // Producer warp s fills stage s: local units k = s, s + NS, ...  Their metadata
+    // chains (request lookup, block-table load) thus run NS at a time.
+    const int ps = warp - KVS_CONSUMER_WARPS;
+    if (ps >= NS) return;
+    int k = ps;
+    int issued = 0;
+    for (int u = blockIdx.x + ps * gridDim.x; u < units; u += NS * gridDim.x, k += NS) {
+      const int s = ps;
+      if (k >= NS && !mbar_wait_bounded(&empty[s], ((k / NS) - 1) & 1)) {
+        if (lane == 0) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
+        *reinterpret_cast<volatile int*>(abort_flag) = 1;
+        break;
+      }
+      const int z = u & 1, tile = u >> 1;
+      const int t0 = tile * TT;
+      const int t_end = min(a.T, t0 + TT);
+      const int row0 = max(0, t0 - (KS - 1));
+      if (lane == 0) {
+        const uint32_t bytes = (uint32_t)((size_t)(t_end - row0) * row_bytes);
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_copy_g2s(smem_u32(stage_base + (size_t)s * stage_bytes), a.x[z] + (size_t)row0 * row_elems, bytes,
+                      &full[s]);
+      }
+      // metadata of token t0 + lane while the copy is in flight
+      if (lane < TT) {
+        const int t = t0 + lane;
+        long long slot = -1;
+        int b = -1, i = 0;
+        if (t < a.T) {
+          b = cached ? find_seq_shared(cu_s, a.B, t) : find_seq(a.cu_q, a.B, t);
+          if (b < 0) {
+            if (z == 0) record_error(a.err, INK_DEVERR_BAD_ROWS);
+          } else {
+            const int seq_start = cached ? cu_s[b] : __ldg(a.cu_q + b);
+            const int n = (cached ? cu_s[b + 1] : __ldg(a.cu_q + b + 1)) - seq_start;
+            const int L = cached ? len_s[b] : __ldg(a.seq_lens + b);
+            i = t - seq_start;
+            if (seq_start < 0) {
+              if (z == 0) record_error(a.err, INK_DEVERR_BAD_ROWS);
+              b = -1;
+              i = 0;                      // no window rows from the stage for a bad request
+            } else if (n > L) {
+              if (z == 0) record_error(a.err, INK_DEVERR_QLEN_EXCEEDS_KV);
+            } else {
+              const int p = L - n + i;
+              const int pidx = p >> a.log2_page;
+              const int page = pidx < a.max_pages ? __ldg(a.block_table + (size_t)b * a.max_pages + pidx) : -1;
+              if (page < 0 || page >= a.num_pages) {
+                if (z == 0) record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
+              } else {
+                slot = ((((long long)page * a.Hkv) << a.log2_page) + (p & ((1 << a.log2_page) - 1))) * a.D;
+              }
+            }
+          }
+        }
+        meta[s].slot[lane] = slot;
+        meta[s].b[lane] = b;
+        meta[s].i[lane] = i;
+      }
+      mbar_arrive(&full[s]);
+      ++issued;
+    }
+    // drain: wait (bounded) until the last copy into this stage has landed, so none is in
+    // flight into shared memory when the CTA exits
+    if (lane == 0 && issued > 0) {
+      const int last = ps + (issued - 1) * NS;   // local index of this stage's last unit
+      if (!mbar_wait_bounded(&full[ps], (last / NS) & 1)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumer warps
+  // carried-state rows first (plain copies, a few per thread)
+  if constexpr (KS > 1) {
+    for (long long sid = (long long)blockIdx.x * KVS_CONSUMERS + threadIdx.x; sid < a.state_items;
+         sid += (long long)gridDim.x * KVS_CONSUMERS) {
+      const int v = (int)(sid % a.nvec);
+      long long rest = sid / a.nvec;
+      const int r = (int)(rest % (KS - 1));
+      rest /= (KS - 1);
+      const int b = (int)(rest % a.B);
+      const int z = (int)(rest / a.B);
+      const int col = v * 8;
+      const int seq_start = cached ? cu_s[b] : __ldg(a.cu_q + b);
+      const int n = max((cached ? cu_s[b + 1] : __ldg(a.cu_q + b + 1)) - seq_start, 0);
+      uint4 row = make_uint4(0, 0, 0, 0);
+      if (r + n < KS - 1) {
+        row = ld_row16(a.st_in[z] + ((size_t)b * (KS - 1) + (r + n)) * row_elems + col);
+      } else {
+        const int t = seq_start + r + n - (KS - 1);
+        if (t >= 0 && t < a.T) row = ld_row16(a.x[z] + (size_t)t * row_elems + col);
+        else record_error(a.err, INK_DEVERR_BAD_ROWS);
+      }
+      *reinterpret_cast<uint4*>(a.st_out[z] + ((size_t)b * (KS - 1) + r) * row_elems + col) = row;
+    }
+  }
+
+  const int nseg = max(1, KVS_CONSUMERS / a.nvec);
+  const int seg_len = (TT + nseg - 1) / nseg;
+  const int items = a.nvec * nseg;
+  int k = 0;
+  for (int u = blockIdx.x; u < units; u += gridDim.x, ++k) {
+    const int s = k % NS;
+    const bool ok = mbar_wait_bounded(&full[s], (k / NS) & 1);
+    if (!ok || *reinterpret_cast<volatile int*>(abort_flag)) {
+      if (!ok) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
+      break;
+    }
+    const int z = u & 1, tile = u >> 1;
+    const int t0 = tile * TT;
+    const int n_tile = min(a.T, t0 + TT) - t0;
+    const int row0 = max(0, t0 - (KS - 1));
+    const unsigned char* stage = stage_base + (size_t)s * stage_bytes;
+    const KvsMeta& m = meta[s];
+    uint16_t* __restrict__ cache = a.cache[z];
+    for (int it = threadIdx.x; it < items; it += KVS_CONSUMERS) {
+      const int v = it % a.nvec, seg = it / a.nvec;
+      const int r0 = seg * seg_len, r1 = min(n_tile, r0 + seg_len);
+      if (r0 >= r1) continue;
+      const int col = v * 8;
+      const int g = col / a.D, d = col % a.D;
+      float w[KS][8];
+      {
+        const float4* wp = reinterpret_cast<const float4*>(a.w[z] + (size_t)(g * a.D + d) * KS);
+        float flat[8 * KS];
+#pragma unroll
+        for (int q = 0; q < 2 * KS; ++q) {
+          const float4 f = __ldg(wp + q);
+          flat[4 * q] = f.x; flat[4 * q + 1] = f.y; flat[4 * q + 2] = f.z; flat[4 * q + 3] = f.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+#pragma unroll
+          for (int j = 0; j < KS; ++j) w[j][e] = flat[e * KS + j];
+      }
+      const unsigned char* col_base = stage + (size_t)col * 2;
+      float win[KS > 1 ? KS - 1 : 1][8];
+      for (int r = r0; r < r1; ++r) {
+        const int b = m.b[r], i = m.i[r];
+        const int t = t0 + r;
+        if (r == r0 || i == 0) {
+          // (re)load the window: rows of the same request from the stage, else state rows
+#pragma unroll
+          for (int mm = 0; mm < KS - 1; ++mm) {
+            const int rr = i - (KS - 1) + mm;
+            uint4 row = make_uint4(0, 0, 0, 0);
+            if (rr >= 0)
+              row = *reinterpret_cast<const uint4*>(col_base + (size_t)(t - (KS - 1) + mm - row0) * row_bytes);
+            else if (b >= 0)
+              row = ld_row16(a.st_in[z] + ((size_t)b * (KS - 1) + (KS - 1 + rr)) * row_elems + col);
+            unpack8(row, win[mm]);
+          }
+        }
+        float cur[8];
+        unpack8(*reinterpret_cast<const uint4*>(col_base + (size_t)(t - row0) * row_bytes), cur);
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float acc = 0.f;
+#pragma unroll
+          for (int j = 0; j < KS - 1; ++j) acc = fmaf(w[j][e], win[j][e], acc);
+          y[e] = fmaf(w[KS - 1][e], cur[e], acc);
+        }
+#pragma unroll
+        for (int mm = 0; mm + 1 < KS - 1; ++mm)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) win[mm][e] = win[mm + 1][e];
+        if constexpr (KS > 1) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) win[KS - 2][e] = cur[e];
+        }
+        const long long slot = m.slot[r];
+        if (slot >= 0)
+          *reinterpret_cast<uint4*>(cache + slot + ((size_t)g << a.log2_page) * a.D + d) = pack8(y);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+}
+
 template <int KS>
 cudaError_t launch_ks(const KvConvArgs& a, int tok, cudaStream_t stream) {
+  if (a.stages >= 2) {
+    static std::atomic<unsigned long long> opted{0};
+    const cudaError_t e = smem_opt_in_once(kv_conv_staged_kernel<KS>, KV_STAGED_SMEM_MAX, opted);
+    if (e != cudaSuccess) return e;
+    const int units = 2 * ((a.T + a.tile_tokens - 1) / a.tile_tokens);
+    int dev = 0;
+    const int sms = current_device_sms(&dev);
+    const int grid = units < sms ? units : sms;
+    const size_t smem = kv_staged_smem_bytes(a.tile_tokens, KS, a.nvec, a.stages);
+    kv_conv_staged_kernel<KS><<<grid, KVS_THREADS, smem, stream>>>(a);
+    return cudaGetLastError();
+  }
   const long long items = a.conv_items + a.state_items;
   const unsigned blocks = (unsigned)((items + KV_CONV_THREADS - 1) / KV_CONV_THREADS);
   if (tok == 8) kv_conv_write_kernel<KS, 8><<<blocks, KV_CONV_THREADS, 0, stream>>>(a);
@@ -211,6 +483,34 @@ cudaError_t launch_ks(const KvConvArgs& a, int tok, cudaStream_t stream) {
 }
 
 }  // namespace
+
+size_t kv_staged_smem_bytes(int tile_tokens, int kernel_size, int nvec, int stages) {
+  return KVS_STAGE_OFFSET + (size_t)stages * (tile_tokens + kernel_size - 1) * (size_t)nvec * 16;
+}
+
+void kv_conv_plan(KvConvArgs& a, int kernel_size, int num_sms) {
+  // Staged path: tiles of about 32 KB of new rows, up to four stages in KV_STAGED_SMEM_MAX
+  // bytes, and enough tiles for every SM; otherwise (few rows, or rows too long for two
+  // stages) the one-thread-per-vector kernel.
+  const size_t row_bytes = (size_t)a.nvec * 16;
+  int tt = (int)(32768 / row_bytes);
+  tt = tt < 1 ? 1 : (tt > KVS_MAX_TT ? KVS_MAX_TT : tt);
+  int stages = 0;
+  while (true) {
+    const size_t fixed = kv_staged_smem_bytes(tt, kernel_size, a.nvec, 0);
+    const size_t per = kv_staged_smem_bytes(tt, kernel_size, a.nvec, 1) - fixed;
+    stages = (int)((KV_STAGED_SMEM_MAX - fixed) / per);
+    if (stages >= 2 || tt == 1) break;
+    --tt;
+  }
+  if (stages > KVS_MAX_STAGES) stages = KVS_MAX_STAGES;
+  const long long units = 2ll * ((a.T + tt - 1) / tt);
+  a.tile_tokens = tt;
+  a.stages = (stages >= 2 && units >= num_sms) ? stages : 0;
+  a.tok = kv_conv_tokens_per_thread(a.T, a.nvec);
+  a.nchunks = (a.T + a.tok - 1) / a.tok;
+  a.conv_items = 2ll * a.nchunks * a.nvec;
+}
 
 int kv_conv_tokens_per_thread(long long total_q, int nvec) {
   // Runs of 8 tokens amortise the window reload and keep 8 loads in flight per thread,

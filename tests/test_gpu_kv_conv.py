@@ -121,6 +121,46 @@ def test_kv_conv_write_matches_oracle(case):
     check(step, run_gpu(step), f"kv case {CASES[case]}")
 
 
+# Steps with enough new rows for the staged (shared-memory ring) kernel: at least one
+# tile of K and one of V per SM (tiles hold about 32 KB of new rows, at most 32 tokens).
+STAGED = [
+    (8, 128, 64, 4, [1500, 1, 2, 700, 1], [1500, 5000, 3, 900, 64]),   # tiles cut requests, n < ks - 1
+    (16, 128, 64, 8, [3000, 5, 1], [3000, 40, 100]),                    # 8-token tiles, ks 8
+    (32, 128, 16, 2, [2000, 300], [2100, 300]),                         # 512 vectors per row, 4-token tiles
+    (4, 64, 8, 1, [5000], [5000]),                                      # ks 1
+    (2, 64, 32, 3, [1] * 300 + [4000], list(range(50, 350)) + [4000]),  # 300 one-row requests, then a prompt
+]
+
+
+@pytest.mark.parametrize("case", range(len(STAGED)))
+def test_kv_conv_write_staged_matches_oracle(case):
+    Hkv, D, P, ks, ql, sl = STAGED[case]
+    step = W.make_kv_step(num_kv_heads=Hkv, head_dim=D, page_size=P, kernel_size=ks, q_lens=ql,
+                          seq_lens=sl, seed=500 + case, device=DEV)
+    check(step, run_gpu(step), f"kv staged case {case}")
+
+
+def test_kv_conv_write_staged_reports_bad_pages():
+    step = W.make_kv_step(num_kv_heads=8, head_dim=128, page_size=64, kernel_size=4, q_lens=[2000, 1500],
+                          seq_lens=[2000, 1600], seed=9, device=DEV)
+    bt = step.block_table.clone()
+    bt[1, 10] = -3                           # positions 640..703 of request 1
+    step.block_table = bt
+    kc, vc, sk, sv, err = run_gpu(step)
+    assert err == binding.DEVERR_PAGE_OUT_OF_RANGE
+    keep = ~written_mask(step, only=(0,))
+    # request 0 is written in full; request 1 everywhere but page slot 10
+    m1 = np.zeros_like(keep)
+    P = step.page_size
+    bt_np = bt.cpu().numpy()
+    for p in range(100, 1600):
+        if p // P != 10:
+            m1[bt_np[1, p // P], :, p % P] = True
+    keep &= ~m1
+    assert np.array_equal(bits(kc)[keep], bits(step.k_cache)[keep])
+    assert np.array_equal(bits(vc)[keep], bits(step.v_cache)[keep])
+
+
 def test_kv_conv_write_global_prefill_full_size():
     """4 x 8192 fresh prompts, 8 KV heads, ks 4: every written slot and the state."""
     step = W.kv_prefill_global(DEV)
