@@ -214,6 +214,30 @@ __global__ void __launch_bounds__(KV_CONV_THREADS, 2) kv_conv_write_kernel(const
   }
 }
 
+// One output row of 8 channels: y = sum_j w[j] * (window rows, then the current row), in
+// fp32 with one fma per tap; then the current row enters the window.
+template <int KS>
+__device__ __forceinline__ void conv_step(const float (&w)[KS][8], float (&win)[KS > 1 ? KS - 1 : 1][8],
+                                          const uint4 raw, float (&y)[8]) {
+  float cur[8];
+  unpack8(raw, cur);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < KS - 1; ++j) acc = fmaf(w[j][e], win[j][e], acc);
+    y[e] = fmaf(w[KS - 1][e], cur[e], acc);
+  }
+#pragma unroll
+  for (int mm = 0; mm + 1 < KS - 1; ++mm)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) win[mm][e] = win[mm + 1][e];
+  if constexpr (KS > 1) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) win[KS - 2][e] = cur[e];
+  }
+}
+
 // ---------------------------------------------------------------------------------------
 // Staged kernel for steps with many new rows (prefill).  The step's rows of K (or V) are
 // one contiguous array in token order, so a tile of TT consecutive tokens plus the ks - 1
@@ -236,6 +260,8 @@ struct KvsMeta {
   long long slot[KVS_MAX_TT];   // element offset of the token's cache row for head 0, or -1
   int b[KVS_MAX_TT];            // request of the token (-1: none)
   int i[KVS_MAX_TT];            // index of the token among its request's new rows
+  uint32_t starts;              // bit r: token r has no earlier row of its request here (i == 0)
+  uint32_t pad[31];
 };
 
 // Shared memory: barriers and flag (128 B), per-stage metadata, cached cu_q and seq_lens,
@@ -339,6 +365,8 @@ __global__ void __launch_bounds__(KVS_THREADS, 1) kv_conv_staged_kernel(const Kv
         meta[s].b[lane] = b;
         meta[s].i[lane] = i;
       }
+      const uint32_t starts = __ballot_sync(0xffffffffu, lane < TT && meta[s].i[lane] == 0);
+      if (lane == 0) meta[s].starts = starts;
       mbar_arrive(&full[s]);
       ++issued;
     }
@@ -380,6 +408,11 @@ __global__ void __launch_bounds__(KVS_THREADS, 1) kv_conv_staged_kernel(const Kv
   const int nseg = max(1, KVS_CONSUMERS / a.nvec);
   const int seg_len = (TT + nseg - 1) / nseg;
   const int items = a.nvec * nseg;
+  // A thread's filter taps stay in registers while its (tensor, vector) pair repeats: with
+  // an even grid every tile of a CTA is of the same tensor, and with at most one item per
+  // thread every tile gives the thread the same vector.
+  float w[KS][8];
+  int w_key = -1;
   int k = 0;
   for (int u = blockIdx.x; u < units; u += gridDim.x, ++k) {
     const int s = k % NS;
@@ -395,14 +428,15 @@ __global__ void __launch_bounds__(KVS_THREADS, 1) kv_conv_staged_kernel(const Kv
     const unsigned char* stage = stage_base + (size_t)s * stage_bytes;
     const KvsMeta& m = meta[s];
     uint16_t* __restrict__ cache = a.cache[z];
+    const uint64_t starts = m.starts;
     for (int it = threadIdx.x; it < items; it += KVS_CONSUMERS) {
       const int v = it % a.nvec, seg = it / a.nvec;
       const int r0 = seg * seg_len, r1 = min(n_tile, r0 + seg_len);
       if (r0 >= r1) continue;
       const int col = v * 8;
       const int g = col / a.D, d = col % a.D;
-      float w[KS][8];
-      {
+      if (w_key != z * a.nvec + v) {
+        w_key = z * a.nvec + v;
         const float4* wp = reinterpret_cast<const float4*>(a.w[z] + (size_t)(g * a.D + d) * KS);
         float flat[8 * KS];
 #pragma unroll
@@ -413,47 +447,60 @@ __global__ void __launch_bounds__(KVS_THREADS, 1) kv_conv_staged_kernel(const Kv
 #pragma unroll
         for (int e = 0; e < 8; ++e)
 #pragma unroll
-          for (int j = 0; j < KS; ++j) w[j][e] = flat[e * KS + j];
+          for (int jj = 0; jj < KS; ++jj) w[jj][e] = flat[e * KS + jj];
       }
-      const unsigned char* col_base = stage + (size_t)col * 2;
+      // stage row of tile token r: col_base + (t0 + r - row0) * row_bytes
+      const unsigned char* col_base = stage + (size_t)col * 2 + (size_t)(t0 - row0) * row_bytes;
+      uint16_t* cache_col = cache + ((size_t)g << a.log2_page) * a.D + d;
+      const uint16_t* st_col = a.st_in[z] + col;
       float win[KS > 1 ? KS - 1 : 1][8];
-      for (int r = r0; r < r1; ++r) {
-        const int b = m.b[r], i = m.i[r];
-        const int t = t0 + r;
-        if (r == r0 || i == 0) {
-          // (re)load the window: rows of the same request from the stage, else state rows
+      {
+        // window of token r0: earlier rows of its request from the stage, else state rows
+        const int b0 = m.b[r0], i0 = m.i[r0];
+#pragma unroll
+        for (int mm = 0; mm < KS - 1; ++mm) {
+          const int rr = i0 - (KS - 1) + mm;
+          uint4 row = make_uint4(0, 0, 0, 0);
+          if (rr >= 0)
+            row = *reinterpret_cast<const uint4*>(col_base + (ptrdiff_t)(r0 - (KS - 1) + mm) * (ptrdiff_t)row_bytes);
+          else if (b0 >= 0)
+            row = ld_row16(st_col + ((size_t)b0 * (KS - 1) + (KS - 1 + rr)) * row_elems);
+          unpack8(row, win[mm]);
+        }
+      }
+      int r = r0;
+      while (r < r1) {
+        if (r != r0 && ((starts >> r) & 1)) {
+          // first new row of the next request: its window is that request's state
+          const int b = m.b[r];
 #pragma unroll
           for (int mm = 0; mm < KS - 1; ++mm) {
-            const int rr = i - (KS - 1) + mm;
             uint4 row = make_uint4(0, 0, 0, 0);
-            if (rr >= 0)
-              row = *reinterpret_cast<const uint4*>(col_base + (size_t)(t - (KS - 1) + mm - row0) * row_bytes);
-            else if (b >= 0)
-              row = ld_row16(a.st_in[z] + ((size_t)b * (KS - 1) + (KS - 1 + rr)) * row_elems + col);
+            if (b >= 0) row = ld_row16(st_col + ((size_t)b * (KS - 1) + mm) * row_elems);
             unpack8(row, win[mm]);
           }
         }
-        float cur[8];
-        unpack8(*reinterpret_cast<const uint4*>(col_base + (size_t)(t - row0) * row_bytes), cur);
-        float y[8];
+        if (r + 8 <= r1 && ((starts >> (r + 1)) & 0x7Full) == 0) {
+          // eight tokens of one request: unrolled, the window shift is register renaming
+          uint4 raw[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float acc = 0.f;
+          for (int kk = 0; kk < 8; ++kk)
+            raw[kk] = *reinterpret_cast<const uint4*>(col_base + (size_t)(r + kk) * row_bytes);
 #pragma unroll
-          for (int j = 0; j < KS - 1; ++j) acc = fmaf(w[j][e], win[j][e], acc);
-          y[e] = fmaf(w[KS - 1][e], cur[e], acc);
+          for (int kk = 0; kk < 8; ++kk) {
+            float y[8];
+            conv_step<KS>(w, win, raw[kk], y);
+            const long long slot = m.slot[r + kk];
+            if (slot >= 0) *reinterpret_cast<uint4*>(cache_col + slot) = pack8(y);
+          }
+          r += 8;
+        } else {
+          float y[8];
+          conv_step<KS>(w, win, *reinterpret_cast<const uint4*>(col_base + (size_t)r * row_bytes), y);
+          const long long slot = m.slot[r];
+          if (slot >= 0) *reinterpret_cast<uint4*>(cache_col + slot) = pack8(y);
+          ++r;
         }
-#pragma unroll
-        for (int mm = 0; mm + 1 < KS - 1; ++mm)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) win[mm][e] = win[mm + 1][e];
-        if constexpr (KS > 1) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) win[KS - 2][e] = cur[e];
-        }
-        const long long slot = m.slot[r];
-        if (slot >= 0)
-          *reinterpret_cast<uint4*>(cache + slot + ((size_t)g << a.log2_page) * a.D + d) = pack8(y);
       }
     }
     __syncwarp();
