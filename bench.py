@@ -456,7 +456,7 @@ def run_ours(args, rank, world, local_rank):
         line["roofline"] = {"bound": "hbm", "achieved": round(r["GB/s"], 2), "peak": hbm_peak, "unit": "GB/s",
                             "frac": round(r["GB/s"] / hbm_peak, 4), "peak_source": peak_src,
                             "traffic": profiled_traffic("kv_conv.cu", name), "algorithmic_bytes": r["bytes"],
-                            "kernel": "kv_conv_write_kernel"}
+                            "kernel": "kv_conv_staged_kernel" if name == "kv_prefill_global" else "kv_conv_write_kernel"}
         e2e_ms, h2d, d2h = e2e_kv(binding, step, max(5, args.steps // 4), args.warmup, stream)
         line["e2e"] = {"value": round(r["bytes"] / e2e_ms / 1e6 * world, 2), "unit": "GB/s",
                        "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
