@@ -143,6 +143,29 @@ ink_status_t inkling_attn_prefill_bf16bias(const ink_attn_params_t* params, cons
                                            size_t workspace_bytes, void* stream);
 
 /*
+ * inkling_attn_prefill with the bias given in low-rank form: the kernel computes each bias
+ * tile itself, so the [total_q, Hq, E] bias tensor is never built or read.  "Support
+ * Inkling-NVFP4 model" (TensorRT-LLM PR #17062), review of _build_rel_logits: a layer's
+ * bias is the product over d_rel of a per-(token, head) vector r and the layer's
+ * projection rel_logits_proj [d_rel, E]:
+ *     rel[t, h, e] = sum_c r[t, h, c] * rel_logits_proj[c, e]
+ *   r           device, bf16 [total_q, Hq, d_rel], 16-byte aligned
+ *   rel_proj_t  device, bf16 [E, d_rel]: rel_logits_proj transposed (bucket-major, so each
+ *               bucket's d_rel coefficients are contiguous), 16-byte aligned
+ *   d_rel       a multiple of 16 in [16, 256] (else INK_ERR_BAD_SHAPE)
+ * The products are summed in fp32 from the bf16 operands (tensor-core warp MMA for the
+ * buckets of a tile, a plain fp32 dot product for the clamped bucket E - 1); the rest of
+ * the arithmetic is that of inkling_attn_prefill.  Every other argument and result as for
+ * inkling_attn_prefill.
+ */
+ink_status_t inkling_attn_prefill_lowrank_bias(const ink_attn_params_t* params, const void* q,
+                                               const int32_t* cu_q_lens, int32_t max_q_len, int32_t total_q,
+                                               const void* k_cache, const void* v_cache,
+                                               const int32_t* block_table, const int32_t* seq_lens,
+                                               const void* r, const void* rel_proj_t, int32_t d_rel, void* out,
+                                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Paged decode: one new token per sequence (row b of q is sequence b, at p = L_b - 1).
  *   q          device, bf16 [B, Hq, D]
  *   rel_logits device, fp32 [B, Hq, E]

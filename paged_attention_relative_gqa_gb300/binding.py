@@ -28,7 +28,8 @@ DEVERR_QLEN_EXCEEDS_MAX = 0x8
 DEVERR_BAD_ROWS = 0x10
 
 EXPORTED_SYMBOLS = ("inkling_attn_workspace_bytes", "inkling_attn_workspace_init",
-                    "inkling_attn_prefill", "inkling_attn_prefill_bf16bias", "inkling_attn_decode",
+                    "inkling_attn_prefill", "inkling_attn_prefill_bf16bias",
+                    "inkling_attn_prefill_lowrank_bias", "inkling_attn_decode",
                     "inkling_attn_decode_noalloc", "inkling_attn_kv_conv_write",
                     "inkling_attn_read_device_error", "inkling_attn_status_string",
                     "inkling_attn_version")
@@ -72,6 +73,8 @@ def load_library(path: Optional[str] = None):
     lib.inkling_attn_prefill.restype = ctypes.c_int
     lib.inkling_attn_prefill_bf16bias.argtypes = [PP, V, V, I32, I32, V, V, V, V, V, V, V, S, V]
     lib.inkling_attn_prefill_bf16bias.restype = ctypes.c_int
+    lib.inkling_attn_prefill_lowrank_bias.argtypes = [PP, V, V, I32, I32, V, V, V, V, V, V, I32, V, V, S, V]
+    lib.inkling_attn_prefill_lowrank_bias.restype = ctypes.c_int
     lib.inkling_attn_decode.argtypes = [PP, V, V, V, V, V, V, V, V, S, V]
     lib.inkling_attn_decode.restype = ctypes.c_int
     lib.inkling_attn_decode_noalloc.argtypes = [PP, V, V, V, V, V, V, V, V]
@@ -172,6 +175,23 @@ def inkling_attn_prefill(params, q, cu_q_lens, max_q_len, k_cache, v_cache, bloc
     return out
 
 
+def inkling_attn_prefill_lowrank_bias(params, q, cu_q_lens, max_q_len, k_cache, v_cache, block_table,
+                                      seq_lens, r, rel_proj_t, out, workspace, stream=None):
+    """Paged prefill with the bias given as r [T, Hq, d_rel] and rel_proj_t [E, d_rel]."""
+    lib = load_library()
+    if r.dim() != 3 or rel_proj_t.dim() != 2 or rel_proj_t.shape[1] != r.shape[2]:
+        raise ValueError("r must be [T, Hq, d_rel] and rel_proj_t [E, d_rel]")
+    code = lib.inkling_attn_prefill_lowrank_bias(
+        ctypes.byref(params), _dev(q, "q", torch.bfloat16), _dev(cu_q_lens, "cu_q_lens", torch.int32),
+        int(max_q_len), int(q.shape[0]), _dev(k_cache, "k_cache", torch.bfloat16),
+        _dev(v_cache, "v_cache", torch.bfloat16), _dev(block_table, "block_table", torch.int32),
+        _dev(seq_lens, "seq_lens", torch.int32), _dev(r, "r", torch.bfloat16),
+        _dev(rel_proj_t, "rel_proj_t", torch.bfloat16), int(r.shape[2]), _dev(out, "out", torch.bfloat16),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream_handle(stream))
+    _check(code, "inkling_attn_prefill_lowrank_bias")
+    return out
+
+
 def inkling_attn_decode(params, q, k_cache, v_cache, block_table, seq_lens, rel_logits, out,
                         workspace, stream=None):
     lib = load_library()
@@ -241,6 +261,10 @@ def run(prob, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tens
         out = torch.empty_like(prob.q)
     if workspace is None:
         workspace = alloc_workspace(params, True, prob.q.device)
+    if prob.r is not None:
+        return inkling_attn_prefill_lowrank_bias(params, prob.q, prob.cu_q_lens, prob.max_q_len, prob.k_cache,
+                                                 prob.v_cache, prob.block_table, prob.seq_lens, prob.r,
+                                                 prob.rel_proj_t, out, workspace, stream)
     if prob.is_decode:
         return inkling_attn_decode(params, prob.q, prob.k_cache, prob.v_cache, prob.block_table,
                                    prob.seq_lens, prob.rel_logits, out, workspace, stream)

@@ -310,21 +310,28 @@ ink_status_t inkling_attn_decode(const ink_attn_params_t* params, const void* q,
 
 namespace {
 
-// Shared by the fp32-bias and bf16-bias prefill entry points.
+// The bias of a prefill call: rel_logits in fp32 or bf16, or its low-rank factors.
+enum class BiasIn { F32, BF16, LOWRANK };
+
+// Shared by the fp32-bias, bf16-bias and low-rank-bias prefill entry points.
 ink_status_t prefill_impl(const ink_attn_params_t* params, const void* q, const int32_t* cu_q_lens,
                           int32_t max_q_len, int32_t total_q, const void* k_cache, const void* v_cache,
                           const int32_t* block_table, const int32_t* seq_lens, const void* rel_logits,
-                          bool bias_bf16, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+                          BiasIn bias_in, const void* lr_r, const void* lr_proj_t, int32_t d_rel, void* out,
+                          void* workspace, size_t workspace_bytes, void* stream) {
   ink_status_t st = validate(params);
   if (st != INK_OK) return st;
-  if (!q || !cu_q_lens || !k_cache || !v_cache || !block_table || !seq_lens || !rel_logits ||
-      !out || !workspace)
+  const bool bias_bf16 = bias_in == BiasIn::BF16, lowrank = bias_in == BiasIn::LOWRANK;
+  if (!q || !cu_q_lens || !k_cache || !v_cache || !block_table || !seq_lens || !out || !workspace)
     return INK_ERR_NULL_PTR;
+  if (lowrank ? (!lr_r || !lr_proj_t) : !rel_logits) return INK_ERR_NULL_PTR;
   if (max_q_len < 0 || total_q < 0) return INK_ERR_BAD_SHAPE;
+  if (lowrank && (d_rel < 16 || d_rel > 256 || d_rel % 16 != 0)) return INK_ERR_BAD_SHAPE;
   if ((long long)total_q * params->num_q_heads >= (1ll << 31)) return INK_ERR_TOO_LARGE;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-      !aligned(cu_q_lens, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
-      !aligned(rel_logits, bias_bf16 ? 16 : 4) || !aligned(workspace, 256))
+      !aligned(cu_q_lens, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
+    return INK_ERR_ALIGNMENT;
+  if (lowrank ? (!aligned(lr_r, 16) || !aligned(lr_proj_t, 16)) : !aligned(rel_logits, bias_bf16 ? 16 : 4))
     return INK_ERR_ALIGNMENT;
   if (bias_bf16 && params->rel_extent % 8 != 0) return INK_ERR_BAD_SHAPE;   // 16-byte bias rows
   if (workspace_bytes < kHeaderBytes) return INK_ERR_WORKSPACE;
@@ -365,7 +372,11 @@ ink_status_t prefill_impl(const ink_attn_params_t* params, const void* q, const 
   a.max_q_len = max_q_len;
   a.num_q_tiles = num_q_tiles;
   a.bias_bf16 = bias_bf16 ? 1 : 0;
-  a.bias_bulk = bias_bf16 || ((params->rel_extent % 4 == 0) && aligned(rel_logits, 16));
+  a.bias_lowrank = lowrank ? 1 : 0;
+  a.lr_r = lr_r;
+  a.lr_proj_t = lr_proj_t;
+  a.d_rel = d_rel;
+  a.bias_bulk = !lowrank && (bias_bf16 || ((params->rel_extent % 4 == 0) && aligned(rel_logits, 16)));
   std::memset(&maps.bias, 0, sizeof maps.bias);
   if (a.bias_bulk && !make_bias_map(&maps.bias, rel_logits, bias_bf16, params, total_q)) return INK_ERR_CUDA;
   if (ink::launch_prefill_tc(maps, a, params->head_dim, (cudaStream_t)stream) != cudaSuccess)
@@ -384,7 +395,7 @@ ink_status_t inkling_attn_prefill(const ink_attn_params_t* params, const void* q
                                   const int32_t* seq_lens, const float* rel_logits, void* out,
                                   void* workspace, size_t workspace_bytes, void* stream) {
   return prefill_impl(params, q, cu_q_lens, max_q_len, total_q, k_cache, v_cache, block_table, seq_lens,
-                      rel_logits, false, out, workspace, workspace_bytes, stream);
+                      rel_logits, BiasIn::F32, nullptr, nullptr, 0, out, workspace, workspace_bytes, stream);
 }
 
 ink_status_t inkling_attn_prefill_bf16bias(const ink_attn_params_t* params, const void* q,
@@ -394,7 +405,17 @@ ink_status_t inkling_attn_prefill_bf16bias(const ink_attn_params_t* params, cons
                                            const void* rel_logits_bf16, void* out, void* workspace,
                                            size_t workspace_bytes, void* stream) {
   return prefill_impl(params, q, cu_q_lens, max_q_len, total_q, k_cache, v_cache, block_table, seq_lens,
-                      rel_logits_bf16, true, out, workspace, workspace_bytes, stream);
+                      rel_logits_bf16, BiasIn::BF16, nullptr, nullptr, 0, out, workspace, workspace_bytes, stream);
+}
+
+ink_status_t inkling_attn_prefill_lowrank_bias(const ink_attn_params_t* params, const void* q,
+                                               const int32_t* cu_q_lens, int32_t max_q_len, int32_t total_q,
+                                               const void* k_cache, const void* v_cache,
+                                               const int32_t* block_table, const int32_t* seq_lens,
+                                               const void* r, const void* rel_proj_t, int32_t d_rel, void* out,
+                                               void* workspace, size_t workspace_bytes, void* stream) {
+  return prefill_impl(params, q, cu_q_lens, max_q_len, total_q, k_cache, v_cache, block_table, seq_lens,
+                      nullptr, BiasIn::LOWRANK, r, rel_proj_t, d_rel, out, workspace, workspace_bytes, stream);
 }
 
 ink_status_t inkling_attn_kv_conv_write(const ink_attn_params_t* params, const void* k_new,

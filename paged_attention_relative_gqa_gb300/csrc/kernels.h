@@ -46,6 +46,10 @@ struct PrefillArgs {
   int max_q_len, num_q_tiles;
   int bias_bulk;              // rows of rel are 16-byte aligned (E a multiple of 16 bytes, aligned base)
   int bias_bf16;              // rel holds bf16 values (always with bias_bulk)
+  int bias_lowrank;           // bias from r and proj_t (rel unused)
+  const void* lr_r;           // bf16 [total_q, Hq, d_rel]
+  const void* lr_proj_t;      // bf16 [E, d_rel]
+  int d_rel;                  // a multiple of 16
 };
 
 // TMA descriptors of one decode call: K/V pools viewed as [num_pages*Hkv*P rows, D]

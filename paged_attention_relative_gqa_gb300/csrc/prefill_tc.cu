@@ -49,11 +49,17 @@ constexpr int PT_THREADS = 384;
 // each bank at most twice); bf16: COLS 88 (also at most two rows per bank word).
 // Each softmax warpgroup owns PER_WG slots that it fills in turn; every slot then has one
 // consumer taking its fills in order, so a parity wait never matches a phase two behind.
-template <bool BF>
+// Bias modes: BM_F32 and BM_BF16 load the slot from rel_logits by TMA; BM_LOWRANK computes
+// it from r and the projection with warp MMA (fp32 slot, groups aligned to 8 buckets so
+// that the 8-bucket n-tiles of the product tile a group's 88 columns exactly).
+constexpr int BM_F32 = 0, BM_BF16 = 1, BM_LOWRANK = 2;
+constexpr int BIAS_LOWRANK_COLS = 88;
+
+template <int BM>
 struct BiasShape {
-  using T = typename std::conditional<BF, __nv_bfloat16, float>::type;
-  static constexpr int COLS = BF ? BIAS_BOX_COLS_BF16 : BIAS_BOX_COLS;
-  static constexpr int ALIGN = 16 / (int)sizeof(T);          // elements per 16 bytes
+  using T = typename std::conditional<BM == BM_BF16, __nv_bfloat16, float>::type;
+  static constexpr int COLS = BM == BM_BF16 ? BIAS_BOX_COLS_BF16 : (BM == BM_LOWRANK ? BIAS_LOWRANK_COLS : BIAS_BOX_COLS);
+  static constexpr int ALIGN = BM == BM_LOWRANK ? 8 : 16 / (int)sizeof(T);   // x_g is a multiple of ALIGN
   static constexpr int GROUP = BIAS_BOX_ROWS * COLS;          // elements per group
   static constexpr int NGROUP = PT_ROWS / BIAS_BOX_ROWS;      // groups per tile
   static constexpr int SLOT_BYTES = NGROUP * GROUP * (int)sizeof(T);
@@ -75,21 +81,21 @@ constexpr float RESCALE_NAT = 5.545177444479562f;   // rescale O when a max grow
 // Ring depths (D = 128): V gets two slots per softmax warpgroup (a V tile waits for the P V
 // product two tiles back, so one slot each left the P V issue waiting for V); K gets three
 // stages when the smaller bf16 bias slots leave room, two with the fp32 bias.
-template <int D, bool BF>
+template <int D, int BM>
 struct PtShape {
   static constexpr int CB = D / 64;
   static constexpr int Q_SUB = PT_ROWS * 128;
   static constexpr int Q_BYTES = CB * Q_SUB;
   static constexpr int KV_SUB = TILE_KEYS * 128;
   static constexpr int KV_TILE = CB * KV_SUB;   // one K or one V tile
-  static constexpr int NK = D == 128 ? (BF ? 3 : 2) : 4;   // K ring: freed once S = Q K^T is done
+  static constexpr int NK = D == 128 ? (BM == BM_BF16 ? 3 : 2) : 4;   // K ring: freed once S = Q K^T is done
   static constexpr int NV = 4;   // V ring (even: slot g % NV serves warpgroup g % 2)
 };
 
-template <int D, bool BF>
+template <int D, int BM>
 struct PtSmem {
-  using S = PtShape<D, BF>;
-  using BS = BiasShape<BF>;
+  using S = PtShape<D, BM>;
+  using BS = BiasShape<BM>;
   static constexpr size_t q = 0;
   static constexpr size_t kst = q + S::Q_BYTES;
   static constexpr size_t vst = kst + (size_t)S::NK * S::KV_TILE;
@@ -183,15 +189,15 @@ __device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, volati
   return false;
 }
 
-template <int D, bool BF>
+template <int D, int BM>
 __global__ void __launch_bounds__(PT_THREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmK3, const __grid_constant__ CUtensorMap tmV3,
                   const __grid_constant__ CUtensorMap tmQ3, const __grid_constant__ CUtensorMap tmB,
                   const PrefillArgs a) {
-  using S = PtShape<D, BF>;
-  using L_ = PtSmem<D, BF>;
-  using BS = BiasShape<BF>;
+  using S = PtShape<D, BM>;
+  using L_ = PtSmem<D, BM>;
+  using BS = BiasShape<BM>;
   using BT = typename BS::T;
   constexpr int NK = S::NK, NV = S::NV;
   constexpr uint32_t IDESC_S = umma_idesc_bf16(PT_ROWS, TILE_KEYS, false, false);
@@ -390,7 +396,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     // behind.  (V slots follow the same rule: NV is even.)
     int bcnt[2] = {0, 0};   // bias tiles loaded per warpgroup
     int g = 0;
-    if (lane == 0) prefetch_tensormap(&tmB);
+    if (lane == 0 && a.bias_bulk) prefetch_tensormap(&tmB);
     for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
       PItem it;
       if (!get_item(a, i, it) || it.ntile == 0) continue;
@@ -402,7 +408,61 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         if (use >= 1) (void)wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err);
         BT* sb = reinterpret_cast<BT*>(smem + L_::bias + (size_t)slot * BS::SLOT_BYTES);
         const int dmin0 = it.pos0 - (k0 + TILE_KEYS - 1);
-        if (a.bias_bulk) {
+        if constexpr (BM == BM_LOWRANK) {
+          // Group gr (rows 16 gr .. 16 gr + 15) holds buckets [x_g, x_g + 88):
+          // G = R_g (16 x d_rel) * Pt_g^T (d_rel x 88), as 11 m16n8k16 n-tiles per k-step,
+          // fp32 accumulate; fragments loaded straight from r and proj_t (L2-resident).
+          // Rows past the item and buckets outside [0, E) read clamped addresses; those
+          // values are never used (invisible rows and keys, or distances >= E - 1).
+          const uint32_t nm =
+              __ballot_sync(0xffffffffu, lane < BS::NGROUP && bias_group_needed(a, it, k0, lane));
+          const int q4 = lane & 3, rq = lane >> 2;
+          const int kw = a.d_rel >> 1;   // 4-byte words per row of r / proj_t
+          const uint32_t* rbase = static_cast<const uint32_t*>(a.lr_r);
+          const uint32_t* pbase = static_cast<const uint32_t*>(a.lr_proj_t);
+#pragma unroll 1
+          for (uint32_t mm = nm; mm; mm &= mm - 1) {
+            const int gr = __ffs(mm) - 1;
+            const int xg = bias_group_x<BS::ALIGN>(dmin0, gr);
+            const int ra = min(BIAS_BOX_ROWS * gr + rq, it.rows - 1);
+            const int rb = min(BIAS_BOX_ROWS * gr + rq + 8, it.rows - 1);
+            const uint32_t* pa = rbase + ((size_t)(it.t0 + ra) * a.Hq + it.h) * kw + q4;
+            const uint32_t* pb = rbase + ((size_t)(it.t0 + rb) * a.Hq + it.h) * kw + q4;
+            const uint32_t* pn[11];
+#pragma unroll
+            for (int nt = 0; nt < 11; ++nt) {
+              const int bucket = min(max(xg + 8 * nt + rq, 0), a.E - 1);
+              pn[nt] = pbase + (size_t)bucket * kw + q4;
+            }
+            float acc[11][4];
+#pragma unroll
+            for (int nt = 0; nt < 11; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll 1
+            for (int kb = 0; kb < kw; kb += 8) {   // one k-step of 16: words kb .. kb + 7
+              uint32_t af[4];
+              af[0] = __ldg(pa + kb);
+              af[1] = __ldg(pb + kb);
+              af[2] = __ldg(pa + kb + 4);
+              af[3] = __ldg(pb + kb + 4);
+              uint32_t bf[11][2];
+#pragma unroll
+              for (int nt = 0; nt < 11; ++nt) {
+                bf[nt][0] = __ldg(pn[nt] + kb);
+                bf[nt][1] = __ldg(pn[nt] + kb + 4);
+              }
+#pragma unroll
+              for (int nt = 0; nt < 11; ++nt) mma_bf16_16816(acc[nt], af, bf[nt][0], bf[nt][1]);
+            }
+            float* gdst = reinterpret_cast<float*>(sb) + gr * BS::GROUP;
+#pragma unroll
+            for (int nt = 0; nt < 11; ++nt) {
+              *reinterpret_cast<float2*>(gdst + rq * BS::COLS + 8 * nt + 2 * q4) = make_float2(acc[nt][0], acc[nt][1]);
+              *reinterpret_cast<float2*>(gdst + (rq + 8) * BS::COLS + 8 * nt + 2 * q4) =
+                  make_float2(acc[nt][2], acc[nt][3]);
+            }
+          }
+          mbar_arrive(&b_full[slot]);   // all 32 lanes: their stores are in the slot
+        } else if (a.bias_bulk) {
           // lane gr < NGROUP decides whether group gr of this tile is read; the warp loads those
           const uint32_t nm =
               __ballot_sync(0xffffffffu, lane < BS::NGROUP && bias_group_needed(a, it, k0, lane));
@@ -413,7 +473,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             tma_load_3d_warp(sb + gr * BS::GROUP, &tmB, bias_group_x<BS::ALIGN>(dmin0, gr), it.h,
                              it.t0 + BIAS_BOX_ROWS * gr, &b_full[slot]);
           }
-        } else if constexpr (!BF) {   // fp32 rows that are not 16-byte aligned (never bf16)
+        } else if constexpr (BM == BM_F32) {   // fp32 rows that are not 16-byte aligned (never bf16)
 #pragma unroll 1
           for (int r = 0; r < it.rows; ++r) {
             const int pr = it.pos0 + r;
@@ -469,9 +529,30 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         continue;
       }
       const int pr = it.pos0 + r;
-      // (rows past the item's last use its last row's address: never outside rel)
-      const BT* relrow = static_cast<const BT*>(a.rel) + ((size_t)(it.t0 + (rv ? r : it.rows - 1)) * a.Hq + it.h) * a.E;
-      const float clamp_ld = to_float(__ldg(relrow + a.E - 1));
+      float clamp_ld;
+      if constexpr (BM == BM_LOWRANK) {
+        // bucket E - 1 of this row: r[t, h, :] . proj_t[E - 1, :], in fp32
+        const uint4* rr = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.lr_r) +
+                                                         ((size_t)(it.t0 + (rv ? r : it.rows - 1)) * a.Hq + it.h) * a.d_rel);
+        const uint4* pe = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.lr_proj_t) +
+                                                         (size_t)(a.E - 1) * a.d_rel);
+        float acc = 0.f;
+#pragma unroll 1
+        for (int w8 = 0; w8 < a.d_rel / 8; ++w8) {
+          const uint4 x = __ldg(rr + w8), y = __ldg(pe + w8);
+          const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), acc);
+            acc = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), acc);
+          }
+        }
+        clamp_ld = acc;
+      } else {
+        // (rows past the item's last use its last row's address: never outside rel)
+        const BT* relrow = static_cast<const BT*>(a.rel) + ((size_t)(it.t0 + (rv ? r : it.rows - 1)) * a.Hq + it.h) * a.E;
+        clamp_ld = to_float(__ldg(relrow + a.E - 1));
+      }
       const float clampv = rv ? clamp_ld : 0.f;   // bucket of distances >= E - 1
       const int32_t* bt = a.block_table + (size_t)it.b * a.max_pages;
       const int seg = P < TILE_KEYS ? P : TILE_KEYS;
@@ -741,26 +822,29 @@ int num_sms_pf() {
   return n > 0 ? n : 148;
 }
 
-template <int D, bool BF>
+template <int D, int BM>
 cudaError_t launch_prefill_tc_t(const PrefillMaps& m, const PrefillArgs& a, cudaStream_t stream) {
-  constexpr size_t smem = PtSmem<D, BF>::alloc;
+  constexpr size_t smem = PtSmem<D, BM>::alloc;
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  static_assert(PtShape<D, BF>::NV % 2 == 0, "each V slot must serve one softmax warpgroup");
+  static_assert(PtShape<D, BM>::NV % 2 == 0, "each V slot must serve one softmax warpgroup");
   static std::atomic<unsigned long long> opted{0};
-  cudaError_t e = smem_opt_in_once(prefill_tc_kernel<D, BF>, (int)smem, opted);
+  cudaError_t e = smem_opt_in_once(prefill_tc_kernel<D, BM>, (int)smem, opted);
   if (e != cudaSuccess) return e;
   const long long items = (long long)a.num_q_tiles * a.B * a.Hq;
   const int grid = (int)std::min<long long>(items, num_sms_pf());
-  prefill_tc_kernel<D, BF><<<grid, PT_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.q3, m.bias, a);
+  prefill_tc_kernel<D, BM><<<grid, PT_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.q3, m.bias, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PrefillMaps& m, const PrefillArgs& a, int head_dim, cudaStream_t stream) {
+  if (a.bias_lowrank)
+    return head_dim == 128 ? launch_prefill_tc_t<128, BM_LOWRANK>(m, a, stream)
+                           : launch_prefill_tc_t<64, BM_LOWRANK>(m, a, stream);
   if (a.bias_bf16)
-    return head_dim == 128 ? launch_prefill_tc_t<128, true>(m, a, stream) : launch_prefill_tc_t<64, true>(m, a, stream);
-  return head_dim == 128 ? launch_prefill_tc_t<128, false>(m, a, stream) : launch_prefill_tc_t<64, false>(m, a, stream);
+    return head_dim == 128 ? launch_prefill_tc_t<128, BM_BF16>(m, a, stream) : launch_prefill_tc_t<64, BM_BF16>(m, a, stream);
+  return head_dim == 128 ? launch_prefill_tc_t<128, BM_F32>(m, a, stream) : launch_prefill_tc_t<64, BM_F32>(m, a, stream);
 }
 
 }  // namespace ink

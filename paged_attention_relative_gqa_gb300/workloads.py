@@ -55,8 +55,10 @@ class Problem:
     block_table: torch.Tensor  # [B, max_pages] int32
     seq_lens: torch.Tensor     # [B] int32
     cu_q_lens: torch.Tensor    # [B + 1] int32
-    rel_logits: torch.Tensor   # [total_q, Hq, E] fp32
+    rel_logits: torch.Tensor   # [total_q, Hq, E] fp32 (empty when the bias is low-rank)
     seed: int = 0
+    r: Optional[torch.Tensor] = None           # low-rank bias: [total_q, Hq, d_rel] bf16
+    rel_proj_t: Optional[torch.Tensor] = None  # low-rank bias: [E, d_rel] bf16
 
     @property
     def num_seqs(self) -> int:
@@ -110,6 +112,12 @@ class Problem:
                     block_table=self.block_table.cpu().numpy(),
                     rel=self.rel_logits.detach().float().cpu().numpy())
 
+    def lowrank_bits(self):
+        """(r bits, proj_t bits) of a low-rank-bias problem, as the oracle takes them."""
+        def bits(t):
+            return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+        return bits(self.r), bits(self.rel_proj_t)
+
 
 def _randn(shape, gen, device, dtype, std=1.0):
     x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
@@ -123,11 +131,15 @@ def make_problem(*, num_q_heads: int, num_kv_heads: int, head_dim: int, page_siz
                  seed: int, device="cpu", sm_scale: Optional[float] = None,
                  extra_page_frac: float = 0.1, max_pages: Optional[int] = None,
                  rel_std: float = 0.5, nan_spare_pages: bool = True,
-                 bias_dtype=torch.float32) -> Problem:
+                 bias_dtype=torch.float32, lowrank_d: Optional[int] = None) -> Problem:
     """Build a seeded problem.  ``q_lens[b]`` new tokens are the last of ``seq_lens[b]``.
 
     ``bias_dtype=torch.bfloat16`` rounds the same seeded bias to bf16 (the input of the
-    bf16-bias prefill); the oracle then reads those rounded values."""
+    bf16-bias prefill); the oracle then reads those rounded values.
+
+    ``lowrank_d`` gives the bias in low-rank form instead: r ``[T, Hq, d]`` bf16 N(0,1) and
+    the transposed projection ``[E, d]`` bf16 N(0, rel_std^2 / d), so that the bias they
+    define has standard deviation ``rel_std``; ``rel_logits`` is then empty."""
     assert len(q_lens) == len(seq_lens)
     for n, L in zip(q_lens, seq_lens):
         assert 0 <= n <= L or (L == 0 and n == 0)
@@ -159,7 +171,13 @@ def make_problem(*, num_q_heads: int, num_kv_heads: int, head_dim: int, page_siz
         v_cache[idx] = float("nan")
     total_q = int(sum(q_lens))
     q = _randn((total_q, num_q_heads, head_dim), gen, device, torch.bfloat16)
-    rel = _randn((total_q, num_q_heads, rel_extent), gen, device, bias_dtype, std=rel_std)
+    r = proj_t = None
+    if lowrank_d is None:
+        rel = _randn((total_q, num_q_heads, rel_extent), gen, device, bias_dtype, std=rel_std)
+    else:
+        rel = torch.empty(0, dtype=torch.float32, device=device)
+        r = _randn((total_q, num_q_heads, lowrank_d), gen, device, torch.bfloat16)
+        proj_t = _randn((rel_extent, lowrank_d), gen, device, torch.bfloat16, std=rel_std / math.sqrt(lowrank_d))
     cu = torch.zeros(B + 1, dtype=torch.int32)
     cu[1:] = torch.cumsum(torch.tensor(q_lens, dtype=torch.int64), 0).to(torch.int32)
     return Problem(num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
@@ -168,7 +186,7 @@ def make_problem(*, num_q_heads: int, num_kv_heads: int, head_dim: int, page_siz
                    q_lens=list(q_lens), seq_lens_list=list(seq_lens), q=q,
                    k_cache=k_cache, v_cache=v_cache, block_table=bt.to(device),
                    seq_lens=torch.tensor(seq_lens, dtype=torch.int32, device=device),
-                   cu_q_lens=cu.to(device), rel_logits=rel, seed=seed)
+                   cu_q_lens=cu.to(device), rel_logits=rel, seed=seed, r=r, rel_proj_t=proj_t)
 
 
 def _uniform_lengths(n, lo, hi, seed):
@@ -214,6 +232,17 @@ def global_prefill(device="cpu", seed=4, batch=4, tokens=8192, bias_dtype=torch.
     """Global-layer prefill: 4 x 8192 tokens, full causal, E 4096, page 64."""
     return make_problem(**GLOBAL_LAYER, page_size=64, q_lens=[tokens] * batch,
                         seq_lens=[tokens] * batch, seed=seed, device=device, bias_dtype=bias_dtype)
+
+
+# Rank of the low-rank bias workloads: the pages do not give d_rel; 64 is a plausible size
+# for a per-head relative-position code.
+LOWRANK_D = 64
+
+
+def global_prefill_lowrank(device="cpu", seed=4, batch=4, tokens=8192, d_rel=LOWRANK_D) -> Problem:
+    """Global-layer prefill with the bias in low-rank form: 4 x 8192 tokens, E 4096, d_rel 64."""
+    return make_problem(**GLOBAL_LAYER, page_size=64, q_lens=[tokens] * batch,
+                        seq_lens=[tokens] * batch, seed=seed, device=device, lowrank_d=d_rel)
 
 
 def mixed_layer(kind: str, layer: int, device="cpu", seed=5,

@@ -30,7 +30,11 @@ def run_gpu(prob, workspace=None, check_error=True):
 
 
 def oracle_full(prob) -> np.ndarray:
-    return oracle.attention(**prob.oracle_kwargs())
+    kw = prob.oracle_kwargs()
+    if prob.r is not None:
+        import oracle.lowrank as lr
+        kw["rel"] = lr.rel_from_lowrank(*prob.lowrank_bits())
+    return oracle.attention(**kw)
 
 
 def oracle_rows(prob, rows: np.ndarray) -> np.ndarray:
@@ -40,7 +44,11 @@ def oracle_rows(prob, rows: np.ndarray) -> np.ndarray:
     t = torch.from_numpy(rows[:, 0].astype(np.int64)).to(dev)
     h = torch.from_numpy(rows[:, 1].astype(np.int64)).to(dev)
     q_rows = bits(prob.q[t, h])
-    rel_rows = prob.rel_logits[t, h].float().cpu().numpy()
+    if prob.r is not None:
+        import oracle.lowrank as lr
+        rel_rows = lr.rel_rows_from_lowrank(bits(prob.r[t, h]), bits(prob.rel_proj_t))
+    else:
+        rel_rows = prob.rel_logits[t, h].float().cpu().numpy()
     return oracle.attention_rows(
         num_q_heads=prob.num_q_heads, num_kv_heads=prob.num_kv_heads, head_dim=prob.head_dim,
         page_size=prob.page_size, rel_extent=prob.rel_extent, window=prob.window,

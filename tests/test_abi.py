@@ -163,3 +163,19 @@ def test_kv_conv_write_kernel_size_one_needs_no_state(lib):
     nothing (B = 0 rows of state are also nothing), so the call returns without a GPU."""
     params = good_params(num_seqs=0)
     assert _kv_call(lib, params, ks=1, st=ctypes.c_void_p(0), total_q=0) == 0
+
+
+def test_lowrank_bias_prefill_rejects_bad_rank_and_alignment(lib):
+    ok = ctypes.c_void_p(1 << 20)
+    params = good_params()
+    for d in (0, 8, 24, 272):
+        r = lib.inkling_attn_prefill_lowrank_bias(ctypes.byref(params), ok, ok, 16, 64, ok, ok, ok, ok, ok, ok, d,
+                                                  ok, ok, 1 << 30, None)
+        assert r == 2, d
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    r = lib.inkling_attn_prefill_lowrank_bias(ctypes.byref(params), ok, ok, 16, 64, ok, ok, ok, ok, odd, ok, 64,
+                                              ok, ok, 1 << 30, None)
+    assert r == 5
+    r = lib.inkling_attn_prefill_lowrank_bias(ctypes.byref(params), ok, ok, 16, 64, ok, ok, ok, ok, None, ok, 64,
+                                              ok, ok, 1 << 30, None)
+    assert r == 1

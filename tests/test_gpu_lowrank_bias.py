@@ -1,0 +1,82 @@
+"""GPU parity of the prefill with the bias in low-rank form
+(inkling_attn_prefill_lowrank_bias): the kernel computes every bias tile from r and the
+transposed projection; the oracle builds the whole bias tensor in fp64 (``oracle/lowrank.py``)
+and runs the attention oracle on it.  Tolerances are those of every prefill."""
+import pytest
+import torch
+
+from paged_attention_relative_gqa_gb300 import binding
+from paged_attention_relative_gqa_gb300 import workloads as W
+from tests.parity import compare, gpu_rows, oracle_full, oracle_rows, run_gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load_library()
+    yield
+    torch.cuda.empty_cache()
+
+
+def test_lowrank_bias_swa_prefill_tiny_every_row():
+    prob = W.make_problem(num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=16, rel_extent=512,
+                          window=512, q_lens=[1024], seq_lens=[1024], seed=0, device=DEV, lowrank_d=64)
+    out, err = run_gpu(prob)
+    assert err == 0
+    compare(out.float().cpu().numpy(), oracle_full(prob), "low-rank bias swa_prefill_tiny")
+
+
+# (Hq, Hkv, D, P, W, E, q_lens, seq_lens, d_rel)
+EDGE_LR = [
+    (8, 8, 128, 16, 5, 16, [33, 1, 64], [33, 2, 300], 16),        # MHA, tiny window, cached prefix, d_rel 16
+    (16, 1, 128, 32, 64, 600, [65, 129], [100, 129], 32),         # G16, window == tile
+    (8, 2, 128, 256, 512, 512, [300, 1], [1500, 777], 64),        # P256, SWA
+    (8, 2, 64, 8, -1, 7, [1, 5, 70], [1, 40, 200], 128),          # P8, D64, E7 (clamp), d_rel 128
+    (4, 4, 128, 64, -1, 1, [200], [300], 48),                     # E1: every key clamped
+    (8, 2, 128, 64, -1, 4096, [700, 0, 130], [5000, 3, 130], 64), # long cached prefix, empty row
+]
+
+
+@pytest.mark.parametrize("case", range(len(EDGE_LR)))
+def test_lowrank_bias_edge_shapes(case):
+    Hq, Hkv, D, P, Wn, E, ql, sl, d = EDGE_LR[case]
+    prob = W.make_problem(num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P, rel_extent=E,
+                          window=Wn, q_lens=ql, seq_lens=sl, seed=600 + case, device=DEV,
+                          max_pages=max(-(-L // P) for L in sl) + 3, lowrank_d=d)
+    out, err = run_gpu(prob)
+    assert err == 0
+    compare(out.float().cpu().numpy(), oracle_full(prob), f"low-rank bias edge prefill {EDGE_LR[case]}")
+
+
+def test_lowrank_bias_matches_the_materialised_bias_entry():
+    """The low-rank entry against the fp32 entry fed rel = r x proj (built in fp32 by a
+    library GEMM): the same attention up to the order of the fp32 bias sums."""
+    prob = W.mixed_layer("swa", 0, DEV)[0]
+    lr = W.make_problem(num_q_heads=prob.num_q_heads, num_kv_heads=prob.num_kv_heads, head_dim=prob.head_dim,
+                        page_size=prob.page_size, rel_extent=prob.rel_extent, window=prob.window,
+                        q_lens=prob.q_lens, seq_lens=prob.seq_lens_list, seed=77, device=DEV, lowrank_d=64)
+    a, err_a = run_gpu(lr)
+    mat = (lr.r.float().reshape(-1, 64) @ lr.rel_proj_t.float().t()).reshape(lr.total_q, lr.num_q_heads, -1)
+    r_saved, p_saved = lr.r, lr.rel_proj_t
+    lr.r, lr.rel_proj_t, lr.rel_logits = None, None, mat.contiguous()
+    b, err_b = run_gpu(lr)
+    assert err_a == 0 and err_b == 0
+    diff = (a.float() - b.float()).abs().max().item()
+    assert diff <= 1e-2, f"low-rank vs materialised bias: max diff {diff}"
+    lr.r, lr.rel_proj_t = r_saved, p_saved
+
+
+def test_lowrank_bias_global_prefill_sampled_rows_and_repeats():
+    prob = W.global_prefill_lowrank(DEV)
+    out, err = run_gpu(prob)
+    assert err == 0
+    rows = W.sample_rows(prob, per_seq=1024, seed=46)
+    compare(gpu_rows(out, rows), oracle_rows(prob, rows), "low-rank bias global_prefill (4x8192, sampled)")
+    again, _ = run_gpu(prob)
+    assert torch.equal(out, again)
+    del prob, out, again
+    torch.cuda.empty_cache()
