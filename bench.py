@@ -62,17 +62,27 @@ def decode_bytes(prob) -> int:
 
 
 def prefill_work(prob):
-    """(FLOPs, bytes): 4*D per visible (row, key, head); bias read once, Q/out, K/V once."""
+    """(FLOPs, bytes, bias FLOPs): 4*D per visible (row, key, head); bias read once (or,
+    in low-rank form, r and the projection read once, plus 2*d_rel FLOPs per bias bucket
+    used), Q/out, K/V once."""
     D, Hq, Hkv, E = prob.head_dim, prob.num_q_heads, prob.num_kv_heads, prob.rel_extent
     flops = 0
     bias = 0
+    buckets = 0
     for (pos, lo) in visible_ranges(prob):
         vis = pos - lo + 1
         flops += int(vis.sum()) * 4 * D * Hq
-        bias += int(np.minimum(vis, E).sum()) * Hq * prob.rel_logits.element_size()
+        buckets += int(np.minimum(vis, E).sum()) * Hq
+    bias_flops = 0
+    if prob.r is not None:
+        d = prob.r.shape[-1]
+        bias = prob.r.numel() * 2 + prob.rel_proj_t.numel() * 2
+        bias_flops = buckets * 2 * d
+    else:
+        bias = buckets * prob.rel_logits.element_size()
     kv = sum(prob.seq_lens_list) * Hkv * D * 2 * 2
     qo = prob.total_q * Hq * D * 2 * 2
-    return flops, bias + kv + qo
+    return flops, bias + kv + qo, bias_flops
 
 
 def kv_write_bytes(step) -> int:
@@ -211,6 +221,10 @@ def profiled_traffic(kernel_file: str, workload: str):
 
 def make_call(binding, prob, out, ws):
     params = binding.params_of(prob)
+    if prob.r is not None:
+        return lambda: binding.inkling_attn_prefill_lowrank_bias(params, prob.q, prob.cu_q_lens, prob.max_q_len,
+                                                                 prob.k_cache, prob.v_cache, prob.block_table,
+                                                                 prob.seq_lens, prob.r, prob.rel_proj_t, out, ws)
     if prob.is_decode:
         return lambda: binding.inkling_attn_decode(params, prob.q, prob.k_cache, prob.v_cache,
                                                    prob.block_table, prob.seq_lens, prob.rel_logits,
@@ -287,6 +301,9 @@ WORKLOAD_DESC = {
     "global_prefill_bf16bias": "global_prefill with the bias in bf16 (inkling_attn_prefill_bf16bias): "
                                "4 x 8192 tokens, 64 q heads / 8 kv heads, head_dim 128, full causal, "
                                "page 64, bias [32768,64,4096] bf16 (clamped)",
+    "global_prefill_lowrank": "global_prefill with the bias in low-rank form (inkling_attn_prefill_lowrank_bias): "
+                              "4 x 8192 tokens, 64 q heads / 8 kv heads, head_dim 128, full causal, page 64, "
+                              "E 4096 (clamped), r [32768,64,64] bf16, projection [4096,64] bf16",
     "global_prefill_small": "global_prefill_small (profiling size): 1 x 2048 tokens, 64 q heads / "
                             "8 kv heads, head_dim 128, full causal, page 64, bias [2048,64,4096] fp32",
     "kv_prefill_global": "K/V short convolution (ks 4) + paged write of a global-layer prefill step: "
@@ -314,6 +331,8 @@ def workload_instances(name, dev):
         return [W.global_prefill(dev, seed=4)]                       # 36 GB > L2
     if name == "global_prefill_bf16bias":
         return [W.global_prefill(dev, seed=4, bias_dtype=torch.bfloat16)]   # 19 GB > L2
+    if name == "global_prefill_lowrank":
+        return [W.global_prefill_lowrank(dev, seed=4)]                # r 268 MB + Q/out 1 GB > L2
     if name == "global_prefill_small":
         return [W.global_prefill(dev, seed=4, batch=1, tokens=2048)]  # 2.2 GB > L2
     raise ValueError(name)
@@ -399,15 +418,17 @@ def measure(binding, name, dev, steps, warmup, stream, hbm_peak, bf16_peak):
         return {"ms": m, "value": gbs, "unit": "GB/s", "GB/s": gbs, "hbm_frac": gbs / hbm_peak,
                 "tok_s": p0.num_seqs / m * 1e3, "bytes": nbytes, "launches_per_step": 1,
                 "bound": "hbm", "probs": probs}
-    flops, nbytes = prefill_work(p0)
+    flops, nbytes, bias_flops = prefill_work(p0)
     tfs = flops / m / 1e9
     # the roof that binds is the one whose minimum time is longer (the bias bytes on
-    # long-context configurations, the tensor cores on short ones)
-    t_hbm, t_tensor = nbytes / (hbm_peak * 1e6), flops / (bf16_peak * 1e9)
-    return {"ms": m, "value": tfs, "unit": "TFLOP/s", "TFLOP/s": tfs, "tensor_frac": tfs / bf16_peak,
+    # long-context configurations, the tensor cores on short ones); a low-rank bias adds
+    # its own products to the tensor work
+    t_hbm, t_tensor = nbytes / (hbm_peak * 1e6), (flops + bias_flops) / (bf16_peak * 1e9)
+    tensor_tfs = (flops + bias_flops) / m / 1e9
+    return {"ms": m, "value": tfs, "unit": "TFLOP/s", "TFLOP/s": tfs, "tensor_frac": tensor_tfs / bf16_peak,
             "GB/s": nbytes / m / 1e6, "hbm_frac": nbytes / m / 1e6 / hbm_peak,
-            "tok_s": p0.total_q / m * 1e3, "flops": flops, "bytes": nbytes, "launches_per_step": 1,
-            "bound": "hbm" if t_hbm >= t_tensor else "tensor", "probs": probs}
+            "tok_s": p0.total_q / m * 1e3, "flops": flops, "bias_flops": bias_flops, "bytes": nbytes,
+            "launches_per_step": 1, "bound": "hbm" if t_hbm >= t_tensor else "tensor", "probs": probs}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -470,19 +491,24 @@ def run_ours(args, rank, world, local_rank):
                                 "peak_source": peak_src, "traffic": profiled_traffic(src, name),
                                 "algorithmic_bytes": r["bytes"], "kernel": kernel}
         else:
-            line["roofline"] = {"bound": "tensor", "achieved": round(r["TFLOP/s"], 2), "peak": bf16_peak,
-                                "unit": "TFLOP/s", "frac": round(r["TFLOP/s"] / bf16_peak, 4),
+            tens = (r["flops"] + r.get("bias_flops", 0)) / r["ms"] / 1e9
+            line["roofline"] = {"bound": "tensor", "achieved": round(tens, 2), "peak": bf16_peak,
+                                "unit": "TFLOP/s", "frac": round(tens / bf16_peak, 4),
                                 "peak_source": peak_src, "traffic": profiled_traffic(src, name),
                                 "algorithmic_bytes": r["bytes"], "kernel": kernel}
         if not decode:
-            line["roofline"].update({"algorithmic_flops": r["flops"], "tensor_frac": round(r["tensor_frac"], 4),
-                                     "hbm_frac": round(r["hbm_frac"], 4)})
+            line["roofline"].update({"algorithmic_flops": r["flops"] + r.get("bias_flops", 0),
+                                     "attention_flops": r["flops"], "bias_flops": r.get("bias_flops", 0),
+                                     "tensor_frac": round(r["tensor_frac"], 4), "hbm_frac": round(r["hbm_frac"], 4)})
         probs = r.pop("probs")
         if probs[0].is_decode:
             e2e_ms, h2d, d2h = e2e_decode(binding, probs[0], max(10, args.steps // 2), args.warmup, stream)
             line["e2e"] = {"value": round(r["bytes"] / e2e_ms / 1e6 * world, 2), "unit": "GB/s",
                            "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                            "d2h_bytes_per_step": d2h}
+        elif probs[0].r is not None:
+            line["e2e"] = {"value": None, "unit": "TFLOP/s",
+                           "skipped": "the low-rank bias prefill is timed device-resident only"}
         elif probs[0].rel_logits.numel() * 4 > (4 << 30):
             line["e2e"] = {"value": None, "unit": "TFLOP/s",
                            "skipped": "inputs above 4 GB are not staged through pinned host memory"}
@@ -501,8 +527,8 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_extra:
         wl = {}
         steps_x = max(5, args.steps // 4)
-        for other in ("global_decode", "swa_prefill_tiny", "global_prefill", "global_prefill_bf16bias", "mixed",
-                      "mixed_graph", "kv_prefill_global", "kv_decode_swa"):
+        for other in ("global_decode", "swa_prefill_tiny", "global_prefill", "global_prefill_bf16bias",
+                      "global_prefill_lowrank", "mixed", "mixed_graph", "kv_prefill_global", "kv_decode_swa"):
             if other == name:
                 continue
             st = steps_x if other in ("global_decode", "swa_prefill_tiny", "kv_prefill_global",

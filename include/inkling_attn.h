@@ -152,7 +152,7 @@ ink_status_t inkling_attn_prefill_bf16bias(const ink_attn_params_t* params, cons
  *   r           device, bf16 [total_q, Hq, d_rel], 16-byte aligned
  *   rel_proj_t  device, bf16 [E, d_rel]: rel_logits_proj transposed (bucket-major, so each
  *               bucket's d_rel coefficients are contiguous), 16-byte aligned
- *   d_rel       a multiple of 16 in [16, 256] (else INK_ERR_BAD_SHAPE)
+ *   d_rel       32 or 64 (else INK_ERR_BAD_SHAPE); the pages do not give it
  * The products are summed in fp32 from the bf16 operands (tensor-core warp MMA for the
  * buckets of a tile, a plain fp32 dot product for the clamped bucket E - 1); the rest of
  * the arithmetic is that of inkling_attn_prefill.  Every other argument and result as for

@@ -192,6 +192,32 @@ bool make_bias_map(CUtensorMap* map, const void* rel, bool bf16, const ink_attn_
   return r == CUDA_SUCCESS;
 }
 
+// Low-rank bias operands: r [total_q, Hq, d_rel] as {d_rel, Hq, total_q} with boxes of
+// 128 tokens of one head, and proj_t [E, d_rel] as {d_rel, E} with boxes of
+// LOWRANK_CHUNK buckets; 128-byte swizzle for d_rel 64, 64-byte for d_rel 32 (rows of
+// 128 / 64 bytes).  Out-of-range rows (tokens past total_q, buckets outside [0, E)) read 0.
+bool make_lowrank_maps(ink::PrefillMaps* m, const void* r, const void* proj_t, const ink_attn_params_t* p,
+                       int total_q, int d_rel) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const CUtensorMapSwizzle sw = d_rel == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  cuuint64_t dims_r[3] = {(cuuint64_t)d_rel, (cuuint64_t)p->num_q_heads, (cuuint64_t)total_q};
+  cuuint64_t str_r[2] = {(cuuint64_t)d_rel * 2, (cuuint64_t)d_rel * 2 * p->num_q_heads};
+  cuuint32_t box_r[3] = {(cuuint32_t)d_rel, 1, (cuuint32_t)ink::PREFILL_ROWS};
+  cuuint32_t e3[3] = {1, 1, 1};
+  CUresult e = fn(&m->lr_r, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(r), dims_r, str_r, box_r, e3,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (e != CUDA_SUCCESS) return false;
+  cuuint64_t dims_p[2] = {(cuuint64_t)d_rel, (cuuint64_t)p->rel_extent};
+  cuuint64_t str_p[1] = {(cuuint64_t)d_rel * 2};
+  cuuint32_t box_p[2] = {(cuuint32_t)d_rel, (cuuint32_t)ink::LOWRANK_CHUNK};
+  cuuint32_t e2[2] = {1, 1};
+  e = fn(&m->lr_p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(proj_t), dims_p, str_p, box_p, e2,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return e == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -326,7 +352,7 @@ ink_status_t prefill_impl(const ink_attn_params_t* params, const void* q, const 
     return INK_ERR_NULL_PTR;
   if (lowrank ? (!lr_r || !lr_proj_t) : !rel_logits) return INK_ERR_NULL_PTR;
   if (max_q_len < 0 || total_q < 0) return INK_ERR_BAD_SHAPE;
-  if (lowrank && (d_rel < 16 || d_rel > 256 || d_rel % 16 != 0)) return INK_ERR_BAD_SHAPE;
+  if (lowrank && d_rel != 32 && d_rel != 64) return INK_ERR_BAD_SHAPE;
   if ((long long)total_q * params->num_q_heads >= (1ll << 31)) return INK_ERR_TOO_LARGE;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(cu_q_lens, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
@@ -378,6 +404,9 @@ ink_status_t prefill_impl(const ink_attn_params_t* params, const void* q, const 
   a.d_rel = d_rel;
   a.bias_bulk = !lowrank && (bias_bf16 || ((params->rel_extent % 4 == 0) && aligned(rel_logits, 16)));
   std::memset(&maps.bias, 0, sizeof maps.bias);
+  std::memset(&maps.lr_r, 0, sizeof maps.lr_r);
+  std::memset(&maps.lr_p, 0, sizeof maps.lr_p);
+  if (lowrank && !make_lowrank_maps(&maps, lr_r, lr_proj_t, params, total_q, d_rel)) return INK_ERR_CUDA;
   if (a.bias_bulk && !make_bias_map(&maps.bias, rel_logits, bias_bf16, params, total_q)) return INK_ERR_CUDA;
   if (ink::launch_prefill_tc(maps, a, params->head_dim, (cudaStream_t)stream) != cudaSuccess)
     return INK_ERR_CUDA;

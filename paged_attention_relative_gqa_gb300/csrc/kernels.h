@@ -87,6 +87,8 @@ cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& a, int head_
 // 84 buckets x 1 head x 16 tokens (only built when rows of rel are 16-byte aligned).
 struct PrefillMaps {
   CUtensorMap k, v, bias;
+  CUtensorMap lr_r;     // low-rank bias: r viewed as {d_rel, Hq, total_q}, box {d_rel, 1, 128}
+  CUtensorMap lr_p;     // low-rank bias: proj_t viewed as {d_rel, E}, box {d_rel, LOWRANK_CHUNK}
   CUtensorMap k3, v3;   // whole 64-key tiles, all column blocks in one box (P >= 64 only)
   CUtensorMap q3;       // 128 query rows of one head, all column blocks in one box
 };
@@ -95,6 +97,9 @@ constexpr int BIAS_BOX_COLS = 84;   // buckets per bias box row
 constexpr int BIAS_BOX_ROWS = 16;   // tokens per bias box
 constexpr int BIAS_BOX_COLS_BF16 = 88;   // buckets per bias box row, bf16 bias
 constexpr int PREFILL_ROWS = 128;        // new tokens per prefill work item
+constexpr int LOWRANK_CHUNK = 64;        // projection rows per TMA box (one key tile's new buckets)
+constexpr int LOWRANK_RING_ROWS = 256;   // projection rows held: a tile's 192 plus the next tile's 64
+constexpr int LOWRANK_MAX_D = 64;        // largest d_rel of the low-rank bias
 
 cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int head_dim,
                               cudaStream_t stream);

@@ -50,16 +50,16 @@ constexpr int PT_THREADS = 384;
 // Each softmax warpgroup owns PER_WG slots that it fills in turn; every slot then has one
 // consumer taking its fills in order, so a parity wait never matches a phase two behind.
 // Bias modes: BM_F32 and BM_BF16 load the slot from rel_logits by TMA; BM_LOWRANK computes
-// it from r and the projection with warp MMA (fp32 slot, groups aligned to 8 buckets so
-// that the 8-bucket n-tiles of the product tile a group's 88 columns exactly).
+// an fp32 slot from r and the projection with warp MMA, one group at x_g = dmin0 + 16 g
+// exactly (no TMA alignment to keep), so 64 + 15 = 79 buckets a row: 80 columns, ten
+// 8-bucket n-tiles.
 constexpr int BM_F32 = 0, BM_BF16 = 1, BM_LOWRANK = 2;
-constexpr int BIAS_LOWRANK_COLS = 88;
 
 template <int BM>
 struct BiasShape {
   using T = typename std::conditional<BM == BM_BF16, __nv_bfloat16, float>::type;
-  static constexpr int COLS = BM == BM_BF16 ? BIAS_BOX_COLS_BF16 : (BM == BM_LOWRANK ? BIAS_LOWRANK_COLS : BIAS_BOX_COLS);
-  static constexpr int ALIGN = BM == BM_LOWRANK ? 8 : 16 / (int)sizeof(T);   // x_g is a multiple of ALIGN
+  static constexpr int COLS = BM == BM_BF16 ? BIAS_BOX_COLS_BF16 : (BM == BM_LOWRANK ? 80 : BIAS_BOX_COLS);
+  static constexpr int ALIGN = BM == BM_LOWRANK ? 1 : 16 / (int)sizeof(T);   // x_g is a multiple of ALIGN
   static constexpr int GROUP = BIAS_BOX_ROWS * COLS;          // elements per group
   static constexpr int NGROUP = PT_ROWS / BIAS_BOX_ROWS;      // groups per tile
   static constexpr int SLOT_BYTES = NGROUP * GROUP * (int)sizeof(T);
@@ -89,7 +89,9 @@ struct PtShape {
   static constexpr int KV_SUB = TILE_KEYS * 128;
   static constexpr int KV_TILE = CB * KV_SUB;   // one K or one V tile
   static constexpr int NK = D == 128 ? (BM == BM_BF16 ? 3 : 2) : 4;   // K ring: freed once S = Q K^T is done
-  static constexpr int NV = 4;   // V ring (even: slot g % NV serves warpgroup g % 2)
+  // V ring (even: slot g % NV serves warpgroup g % 2); the low-rank mode gives up two V
+  // slots for its r tile and projection window
+  static constexpr int NV = BM == BM_LOWRANK ? 2 : 4;
 };
 
 template <int D, int BM>
@@ -100,10 +102,14 @@ struct PtSmem {
   static constexpr size_t kst = q + S::Q_BYTES;
   static constexpr size_t vst = kst + (size_t)S::NK * S::KV_TILE;
   static constexpr size_t bias = vst + (size_t)S::NV * S::KV_TILE;
-  static constexpr size_t bars = bias + (size_t)BS::SLOTS * BS::SLOT_BYTES;
+  // low-rank mode: the item's r rows [128][d_rel] and a ring of projection rows
+  // [LOWRANK_RING_ROWS][d_rel] (bf16, swizzled like their TMA boxes), sized for d_rel 64
+  static constexpr size_t lr_r = bias + (size_t)BS::SLOTS * BS::SLOT_BYTES;
+  static constexpr size_t lr_w = lr_r + (BM == BM_LOWRANK ? (size_t)PT_ROWS * LOWRANK_MAX_D * 2 : 0);
+  static constexpr size_t bars = lr_w + (BM == BM_LOWRANK ? (size_t)LOWRANK_RING_ROWS * LOWRANK_MAX_D * 2 : 0);
   // q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2],
-  // s_empty[2], o_done[2], o_free, b_full[NB], b_empty[NB], ml_full, ml_free
-  static constexpr int NBAR = 2 + 2 * S::NK + 2 * S::NV + 2 + 2 + 2 + 1 + 2 * BS::SLOTS + 2;
+  // s_empty[2], o_done[2], o_free, b_full[NB], b_empty[NB], ml_full, ml_free, w_full[2]
+  static constexpr int NBAR = 2 + 2 * S::NK + 2 * S::NV + 2 + 2 + 2 + 1 + 2 * BS::SLOTS + 2 + 2;
   static constexpr size_t vbad = bars + NBAR * 8;
   static constexpr size_t ml1 = vbad + S::NV * 8;          // float2 [128]
   static constexpr size_t misc = ml1 + PT_ROWS * 8;
@@ -194,6 +200,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmK3, const __grid_constant__ CUtensorMap tmV3,
                   const __grid_constant__ CUtensorMap tmQ3, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmP,
                   const PrefillArgs a) {
   using S = PtShape<D, BM>;
   using L_ = PtSmem<D, BM>;
@@ -221,6 +228,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   uint64_t* b_empty = b_full + BS::SLOTS;
   uint64_t* ml_full = b_empty + BS::SLOTS;
   uint64_t* ml_free = ml_full + 1;
+  uint64_t* w_full = ml_free + 1;   // low-rank mode [2]: loads of r rows / projection chunks, alternating
   float2* ml1 = reinterpret_cast<float2*>(smem + L_::ml1);
   uint64_t* vbad = reinterpret_cast<uint64_t*>(smem + L_::vbad);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L_::misc);
@@ -249,6 +257,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     mbar_init(o_free, 4);
     mbar_init(ml_full, 4);
     mbar_init(ml_free, 4);
+    mbar_init(&w_full[0], 1);
+    mbar_init(&w_full[1], 1);
     for (int x = 0; x < BS::SLOTS; ++x) {
       mbar_init(&b_full[x], a.bias_bulk ? 1 : 32);
       mbar_init(&b_empty[x], 4);
@@ -396,7 +406,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     // behind.  (V slots follow the same rule: NV is even.)
     int bcnt[2] = {0, 0};   // bias tiles loaded per warpgroup
     int g = 0;
+    // low-rank mode: the item whose r rows and projection ring are loaded, the ring's base
+    // bucket (x_0 of that item's first bias tile), and the load events issued / waited for
+    int lr_item = -1, lr_base = 0, ev_issued = 0, ev_waited = 0;
     if (lane == 0 && a.bias_bulk) prefetch_tensormap(&tmB);
+    if (BM == BM_LOWRANK && lane == 0) {
+      prefetch_tensormap(&tmR);
+      prefetch_tensormap(&tmP);
+    }
     for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
       PItem it;
       if (!get_item(a, i, it) || it.ntile == 0) continue;
@@ -405,64 +422,100 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         if (!tile_needs_bias(it.pos0, k0, a.E)) continue;
         const int u = bcnt[g & 1]++;
         const int slot = (g & 1) * BS::PER_WG + u % BS::PER_WG, use = u / BS::PER_WG;
-        if (use >= 1) (void)wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err);
         BT* sb = reinterpret_cast<BT*>(smem + L_::bias + (size_t)slot * BS::SLOT_BYTES);
         const int dmin0 = it.pos0 - (k0 + TILE_KEYS - 1);
         if constexpr (BM == BM_LOWRANK) {
-          // Group gr (rows 16 gr .. 16 gr + 15) holds buckets [x_g, x_g + 88):
-          // G = R_g (16 x d_rel) * Pt_g^T (d_rel x 88), as 11 m16n8k16 n-tiles per k-step,
-          // fp32 accumulate; fragments loaded straight from r and proj_t (L2-resident).
-          // Rows past the item and buckets outside [0, E) read clamped addresses; those
-          // values are never used (invisible rows and keys, or distances >= E - 1).
+          // Group gr (rows 16 gr .. 16 gr + 15) holds buckets [x_g, x_g + 80), x_g = x_0 + 16 gr:
+          // G = R_g (16 x d_rel) Pt[x_g .. x_g + 79]^T, ten m16n8k16 n-tiles per k-step, fp32
+          // accumulate, operands by ldmatrix from the item's r rows and a ring of proj_t rows.
+          // Bucket b sits at ring row (b - base) mod 256, base = x_0 of the item's first bias
+          // tile; a tile reads 192 buckets [x_0, x_0 + 192), and each next tile of the item
+          // (x_0 - 64) needs only 64 new ones, whose 64-row chunk (never wrapping the ring) is
+          // loaded while this tile computes.  Rows past the item and buckets outside [0, E)
+          // arrive as zeros and are never used (invisible rows and keys, or distances >= E - 1).
           const uint32_t nm =
               __ballot_sync(0xffffffffu, lane < BS::NGROUP && bias_group_needed(a, it, k0, lane));
-          const int q4 = lane & 3, rq = lane >> 2;
-          const int kw = a.d_rel >> 1;   // 4-byte words per row of r / proj_t
-          const uint32_t* rbase = static_cast<const uint32_t*>(a.lr_r);
-          const uint32_t* pbase = static_cast<const uint32_t*>(a.lr_proj_t);
+          const int x0 = dmin0;
+          const uint32_t chunk_bytes = (uint32_t)(LOWRANK_CHUNK * a.d_rel * 2);
+          const uint32_t pitch = (uint32_t)a.d_rel * 2;
+          if (lr_item != i) {
+            // first bias tile of the item: its r rows and chunks [x_0 + 64 m, +64), m = 0..2
+            if (lane == 0) {
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier ldmatrix reads first
+              uint64_t* bar = &w_full[ev_issued & 1];
+              mbar_arrive_expect_tx(bar, (uint32_t)(PT_ROWS * a.d_rel * 2) + 3 * chunk_bytes);
+              tma_load_3d(smem + L_::lr_r, &tmR, 0, it.h, it.t0, bar);
 #pragma unroll 1
-          for (uint32_t mm = nm; mm; mm &= mm - 1) {
-            const int gr = __ffs(mm) - 1;
-            const int xg = bias_group_x<BS::ALIGN>(dmin0, gr);
-            const int ra = min(BIAS_BOX_ROWS * gr + rq, it.rows - 1);
-            const int rb = min(BIAS_BOX_ROWS * gr + rq + 8, it.rows - 1);
-            const uint32_t* pa = rbase + ((size_t)(it.t0 + ra) * a.Hq + it.h) * kw + q4;
-            const uint32_t* pb = rbase + ((size_t)(it.t0 + rb) * a.Hq + it.h) * kw + q4;
-            const uint32_t* pn[11];
-#pragma unroll
-            for (int nt = 0; nt < 11; ++nt) {
-              const int bucket = min(max(xg + 8 * nt + rq, 0), a.E - 1);
-              pn[nt] = pbase + (size_t)bucket * kw + q4;
+              for (int m = 0; m < 3; ++m)
+                tma_load_2d(smem + L_::lr_w + (size_t)m * LOWRANK_CHUNK * pitch, &tmP, 0, x0 + LOWRANK_CHUNK * m, bar);
             }
-            float acc[11][4];
-#pragma unroll
-            for (int nt = 0; nt < 11; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+            ++ev_issued;
+            lr_item = i;
+            lr_base = x0;
+          }
+          if (j + 1 < it.ntile) {
+            // the next tile of this item needs buckets [x_0 - 64, x_0): load their chunk now
+            if (lane == 0) {
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              uint64_t* bar = &w_full[ev_issued & 1];
+              const int ring_row = (x0 - LOWRANK_CHUNK - lr_base) & (LOWRANK_RING_ROWS - 1);
+              mbar_arrive_expect_tx(bar, chunk_bytes);
+              tma_load_2d(smem + L_::lr_w + (size_t)ring_row * pitch, &tmP, 0, x0 - LOWRANK_CHUNK, bar);
+            }
+            ++ev_issued;
+          }
+          if (use >= 1) (void)wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err);
+          // this tile's rows arrived with event ev_waited (the item's first load, or the chunk
+          // loaded during the previous tile)
+          const bool ok = wait_flag(&w_full[ev_waited & 1], (uint32_t)(ev_waited >> 1) & 1u, abort_flag, a.err);
+          ++ev_waited;
+          if (nm && ok) {
+            const int q4 = lane & 3, rq = lane >> 2;
+            const uint32_t swm = (uint32_t)(a.d_rel / 8 - 1);   // 128- or 64-byte swizzle
+            const uint32_t rbase = smem_u32(smem + L_::lr_r), wbase = smem_u32(smem + L_::lr_w);
+            const int rel0 = x0 - lr_base;   // ring row of bucket x_0 is rel0 mod 256
 #pragma unroll 1
-            for (int kb = 0; kb < kw; kb += 8) {   // one k-step of 16: words kb .. kb + 7
-              uint32_t af[4];
-              af[0] = __ldg(pa + kb);
-              af[1] = __ldg(pb + kb);
-              af[2] = __ldg(pa + kb + 4);
-              af[3] = __ldg(pb + kb + 4);
-              uint32_t bf[11][2];
+            for (uint32_t mm = nm; mm; mm &= mm - 1) {
+              const int gr = __ffs(mm) - 1;
+              float acc[10][4];
 #pragma unroll
-              for (int nt = 0; nt < 11; ++nt) {
-                bf[nt][0] = __ldg(pn[nt] + kb);
-                bf[nt][1] = __ldg(pn[nt] + kb + 4);
+              for (int nt = 0; nt < 10; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll 1
+              for (int kp = 0; kp < a.d_rel / 16; kp += 2) {   // k-steps kp and kp + 1
+                uint32_t af[2][4];
+#pragma unroll
+                for (int s2 = 0; s2 < 2; ++s2) {
+                  const uint32_t off = (uint32_t)(BIAS_BOX_ROWS * gr + (lane & 15)) * pitch +
+                                       (uint32_t)(2 * (kp + s2) + (lane >> 4)) * 16;
+                  ldmatrix_x4(rbase + (off ^ (((off >> 7) & swm) << 4)), af[s2][0], af[s2][1], af[s2][2], af[s2][3]);
+                }
+                // all 10 B fragments first, then the 20 products (independent accumulators)
+                uint32_t bf[10][4];
+#pragma unroll
+                for (int nt = 0; nt < 10; ++nt) {
+                  const uint32_t row = (uint32_t)(rel0 + BIAS_BOX_ROWS * gr + 8 * nt + (lane & 7)) & (LOWRANK_RING_ROWS - 1);
+                  const uint32_t off = row * pitch + (uint32_t)(2 * kp + (lane >> 3)) * 16;
+                  ldmatrix_x4(wbase + (off ^ (((off >> 7) & swm) << 4)), bf[nt][0], bf[nt][1], bf[nt][2], bf[nt][3]);
+                }
+#pragma unroll
+                for (int nt = 0; nt < 10; ++nt) mma_bf16_16816(acc[nt], af[0], bf[nt][0], bf[nt][1]);
+#pragma unroll
+                for (int nt = 0; nt < 10; ++nt) mma_bf16_16816(acc[nt], af[1], bf[nt][2], bf[nt][3]);
               }
+              float* gdst = reinterpret_cast<float*>(sb) + gr * BS::GROUP;
 #pragma unroll
-              for (int nt = 0; nt < 11; ++nt) mma_bf16_16816(acc[nt], af, bf[nt][0], bf[nt][1]);
-            }
-            float* gdst = reinterpret_cast<float*>(sb) + gr * BS::GROUP;
-#pragma unroll
-            for (int nt = 0; nt < 11; ++nt) {
-              *reinterpret_cast<float2*>(gdst + rq * BS::COLS + 8 * nt + 2 * q4) = make_float2(acc[nt][0], acc[nt][1]);
-              *reinterpret_cast<float2*>(gdst + (rq + 8) * BS::COLS + 8 * nt + 2 * q4) =
-                  make_float2(acc[nt][2], acc[nt][3]);
+              for (int nt = 0; nt < 10; ++nt) {
+                const int col = 8 * nt + 2 * q4;
+                *reinterpret_cast<float2*>(gdst + rq * BS::COLS + col) = make_float2(acc[nt][0], acc[nt][1]);
+                *reinterpret_cast<float2*>(gdst + (rq + 8) * BS::COLS + col) = make_float2(acc[nt][2], acc[nt][3]);
+              }
             }
           }
           mbar_arrive(&b_full[slot]);   // all 32 lanes: their stores are in the slot
-        } else if (a.bias_bulk) {
+          continue;
+        }
+        if (use >= 1) (void)wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err);
+        if (a.bias_bulk) {
           // lane gr < NGROUP decides whether group gr of this tile is read; the warp loads those
           const uint32_t nm =
               __ballot_sync(0xffffffffu, lane < BS::NGROUP && bias_group_needed(a, it, k0, lane));
@@ -497,6 +550,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
+    if (BM == BM_LOWRANK && lane == 0) {
+      // after an abort, loads may still be landing: wait (bounded) for the last event on each
+      // of the two barriers (each barrier's phases complete in order, and no later phase
+      // follows these), so no load is in flight when the CTA exits
+#pragma unroll 1
+      for (int e = ev_issued >= 2 ? ev_issued - 2 : 0; e < ev_issued; ++e)
+        if (!mbar_wait_bounded(&w_full[e & 1], (uint32_t)(e >> 1) & 1u)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
+    }
   } else {
     // -------------------------------------------------------------- softmax warpgroups
     // Warpgroup wg (warps 4-7: wg 0, warps 8-11: wg 1) owns the tiles g with g % 2 == wg
@@ -832,7 +893,7 @@ cudaError_t launch_prefill_tc_t(const PrefillMaps& m, const PrefillArgs& a, cuda
   if (e != cudaSuccess) return e;
   const long long items = (long long)a.num_q_tiles * a.B * a.Hq;
   const int grid = (int)std::min<long long>(items, num_sms_pf());
-  prefill_tc_kernel<D, BM><<<grid, PT_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.q3, m.bias, a);
+  prefill_tc_kernel<D, BM><<<grid, PT_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.q3, m.bias, m.lr_r, m.lr_p, a);
   return cudaGetLastError();
 }
 

@@ -32,11 +32,11 @@ def test_lowrank_bias_swa_prefill_tiny_every_row():
 
 # (Hq, Hkv, D, P, W, E, q_lens, seq_lens, d_rel)
 EDGE_LR = [
-    (8, 8, 128, 16, 5, 16, [33, 1, 64], [33, 2, 300], 16),        # MHA, tiny window, cached prefix, d_rel 16
+    (8, 8, 128, 16, 5, 16, [33, 1, 64], [33, 2, 300], 32),        # MHA, tiny window, cached prefix, d_rel 32
     (16, 1, 128, 32, 64, 600, [65, 129], [100, 129], 32),         # G16, window == tile
     (8, 2, 128, 256, 512, 512, [300, 1], [1500, 777], 64),        # P256, SWA
-    (8, 2, 64, 8, -1, 7, [1, 5, 70], [1, 40, 200], 128),          # P8, D64, E7 (clamp), d_rel 128
-    (4, 4, 128, 64, -1, 1, [200], [300], 48),                     # E1: every key clamped
+    (8, 2, 64, 8, -1, 7, [1, 5, 70], [1, 40, 200], 64),           # P8, D64, E7 (clamp)
+    (4, 4, 128, 64, -1, 1, [200], [300], 32),                     # E1: every key clamped
     (8, 2, 128, 64, -1, 4096, [700, 0, 130], [5000, 3, 130], 64), # long cached prefix, empty row
 ]
 
