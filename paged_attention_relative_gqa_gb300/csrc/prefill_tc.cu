@@ -40,6 +40,13 @@ namespace {
 
 constexpr int PT_ROWS = PREFILL_ROWS;
 constexpr int PT_THREADS = 384;
+// The low-rank mode adds a fourth warpgroup (warps 12-15) that computes the bias products,
+// one warp per SM sub-partition, so it runs with 512 threads and rebalances registers
+// with setmaxnreg: warps 0-3 and 12-15 give theirs to the softmax warpgroups.
+constexpr int PT_THREADS_LR = 512;
+constexpr int LR_REGS_PRODUCERS = 72, LR_REGS_SOFTMAX = 168, LR_REGS_BIAS = 104;
+static_assert(LR_REGS_PRODUCERS + 2 * LR_REGS_SOFTMAX + LR_REGS_BIAS <= 4 * (65536 / PT_THREADS_LR),
+              "the four warpgroups' registers must fit the 512-thread launch budget");
 // Bias slot: 8 groups of 16 rows (tokens); group g holds buckets [x_g, x_g + COLS) of its
 // rows, row i of it at +COLS i, x_g = ALIGN*floor((dmin0 + 16g)/ALIGN), where
 // dmin0 = pos0 - (k0 + 63) is row 0's smallest distance in the tile (x_g is 16-byte
@@ -108,8 +115,8 @@ struct PtSmem {
   static constexpr size_t lr_w = lr_r + (BM == BM_LOWRANK ? (size_t)PT_ROWS * LOWRANK_MAX_D * 2 : 0);
   static constexpr size_t bars = lr_w + (BM == BM_LOWRANK ? (size_t)LOWRANK_RING_ROWS * LOWRANK_MAX_D * 2 : 0);
   // q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2],
-  // s_empty[2], o_done[2], o_free, b_full[NB], b_empty[NB], ml_full, ml_free, w_full[2]
-  static constexpr int NBAR = 2 + 2 * S::NK + 2 * S::NV + 2 + 2 + 2 + 1 + 2 * BS::SLOTS + 2 + 2;
+  // s_empty[2], o_done[2], o_free, b_full[NB], b_empty[NB], ml_full, ml_free, w_full[2], c_done[2]
+  static constexpr int NBAR = 2 + 2 * S::NK + 2 * S::NV + 2 + 2 + 2 + 1 + 2 * BS::SLOTS + 2 + 2 + 2;
   static constexpr size_t vbad = bars + NBAR * 8;
   static constexpr size_t ml1 = vbad + S::NV * 8;          // float2 [128]
   static constexpr size_t misc = ml1 + PT_ROWS * 8;
@@ -196,7 +203,7 @@ __device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, volati
 }
 
 template <int D, int BM>
-__global__ void __launch_bounds__(PT_THREADS, 1)
+__global__ void __launch_bounds__(BM == BM_LOWRANK ? PT_THREADS_LR : PT_THREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmK3, const __grid_constant__ CUtensorMap tmV3,
                   const __grid_constant__ CUtensorMap tmQ3, const __grid_constant__ CUtensorMap tmB,
@@ -229,6 +236,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   uint64_t* ml_full = b_empty + BS::SLOTS;
   uint64_t* ml_free = ml_full + 1;
   uint64_t* w_full = ml_free + 1;   // low-rank mode [2]: loads of r rows / projection chunks, alternating
+  // low-rank mode [2]: the four bias warps are done with bias tile t (barrier t % 2; the
+  // loader waits for tile t - 1 before loading tile t + 1's rows, so neither barrier can
+  // run two phases ahead of its waiter)
+  uint64_t* c_done = w_full + 2;
   float2* ml1 = reinterpret_cast<float2*>(smem + L_::ml1);
   uint64_t* vbad = reinterpret_cast<uint64_t*>(smem + L_::vbad);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L_::misc);
@@ -259,8 +270,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     mbar_init(ml_free, 4);
     mbar_init(&w_full[0], 1);
     mbar_init(&w_full[1], 1);
+    mbar_init(&c_done[0], 4);
+    mbar_init(&c_done[1], 4);
     for (int x = 0; x < BS::SLOTS; ++x) {
-      mbar_init(&b_full[x], a.bias_bulk ? 1 : 32);
+      mbar_init(&b_full[x], BM == BM_LOWRANK ? 128 : (a.bias_bulk ? 1 : 32));
       mbar_init(&b_empty[x], 4);
     }
     fence_mbar_init();
@@ -277,6 +290,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 || warp == 3) {
+    if constexpr (BM == BM_LOWRANK) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(LR_REGS_PRODUCERS));
     // -------------------------------------------------------------- producers (TMA)
     // warp 0 loads the query tile of each item and the K tiles, warp 3 the V tiles;
     // each walks the block table on its own (entries held 32 at a time in lanes).
@@ -362,6 +376,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       ++icount;
     }
   } else if (warp == 1) {
+    if constexpr (BM == BM_LOWRANK) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(LR_REGS_PRODUCERS));
     // -------------------------------------------------------------- S issuer
     // S(g) = Q K(g)^T into S buffer g % 2 as soon as K(g) is in and the warpgroup that
     // owns tile g - 2 has read S(g - 2) out of TMEM, which it does first thing, so each
@@ -394,6 +409,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       ++icount;
     }
   } else if (warp == 2) {
+    if constexpr (BM == BM_LOWRANK) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(LR_REGS_PRODUCERS));
     // -------------------------------------------------------------- bias loader
     // Fast path (rows of rel 16-byte aligned): one 3-D TMA box per group of 16 tokens
     // (84 buckets x 16 rows, laid out so the softmax reads see at most 2-way bank
@@ -425,19 +441,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         BT* sb = reinterpret_cast<BT*>(smem + L_::bias + (size_t)slot * BS::SLOT_BYTES);
         const int dmin0 = it.pos0 - (k0 + TILE_KEYS - 1);
         if constexpr (BM == BM_LOWRANK) {
-          // Group gr (rows 16 gr .. 16 gr + 15) holds buckets [x_g, x_g + 80), x_g = x_0 + 16 gr:
-          // G = R_g (16 x d_rel) Pt[x_g .. x_g + 79]^T, ten m16n8k16 n-tiles per k-step, fp32
-          // accumulate, operands by ldmatrix from the item's r rows and a ring of proj_t rows.
-          // Bucket b sits at ring row (b - base) mod 256, base = x_0 of the item's first bias
-          // tile; a tile reads 192 buckets [x_0, x_0 + 192), and each next tile of the item
-          // (x_0 - 64) needs only 64 new ones, whose 64-row chunk (never wrapping the ring) is
-          // loaded while this tile computes.  Rows past the item and buckets outside [0, E)
-          // arrive as zeros and are never used (invisible rows and keys, or distances >= E - 1).
-          const uint32_t nm =
-              __ballot_sync(0xffffffffu, lane < BS::NGROUP && bias_group_needed(a, it, k0, lane));
+          // Loader of the low-rank operands (the bias warps 12-15 compute the slot).  Bucket
+          // b sits at ring row (b - base) mod 256, base = x_0 of the item's first bias tile; a
+          // tile reads the 192 buckets [x_0, x_0 + 192), and each next tile of the item
+          // (x_0 - 64) needs only 64 new ones, whose 64-row chunk (never wrapping the ring)
+          // goes where bias tile t - 1 read, once the bias warps are done with it.  One load
+          // event per bias tile t: the item's r rows and first three chunks, or the chunk
+          // loaded during tile t - 1.  Rows past the item and buckets outside [0, E) arrive
+          // as zeros and are never used.
+          (void)sb;
+          (void)use;
           const int x0 = dmin0;
           const uint32_t chunk_bytes = (uint32_t)(LOWRANK_CHUNK * a.d_rel * 2);
           const uint32_t pitch = (uint32_t)a.d_rel * 2;
+          if (ev_waited >= 1)
+            (void)wait_flag(&c_done[(ev_waited - 1) & 1], (uint32_t)((ev_waited - 1) >> 1) & 1u, abort_flag, a.err);
+          ++ev_waited;   // here: bias tiles seen
           if (lr_item != i) {
             // first bias tile of the item: its r rows and chunks [x_0 + 64 m, +64), m = 0..2
             if (lane == 0) {
@@ -464,54 +483,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             }
             ++ev_issued;
           }
-          if (use >= 1) (void)wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err);
-          // this tile's rows arrived with event ev_waited (the item's first load, or the chunk
-          // loaded during the previous tile)
-          const bool ok = wait_flag(&w_full[ev_waited & 1], (uint32_t)(ev_waited >> 1) & 1u, abort_flag, a.err);
-          ++ev_waited;
-          if (nm && ok) {
-            const int q4 = lane & 3, rq = lane >> 2;
-            const uint32_t swm = (uint32_t)(a.d_rel / 8 - 1);   // 128- or 64-byte swizzle
-            const uint32_t rbase = smem_u32(smem + L_::lr_r), wbase = smem_u32(smem + L_::lr_w);
-            const int rel0 = x0 - lr_base;   // ring row of bucket x_0 is rel0 mod 256
-#pragma unroll 1
-            for (uint32_t mm = nm; mm; mm &= mm - 1) {
-              const int gr = __ffs(mm) - 1;
-              float acc[10][4];
-#pragma unroll
-              for (int nt = 0; nt < 10; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-#pragma unroll 1
-              for (int kp = 0; kp < a.d_rel / 16; kp += 2) {   // k-steps kp and kp + 1
-                uint32_t af[2][4];
-#pragma unroll
-                for (int s2 = 0; s2 < 2; ++s2) {
-                  const uint32_t off = (uint32_t)(BIAS_BOX_ROWS * gr + (lane & 15)) * pitch +
-                                       (uint32_t)(2 * (kp + s2) + (lane >> 4)) * 16;
-                  ldmatrix_x4(rbase + (off ^ (((off >> 7) & swm) << 4)), af[s2][0], af[s2][1], af[s2][2], af[s2][3]);
-                }
-                // all 10 B fragments first, then the 20 products (independent accumulators)
-                uint32_t bf[10][4];
-#pragma unroll
-                for (int nt = 0; nt < 10; ++nt) {
-                  const uint32_t row = (uint32_t)(rel0 + BIAS_BOX_ROWS * gr + 8 * nt + (lane & 7)) & (LOWRANK_RING_ROWS - 1);
-                  const uint32_t off = row * pitch + (uint32_t)(2 * kp + (lane >> 3)) * 16;
-                  ldmatrix_x4(wbase + (off ^ (((off >> 7) & swm) << 4)), bf[nt][0], bf[nt][1], bf[nt][2], bf[nt][3]);
-                }
-#pragma unroll
-                for (int nt = 0; nt < 10; ++nt) mma_bf16_16816(acc[nt], af[0], bf[nt][0], bf[nt][1]);
-#pragma unroll
-                for (int nt = 0; nt < 10; ++nt) mma_bf16_16816(acc[nt], af[1], bf[nt][2], bf[nt][3]);
-              }
-              float* gdst = reinterpret_cast<float*>(sb) + gr * BS::GROUP;
-#pragma unroll
-              for (int nt = 0; nt < 10; ++nt) {
-                const int col = 8 * nt + 2 * q4;
-                *reinterpret_cast<float2*>(gdst + rq * BS::COLS + col) = make_float2(acc[nt][0], acc[nt][1]);
-                *reinterpret_cast<float2*>(gdst + (rq + 8) * BS::COLS + col) = make_float2(acc[nt][2], acc[nt][3]);
-              }
-            }
-          }
-          mbar_arrive(&b_full[slot]);   // all 32 lanes: their stores are in the slot
           continue;
         }
         if (use >= 1) (void)wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err);
@@ -558,7 +529,91 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       for (int e = ev_issued >= 2 ? ev_issued - 2 : 0; e < ev_issued; ++e)
         if (!mbar_wait_bounded(&w_full[e & 1], (uint32_t)(e >> 1) & 1u)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
     }
+  } else if (warp >= 12) {
+    if constexpr (BM == BM_LOWRANK) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(LR_REGS_BIAS));
+    // -------------------------------------------------------------- bias warps (low-rank)
+    // Warp 12 + w computes groups 2w and 2w + 1 (rows 32w .. 32w + 31) of every bias tile:
+    // G = R_g (16 x d_rel) Pt[x_g .. x_g + 79]^T, x_g = x_0 + 16 g, ten m16n8k16 n-tiles per
+    // k-step, fp32 accumulate, operands by ldmatrix from the r rows and the projection ring
+    // the loader keeps (bucket b at ring row (b - base) mod 256).
+    if constexpr (BM == BM_LOWRANK) {
+      const int wb = warp - 12;
+      int bcnt[2] = {0, 0};
+      int g = 0, bt = 0, lr_item = -1, lr_base = 0;
+      const int q4 = lane & 3, rq = lane >> 2;
+      const uint32_t pitch = (uint32_t)a.d_rel * 2;
+      const uint32_t swm = (uint32_t)(a.d_rel / 8 - 1);   // 128- or 64-byte swizzle
+      const uint32_t rbase = smem_u32(smem + L_::lr_r), wbase = smem_u32(smem + L_::lr_w);
+      for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
+        PItem it;
+        if (!get_item(a, i, it) || it.ntile == 0) continue;
+        for (int j = 0; j < it.ntile; ++j, ++g) {
+          const int k0 = (it.kt0 + j) * TILE_KEYS;
+          if (!tile_needs_bias(it.pos0, k0, a.E)) continue;
+          const int u = bcnt[g & 1]++;
+          const int slot = (g & 1) * BS::PER_WG + u % BS::PER_WG, use = u / BS::PER_WG;
+          float* sb = reinterpret_cast<float*>(smem + L_::bias + (size_t)slot * BS::SLOT_BYTES);
+          const int x0 = it.pos0 - (k0 + TILE_KEYS - 1);
+          if (lr_item != i) {
+            lr_item = i;
+            lr_base = x0;
+          }
+          const uint32_t nm =
+              __ballot_sync(0xffffffffu, lane < BS::NGROUP && bias_group_needed(a, it, k0, lane)) & (3u << (2 * wb));
+          if (use >= 1) (void)wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err);
+          const bool ok = wait_flag(&w_full[bt & 1], (uint32_t)(bt >> 1) & 1u, abort_flag, a.err);
+          if (nm && ok) {
+            const int rel0 = x0 - lr_base;   // ring row of bucket x_0 is rel0 mod 256
+#pragma unroll 1
+            for (uint32_t mm = nm; mm; mm &= mm - 1) {
+              const int gr = __ffs(mm) - 1;
+              float acc[10][4];
+#pragma unroll
+              for (int nt = 0; nt < 10; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+              // every B row address of a lane has the same row mod 8, so one swizzled chunk offset
+              const uint32_t brow0 = (uint32_t)(rel0 + BIAS_BOX_ROWS * gr + (lane & 7));
+#pragma unroll 1
+              for (int kp = 0; kp < a.d_rel / 16; kp += 2) {   // k-steps kp and kp + 1
+                uint32_t af[2][4];
+#pragma unroll
+                for (int s2 = 0; s2 < 2; ++s2) {
+                  const uint32_t off = (uint32_t)(BIAS_BOX_ROWS * gr + (lane & 15)) * pitch +
+                                       (uint32_t)(2 * (kp + s2) + (lane >> 4)) * 16;
+                  ldmatrix_x4(rbase + (off ^ (((off >> 7) & swm) << 4)), af[s2][0], af[s2][1], af[s2][2], af[s2][3]);
+                }
+#pragma unroll
+                for (int h5 = 0; h5 < 10; h5 += 5) {   // five n-tiles at a time
+                  uint32_t bf[5][4];
+#pragma unroll
+                  for (int n5 = 0; n5 < 5; ++n5) {
+                    const uint32_t row = (brow0 + 8 * (h5 + n5)) & (LOWRANK_RING_ROWS - 1);
+                    const uint32_t off = row * pitch + (uint32_t)(2 * kp + (lane >> 3)) * 16;
+                    ldmatrix_x4(wbase + (off ^ (((off >> 7) & swm) << 4)), bf[n5][0], bf[n5][1], bf[n5][2], bf[n5][3]);
+                  }
+#pragma unroll
+                  for (int n5 = 0; n5 < 5; ++n5) mma_bf16_16816(acc[h5 + n5], af[0], bf[n5][0], bf[n5][1]);
+#pragma unroll
+                  for (int n5 = 0; n5 < 5; ++n5) mma_bf16_16816(acc[h5 + n5], af[1], bf[n5][2], bf[n5][3]);
+                }
+              }
+              float* gdst = sb + gr * BS::GROUP;
+#pragma unroll
+              for (int nt = 0; nt < 10; ++nt) {
+                const int col = 8 * nt + 2 * q4;
+                *reinterpret_cast<float2*>(gdst + rq * BS::COLS + col) = make_float2(acc[nt][0], acc[nt][1]);
+                *reinterpret_cast<float2*>(gdst + (rq + 8) * BS::COLS + col) = make_float2(acc[nt][2], acc[nt][3]);
+              }
+            }
+          }
+          __syncwarp();
+          mbar_arrive(&b_full[slot]);        // all 32 lanes: their stores are in the slot
+          if (lane == 0) mbar_arrive(&c_done[bt & 1]);   // this warp's reads of the ring and r rows are done
+          ++bt;
+        }
+      }
+    }
   } else {
+    if constexpr (BM == BM_LOWRANK) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(LR_REGS_SOFTMAX));
     // -------------------------------------------------------------- softmax warpgroups
     // Warpgroup wg (warps 4-7: wg 0, warps 8-11: wg 1) owns the tiles g with g % 2 == wg
     // and its own O accumulator in TMEM; thread r of a warpgroup owns row r.  At the end
@@ -893,7 +948,8 @@ cudaError_t launch_prefill_tc_t(const PrefillMaps& m, const PrefillArgs& a, cuda
   if (e != cudaSuccess) return e;
   const long long items = (long long)a.num_q_tiles * a.B * a.Hq;
   const int grid = (int)std::min<long long>(items, num_sms_pf());
-  prefill_tc_kernel<D, BM><<<grid, PT_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.q3, m.bias, m.lr_r, m.lr_p, a);
+  prefill_tc_kernel<D, BM><<<grid, BM == BM_LOWRANK ? PT_THREADS_LR : PT_THREADS, smem, stream>>>(
+      m.k, m.v, m.k3, m.v3, m.q3, m.bias, m.lr_r, m.lr_p, a);
   return cudaGetLastError();
 }
 
