@@ -304,6 +304,8 @@ WORKLOAD_DESC = {
     "global_prefill_lowrank": "global_prefill with the bias in low-rank form (inkling_attn_prefill_lowrank_bias): "
                               "4 x 8192 tokens, 64 q heads / 8 kv heads, head_dim 128, full causal, page 64, "
                               "E 4096 (clamped), r [32768,64,64] bf16, projection [4096,64] bf16",
+    "global_prefill_lowrank_small": "global_prefill_lowrank_small (profiling size): 1 x 2048 tokens, 64 q heads / "
+                                    "8 kv heads, head_dim 128, full causal, page 64, E 4096, r [2048,64,64] bf16",
     "global_prefill_small": "global_prefill_small (profiling size): 1 x 2048 tokens, 64 q heads / "
                             "8 kv heads, head_dim 128, full causal, page 64, bias [2048,64,4096] fp32",
     "kv_prefill_global": "K/V short convolution (ks 4) + paged write of a global-layer prefill step: "
@@ -333,6 +335,8 @@ def workload_instances(name, dev):
         return [W.global_prefill(dev, seed=4, bias_dtype=torch.bfloat16)]   # 19 GB > L2
     if name == "global_prefill_lowrank":
         return [W.global_prefill_lowrank(dev, seed=4)]                # r 268 MB + Q/out 1 GB > L2
+    if name == "global_prefill_lowrank_small":
+        return [W.global_prefill_lowrank(dev, seed=4, batch=1, tokens=2048)]   # profiling size
     if name == "global_prefill_small":
         return [W.global_prefill(dev, seed=4, batch=1, tokens=2048)]  # 2.2 GB > L2
     raise ValueError(name)
