@@ -435,6 +435,19 @@ def measure(binding, name, dev, steps, warmup, stream, hbm_peak, bf16_peak):
             "launches_per_step": 1, "bound": "hbm" if t_hbm >= t_tensor else "tensor", "probs": probs}
 
 
+def whole_job(ms_local, value_local, world, device):
+    """(ms, value, scale) of the whole job: the step time is the slowest rank's (max over
+    ranks), and the value is this rank's throughput recomputed at that time, times the
+    number of replicas (every rank runs the same workload)."""
+    ms = ms_local
+    if world > 1:
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    scale = ms_local / ms
+    return ms, value_local * scale * world, scale
+
+
 def run_ours(args, rank, world, local_rank):
     from paged_attention_relative_gqa_gb300 import binding, build
 
@@ -457,13 +470,7 @@ def run_ours(args, rank, world, local_rank):
     r = measure(binding, name, dev, args.steps, args.warmup, stream, hbm_peak, bf16_peak)
     clk = clocks.stop()
     barrier()
-    ms = r["ms"]
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    scale = r["ms"] / ms  # value recomputed at the slowest rank's time
-    value = r["value"] * scale * world
+    ms, value, scale = whole_job(r["ms"], r["value"], world, dev)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": r["unit"], "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
