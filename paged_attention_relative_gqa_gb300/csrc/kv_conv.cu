@@ -80,10 +80,24 @@ __device__ __forceinline__ int find_seq_shared(const int* cu_q, int B, int t) {
   return lo;
 }
 
+// Requests whose offsets and lengths the per-thread kernel stages in shared memory (one
+// parallel load per block instead of a chain of dependent loads per thread).
+constexpr int KV_SMALL_CACHED_SEQS = 1023;
+
 template <int KS, int TOK>
 __global__ void __launch_bounds__(KV_CONV_THREADS, 2) kv_conv_write_kernel(const KvConvArgs a) {
   const long long gid = (long long)blockIdx.x * KV_CONV_THREADS + threadIdx.x;
   const int row_elems = a.nvec * 8;
+  __shared__ int cu_s[KV_SMALL_CACHED_SEQS + 1];
+  __shared__ int len_s[KV_SMALL_CACHED_SEQS];
+  const bool cached = a.B <= KV_SMALL_CACHED_SEQS;
+  if (cached) {
+    for (int j = threadIdx.x; j <= a.B; j += KV_CONV_THREADS) {
+      cu_s[j] = __ldg(a.cu_q + j);
+      if (j < a.B) len_s[j] = __ldg(a.seq_lens + j);
+    }
+  }
+  __syncthreads();
   if (gid < a.conv_items) {
     // ---------------------------------------------------------------- convolution
     const int v = (int)(gid % a.nvec);
@@ -125,14 +139,14 @@ __global__ void __launch_bounds__(KV_CONV_THREADS, 2) kv_conv_write_kernel(const
     int k = 0;
     while (k < TOK && t0 + k < a.T) {
       const int t = t0 + k;
-      const int b = find_seq(a.cu_q, a.B, t);
+      const int b = cached ? find_seq_shared(cu_s, a.B, t) : find_seq(a.cu_q, a.B, t);
       if (b < 0) {                                    // token outside every request
         record_error(a.err, INK_DEVERR_BAD_ROWS);
         ++k;
         continue;
       }
-      const int seq_start = __ldg(a.cu_q + b);
-      const int seq_end = __ldg(a.cu_q + b + 1);
+      const int seq_start = cached ? cu_s[b] : __ldg(a.cu_q + b);
+      const int seq_end = cached ? cu_s[b + 1] : __ldg(a.cu_q + b + 1);
       const int k_end = min(TOK, seq_end - t0);
       if (seq_start < 0) {                            // request rows named before row 0
         record_error(a.err, INK_DEVERR_BAD_ROWS);
@@ -140,7 +154,7 @@ __global__ void __launch_bounds__(KV_CONV_THREADS, 2) kv_conv_write_kernel(const
         continue;
       }
       const int n = seq_end - seq_start;
-      const int L = __ldg(a.seq_lens + b);
+      const int L = cached ? len_s[b] : __ldg(a.seq_lens + b);
       const bool seq_ok = n <= L;
       if (!seq_ok) record_error(a.err, INK_DEVERR_QLEN_EXCEEDS_KV);
       const int i0 = t - seq_start;                   // index of token t among the request's new rows
@@ -200,8 +214,8 @@ __global__ void __launch_bounds__(KV_CONV_THREADS, 2) kv_conv_write_kernel(const
     const int b = (int)(rest % a.B);
     const int z = (int)(rest / a.B);
     const int col = v * 8;
-    const int seq_start = __ldg(a.cu_q + b);
-    const int n = max(__ldg(a.cu_q + b + 1) - seq_start, 0);
+    const int seq_start = cached ? cu_s[b] : __ldg(a.cu_q + b);
+    const int n = max((cached ? cu_s[b + 1] : __ldg(a.cu_q + b + 1)) - seq_start, 0);
     uint4 row = make_uint4(0, 0, 0, 0);
     if (r + n < KS - 1) {
       row = ld_row16(a.st_in[z] + ((size_t)b * (KS - 1) + (r + n)) * row_elems + col);
