@@ -314,6 +314,9 @@ WORKLOAD_DESC = {
                      "16 kv heads, head_dim 128, contexts U{1024..8192}, page 64 (L2 flushed before each call)",
     "mixed": "mixed serving step: 5 SWA + 1 global layer, each one prefill call (8 x 2048 tokens) "
              "and one decode call (128 requests, contexts log-uniform 512..16384)",
+    "mixed_kv_graph": "mixed serving step with each layer's K/V write, replayed from one CUDA graph (24 calls): "
+                      "5 SWA + 1 global layer, each: K/V short convolution (ks 4) + paged write of the prefill "
+                      "rows (8 x 2048) and of the decode rows (128), then the prefill call and the decode call",
     "mixed_graph": "mixed serving step replayed from one CUDA graph (its 12 calls captured once): 5 SWA + "
                    "1 global layer, each one prefill call (8 x 2048 tokens) and one decode call (128 "
                    "requests, contexts log-uniform 512..16384)",
@@ -379,10 +382,16 @@ def measure(binding, name, dev, steps, warmup, stream, hbm_peak, bf16_peak):
     """Time one workload; returns a dict of its numbers (value in its own unit)."""
     if name.startswith("kv_"):
         return measure_kv(binding, name, dev, steps, warmup, stream, hbm_peak)
-    if name in ("mixed", "mixed_graph"):
+    if name in ("mixed", "mixed_graph", "mixed_kv_graph"):
         layers = [W.mixed_layer(k, i, dev) for i, k in enumerate(W.MIXED_STACK)]
         calls, keep = [], []
-        for pre, dec in layers:
+        for li, (pre, dec) in enumerate(layers):
+            if name == "mixed_kv_graph":
+                # the layer's K/V write comes first: prefill rows, then decode rows
+                for j, prob in enumerate((pre, dec)):
+                    fn, ws = kv_call(binding, W.kv_step_for(prob, W.KV_CONV_KERNEL, seed=7000 + 10 * li + j), dev)
+                    keep.append((ws, None))
+                    calls.append(fn)
             for prob in (pre, dec):
                 params = binding.params_of(prob)
                 ws = binding.alloc_workspace(params, True, dev)
@@ -394,7 +403,7 @@ def measure(binding, name, dev, steps, warmup, stream, hbm_peak, bf16_peak):
             for c in calls:
                 c()
 
-        if name == "mixed_graph":
+        if name in ("mixed_graph", "mixed_kv_graph"):
             with torch.cuda.stream(stream):
                 mixed_step()               # eager once: one-time per-device setup
             torch.cuda.synchronize()
@@ -411,8 +420,8 @@ def measure(binding, name, dev, steps, warmup, stream, hbm_peak, bf16_peak):
         # every token of the step passes through all 6 layers once
         ntok = layers[0][0].total_q + layers[0][1].total_q
         return {"ms": m, "value": ntok / m * 1e3, "unit": "tok/s", "tok_s": ntok / m * 1e3,
-                "tokens_per_step": ntok, "launches_per_step": len(calls), "graph": name == "mixed_graph",
-                "per_call_ms(prefill,decode)xlayer": per_call}
+                "tokens_per_step": ntok, "launches_per_step": len(calls), "graph": name != "mixed",
+                "per_call_ms_in_step_order": per_call}
     probs = workload_instances(name, dev)
     m = bench_workload(binding, probs, steps, warmup, stream)
     p0 = probs[0]
@@ -493,7 +502,7 @@ def run_ours(args, rank, world, local_rank):
         line["e2e"] = {"value": round(r["bytes"] / e2e_ms / 1e6 * world, 2), "unit": "GB/s",
                        "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         del step
-    elif name not in ("mixed", "mixed_graph"):
+    elif name not in ("mixed", "mixed_graph", "mixed_kv_graph"):
         decode = "flops" not in r
         src, kernel = ("decode.cu", "decode_persistent_kernel") if decode else ("prefill_tc.cu", "prefill_tc_kernel")
         if r["bound"] == "hbm":
@@ -539,7 +548,8 @@ def run_ours(args, rank, world, local_rank):
         wl = {}
         steps_x = max(5, args.steps // 4)
         for other in ("global_decode", "swa_prefill_tiny", "global_prefill", "global_prefill_bf16bias",
-                      "global_prefill_lowrank", "mixed", "mixed_graph", "kv_prefill_global", "kv_decode_swa"):
+                      "global_prefill_lowrank", "mixed", "mixed_graph", "mixed_kv_graph", "kv_prefill_global",
+                      "kv_decode_swa"):
             if other == name:
                 continue
             st = steps_x if other in ("global_decode", "swa_prefill_tiny", "kv_prefill_global",

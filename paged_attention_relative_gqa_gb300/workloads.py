@@ -378,6 +378,31 @@ def make_kv_step(*, num_kv_heads: int, head_dim: int, page_size: int, kernel_siz
                   cu_q_lens=cu.to(device))
 
 
+def kv_step_for(prob: Problem, kernel_size: int, seed: int) -> KvStep:
+    """K/V write inputs for an attention problem's step, writing into that problem's own pools
+    (its cache, block table, lengths and query offsets are shared, not copied): the new rows,
+    filters and carried state are drawn as in ``make_kv_step``."""
+    dev = prob.k_cache.device
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    T, B, Hkv, D, ks = prob.total_q, prob.num_seqs, prob.num_kv_heads, prob.head_dim, kernel_size
+    k_new = _randn((T, Hkv, D), gen, dev, torch.bfloat16)
+    v_new = _randn((T, Hkv, D), gen, dev, torch.bfloat16)
+    w_k = _randn((Hkv, D, ks), gen, dev, torch.float32, std=1.0 / math.sqrt(ks))
+    w_v = _randn((Hkv, D, ks), gen, dev, torch.float32, std=1.0 / math.sqrt(ks))
+    state_k = _randn((B, ks - 1, Hkv, D), gen, dev, torch.bfloat16)
+    state_v = _randn((B, ks - 1, Hkv, D), gen, dev, torch.bfloat16)
+    fresh = [b for b, (n, L) in enumerate(zip(prob.q_lens, prob.seq_lens_list)) if n == L]
+    if fresh and ks > 1:
+        idx = torch.tensor(fresh, device=dev)
+        state_k[idx] = 0
+        state_v[idx] = 0
+    return KvStep(num_kv_heads=Hkv, head_dim=D, page_size=prob.page_size, kernel_size=ks, q_lens=list(prob.q_lens),
+                  seq_lens_list=list(prob.seq_lens_list), k_new=k_new, v_new=v_new, w_k=w_k, w_v=w_v,
+                  state_k=state_k, state_v=state_v, k_cache=prob.k_cache, v_cache=prob.v_cache,
+                  block_table=prob.block_table, seq_lens=prob.seq_lens, cu_q_lens=prob.cu_q_lens)
+
+
 # Short-convolution kernel size of the K/V write workloads: the pages give none; 4 is the
 # usual width of a causal short convolution in hybrid models.
 KV_CONV_KERNEL = 4

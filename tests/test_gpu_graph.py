@@ -80,3 +80,45 @@ def test_noalloc_decode_replays_from_a_cuda_graph():
         graph.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, eager)
+
+
+def test_layer_step_with_kv_write_replays_and_matches_the_oracle():
+    """A layer's K/V write (conv + paged write of the prefill rows) and its prefill attention
+    captured together: replays give the eager bits, and the attention output, checked on
+    sampled rows against the oracle run on the pools as written, is within the prefill
+    tolerances."""
+    import numpy as np
+    from tests.parity import compare, gpu_rows, oracle_rows
+
+    pre, _ = W.mixed_layer("swa", 1, DEV)
+    step = W.kv_step_for(pre, W.KV_CONV_KERNEL, seed=123)
+    kvp = binding.make_params(num_seqs=step.num_seqs, num_q_heads=step.num_kv_heads, num_kv_heads=step.num_kv_heads,
+                              head_dim=step.head_dim, page_size=step.page_size, max_pages_per_seq=step.max_pages,
+                              num_pages=step.num_pages, rel_extent=1, window=-1, sm_scale=1.0)
+    ws_kv = binding.alloc_workspace(kvp, False, torch.device(DEV))
+    sk, sv = torch.empty_like(step.state_k), torch.empty_like(step.state_v)
+    out = torch.empty_like(pre.q)
+    ws = binding.alloc_workspace(binding.params_of(pre), True, torch.device(DEV))
+    attn = _calls(pre, out, ws)
+
+    def layer():
+        binding.inkling_attn_kv_conv_write(kvp, step.k_new, step.v_new, step.cu_q_lens, step.seq_lens,
+                                           step.block_table, step.w_k, step.w_v, step.state_k, step.state_v,
+                                           sk, sv, step.k_cache, step.v_cache, ws_kv)
+        attn()
+
+    layer()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer()
+    for _ in range(2):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    assert binding.inkling_attn_read_device_error(ws_kv) == 0
+    assert binding.inkling_attn_read_device_error(ws) == 0
+    rows = W.sample_rows(pre, per_seq=64, seed=9)
+    compare(gpu_rows(out, rows), oracle_rows(pre, rows), "layer step with K/V write (sampled rows)")
