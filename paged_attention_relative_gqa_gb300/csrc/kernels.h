@@ -129,7 +129,7 @@ struct KvConvArgs {
 // Largest dynamic shared memory of the staged K/V kernel.
 constexpr size_t KV_STAGED_SMEM_MAX = 216 * 1024;
 
-int kv_conv_tokens_per_thread(long long total_q, int nvec);
+int kv_conv_tokens_per_thread(long long total_q, int nvec, int num_sms);
 size_t kv_staged_smem_bytes(int tile_tokens, int kernel_size, int nvec, int stages);
 // Fill tile_tokens, stages, tok, nchunks and conv_items of `a` (T, nvec, B set).
 void kv_conv_plan(KvConvArgs& a, int kernel_size, int num_sms);

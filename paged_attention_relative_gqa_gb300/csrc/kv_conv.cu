@@ -568,18 +568,18 @@ void kv_conv_plan(KvConvArgs& a, int kernel_size, int num_sms) {
   const long long units = 2ll * ((a.T + tt - 1) / tt);
   a.tile_tokens = tt;
   a.stages = (stages >= 2 && units >= num_sms) ? stages : 0;
-  a.tok = kv_conv_tokens_per_thread(a.T, a.nvec);
+  a.tok = kv_conv_tokens_per_thread(a.T, a.nvec, num_sms);
   a.nchunks = (a.T + a.tok - 1) / a.tok;
   a.conv_items = 2ll * a.nchunks * a.nvec;
 }
 
-int kv_conv_tokens_per_thread(long long total_q, int nvec) {
+int kv_conv_tokens_per_thread(long long total_q, int nvec, int num_sms) {
   // Runs of 8 tokens amortise the window reload and keep 8 loads in flight per thread,
   // but leave few threads when the step has few tokens (decode: one token per request,
   // where every token also starts a new request); there one token per thread keeps the
-  // GPU's threads busy instead.
+  // GPU's threads busy instead (at least 1024 threads per SM at 8).
   const long long threads_at_8 = 2ll * nvec * ((total_q + 7) / 8);
-  return threads_at_8 >= 152ll * 1024 ? 8 : 1;
+  return threads_at_8 >= (long long)num_sms * 1024 ? 8 : 1;
 }
 
 cudaError_t launch_kv_conv(const KvConvArgs& a, int kernel_size, cudaStream_t stream) {
