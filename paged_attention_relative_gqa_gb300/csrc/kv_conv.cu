@@ -12,14 +12,18 @@
 // the last ks - 1 raw rows of (state, new rows).
 //
 // The work is pure streaming: every input row is read once from HBM and every output row
-// written once, so the kernel is HBM-bound.  One thread owns one 16-byte vector (8
-// channels) of either K or V over a run of TOK consecutive tokens: it loads its TOK rows
-// up front (TOK independent 16-byte loads in flight), keeps the last ks - 1 rows of the
-// run in registers as a sliding window, and reloads the window only where a run starts or
-// crosses into the next request.  Consecutive threads take consecutive vectors of a row,
-// so every load and store of a warp is 512 contiguous bytes of one row (or 256 bytes per
-// KV head in the cache).  A second set of threads in the same launch copies the carried
-// state rows.
+// written once, so it is HBM-bound.  Two kernels do it:
+//  - kv_conv_staged_kernel, for steps with at least one tile of K and one of V per SM
+//    (prefill): persistent, token tiles bulk-copied into a shared-memory ring (see the
+//    comment above it);
+//  - kv_conv_write_kernel, for smaller steps (decode): one thread owns one 16-byte vector
+//    (8 channels) of either K or V over a run of TOK consecutive tokens (1 or 8).  It loads
+//    its TOK rows up front (TOK independent 16-byte loads in flight), keeps the last
+//    ks - 1 rows in registers as a sliding window, and reloads the window only where a run
+//    starts or crosses into the next request.  Consecutive threads take consecutive vectors
+//    of a row, so every load and store of a warp is 512 contiguous bytes of one row (or 256
+//    bytes per KV head in the cache).
+// In both, extra threads of the same launch copy the carried state rows.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
