@@ -28,6 +28,10 @@
 //           pattern there is harmless.  O is rescaled in TMEM only when a row's max grows
 //           by more than 2^8.  Epilogue: the two partial results are merged,
 //           O / l -> bf16 -> out.
+// Bias modes: fp32 or bf16 rel_logits (the slot loaded by TMA, as above), or the bias in
+// low-rank form (BM_LOWRANK, 512 threads): there warp 2 only loads r rows and projection
+// rows by TMA, and warps 12-15 compute the slot with warp MMA; the softmax warpgroups are
+// the same in every mode.
 #include <algorithm>
 #include <type_traits>
 
