@@ -152,11 +152,12 @@ ink_status_t inkling_attn_prefill_bf16bias(const ink_attn_params_t* params, cons
  *   r           device, bf16 [total_q, Hq, d_rel], 16-byte aligned
  *   rel_proj_t  device, bf16 [E, d_rel]: rel_logits_proj transposed (bucket-major, so each
  *               bucket's d_rel coefficients are contiguous), 16-byte aligned
- *   d_rel       32 or 64 (else INK_ERR_BAD_SHAPE); the pages do not give it
- * The products are summed in fp32 from the bf16 operands (tensor-core warp MMA for the
- * buckets of a tile, a plain fp32 dot product for the clamped bucket E - 1); the rest of
- * the arithmetic is that of inkling_attn_prefill.  Every other argument and result as for
- * inkling_attn_prefill.
+ *   d_rel       64 (else INK_ERR_BAD_SHAPE); the pages do not give it
+ * The products are summed in fp32 from the bf16 operands (tensor-core MMA for the buckets
+ * of a tile, a plain fp32 dot product for the clamped bucket E - 1) and the tile's bias
+ * values are kept in fp16 until they are added to the fp32 scores (relative rounding
+ * 2^-11); the rest of the arithmetic is that of inkling_attn_prefill.  Every other
+ * argument and result as for inkling_attn_prefill.
  */
 ink_status_t inkling_attn_prefill_lowrank_bias(const ink_attn_params_t* params, const void* q,
                                                const int32_t* cu_q_lens, int32_t max_q_len, int32_t total_q,

@@ -352,7 +352,7 @@ ink_status_t prefill_impl(const ink_attn_params_t* params, const void* q, const 
     return INK_ERR_NULL_PTR;
   if (lowrank ? (!lr_r || !lr_proj_t) : !rel_logits) return INK_ERR_NULL_PTR;
   if (max_q_len < 0 || total_q < 0) return INK_ERR_BAD_SHAPE;
-  if (lowrank && d_rel != 32 && d_rel != 64) return INK_ERR_BAD_SHAPE;
+  if (lowrank && d_rel != ink::LOWRANK_MAX_D) return INK_ERR_BAD_SHAPE;
   if ((long long)total_q * params->num_q_heads >= (1ll << 31)) return INK_ERR_TOO_LARGE;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(cu_q_lens, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))

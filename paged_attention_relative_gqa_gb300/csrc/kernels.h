@@ -98,8 +98,7 @@ constexpr int BIAS_BOX_ROWS = 16;   // tokens per bias box
 constexpr int BIAS_BOX_COLS_BF16 = 88;   // buckets per bias box row, bf16 bias
 constexpr int PREFILL_ROWS = 128;        // new tokens per prefill work item
 constexpr int LOWRANK_CHUNK = 64;        // projection rows per TMA box (one key tile's new buckets)
-constexpr int LOWRANK_RING_ROWS = 256;   // projection rows held: a tile's 192 plus the next tile's 64
-constexpr int LOWRANK_MAX_D = 64;        // largest d_rel of the low-rank bias
+constexpr int LOWRANK_MAX_D = 64;        // d_rel of the low-rank bias (the MMA's K: four K-steps of 16)
 
 cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int head_dim,
                               cudaStream_t stream);

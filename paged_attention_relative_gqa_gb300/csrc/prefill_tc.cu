@@ -60,31 +60,39 @@ static_assert(LR_REGS_PRODUCERS + 2 * LR_REGS_SOFTMAX + LR_REGS_BIAS <= 4 * (655
 // each bank at most twice); bf16: COLS 88 (also at most two rows per bank word).
 // Each softmax warpgroup owns PER_WG slots that it fills in turn; every slot then has one
 // consumer taking its fills in order, so a parity wait never matches a phase two behind.
-// Bias modes: BM_F32 and BM_BF16 load the slot from rel_logits by TMA; BM_LOWRANK computes
-// an fp32 slot from r and the projection with warp MMA, one group at x_g = dmin0 + 16 g
-// exactly (no TMA alignment to keep), so 64 + 15 = 79 buckets a row: 80 columns, ten
-// 8-bucket n-tiles.
+// Bias modes: BM_F32 and BM_BF16 load the slot from rel_logits by TMA; BM_LOWRANK builds an
+// fp16 slot from tcgen05 products of r and the projection, one group at x_g = dmin0 + 16 g
+// exactly (no TMA alignment to keep), so 64 + 15 = 79 buckets a row: 80 columns.  It keeps
+// four slots, one per bias tile mod 4 (a tile's buckets are written as the products of
+// three consecutive tiles arrive).
 constexpr int BM_F32 = 0, BM_BF16 = 1, BM_LOWRANK = 2;
 
 template <int BM>
 struct BiasShape {
-  using T = typename std::conditional<BM == BM_BF16, __nv_bfloat16, float>::type;
+  using T = typename std::conditional<BM == BM_BF16, __nv_bfloat16,
+                                      typename std::conditional<BM == BM_LOWRANK, __half, float>::type>::type;
   static constexpr int COLS = BM == BM_BF16 ? BIAS_BOX_COLS_BF16 : (BM == BM_LOWRANK ? 80 : BIAS_BOX_COLS);
   static constexpr int ALIGN = BM == BM_LOWRANK ? 1 : 16 / (int)sizeof(T);   // x_g is a multiple of ALIGN
   static constexpr int GROUP = BIAS_BOX_ROWS * COLS;          // elements per group
   static constexpr int NGROUP = PT_ROWS / BIAS_BOX_ROWS;      // groups per tile
   static constexpr int SLOT_BYTES = NGROUP * GROUP * (int)sizeof(T);
   static constexpr int PER_WG = 1;                            // slots per softmax warpgroup
-  static constexpr int SLOTS = 2 * PER_WG;
+  static constexpr int SLOTS = BM == BM_LOWRANK ? 4 : 2 * PER_WG;
   static_assert(COLS >= TILE_KEYS + BIAS_BOX_ROWS - 1 + ALIGN - 1, "bias box too narrow");
   static_assert((COLS * (int)sizeof(T)) % 16 == 0 && (GROUP * (int)sizeof(T)) % 128 == 0, "TMA alignment");
 };
 
 __device__ __forceinline__ float to_float(float x) { return x; }
 __device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_float(__half x) { return __half2float(x); }
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
 
 constexpr uint32_t TM_S = 0;     // S[2]: 64 fp32 columns each
 constexpr uint32_t TM_P = 128;   // P[2]: 32 columns (64 bf16) each
+constexpr uint32_t TM_BC = 192;  // low-rank mode: a bias chunk, 64 fp32 columns (128 rows x 64 buckets)
 constexpr uint32_t TM_O = 256;   // O[2]: D fp32 columns each (one per softmax warpgroup)
 constexpr uint32_t TM_COLS = 512;
 constexpr float RESCALE_NAT = 5.545177444479562f;   // rescale O when a max grows by > 2^8
@@ -113,14 +121,15 @@ struct PtSmem {
   static constexpr size_t kst = q + S::Q_BYTES;
   static constexpr size_t vst = kst + (size_t)S::NK * S::KV_TILE;
   static constexpr size_t bias = vst + (size_t)S::NV * S::KV_TILE;
-  // low-rank mode: the item's r rows [128][d_rel] and a ring of projection rows
-  // [LOWRANK_RING_ROWS][d_rel] (bf16, swizzled like their TMA boxes), sized for d_rel 64
+  // low-rank mode: the item's r rows [128][64] and three chunks of projection rows
+  // [64 buckets][64] (bf16, 128-byte swizzle as TMA lands them; MMA operands A and B)
   static constexpr size_t lr_r = bias + (size_t)BS::SLOTS * BS::SLOT_BYTES;
-  static constexpr size_t lr_w = lr_r + (BM == BM_LOWRANK ? (size_t)PT_ROWS * LOWRANK_MAX_D * 2 : 0);
-  static constexpr size_t bars = lr_w + (BM == BM_LOWRANK ? (size_t)LOWRANK_RING_ROWS * LOWRANK_MAX_D * 2 : 0);
+  static constexpr size_t lr_p = lr_r + (BM == BM_LOWRANK ? (size_t)PT_ROWS * LOWRANK_MAX_D * 2 : 0);
+  static constexpr size_t bars = lr_p + (BM == BM_LOWRANK ? (size_t)3 * LOWRANK_CHUNK * LOWRANK_MAX_D * 2 : 0);
   // q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2],
-  // s_empty[2], o_done[2], o_free, b_full[NB], b_empty[NB], ml_full, ml_free, w_full[2], c_done[2]
-  static constexpr int NBAR = 2 + 2 * S::NK + 2 * S::NV + 2 + 2 + 2 + 1 + 2 * BS::SLOTS + 2 + 2 + 2;
+  // s_empty[2], o_done[2], o_free, b_full[NB], b_empty[NB], ml_full, ml_free,
+  // pt_full[3], r_full, bc_full, bc_empty
+  static constexpr int NBAR = 2 + 2 * S::NK + 2 * S::NV + 2 + 2 + 2 + 1 + 2 * BS::SLOTS + 2 + 6;
   static constexpr size_t vbad = bars + NBAR * 8;
   static constexpr size_t ml1 = vbad + S::NV * 8;          // float2 [128]
   static constexpr size_t misc = ml1 + PT_ROWS * 8;
@@ -195,6 +204,60 @@ __device__ __forceinline__ bool tile_needs_bias(int pos0, int k0, int E) {
   return pos0 - (k0 + TILE_KEYS - 1) < E - 1;
 }
 
+// ---- low-rank bias: the chunk sequence of a CTA.  An item's tiles that need bias are its
+// last ones (distances only shrink as k0 grows).  Tile t's bias window is the 192 buckets
+// [x_0, x_0 + 192), x_0 = pos0 - (k0 + 63); the next tile's window starts 64 lower.  So the
+// item's first bias tile needs three 64-bucket chunks [x_0 + 64 m, +64), m = 0..2, and every
+// further tile one new chunk [x_0, x_0 + 64).
+__device__ __forceinline__ int lr_first_bias_tile(const PrefillArgs& a, const PItem& it) {
+  int j = 0;
+  while (j < it.ntile && !tile_needs_bias(it.pos0, (it.kt0 + j) * TILE_KEYS, a.E)) ++j;
+  return j;
+}
+
+struct LrCursor {
+  PItem it;
+  int i, j, m, jb;  // item, tile, chunk of the first bias tile (0..2), first bias tile
+  int s;            // first bucket of the chunk
+  bool first;       // first chunk of its item (the item's r rows are needed)
+  bool valid;
+};
+
+__device__ __forceinline__ void lr_set(LrCursor& c) {
+  const int x0 = c.it.pos0 - ((c.it.kt0 + c.j) * TILE_KEYS + TILE_KEYS - 1);
+  c.s = c.j == c.jb ? x0 + LOWRANK_CHUNK * c.m : x0;
+  c.first = c.j == c.jb && c.m == 0;
+}
+
+__device__ __forceinline__ void lr_seek(const PrefillArgs& a, int total_items, int i, LrCursor& c) {
+  for (; i < total_items; i += gridDim.x) {
+    if (!get_item(a, i, c.it) || c.it.ntile == 0) continue;
+    const int jb = lr_first_bias_tile(a, c.it);
+    if (jb >= c.it.ntile) continue;
+    c.i = i;
+    c.jb = jb;
+    c.j = jb;
+    c.m = 0;
+    c.valid = true;
+    lr_set(c);
+    return;
+  }
+  c.valid = false;
+}
+
+__device__ __forceinline__ void lr_advance(const PrefillArgs& a, int total_items, LrCursor& c) {
+  if (c.j == c.jb && c.m < 2) {
+    ++c.m;
+  } else if (c.j + 1 < c.it.ntile) {
+    ++c.j;
+    c.m = 0;
+  } else {
+    lr_seek(a, total_items, c.i + gridDim.x, c);
+    return;
+  }
+  lr_set(c);
+}
+
 // A completed phase returns at once; otherwise give up at once if another warp of the
 // CTA has timed out, else wait (bounded) and on a timeout record it and tell the others.
 __device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err) {
@@ -239,11 +302,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   uint64_t* b_empty = b_full + BS::SLOTS;
   uint64_t* ml_full = b_empty + BS::SLOTS;
   uint64_t* ml_free = ml_full + 1;
-  uint64_t* w_full = ml_free + 1;   // low-rank mode [2]: loads of r rows / projection chunks, alternating
-  // low-rank mode [2]: the four bias warps are done with bias tile t (barrier t % 2; the
-  // loader waits for tile t - 1 before loading tile t + 1's rows, so neither barrier can
-  // run two phases ahead of its waiter)
-  uint64_t* c_done = w_full + 2;
+  // low-rank mode: projection chunk n is in slot n % 3 (pt_full[3]); the item's r rows are in
+  // (r_full); the bias product of chunk n is in TMEM (bc_full) / has been read out (bc_empty)
+  uint64_t* pt_full = ml_free + 1;
+  uint64_t* r_full = pt_full + 3;
+  uint64_t* bc_full = r_full + 1;
+  uint64_t* bc_empty = bc_full + 1;
   float2* ml1 = reinterpret_cast<float2*>(smem + L_::ml1);
   uint64_t* vbad = reinterpret_cast<uint64_t*>(smem + L_::vbad);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L_::misc);
@@ -272,10 +336,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     mbar_init(o_free, 4);
     mbar_init(ml_full, 4);
     mbar_init(ml_free, 4);
-    mbar_init(&w_full[0], 1);
-    mbar_init(&w_full[1], 1);
-    mbar_init(&c_done[0], 4);
-    mbar_init(&c_done[1], 4);
+    for (int x = 0; x < 3; ++x) mbar_init(&pt_full[x], 1);
+    mbar_init(r_full, 1);
+    mbar_init(bc_full, 1);
+    mbar_init(bc_empty, 4);
     for (int x = 0; x < BS::SLOTS; ++x) {
       mbar_init(&b_full[x], BM == BM_LOWRANK ? 128 : (a.bias_bulk ? 1 : 32));
       mbar_init(&b_empty[x], 4);
@@ -424,16 +488,84 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     // Warpgroup w's tiles (g % 2 == w) fill its PER_WG slots in turn: each slot has one
     // consumer that takes its fills in order, so a parity wait never sees a phase two
     // behind.  (V slots follow the same rule: NV is even.)
+    if (lane == 0 && a.bias_bulk) prefetch_tensormap(&tmB);
+    if constexpr (BM == BM_LOWRANK) {
+      // ------------------------------------------------------------ low-rank bias products
+      // For each chunk n of the CTA's chunk sequence: bias[row, bucket] for the item's 128
+      // rows and the chunk's 64 buckets, one tcgen05 MMA (M 128, N 64, K 64: four K-steps)
+      // into TMEM columns TM_BC, A = the item's r rows, B = the chunk's projection rows
+      // (both K-major, 128-byte swizzle).  Projection chunks are loaded two ahead into three
+      // slots; the single TMEM chunk is reused once the bias warps have read it out.
+      if (lane == 0) {
+        prefetch_tensormap(&tmR);
+        prefetch_tensormap(&tmP);
+      }
+      constexpr uint32_t PT_BYTES = LOWRANK_CHUNK * LOWRANK_MAX_D * 2;
+      LrCursor cur, pf;
+      lr_seek(a, total_items, blockIdx.x, cur);
+      pf = cur;
+      int issued = 0;
+#pragma unroll 1
+      for (int q = 0; q < 2 && pf.valid; ++q, ++issued) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&pt_full[q], PT_BYTES);
+          tma_load_2d(smem + L_::lr_p + (size_t)q * PT_BYTES, &tmP, 0, pf.s, &pt_full[q]);
+        }
+        lr_advance(a, total_items, pf);
+      }
+      int n = 0, ritems = 0;
+      bool r_pending = false;
+      while (cur.valid) {
+        bool ok = true;
+        // the product of chunk n - 1 has been read out of TMEM: its MMA is complete, so
+        // TMEM, the r rows and chunk slot (n - 1) % 3 are free
+        if (n >= 1) ok = wait_flag(bc_empty, (uint32_t)(n - 1) & 1u, abort_flag, a.err);
+        if (ok && cur.first) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(r_full, (uint32_t)(PT_ROWS * LOWRANK_MAX_D * 2));
+            tma_load_3d(smem + L_::lr_r, &tmR, 0, cur.it.h, cur.it.t0, r_full);
+          }
+          r_pending = true;
+          ok = wait_flag(r_full, (uint32_t)ritems & 1u, abort_flag, a.err);
+          ++ritems;
+          r_pending = !ok;
+        }
+        if (ok) ok = wait_flag(&pt_full[n % 3], (uint32_t)(n / 3) & 1u, abort_flag, a.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t rb = smem_u32(smem + L_::lr_r);
+        const uint32_t pb = smem_u32(smem + L_::lr_p + (size_t)(n % 3) * PT_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < LOWRANK_MAX_D / 16; ++kk) {
+          const uint64_t ad = umma_desc_sw128(rb + kk * 32, 16, 1024);
+          const uint64_t bd = umma_desc_sw128(pb + kk * 32, 16, 1024);
+          umma_ss_warp(tmem + TM_BC, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        umma_commit_warp(bc_full);
+        __syncwarp();
+        // chunk n + 2 into slot (n + 2) % 3, last read by MMA n - 1 (complete, see above)
+        if (pf.valid) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&pt_full[(n + 2) % 3], PT_BYTES);
+            tma_load_2d(smem + L_::lr_p + (size_t)((n + 2) % 3) * PT_BYTES, &tmP, 0, pf.s, &pt_full[(n + 2) % 3]);
+          }
+          ++issued;
+          lr_advance(a, total_items, pf);
+        }
+        lr_advance(a, total_items, cur);
+        ++n;
+      }
+      if (lane == 0) {
+        // after an abort, loads may still be landing: wait (bounded) for every load not yet
+        // waited for, so none is in flight when the CTA exits
+#pragma unroll 1
+        for (int e = n; e < issued; ++e)
+          if (!mbar_wait_bounded(&pt_full[e % 3], (uint32_t)(e / 3) & 1u)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
+        if (r_pending && !mbar_wait_bounded(r_full, (uint32_t)(ritems - 1) & 1u)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
+      }
+    } else {
     int bcnt[2] = {0, 0};   // bias tiles loaded per warpgroup
     int g = 0;
-    // low-rank mode: the item whose r rows and projection ring are loaded, the ring's base
-    // bucket (x_0 of that item's first bias tile), and the load events issued / waited for
-    int lr_item = -1, lr_base = 0, ev_issued = 0, ev_waited = 0;
-    if (lane == 0 && a.bias_bulk) prefetch_tensormap(&tmB);
-    if (BM == BM_LOWRANK && lane == 0) {
-      prefetch_tensormap(&tmR);
-      prefetch_tensormap(&tmP);
-    }
     for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
       PItem it;
       if (!get_item(a, i, it) || it.ntile == 0) continue;
@@ -444,51 +576,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         const int slot = (g & 1) * BS::PER_WG + u % BS::PER_WG, use = u / BS::PER_WG;
         BT* sb = reinterpret_cast<BT*>(smem + L_::bias + (size_t)slot * BS::SLOT_BYTES);
         const int dmin0 = it.pos0 - (k0 + TILE_KEYS - 1);
-        if constexpr (BM == BM_LOWRANK) {
-          // Loader of the low-rank operands (the bias warps 12-15 compute the slot).  Bucket
-          // b sits at ring row (b - base) mod 256, base = x_0 of the item's first bias tile; a
-          // tile reads the 192 buckets [x_0, x_0 + 192), and each next tile of the item
-          // (x_0 - 64) needs only 64 new ones, whose 64-row chunk (never wrapping the ring)
-          // goes where bias tile t - 1 read, once the bias warps are done with it.  One load
-          // event per bias tile t: the item's r rows and first three chunks, or the chunk
-          // loaded during tile t - 1.  Rows past the item and buckets outside [0, E) arrive
-          // as zeros and are never used.
-          (void)sb;
-          (void)use;
-          const int x0 = dmin0;
-          const uint32_t chunk_bytes = (uint32_t)(LOWRANK_CHUNK * a.d_rel * 2);
-          const uint32_t pitch = (uint32_t)a.d_rel * 2;
-          if (ev_waited >= 1)
-            (void)wait_flag(&c_done[(ev_waited - 1) & 1], (uint32_t)((ev_waited - 1) >> 1) & 1u, abort_flag, a.err);
-          ++ev_waited;   // here: bias tiles seen
-          if (lr_item != i) {
-            // first bias tile of the item: its r rows and chunks [x_0 + 64 m, +64), m = 0..2
-            if (lane == 0) {
-              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier ldmatrix reads first
-              uint64_t* bar = &w_full[ev_issued & 1];
-              mbar_arrive_expect_tx(bar, (uint32_t)(PT_ROWS * a.d_rel * 2) + 3 * chunk_bytes);
-              tma_load_3d(smem + L_::lr_r, &tmR, 0, it.h, it.t0, bar);
-#pragma unroll 1
-              for (int m = 0; m < 3; ++m)
-                tma_load_2d(smem + L_::lr_w + (size_t)m * LOWRANK_CHUNK * pitch, &tmP, 0, x0 + LOWRANK_CHUNK * m, bar);
-            }
-            ++ev_issued;
-            lr_item = i;
-            lr_base = x0;
-          }
-          if (j + 1 < it.ntile) {
-            // the next tile of this item needs buckets [x_0 - 64, x_0): load their chunk now
-            if (lane == 0) {
-              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-              uint64_t* bar = &w_full[ev_issued & 1];
-              const int ring_row = (x0 - LOWRANK_CHUNK - lr_base) & (LOWRANK_RING_ROWS - 1);
-              mbar_arrive_expect_tx(bar, chunk_bytes);
-              tma_load_2d(smem + L_::lr_w + (size_t)ring_row * pitch, &tmP, 0, x0 - LOWRANK_CHUNK, bar);
-            }
-            ++ev_issued;
-          }
-          continue;
-        }
         if (use >= 1) (void)wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err);
         if (a.bias_bulk) {
           // lane gr < NGROUP decides whether group gr of this tile is read; the warp loads those
@@ -525,94 +612,70 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-    if (BM == BM_LOWRANK && lane == 0) {
-      // after an abort, loads may still be landing: wait (bounded) for the last event on each
-      // of the two barriers (each barrier's phases complete in order, and no later phase
-      // follows these), so no load is in flight when the CTA exits
-#pragma unroll 1
-      for (int e = ev_issued >= 2 ? ev_issued - 2 : 0; e < ev_issued; ++e)
-        if (!mbar_wait_bounded(&w_full[e & 1], (uint32_t)(e >> 1) & 1u)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
     }
   } else if (warp >= 12) {
     if constexpr (BM == BM_LOWRANK) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(LR_REGS_BIAS));
     // -------------------------------------------------------------- bias warps (low-rank)
-    // Warp 12 + w computes groups 2w and 2w + 1 (rows 32w .. 32w + 31) of every bias tile:
-    // G = R_g (16 x d_rel) Pt[x_g .. x_g + 79]^T, x_g = x_0 + 16 g, ten m16n8k16 n-tiles per
-    // k-step, fp32 accumulate, operands by ldmatrix from the r rows and the projection ring
-    // the loader keeps (bucket b at ring row (b - base) mod 256).
+    // Warp 12 + q reads TMEM lanes 32 q .. 32 q + 31 (rows of the item) of every bias chunk
+    // and writes each row's 64 values, as fp16, into the slots of the (up to three) tiles
+    // whose windows hold the chunk: tile t + k sees chunk [s, s + 64) at window offset
+    // (s - x_0(t)) + 64 k.  Slot t % 4 row r (group g = r / 16) holds the 80 buckets
+    // x_0 + 16 g + [0, 80).  Before the first write into a slot for tile t', the tile that
+    // used it before (t' - 4) must have been consumed by its softmax warpgroup.
     if constexpr (BM == BM_LOWRANK) {
-      const int wb = warp - 12;
-      int bcnt[2] = {0, 0};
-      int g = 0, bt = 0, lr_item = -1, lr_base = 0;
-      const int q4 = lane & 3, rq = lane >> 2;
-      const uint32_t pitch = (uint32_t)a.d_rel * 2;
-      const uint32_t swm = (uint32_t)(a.d_rel / 8 - 1);   // 128- or 64-byte swizzle
-      const uint32_t rbase = smem_u32(smem + L_::lr_r), wbase = smem_u32(smem + L_::lr_w);
+      const int q = warp - 12;
+      const int row = 32 * q + lane, grp = row >> 4, irow = row & 15;
+      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + TM_BC;
+      int t = 0, n = 0, waited = -1;
       for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
         PItem it;
         if (!get_item(a, i, it) || it.ntile == 0) continue;
-        for (int j = 0; j < it.ntile; ++j, ++g) {
-          const int k0 = (it.kt0 + j) * TILE_KEYS;
-          if (!tile_needs_bias(it.pos0, k0, a.E)) continue;
-          const int u = bcnt[g & 1]++;
-          const int slot = (g & 1) * BS::PER_WG + u % BS::PER_WG, use = u / BS::PER_WG;
-          float* sb = reinterpret_cast<float*>(smem + L_::bias + (size_t)slot * BS::SLOT_BYTES);
-          const int x0 = it.pos0 - (k0 + TILE_KEYS - 1);
-          if (lr_item != i) {
-            lr_item = i;
-            lr_base = x0;
-          }
-          const uint32_t nm =
-              __ballot_sync(0xffffffffu, lane < BS::NGROUP && bias_group_needed(a, it, k0, lane)) & (3u << (2 * wb));
-          if (use >= 1) (void)wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err);
-          const bool ok = wait_flag(&w_full[bt & 1], (uint32_t)(bt >> 1) & 1u, abort_flag, a.err);
-          if (nm && ok) {
-            const int rel0 = x0 - lr_base;   // ring row of bucket x_0 is rel0 mod 256
+        const int jb = lr_first_bias_tile(a, it);
+        for (int j = jb; j < it.ntile; ++j, ++t) {
+          const int nch = j == jb ? 3 : 1;
 #pragma unroll 1
-            for (uint32_t mm = nm; mm; mm &= mm - 1) {
-              const int gr = __ffs(mm) - 1;
-              float acc[10][4];
+          for (int m = 0; m < nch; ++m) {
+            const bool ok = wait_flag(bc_full, (uint32_t)n & 1u, abort_flag, a.err);
+            ++n;
+            tc_fence_after();
+            uint32_t h[32];   // this row's 64 buckets of the chunk, fp16 pairs
+            {
+              uint32_t v[32];
+              tmem_ld32(taddr, v);
+              tmem_wait_ld();
 #pragma unroll
-              for (int nt = 0; nt < 10; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-              // every B row address of a lane has the same row mod 8, so one swizzled chunk offset
-              const uint32_t brow0 = (uint32_t)(rel0 + BIAS_BOX_ROWS * gr + (lane & 7));
+              for (int e = 0; e < 16; ++e) h[e] = pack_half2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+              tmem_ld32(taddr + 32, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                h[16 + e] = pack_half2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bc_empty);   // TMEM may take the next product
+            if (!ok) continue;
+            const int off0 = j == jb ? LOWRANK_CHUNK * m : 0;   // the chunk's offset in tile t's window
 #pragma unroll 1
-              for (int kp = 0; kp < a.d_rel / 16; kp += 2) {   // k-steps kp and kp + 1
-                uint32_t af[2][4];
-#pragma unroll
-                for (int s2 = 0; s2 < 2; ++s2) {
-                  const uint32_t off = (uint32_t)(BIAS_BOX_ROWS * gr + (lane & 15)) * pitch +
-                                       (uint32_t)(2 * (kp + s2) + (lane >> 4)) * 16;
-                  ldmatrix_x4(rbase + (off ^ (((off >> 7) & swm) << 4)), af[s2][0], af[s2][1], af[s2][2], af[s2][3]);
-                }
-#pragma unroll
-                for (int h5 = 0; h5 < 10; h5 += 5) {   // five n-tiles at a time
-                  uint32_t bf[5][4];
-#pragma unroll
-                  for (int n5 = 0; n5 < 5; ++n5) {
-                    const uint32_t row = (brow0 + 8 * (h5 + n5)) & (LOWRANK_RING_ROWS - 1);
-                    const uint32_t off = row * pitch + (uint32_t)(2 * kp + (lane >> 3)) * 16;
-                    ldmatrix_x4(wbase + (off ^ (((off >> 7) & swm) << 4)), bf[n5][0], bf[n5][1], bf[n5][2], bf[n5][3]);
-                  }
-#pragma unroll
-                  for (int n5 = 0; n5 < 5; ++n5) mma_bf16_16816(acc[h5 + n5], af[0], bf[n5][0], bf[n5][1]);
-#pragma unroll
-                  for (int n5 = 0; n5 < 5; ++n5) mma_bf16_16816(acc[h5 + n5], af[1], bf[n5][2], bf[n5][3]);
-                }
+            for (int k = 0; k < 3; ++k) {
+              const int off = off0 + LOWRANK_CHUNK * k;
+              if (off >= 3 * LOWRANK_CHUNK || j + k >= it.ntile) break;
+              const int tt = t + k, sl = tt & 3;
+              if (tt > waited) {
+                if (tt >= 4) (void)wait_flag(&b_empty[sl], (uint32_t)((tt >> 2) - 1) & 1u, abort_flag, a.err);
+                waited = tt;
               }
-              float* gdst = sb + gr * BS::GROUP;
+              __half* dst = reinterpret_cast<__half*>(smem + L_::bias + (size_t)sl * BS::SLOT_BYTES) +
+                            grp * BS::GROUP + irow * BS::COLS;
 #pragma unroll
-              for (int nt = 0; nt < 10; ++nt) {
-                const int col = 8 * nt + 2 * q4;
-                *reinterpret_cast<float2*>(gdst + rq * BS::COLS + col) = make_float2(acc[nt][0], acc[nt][1]);
-                *reinterpret_cast<float2*>(gdst + (rq + 8) * BS::COLS + col) = make_float2(acc[nt][2], acc[nt][3]);
+              for (int qv = 0; qv < 8; ++qv) {
+                const int col = off + 8 * qv - BIAS_BOX_ROWS * grp;   // slot column of bucket s + 8 qv
+                if (col >= 0 && col < BS::COLS)
+                  *reinterpret_cast<uint4*>(dst + col) = make_uint4(h[4 * qv], h[4 * qv + 1], h[4 * qv + 2], h[4 * qv + 3]);
               }
+              if (k == 0 && m == nch - 1) mbar_arrive(&b_full[sl]);   // all 32 lanes: tile t is complete
             }
           }
-          __syncwarp();
-          mbar_arrive(&b_full[slot]);        // all 32 lanes: their stores are in the slot
-          if (lane == 0) mbar_arrive(&c_done[bt & 1]);   // this warp's reads of the ring and r rows are done
-          ++bt;
         }
       }
     }
@@ -630,6 +693,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const uint32_t tm_o = tlane + TM_O + (uint32_t)(wg * D);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
     int icount = 0, g = 0, buse = 0;  // buse: bias tiles this warpgroup has consumed
+    int btile = 0;                     // low-rank mode: bias tiles of the CTA so far (both warpgroups)
     for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
       PItem it;
       if (!get_item(a, i, it)) continue;
@@ -708,8 +772,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       for (int j = 0; j < it.ntile; ++j, ++g) {
         const int k0 = (it.kt0 + j) * TILE_KEYS;
         const bool needs = tile_needs_bias(it.pos0, k0, a.E);
+        const int my_bt = btile;
+        if (BM == BM_LOWRANK && needs) ++btile;
         if ((g & 1) != wg) continue;  // the other warpgroup's tile
-        const int bslot_i = wg * BS::PER_WG + buse % BS::PER_WG;   // this warpgroup's next fill
+        // this tile's bias slot: the warpgroup's next fill, or (low-rank) bias tile my_bt % 4
+        const int bslot_i = BM == BM_LOWRANK ? (my_bt & 3) : wg * BS::PER_WG + buse % BS::PER_WG;
+        const uint32_t bpar = BM == BM_LOWRANK ? (uint32_t)(my_bt >> 2) & 1u : (uint32_t)(buse / BS::PER_WG) & 1u;
         const BT* bslot = reinterpret_cast<const BT*>(smem + L_::bias + (size_t)bslot_i * BS::SLOT_BYTES);
         uint64_t bad = item_bad ? tile_bad(k0) : 0ull;
         bool ok = wait_flag(&s_full[g & 1], (uint32_t)(g >> 1) & 1u, abort_flag, a.err);
@@ -739,7 +807,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         // slot when the tile reads no bucket from it
         const BT* brow = bslot + (TILE_KEYS - 1);
         if (needs) {
-          (void)wait_flag(&b_full[bslot_i], (uint32_t)(buse / BS::PER_WG) & 1u, abort_flag, a.err);
+          (void)wait_flag(&b_full[bslot_i], bpar, abort_flag, a.err);
           const int gr = r / BIAS_BOX_ROWS;
           brow = bslot + gr * BS::GROUP + (r % BIAS_BOX_ROWS) * BS::COLS + (dmin - bias_group_x<BS::ALIGN>(dmin - r, gr)) +
                  (TILE_KEYS - 1);
