@@ -29,9 +29,9 @@
 //           by more than 2^8.  Epilogue: the two partial results are merged,
 //           O / l -> bf16 -> out.
 // Bias modes: fp32 or bf16 rel_logits (the slot loaded by TMA, as above), or the bias in
-// low-rank form (BM_LOWRANK, 512 threads): there warp 2 only loads r rows and projection
-// rows by TMA, and warps 12-15 compute the slot with warp MMA; the softmax warpgroups are
-// the same in every mode.
+// low-rank form (BM_LOWRANK, 512 threads): there warp 2 issues tcgen05 MMAs of the item's r
+// rows and projection rows into free TMEM columns, and warps 12-15 read the products out
+// into fp16 slots; the softmax warpgroups are the same in every mode.
 #include <algorithm>
 #include <type_traits>
 
@@ -44,8 +44,8 @@ namespace {
 
 constexpr int PT_ROWS = PREFILL_ROWS;
 constexpr int PT_THREADS = 384;
-// The low-rank mode adds a fourth warpgroup (warps 12-15) that computes the bias products,
-// one warp per SM sub-partition, so it runs with 512 threads and rebalances registers
+// The low-rank mode adds a fourth warpgroup (warps 12-15, one per TMEM lane quarter) that
+// reads the bias products out of TMEM, so it runs with 512 threads and rebalances registers
 // with setmaxnreg: warps 0-3 and 12-15 give theirs to the softmax warpgroups.
 constexpr int PT_THREADS_LR = 512;
 constexpr int LR_REGS_PRODUCERS = 72, LR_REGS_SOFTMAX = 168, LR_REGS_BIAS = 104;
