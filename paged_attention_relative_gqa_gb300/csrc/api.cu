@@ -192,15 +192,15 @@ bool make_bias_map(CUtensorMap* map, const void* rel, bool bf16, const ink_attn_
   return r == CUDA_SUCCESS;
 }
 
-// Low-rank bias operands: r [total_q, Hq, d_rel] as {d_rel, Hq, total_q} with boxes of
-// 128 tokens of one head, and proj_t [E, d_rel] as {d_rel, E} with boxes of
-// LOWRANK_CHUNK buckets; 128-byte swizzle for d_rel 64, 64-byte for d_rel 32 (rows of
-// 128 / 64 bytes).  Out-of-range rows (tokens past total_q, buckets outside [0, E)) read 0.
+// Low-rank bias operands (d_rel 64): r [total_q, Hq, 64] as {64, Hq, total_q} with boxes of
+// 128 tokens of one head, and proj_t [E, 64] as {64, E} with boxes of LOWRANK_CHUNK buckets;
+// 128-byte rows with the 128-byte swizzle, as the bias MMA's K-major operands want them.
+// Out-of-range rows (tokens past total_q, buckets outside [0, E)) read as zeros.
 bool make_lowrank_maps(ink::PrefillMaps* m, const void* r, const void* proj_t, const ink_attn_params_t* p,
                        int total_q, int d_rel) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const CUtensorMapSwizzle sw = d_rel == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
   cuuint64_t dims_r[3] = {(cuuint64_t)d_rel, (cuuint64_t)p->num_q_heads, (cuuint64_t)total_q};
   cuuint64_t str_r[2] = {(cuuint64_t)d_rel * 2, (cuuint64_t)d_rel * 2 * p->num_q_heads};
   cuuint32_t box_r[3] = {(cuuint32_t)d_rel, 1, (cuuint32_t)ink::PREFILL_ROWS};

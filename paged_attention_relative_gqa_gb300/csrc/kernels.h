@@ -49,7 +49,7 @@ struct PrefillArgs {
   int bias_lowrank;           // bias from r and proj_t (rel unused)
   const void* lr_r;           // bf16 [total_q, Hq, d_rel]
   const void* lr_proj_t;      // bf16 [E, d_rel]
-  int d_rel;                  // a multiple of 16
+  int d_rel;                  // 64
 };
 
 // TMA descriptors of one decode call: K/V pools viewed as [num_pages*Hkv*P rows, D]
@@ -87,8 +87,8 @@ cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& a, int head_
 // 84 buckets x 1 head x 16 tokens (only built when rows of rel are 16-byte aligned).
 struct PrefillMaps {
   CUtensorMap k, v, bias;
-  CUtensorMap lr_r;     // low-rank bias: r viewed as {d_rel, Hq, total_q}, box {d_rel, 1, 128}
-  CUtensorMap lr_p;     // low-rank bias: proj_t viewed as {d_rel, E}, box {d_rel, LOWRANK_CHUNK}
+  CUtensorMap lr_r;     // low-rank bias: r viewed as {64, Hq, total_q}, box {64, 1, 128} (MMA operand A)
+  CUtensorMap lr_p;     // low-rank bias: proj_t viewed as {64, E}, box {64, LOWRANK_CHUNK} (MMA operand B)
   CUtensorMap k3, v3;   // whole 64-key tiles, all column blocks in one box (P >= 64 only)
   CUtensorMap q3;       // 128 query rows of one head, all column blocks in one box
 };
