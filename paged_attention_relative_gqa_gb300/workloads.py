@@ -425,13 +425,17 @@ def kv_decode_swa(device="cpu", seed=7, batch=64) -> KvStep:
 def sample_rows(prob: Problem, per_seq: int, seed: int) -> np.ndarray:
     """A seeded sample of (packed row, head) pairs for oracle checks on big problems.
 
-    Always includes, per sequence, the rows at positions 0, 1, 510, 511, 512, 4094,
-    4095, 4096 and L-1 where they exist, plus page-boundary rows; the rest is uniform.
-    Returns an int32 array ``[n, 2]`` of (t, h).
+    Per sequence: at least ``per_seq`` distinct pairs (every pair when the sequence has
+    fewer), always including the rows at positions 0, 1, 510, 511, 512, 4094, 4095, 4096
+    and L-1 where they exist and the page-boundary rows, each on the first head of every
+    KV group; the rest is drawn uniformly without replacement.
+    Returns an int32 array ``[n, 2]`` of (t, h), sorted.
     """
     rng = np.random.default_rng(seed)
     out = []
     cu = prob.cu_q_lens.cpu().numpy()
+    Hq = prob.num_q_heads
+    step = max(1, Hq // prob.num_kv_heads)
     for b, (n, L) in enumerate(zip(prob.q_lens, prob.seq_lens_list)):
         if n == 0:
             continue
@@ -439,14 +443,20 @@ def sample_rows(prob: Problem, per_seq: int, seed: int) -> np.ndarray:
         want = {0, 1, 510, 511, 512, 4094, 4095, 4096, L - 1,
                 prob.page_size - 1, prob.page_size, 2 * prob.page_size - 1}
         pos = [p for p in want if first <= p < L]
-        extra = rng.integers(first, L, size=max(0, per_seq - len(pos)))
-        for p in list(pos) + extra.tolist():
-            t = int(cu[b]) + (p - first)
-            h = int(rng.integers(0, prob.num_q_heads))
-            out.append((t, h))
-        for p in pos:  # boundary rows on every head group's first head as well
-            t = int(cu[b]) + (p - first)
-            for h in range(0, prob.num_q_heads, max(1, prob.num_q_heads // prob.num_kv_heads)):
-                out.append((t, h))
-    arr = np.unique(np.asarray(out, dtype=np.int32), axis=0)
+        fixed = {(p - first) * Hq + h for p in pos for h in range(0, Hq, step)}
+        k = min(n * Hq, max(per_seq, len(fixed))) - len(fixed)
+        pool = np.setdiff1d(np.arange(n * Hq, dtype=np.int64), np.fromiter(fixed, np.int64, len(fixed)))
+        pick = np.concatenate([np.fromiter(fixed, np.int64, len(fixed)),
+                               rng.choice(pool, size=k, replace=False)])
+        for x in np.sort(pick).tolist():
+            out.append((int(cu[b]) + x // Hq, x % Hq))
+    arr = np.asarray(out, dtype=np.int32).reshape(-1, 2)
     return arr
+
+
+def rows_per_sequence(prob: Problem, rows: np.ndarray) -> List[int]:
+    """How many sampled rows fall in each sequence (for the parity tests' printout)."""
+    cu = prob.cu_q_lens.cpu().numpy()
+    t = np.sort(rows[:, 0]) if rows.size else np.zeros(0, np.int32)
+    edges = np.searchsorted(t, cu, side="left")
+    return np.diff(edges).tolist()

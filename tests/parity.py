@@ -75,6 +75,22 @@ def compare(gpu: np.ndarray, ref: np.ndarray, label: str):
     return max_abs, rel_rms
 
 
+# Rows compared per sequence when the oracle cannot take every row of a workload.
+SAMPLE_PER_SEQ = 4096
+
+
+def sampled_check(prob, out: torch.Tensor, seed: int, label: str, per_seq: int = SAMPLE_PER_SEQ):
+    """Compare a seeded sample of at least ``per_seq`` (t, h) rows of every sequence (all of
+    them when a sequence has fewer) with the oracle, and print the per-sequence counts."""
+    from paged_attention_relative_gqa_gb300 import workloads as W
+    rows = W.sample_rows(prob, per_seq=per_seq, seed=seed)
+    counts = W.rows_per_sequence(prob, rows)
+    for n, c in zip(prob.q_lens, counts):
+        assert c >= min(per_seq, n * prob.num_q_heads), f"{label}: only {c} rows sampled"
+    print(f"{label}: rows per sequence {counts}")
+    return compare(gpu_rows(out, rows), oracle_rows(prob, rows), label)
+
+
 def gpu_rows(out: torch.Tensor, rows: np.ndarray) -> np.ndarray:
     t = torch.from_numpy(rows[:, 0].astype(np.int64)).to(out.device)
     h = torch.from_numpy(rows[:, 1].astype(np.int64)).to(out.device)

@@ -88,7 +88,7 @@ def test_layer_step_with_kv_write_replays_and_matches_the_oracle():
     sampled rows against the oracle run on the pools as written, is within the prefill
     tolerances."""
     import numpy as np
-    from tests.parity import compare, gpu_rows, oracle_rows
+    from tests.parity import sampled_check
 
     pre, _ = W.mixed_layer("swa", 1, DEV)
     step = W.kv_step_for(pre, W.KV_CONV_KERNEL, seed=123)
@@ -120,5 +120,4 @@ def test_layer_step_with_kv_write_replays_and_matches_the_oracle():
         assert torch.equal(out, eager)
     assert binding.inkling_attn_read_device_error(ws_kv) == 0
     assert binding.inkling_attn_read_device_error(ws) == 0
-    rows = W.sample_rows(pre, per_seq=64, seed=9)
-    compare(gpu_rows(out, rows), oracle_rows(pre, rows), "layer step with K/V write (sampled rows)")
+    sampled_check(pre, out, 9, "layer step with K/V write (sampled rows)")

@@ -12,7 +12,7 @@ import torch
 
 from paged_attention_relative_gqa_gb300 import binding
 from paged_attention_relative_gqa_gb300 import workloads as W
-from tests.parity import bits, compare, gpu_rows, oracle_full, oracle_rows, run_gpu
+from tests.parity import bits, compare, gpu_rows, oracle_full, oracle_rows, run_gpu, sampled_check
 
 pytestmark = pytest.mark.gpu
 
@@ -52,8 +52,7 @@ def test_global_decode_every_row():
 def test_global_prefill_sampled_rows():
     prob = W.global_prefill(DEV)
     out, _ = run_gpu(prob)
-    rows = W.sample_rows(prob, per_seq=1024, seed=44)
-    compare(gpu_rows(out, rows), oracle_rows(prob, rows), "global_prefill (4x8192, sampled)")
+    sampled_check(prob, out, 44, "global_prefill (4x8192, sampled)")
     assert torch.isfinite(out.float()).all()
     del prob, out
     torch.cuda.empty_cache()
@@ -64,8 +63,7 @@ def test_mixed_stack_layer(layer):
     kind = W.MIXED_STACK[layer]
     pre, dec = W.mixed_layer(kind, layer, DEV)
     out, _ = run_gpu(pre)
-    rows = W.sample_rows(pre, per_seq=256, seed=layer)
-    compare(gpu_rows(out, rows), oracle_rows(pre, rows), f"mixed layer {layer} ({kind}) prefill, sampled")
+    sampled_check(pre, out, layer, f"mixed layer {layer} ({kind}) prefill, sampled")
     assert torch.isfinite(out.float()).all()
     full_check(dec, f"mixed layer {layer} ({kind}) decode")
     del pre, dec, out

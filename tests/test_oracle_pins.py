@@ -385,3 +385,87 @@ def test_pins_catch_reinjected_bug(name, tmp_path):
             caught = True
             break
     assert caught, f"mutant {name} survived the brute-force pin"
+
+
+# ---------------------------------------------------------------- (8) the sampled-row path
+#
+# Parity on the large workloads calls ``attention_rows`` with only the sampled rows'
+# query vectors and bias rows (``q_rows_bits`` / ``rel_rows``) and placeholders for the
+# whole tensors.  That path must give, row for row and bit for bit, what the full-tensor
+# path gives; and it must never read the whole tensors when the rows are supplied.
+
+def _rows_path(prob, rng, lib=None):
+    """Oracle on a random (t, h) subset through the gathered-rows path.  The gathered rows
+    sit at the front of buffers padded with NaN, so a path that indexes them wrongly
+    (by packed row instead of sampled row, or with another row stride) reads NaN or other
+    rows instead of faulting; the whole q / rel tensors are NaN placeholders."""
+    kw = prob.oracle_kwargs()
+    q_bits, rel = kw["q_bits"], kw["rel"]
+    total_q, Hq, D = q_bits.shape
+    E = rel.shape[2]
+    n_all = total_q * Hq
+    n = int(rng.integers(1, n_all + 1))
+    pick = np.sort(rng.choice(n_all, size=n, replace=False))
+    rows_t = (pick // Hq).astype(np.int32)
+    rows_h = (pick % Hq).astype(np.int32)
+    pad = n + total_q + 1
+    q_big = np.full((pad * max(1, -(-E // D)), D), 0x7FC0, dtype=np.uint16)   # bf16 NaN
+    rel_big = np.full((pad, E), np.nan, dtype=np.float32)
+    q_big[:n] = q_bits[rows_t, rows_h]
+    rel_big[:n] = rel[rows_t, rows_h]
+    kw["q_bits"] = np.full_like(q_bits, 0x7FC0)
+    kw["rel"] = np.full_like(rel, np.nan)
+    extra = {"lib": lib} if lib is not None else {}
+    out = oracle.attention_rows(rows_t=rows_t, rows_h=rows_h, q_rows_bits=q_big[:n],
+                                rel_rows=rel_big[:n], **kw, **extra)
+    return rows_t, rows_h, out
+
+
+def test_sampled_rows_path_equals_full_path_bitwise():
+    rng = np.random.default_rng(2024)
+    rows = 0
+    for case in range(200):
+        prob = random_tiny(rng, seed=500 + case)
+        if int(prob.cu_q_lens[-1]) == 0:
+            continue
+        full = run_oracle(prob)
+        t, h, part = _rows_path(prob, rng)
+        np.testing.assert_array_equal(part, full[t, h], err_msg=f"case {case}")
+        # and against the independent restatement
+        np.testing.assert_allclose(part, run_brute(prob)[t, h], rtol=0, atol=1e-12)
+        rows += part.shape[0]
+    print(f"sampled-row path: {rows} rows compared bit for bit")
+    assert rows > 1000
+
+
+ROW_MUTANTS = {
+    "q_rows_by_packed_row": ("q_rows ? q_rows + r * (int64_t)head_dim", "q_rows ? q_rows + t * (int64_t)head_dim"),
+    "rel_rows_by_packed_row": ("rel_rows ? rel_rows + r * (int64_t)rel_extent",
+                               "rel_rows ? rel_rows + t * (int64_t)rel_extent"),
+    "q_rows_stride_E": ("q_rows ? q_rows + r * (int64_t)head_dim", "q_rows ? q_rows + r * (int64_t)rel_extent"),
+    "rel_rows_stride_D": ("rel_rows ? rel_rows + r * (int64_t)rel_extent",
+                          "rel_rows ? rel_rows + r * (int64_t)head_dim"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ROW_MUTANTS))
+def test_rows_path_pin_catches_reinjected_bug(name, tmp_path):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc missing")
+    old, new = ROW_MUTANTS[name]
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "attn_ref.c")).read()
+    assert old in src, f"mutation target for {name} not found: pin would be vacuous"
+    mpath = tmp_path / "mutant.c"
+    mpath.write_text(src.replace(old, new, 1))
+    lib = oracle.load(oracle.build(str(mpath), str(tmp_path / "libmutant.so")))
+    rng = np.random.default_rng(77)
+    caught = False
+    for case in range(120):
+        prob = random_tiny(rng, seed=900 + case)
+        if int(prob.cu_q_lens[-1]) == 0:
+            continue
+        t, h, part = _rows_path(prob, rng, lib=lib)
+        if not np.allclose(part, run_brute(prob)[t, h], rtol=0, atol=1e-9):
+            caught = True
+            break
+    assert caught, f"mutant {name} survived the sampled-row pin"
