@@ -308,6 +308,9 @@ WORKLOAD_DESC = {
                                     "8 kv heads, head_dim 128, full causal, page 64, E 4096, r [2048,64,64] bf16",
     "global_prefill_small": "global_prefill_small (profiling size): 1 x 2048 tokens, 64 q heads / "
                             "8 kv heads, head_dim 128, full causal, page 64, bias [2048,64,4096] fp32",
+    "global_prefill_bf16bias_small": "global_prefill_bf16bias_small (profiling size): 1 x 2048 tokens, 64 q "
+                                     "heads / 8 kv heads, head_dim 128, full causal, page 64, bias "
+                                     "[2048,64,4096] bf16",
     "kv_prefill_global": "K/V short convolution (ks 4) + paged write of a global-layer prefill step: "
                          "4 fresh prompts x 8192 tokens, 8 kv heads, head_dim 128, page 64",
     "kv_decode_swa": "K/V short convolution (ks 4) + paged write of an SWA-layer decode step: 64 requests, "
@@ -342,6 +345,8 @@ def workload_instances(name, dev):
         return [W.global_prefill_lowrank(dev, seed=4, batch=1, tokens=2048)]   # profiling size
     if name == "global_prefill_small":
         return [W.global_prefill(dev, seed=4, batch=1, tokens=2048)]  # 2.2 GB > L2
+    if name == "global_prefill_bf16bias_small":
+        return [W.global_prefill(dev, seed=4, batch=1, tokens=2048, bias_dtype=torch.bfloat16)]  # 1.1 GB > L2
     raise ValueError(name)
 
 

@@ -270,6 +270,20 @@ const char* inkling_attn_status_string(ink_status_t status);
 /* ABI version of the library (major * 100 + minor). */
 int32_t inkling_attn_version(void);
 
+/*
+ * Time limit, in nanoseconds, of one pipeline wait inside every kernel launched after this
+ * call (process-wide; the default is 2 000 000 000, larger values are clamped to it).  A
+ * wait that runs out sets INK_DEVERR_WAIT_TIMEOUT in the workspace error word; the kernel
+ * then stops issuing work, waits (up to 2 s each) for the copies and tensor-core
+ * operations it has already issued, and returns, leaving the device usable.  0 makes every
+ * wait that finds its data not yet ready give up at once: a way for tests to drive the
+ * timeout path without a fault.  Failure detection by status, not by fault, follows the
+ * epoch-checked "ready" flag of "Inkling attn backend cleanup fake registry" (TensorRT-LLM
+ * PR #17860), where stale decode metadata is detected rather than read.  Not for use in
+ * production: launches in flight keep the limit they were launched with.
+ */
+void inkling_attn_set_wait_limit_ns(uint64_t limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

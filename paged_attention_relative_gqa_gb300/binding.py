@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = ("inkling_attn_workspace_bytes", "inkling_attn_workspace_init
                     "inkling_attn_prefill_lowrank_bias", "inkling_attn_decode",
                     "inkling_attn_decode_noalloc", "inkling_attn_kv_conv_write",
                     "inkling_attn_read_device_error", "inkling_attn_status_string",
-                    "inkling_attn_version")
+                    "inkling_attn_version", "inkling_attn_set_wait_limit_ns")
 
 
 class InkError(RuntimeError):
@@ -87,6 +87,8 @@ def load_library(path: Optional[str] = None):
     lib.inkling_attn_status_string.restype = ctypes.c_char_p
     lib.inkling_attn_version.argtypes = []
     lib.inkling_attn_version.restype = I32
+    lib.inkling_attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.inkling_attn_set_wait_limit_ns.restype = None
     if path is None:
         _lib = lib
     return lib
@@ -243,6 +245,11 @@ def inkling_attn_kv_conv_write(params, k_new, v_new, cu_q_lens, seq_lens, block_
         _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream_handle(stream))
     _check(code, "inkling_attn_kv_conv_write")
     return k_cache, v_cache
+
+
+def inkling_attn_set_wait_limit_ns(limit_ns: int) -> None:
+    """Limit of one pipeline wait in kernels launched from now on (tests of the timeout path)."""
+    load_library().inkling_attn_set_wait_limit_ns(int(limit_ns))
 
 
 def inkling_attn_read_device_error(workspace: torch.Tensor, stream=None, clear: bool = True) -> int:

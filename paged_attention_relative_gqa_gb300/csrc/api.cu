@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 #include <cstring>
 
@@ -18,6 +19,9 @@ using ink::DecodeArgs;
 using ink::PrefillArgs;
 
 constexpr size_t kHeaderBytes = 256;  // error word lives at offset 0
+
+// Limit of one pipeline wait inside the kernels launched from now on (default 2 s).
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -174,16 +178,16 @@ bool make_pool_map(CUtensorMap* map, const void* base, const ink_attn_params_t* 
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// rel_logits [total_q, Hq, E] fp32 as a 3-D tensor {E, Hq, total_q}; boxes of
-// BIAS_BOX_COLS buckets x 1 head x BIAS_BOX_ROWS tokens, out-of-range elements read as 0.
-bool make_bias_map(CUtensorMap* map, const void* rel, bool bf16, const ink_attn_params_t* p, int total_q) {
+// rel_logits [total_q, Hq, E] (fp32 or bf16) as a 3-D tensor {E, Hq, total_q}; boxes of
+// box_cols buckets x 1 head x box_rows tokens, out-of-range elements read as 0.
+bool make_bias_map(CUtensorMap* map, const void* rel, bool bf16, const ink_attn_params_t* p, int total_q,
+                   int box_cols, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t es = bf16 ? 2 : 4;
   cuuint64_t dims[3] = {(cuuint64_t)p->rel_extent, (cuuint64_t)p->num_q_heads, (cuuint64_t)total_q};
   cuuint64_t strides[2] = {(cuuint64_t)p->rel_extent * es, (cuuint64_t)p->rel_extent * es * p->num_q_heads};
-  cuuint32_t box[3] = {(cuuint32_t)(bf16 ? ink::BIAS_BOX_COLS_BF16 : ink::BIAS_BOX_COLS), 1,
-                       (cuuint32_t)ink::BIAS_BOX_ROWS};
+  cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                   const_cast<void*>(rel), dims, strides, box, estr,
@@ -223,6 +227,10 @@ bool make_lowrank_maps(ink::PrefillMaps* m, const void* r, const void* proj_t, c
 extern "C" {
 
 int32_t inkling_attn_version(void) { return 100; }
+
+void inkling_attn_set_wait_limit_ns(uint64_t limit_ns) {
+  g_wait_limit_ns.store(limit_ns > 2000000000ull ? 2000000000ull : limit_ns, std::memory_order_relaxed);
+}
 
 const char* inkling_attn_status_string(ink_status_t s) {
   switch (s) {
@@ -403,11 +411,20 @@ ink_status_t prefill_impl(const ink_attn_params_t* params, const void* q, const 
   a.lr_proj_t = lr_proj_t;
   a.d_rel = d_rel;
   a.bias_bulk = !lowrank && (bias_bf16 || ((params->rel_extent % 4 == 0) && aligned(rel_logits, 16)));
+  a.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   std::memset(&maps.bias, 0, sizeof maps.bias);
   std::memset(&maps.lr_r, 0, sizeof maps.lr_r);
   std::memset(&maps.lr_p, 0, sizeof maps.lr_p);
   if (lowrank && !make_lowrank_maps(&maps, lr_r, lr_proj_t, params, total_q, d_rel)) return INK_ERR_CUDA;
-  if (a.bias_bulk && !make_bias_map(&maps.bias, rel_logits, bias_bf16, params, total_q)) return INK_ERR_CUDA;
+  if (a.bias_bulk) {
+    // the head-pair kernel: 32-token bias boxes
+    if (!make_bias_map(&maps.bias, rel_logits, bias_bf16, params, total_q,
+                       bias_bf16 ? ink::PAIR_BIAS_COLS_BF16 : ink::PAIR_BIAS_COLS_F32, ink::PAIR_BIAS_ROWS))
+      return INK_ERR_CUDA;
+    if (ink::launch_prefill_pair(maps, a, params->head_dim, (cudaStream_t)stream) != cudaSuccess)
+      return INK_ERR_CUDA;
+    return INK_OK;
+  }
   if (ink::launch_prefill_tc(maps, a, params->head_dim, (cudaStream_t)stream) != cudaSuccess)
     return INK_ERR_CUDA;
   return INK_OK;

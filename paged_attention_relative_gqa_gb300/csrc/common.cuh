@@ -63,17 +63,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete; give up after WAIT_LIMIT_NS.
-// Returns false on timeout (the caller records INK_DEVERR_WAIT_TIMEOUT).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Wait for phase `parity` of `bar` to complete; give up after `limit_ns` nanoseconds
+// (0: give up as soon as one probe finds the phase incomplete).  Returns false on timeout
+// (the caller records INK_DEVERR_WAIT_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
+  if (limit_ns == 0) return false;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// The same with the fixed 2 s limit (the waits that drain copies before a CTA exits).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_limit(bar, parity, WAIT_LIMIT_NS);
 }
 
 // Barrier among `count` threads (whole warps) of the CTA on hardware barrier `id` (1-15).
@@ -364,6 +371,9 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float to_float_b(float x) { return x; }
+__device__ __forceinline__ float to_float_b(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 __device__ __forceinline__ void record_error(uint32_t* err, uint32_t bits) {
   if (err) atomicOr(err, bits);

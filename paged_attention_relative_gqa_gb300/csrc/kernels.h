@@ -50,6 +50,7 @@ struct PrefillArgs {
   const void* lr_r;           // bf16 [total_q, Hq, d_rel]
   const void* lr_proj_t;      // bf16 [E, d_rel]
   int d_rel;                  // 64
+  unsigned long long wait_ns; // limit of one pipeline wait (the drain waits keep 2 s)
 };
 
 // TMA descriptors of one decode call: K/V pools viewed as [num_pages*Hkv*P rows, D]
@@ -102,6 +103,14 @@ constexpr int LOWRANK_MAX_D = 64;        // d_rel of the low-rank bias (the MMA'
 
 cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int head_dim,
                               cudaStream_t stream);
+
+// The head-pair prefill (prefill_pair.cu): bias given as rel_logits with 16-byte rows, read by
+// 3-D TMA boxes of PAIR_BIAS_ROWS tokens x PAIR_BIAS_COLS_* buckets of one head.
+constexpr int PAIR_BIAS_ROWS = 32;
+constexpr int PAIR_BIAS_COLS_F32 = 100;
+constexpr int PAIR_BIAS_COLS_BF16 = 104;
+cudaError_t launch_prefill_pair(const PrefillMaps& maps, const PrefillArgs& a, int head_dim,
+                                cudaStream_t stream);
 
 // One call of the K/V short convolution and paged write (kv_conv.cu).  Rows of the
 // step's K/V and of the carried state are Hkv*D bf16 (nvec 16-byte vectors).

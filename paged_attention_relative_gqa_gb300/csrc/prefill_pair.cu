@@ -1,0 +1,809 @@
+// prefill_pair.cu -- paged prefill on the 5th-generation tensor cores (tcgen05 + TMEM) with
+// two query heads of one KV head per work item, so that every K and V tile staged in shared
+// memory feeds two score products and two P V products.
+//
+// What it computes ("Support Inkling-NVFP4 model", TensorRT-LLM PR #17062, sections
+// "Architecture" and "Implementation"): for each new token and query head,
+//   s_k = sm_scale * <q, K[k]> + rel[t, h, min(p - k, E - 1)]   (bias added before the softmax)
+// over the visible keys (sliding window of W keys on local layers, full causal on global
+// ones), then out = softmax(s) V.  New tokens are the last n_b positions of the history; K/V
+// rows are read through the positional block table, page = k >> log2(P), and only keys below
+// seq_len are read ("Inkling attn backend cleanup fake registry", TensorRT-LLM PR #17860).
+//
+// Work item: 128 consecutive new tokens of one sequence, one KV head and two of its query
+// heads (one head when the group has an odd head left over).  One CTA per SM walks the items
+// in order of decreasing causal length (static round-robin); the two heads of an item share
+// their tokens, hence their visible keys, masks and K/V tiles.
+//
+// Tensor memory (512 columns): Q of head 0 and 1 (the A operand of S = Q K^T, D/2 columns
+// each), S of head 0 and 1 (64 fp32 columns each), O of head 0 and 1 (D fp32 columns each).
+// P (softmax numerators, bf16) goes to shared memory, one 16 KB tile per head, so the next S
+// of a head can be computed while its softmax still works on the current one.
+//
+// Warp roles (384 threads):
+//   warp 0   K and V producer: one TMA box per 64-key tile (or one per page segment when
+//            pages are shorter than a tile), block-table entries held 32 at a time in lanes.
+//   warp 1   MMA issuer: S_h(j+1) = Q_h K(j+1)^T (M 128, N 64, A from TMEM) as soon as the
+//            softmax of head h has read S_h(j) out of TMEM, then O_h += P_h(j) V(j) (A = P from
+//            shared memory) once P_h(j) is written.  Before the P V products of a tile it zeroes
+//            the V rows of keys that no row of the item may see (window edges, sequence end,
+//            unreadable pages).
+//   warps 2, 3  bias producers of head 0 and head 1: per tile that reads any bucket below
+//            E - 1, up to four 3-D TMA boxes (32 tokens x COLS buckets) into the head's ring.
+//   warps 4-7, 8-11  softmax of head 0 and head 1: thread r owns row r (TMEM lane r).  Per
+//            item it loads its Q row into TMEM; per tile it reads its 64 scores, adds the bias,
+//            masks, keeps the running max and sum (O rescaled in TMEM only when the max grows
+//            by more than 2^8), writes P; at the end it normalises O and stores bf16.  Pairs of
+//            scores go through packed two-lane fp32 FMA and add (the same rounding as scalar
+//            FMA and add), maxima through three-input max.
+// Every wait is bounded; after a timeout the CTA records INK_DEVERR_WAIT_TIMEOUT, stops
+// issuing copies and MMAs, waits for the copies and MMAs already issued, and exits.
+#include <type_traits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ink {
+
+namespace {
+
+constexpr int PP_THREADS = 384;
+constexpr int PP_ROWS = PREFILL_ROWS;          // new tokens per item
+constexpr int BR = PAIR_BIAS_ROWS;             // tokens per bias box
+constexpr int NGR = PP_ROWS / BR;              // bias boxes per tile and head
+constexpr float RESCALE_NAT = 5.545177444479562f;   // rescale O when a max grows by > 2^8
+
+
+// Bias slot of one head and one tile: NGR boxes of BR rows; box gr holds buckets
+// [x_gr, x_gr + COLS) of its rows, row i at +COLS i, x_gr = ALIGN floor((dmin0 + BR gr) / ALIGN)
+// where dmin0 = pos0 - (k0 + 63) is row 0's smallest distance in the tile (x_gr is 16-byte
+// aligned, as TMA wants).  Row r = BR gr + i finds the bucket of key k0 + c at
+// offset (dmin_r - x_gr) + 63 - c, dmin_r - x_gr in [i, i + ALIGN - 1].  The row pitch plus the
+// one-bucket skew between rows is odd (fp32: 101 words), so the 32 rows of a warp read 32
+// different banks (bf16: at most two rows per bank).
+template <bool BF16>
+struct PBias {
+  using T = typename std::conditional<BF16, __nv_bfloat16, float>::type;
+  static constexpr int COLS = BF16 ? PAIR_BIAS_COLS_BF16 : PAIR_BIAS_COLS_F32;
+  static constexpr int ALIGN = 16 / (int)sizeof(T);
+  static constexpr int GROUP = BR * COLS;                       // elements per box
+  static constexpr int SLOT_BYTES = NGR * GROUP * (int)sizeof(T);
+  static constexpr int NB = BF16 ? 2 : 1;                       // slots per head
+  static_assert(COLS >= TILE_KEYS + BR - 1 + ALIGN - 1, "bias box too narrow");
+  static_assert((COLS * (int)sizeof(T)) % 16 == 0 && SLOT_BYTES % 1024 == 0, "TMA alignment");
+};
+
+template <int D>
+struct PPShape {
+  static constexpr int CB = D / 64;
+  static constexpr int KV_SUB = TILE_KEYS * 128;
+  static constexpr int KV_TILE = CB * KV_SUB;
+  static constexpr int NK = D == 128 ? 2 : 4;   // K ring (freed when both S products are done)
+  static constexpr int NV = D == 128 ? 2 : 4;   // V ring (freed when both P V products are done)
+  static constexpr int P_BYTES = PP_ROWS * TILE_KEYS * 2;   // one head's P tile (bf16, 128-byte swizzle)
+  static constexpr uint32_t QC = D / 2;          // TMEM columns of one Q tile (bf16 pairs)
+  static constexpr uint32_t TQ = 0;              // Q_h at TQ + h QC
+  static constexpr uint32_t TS = 2 * QC;         // S_h at TS + 64 h
+  static constexpr uint32_t TO = 2 * QC + 128;   // O_h at TO + D h
+  static_assert(TO + 2 * D <= 512, "tensor memory budget");
+};
+
+template <int D, bool BF16>
+struct PPSmem {
+  using S = PPShape<D>;
+  using B = PBias<BF16>;
+  static constexpr size_t kst = 0;
+  static constexpr size_t vst = kst + (size_t)S::NK * S::KV_TILE;
+  static constexpr size_t pst = vst + (size_t)S::NV * S::KV_TILE;
+  static constexpr size_t bias = pst + (size_t)2 * S::P_BYTES;
+  static constexpr size_t bars = bias + (size_t)2 * B::NB * B::SLOT_BYTES;
+  // k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], q_ready[2], s_full[2], s_empty[2],
+  // p_full[2], pv_done[2], b_full[2 NB], b_empty[2 NB], drain
+  static constexpr int NBAR = 2 * S::NK + 2 * S::NV + 10 + 4 * B::NB + 1;
+  static constexpr size_t vbad = bars + NBAR * 8;
+  static constexpr size_t misc = vbad + S::NV * 8;
+  static constexpr size_t total = misc + 32;
+  static constexpr size_t alloc = total + 1024;
+};
+
+struct PPItem {
+  int b, kvh, h0, nh, t0, rows, n, L, pos0, lo_min, k_hi, kt0, ntile;
+  bool bad_len;
+};
+
+// Item i: q-tile level (longest first), then sequence, KV head and head pair.
+__device__ __forceinline__ bool pp_item(const PrefillArgs& a, int i, PPItem& it) {
+  const int npair = (a.G + 1) >> 1;
+  const int per_qt = a.B * a.Hkv * npair;
+  const int qrev = i / per_qt;
+  int r = i - qrev * per_qt;
+  it.b = r / (a.Hkv * npair);
+  r -= it.b * (a.Hkv * npair);
+  it.kvh = r / npair;
+  const int pair = r - it.kvh * npair;
+  it.h0 = it.kvh * a.G + 2 * pair;
+  it.nh = min(2, a.G - 2 * pair);
+  const int qt = a.num_q_tiles - 1 - qrev;
+  const int cu0 = __ldg(a.cu_q + it.b);
+  it.n = __ldg(a.cu_q + it.b + 1) - cu0;
+  if (qt * PP_ROWS >= it.n) return false;
+  it.L = __ldg(a.seq_lens + it.b);
+  it.t0 = cu0 + qt * PP_ROWS;
+  it.rows = min(PP_ROWS, it.n - qt * PP_ROWS);
+  it.bad_len = it.n > it.L;
+  if (it.bad_len) {
+    it.ntile = 0;
+    return true;
+  }
+  it.pos0 = it.L - it.n + qt * PP_ROWS;
+  const int p_max = it.pos0 + it.rows - 1;
+  it.lo_min = a.W > 0 ? max(0, it.pos0 - a.W + 1) : 0;
+  const long long cap = (long long)a.max_pages << a.log2_page;
+  const int k_reach = (int)min((long long)it.L, cap) - 1;
+  it.k_hi = min(p_max, k_reach);
+  it.kt0 = it.lo_min / TILE_KEYS;
+  it.ntile = it.k_hi >= it.lo_min ? it.k_hi / TILE_KEYS - it.kt0 + 1 : 0;
+  return true;
+}
+
+// Visible keys of row position pr within tile k0 (kmin > kmax: none).
+__device__ __forceinline__ void pp_row_keys(const PrefillArgs& a, const PPItem& it, int pr, int k0, int& kmin,
+                                            int& kmax) {
+  const int lor = a.W > 0 ? max(0, pr - a.W + 1) : 0;
+  kmin = max(k0, lor);
+  kmax = min(min(k0 + TILE_KEYS - 1, pr), it.k_hi);
+}
+
+// Every visible (row, key) pair of tile k0 is at distance >= E - 1: the tile reads bucket E - 1 only.
+__device__ __forceinline__ bool pp_tile_needs_bias(int pos0, int k0, int E) {
+  return pos0 - (k0 + TILE_KEYS - 1) < E - 1;
+}
+
+// Does bias box gr (rows BR gr .. BR gr + BR - 1) read any bucket below E - 1 in tile k0?
+__device__ __forceinline__ bool pp_group_needed(const PrefillArgs& a, const PPItem& it, int k0, int gr) {
+  const int r0 = BR * gr;
+  if (r0 >= it.rows) return false;
+  const int p_lo = it.pos0 + r0, p_hi = it.pos0 + min(r0 + BR - 1, it.rows - 1);
+  const int lo_lo = a.W > 0 ? max(0, p_lo - a.W + 1) : 0;
+  const bool any_key = p_hi >= k0 && lo_lo <= min(k0 + TILE_KEYS - 1, it.k_hi);
+  const bool all_clamped = p_lo - (k0 + TILE_KEYS - 1) >= a.E - 1;
+  return any_key && !all_clamped;
+}
+
+template <int ALIGN>
+__device__ __forceinline__ int pp_group_x(int dmin0, int gr) {
+  return (dmin0 + BR * gr) & ~(ALIGN - 1);
+}
+
+// Two fp32 lanes in one 64-bit register: packed FMA and add (sm_100-family), three-input max.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Bounded wait with the call's limit; gives up at once when another warp has timed out.
+__device__ __forceinline__ bool pp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                       const PrefillArgs& a) {
+  if (mbar_try_wait(bar, parity)) return true;
+  if (*abort_flag) return false;
+  if (mbar_wait_limit(bar, parity, a.wait_ns)) return true;
+  record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
+// The same, with every lane of the warp waiting and one answer for the whole warp.
+__device__ __forceinline__ bool pp_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                            const PrefillArgs& a) {
+  return __all_sync(0xffffffffu, pp_wait(bar, parity, abort_flag, a));
+}
+
+// After an abort: wait (with the full limit) until fill n of a ring slot has landed, for
+// the last min(depth, issued) fills of the ring, so no copy is in flight at exit.
+__device__ __forceinline__ void pp_drain_ring(uint64_t* full, int depth, int issued, uint32_t* err) {
+#pragma unroll 1
+  for (int n = max(0, issued - depth); n < issued; ++n)
+    if (!mbar_wait_bounded(&full[n % depth], (uint32_t)(n / depth) & 1u)) record_error(err, INK_DEVERR_WAIT_TIMEOUT);
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(PP_THREADS, 1)
+prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmK3, const __grid_constant__ CUtensorMap tmV3,
+                    const __grid_constant__ CUtensorMap tmB, const PrefillArgs a) {
+  using S = PPShape<D>;
+  using L_ = PPSmem<D, BF16>;
+  using BS = PBias<BF16>;
+  using BT = typename BS::T;
+  constexpr int NK = S::NK, NV = S::NV, NB = BS::NB;
+  constexpr uint32_t IDESC_S = umma_idesc_bf16(PP_ROWS, TILE_KEYS, false, false);
+  constexpr uint32_t IDESC_PV = umma_idesc_bf16(PP_ROWS, D, false, true);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L_::bars);
+  uint64_t* k_full = bars;
+  uint64_t* k_empty = k_full + NK;
+  uint64_t* v_full = k_empty + NK;
+  uint64_t* v_empty = v_full + NV;
+  uint64_t* q_ready = v_empty + NV;   // [2] Q of the item in TMEM, O of the previous item read
+  uint64_t* s_full = q_ready + 2;     // [2] S_h in TMEM
+  uint64_t* s_empty = s_full + 2;     // [2] S_h read out by the softmax
+  uint64_t* p_full = s_empty + 2;     // [2] P_h in shared memory
+  uint64_t* pv_done = p_full + 2;     // [2] O_h += P_h V done (P_h may be rewritten; O_h stable)
+  uint64_t* b_full = pv_done + 2;     // [2 NB] head h's slot s at h NB + s
+  uint64_t* b_empty = b_full + 2 * NB;
+  uint64_t* drain = b_empty + 2 * NB;
+  uint64_t* vbad = reinterpret_cast<uint64_t*>(smem + L_::vbad);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L_::misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L_::misc + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int P = 1 << a.log2_page;
+  const int total_items = a.num_q_tiles * a.B * a.Hkv * ((a.G + 1) >> 1);
+
+  if (tid == 0) {
+    for (int x = 0; x < NK; ++x) {
+      mbar_init(&k_full[x], 1);
+      mbar_init(&k_empty[x], 1);
+    }
+    for (int x = 0; x < NV; ++x) {
+      mbar_init(&v_full[x], 1);
+      mbar_init(&v_empty[x], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&q_ready[x], 4);
+      mbar_init(&s_full[x], 1);
+      mbar_init(&s_empty[x], 4);
+      mbar_init(&p_full[x], 4);
+      mbar_init(&pv_done[x], 1);
+    }
+    for (int x = 0; x < 2 * NB; ++x) {
+      mbar_init(&b_full[x], 1);
+      mbar_init(&b_empty[x], 4);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    *abort_flag = 0;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "n"(512));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- K and V producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      if (P >= TILE_KEYS) {
+        prefetch_tensormap(&tmK3);
+        prefetch_tensormap(&tmV3);
+      }
+    }
+    int g = 0, gk = 0, gv = 0;   // tiles walked, K and V fills issued
+    int chunk_b = -1, chunk_base = 0, chunk_val = -1;
+    const int seg = P < TILE_KEYS ? P : TILE_KEYS;
+    const int nseg = TILE_KEYS / seg;
+    bool go = true;
+    for (int i = blockIdx.x; i < total_items && go; i += gridDim.x) {
+      PPItem it;
+      if (!pp_item(a, i, it) || it.ntile == 0) continue;
+      const int32_t* bt = a.block_table + (size_t)it.b * a.max_pages;
+      const int last_idx = it.k_hi >> a.log2_page;   // never read the table past here
+      for (int j = 0; j < it.ntile; ++j, ++g) {
+        const int k0 = (it.kt0 + j) * TILE_KEYS;
+        // lane sg < nseg takes segment sg of the tile: seg keys on one page
+        const int pfirst = k0 >> a.log2_page, plast = (k0 + TILE_KEYS - 1) >> a.log2_page;
+        if (chunk_b != it.b || pfirst < chunk_base || plast >= chunk_base + 32) {
+          chunk_b = it.b;
+          chunk_base = pfirst;
+          const int idx = chunk_base + lane;
+          const int v = __ldg(bt + min(idx, last_idx));   // in bounds even past the last entry
+          chunk_val = idx <= last_idx ? v : -1;
+        }
+        const int ks = k0 + lane * seg;
+        const bool want = lane < nseg && ks <= it.k_hi && ks + seg - 1 >= it.lo_min;
+        const int page = __shfl_sync(0xffffffffu, chunk_val, min(max((ks >> a.log2_page) - chunk_base, 0), 31));
+        const bool bad_seg = want && (page < 0 || page >= a.num_pages);
+        const bool load = want && !bad_seg;
+        const uint32_t lmask = __ballot_sync(0xffffffffu, load);
+        const uint32_t bmask = __ballot_sync(0xffffffffu, bad_seg);
+        const int my_row = ((page * a.Hkv + it.kvh) << a.log2_page) + (ks & (P - 1));
+        const uint32_t bytes = (uint32_t)__popc(lmask) * (uint32_t)(seg * D * 2);
+#pragma unroll 1
+        for (int kv = 0; kv < 2; ++kv) {
+          const bool is_k = kv == 0;
+          const int NR = is_k ? NK : NV;
+          const int n = is_k ? gk : gv;
+          const int st = n % NR;
+          uint64_t* full = is_k ? k_full : v_full;
+          if (n >= NR && !pp_wait_warp(is_k ? &k_empty[st] : &v_empty[st], (uint32_t)((n / NR) - 1) & 1u,
+                                       abort_flag, a)) {
+            go = false;
+            break;
+          }
+          if (!is_k && lane == 0) {   // keys whose page is outside the pool: the MMA warp zeroes their V rows
+            uint64_t bad = 0;
+#pragma unroll 1
+            for (uint32_t mm = bmask; mm; mm &= mm - 1)
+              bad |= seg == 64 ? ~0ull : (((1ull << seg) - 1) << ((__ffs(mm) - 1) * seg));
+            vbad[st] = bad;
+          }
+          if (is_k && bmask && lane == 0) record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
+          __syncwarp();
+          mbar_arrive_expect_tx_warp(&full[st], bytes);
+          uint8_t* ring = smem + (is_k ? L_::kst : L_::vst) + (size_t)st * S::KV_TILE;
+#pragma unroll 1
+          for (uint32_t mm = lmask; mm; mm &= mm - 1) {
+            const int sg = __ffs(mm) - 1;
+            const int row = __shfl_sync(0xffffffffu, my_row, sg);
+            uint8_t* dst = ring + sg * seg * 128;
+            if (seg == TILE_KEYS) {
+              tma_load_3d_warp(dst, is_k ? &tmK3 : &tmV3, 0, row, 0, &full[st]);   // whole tile: one box
+            } else {
+#pragma unroll
+              for (int cb = 0; cb < S::CB; ++cb)
+                tma_load_2d_warp(dst + cb * S::KV_SUB, is_k ? &tmK : &tmV, cb * 64, row, &full[st]);
+            }
+          }
+          if (is_k) ++gk; else ++gv;
+        }
+        if (!go) break;
+      }
+    }
+    if (lane == 0) {
+      pp_drain_ring(k_full, NK, gk, a.err);
+      pp_drain_ring(v_full, NV, gv, a.err);
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    // Per head h a count n_h of S tiles issued: S_h(n) goes into the head's one S buffer after
+    // the softmax has read S_h(n - 1) (s_empty phase n - 1), so every phase of s_empty, p_full
+    // and q_ready is waited for in order.
+    int g = 0;                     // tiles walked
+    int qc[2] = {0, 0};            // items per head
+    int sn[2] = {0, 0};            // S tiles issued per head
+    int pc[2] = {0, 0};            // P tiles consumed per head
+    bool go = true;
+    auto issue_s = [&](int h, int kslot) -> bool {
+      if (sn[h] > 0 && !pp_wait_warp(&s_empty[h], (uint32_t)(sn[h] - 1) & 1u, abort_flag, a)) return false;
+      tc_fence_after();
+      const uint32_t kbase = smem_u32(smem + L_::kst + (size_t)kslot * S::KV_TILE);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t bd = umma_desc_sw128(kbase + (kk >> 2) * S::KV_SUB + (kk & 3) * 32, 16, 1024);
+        umma_ts_warp(tmem + S::TS + 64u * h, tmem + S::TQ + S::QC * h + kk * 8, bd, IDESC_S, kk > 0 ? 1u : 0u);
+      }
+      umma_commit_warp(&s_full[h]);
+      ++sn[h];
+      return true;
+    };
+    for (int i = blockIdx.x; i < total_items && go; i += gridDim.x) {
+      PPItem it;
+      if (!pp_item(a, i, it) || it.ntile == 0) continue;
+      // S of tile 0 for each head once its Q is in TMEM
+      go = pp_wait_warp(&k_full[g % NK], (uint32_t)(g / NK) & 1u, abort_flag, a);
+      for (int h = 0; h < it.nh && go; ++h) {
+        go = pp_wait_warp(&q_ready[h], (uint32_t)qc[h] & 1u, abort_flag, a);
+        ++qc[h];
+        if (go) go = issue_s(h, g % NK);
+      }
+      if (!go) break;
+      umma_commit_warp(&k_empty[g % NK]);
+      __syncwarp();
+      for (int j = 0; j < it.ntile && go; ++j) {
+        const int gj = g + j;
+        const int k0 = (it.kt0 + j) * TILE_KEYS;
+        // S of the next tile for each head, as soon as its softmax has read this tile's S
+        if (j + 1 < it.ntile) {
+          go = pp_wait_warp(&k_full[(gj + 1) % NK], (uint32_t)((gj + 1) / NK) & 1u, abort_flag, a);
+          for (int h = 0; h < it.nh && go; ++h) go = issue_s(h, (gj + 1) % NK);
+          if (!go) break;
+          umma_commit_warp(&k_empty[(gj + 1) % NK]);
+        }
+        // O_h += P_h V for this tile once P_h is in shared memory
+        const int vs = gj % NV;
+        go = pp_wait_warp(&v_full[vs], (uint32_t)(gj / NV) & 1u, abort_flag, a);
+        if (!go) break;
+        {
+          // zero the V rows of keys that no row of the item may read
+          const uint64_t vb = vbad[vs];
+          if (k0 < it.lo_min || k0 + TILE_KEYS - 1 > it.k_hi || vb) {
+            uint8_t* vt = smem + L_::vst + (size_t)vs * S::KV_TILE;
+#pragma unroll 1
+            for (int rr = lane; rr < TILE_KEYS; rr += 32) {
+              const int k = k0 + rr;
+              if (k < it.lo_min || k > it.k_hi || ((vb >> rr) & 1ull)) {
+#pragma unroll 1
+                for (int cb = 0; cb < S::CB; ++cb) {
+                  uint4* row = reinterpret_cast<uint4*>(vt + cb * S::KV_SUB + rr * 128);
+#pragma unroll
+                  for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
+              }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+          }
+        }
+        const uint32_t vbase = smem_u32(smem + L_::vst + (size_t)vs * S::KV_TILE);
+        for (int h = 0; h < it.nh && go; ++h) {
+          go = pp_wait_warp(&p_full[h], (uint32_t)pc[h] & 1u, abort_flag, a);
+          ++pc[h];
+          if (!go) break;
+          tc_fence_after();
+          const uint32_t pbase = smem_u32(smem + L_::pst + (size_t)h * S::P_BYTES);
+#pragma unroll
+          for (int ks = 0; ks < TILE_KEYS / 16; ++ks) {
+            const uint64_t adesc = umma_desc_sw128(pbase + ks * 32, 16, 1024);
+            const uint64_t bdesc = umma_desc_sw128(vbase + ks * 16 * 128, S::KV_SUB, 1024);
+            umma_ss_warp(tmem + S::TO + (uint32_t)(D * h), adesc, bdesc, IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit_warp(&pv_done[h]);
+          if (h == it.nh - 1) umma_commit_warp(&v_empty[vs]);
+          __syncwarp();
+        }
+      }
+      g += it.ntile;
+    }
+    // every MMA issued so far is complete before tensor memory is released
+    umma_commit_warp(drain);
+    __syncwarp();
+    if (!mbar_wait_bounded(drain, 0)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
+  } else if (warp == 2 || warp == 3) {
+    // -------------------------------------------------------------- bias producers
+    // Warp 2 + hs loads the bias of head slot hs: for each tile that reads any bucket below
+    // E - 1, the boxes of the 32-row groups that do, into the head's next ring slot.  Out-of-
+    // range buckets and tokens arrive as zeros and are never used.
+    const int hs = warp - 2;
+    if (lane == 0) prefetch_tensormap(&tmB);
+    int cnt = 0;
+    bool go = true;
+    for (int i = blockIdx.x; i < total_items && go; i += gridDim.x) {
+      PPItem it;
+      if (!pp_item(a, i, it) || it.ntile == 0 || hs >= it.nh) continue;
+      const int h = it.h0 + hs;
+      for (int j = 0; j < it.ntile; ++j) {
+        const int k0 = (it.kt0 + j) * TILE_KEYS;
+        if (!pp_tile_needs_bias(it.pos0, k0, a.E)) continue;
+        const int slot = cnt % NB;
+        if (cnt >= NB && !pp_wait_warp(&b_empty[hs * NB + slot], (uint32_t)((cnt / NB) - 1) & 1u, abort_flag, a)) {
+          go = false;
+          break;
+        }
+        BT* sb = reinterpret_cast<BT*>(smem + L_::bias + (size_t)(hs * NB + slot) * BS::SLOT_BYTES);
+        const int dmin0 = it.pos0 - (k0 + TILE_KEYS - 1);
+        const uint32_t nm = __ballot_sync(0xffffffffu, lane < NGR && pp_group_needed(a, it, k0, lane));
+        mbar_arrive_expect_tx_warp(&b_full[hs * NB + slot], (uint32_t)__popc(nm) * (uint32_t)(BS::GROUP * sizeof(BT)));
+#pragma unroll 1
+        for (uint32_t mm = nm; mm; mm &= mm - 1) {
+          const int gr = __ffs(mm) - 1;
+          tma_load_3d_warp(sb + gr * BS::GROUP, &tmB, pp_group_x<BS::ALIGN>(dmin0, gr), h, it.t0 + BR * gr,
+                           &b_full[hs * NB + slot]);
+        }
+        ++cnt;
+      }
+    }
+    if (lane == 0) pp_drain_ring(b_full + hs * NB, NB, cnt, a.err);
+  } else {
+    // -------------------------------------------------------------- softmax warpgroups
+    const int hs = (warp - 4) >> 2;   // head slot
+    const int sw = (warp - 4) & 3;    // TMEM lane quarter
+    const int r = sw * 32 + lane;
+    const uint32_t tlane = tmem + ((uint32_t)(sw * 32) << 16);
+    const uint32_t tm_q = tlane + S::TQ + S::QC * hs;
+    const uint32_t tm_s = tlane + S::TS + 64u * hs;
+    const uint32_t tm_o = tlane + S::TO + (uint32_t)(D * hs);
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+    int th = 0, ic = 0, bcnt = 0;   // tiles, items and bias tiles of this head slot
+    bool go = true;
+    for (int i = blockIdx.x; i < total_items && go; i += gridDim.x) {
+      PPItem it;
+      if (!pp_item(a, i, it)) continue;
+      if (hs == 0 && sw == 0 && lane == 0 && it.t0 == __ldg(a.cu_q + it.b) && it.h0 == 0) {
+        if (it.n > a.max_q_len) record_error(a.err, INK_DEVERR_QLEN_EXCEEDS_MAX);
+        if (it.bad_len) record_error(a.err, INK_DEVERR_QLEN_EXCEEDS_KV);
+        else if ((long long)it.L > ((long long)a.max_pages << a.log2_page))
+          record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
+      }
+      if (hs >= it.nh) continue;
+      const int h = it.h0 + hs;
+      const bool rv = r < it.rows;
+      if (it.ntile == 0) {  // nothing visible (inconsistent lengths or no readable key): zeros
+        if (rv) {
+          uint4* o = reinterpret_cast<uint4*>(out + ((size_t)(it.t0 + r) * a.Hq + h) * D);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) o[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        continue;
+      }
+      // ---- Q row into TMEM (rows past the item's last are zero); the previous item's S
+      // products that read Q_h are complete (their s_full was seen), and its O_h has been read
+      {
+        const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                           ((size_t)(it.t0 + (rv ? r : 0)) * a.Hq + h) * D);
+#pragma unroll
+        for (int half = 0; half < D / 64; ++half) {
+          uint32_t qv[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 x = rv ? __ldg(qsrc + half * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
+            qv[4 * c] = x.x;
+            qv[4 * c + 1] = x.y;
+            qv[4 * c + 2] = x.z;
+            qv[4 * c + 3] = x.w;
+          }
+          tmem_st32(tm_q + 32 * half, qv);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_ready[hs]);
+      }
+      const int pr = it.pos0 + r;
+      // bucket E - 1 of this row (rows past the item's last read its last row: in bounds)
+      const BT* relrow = static_cast<const BT*>(a.rel) + ((size_t)(it.t0 + (rv ? r : it.rows - 1)) * a.Hq + h) * a.E;
+      const float clampv = rv ? to_float_b(__ldg(relrow + a.E - 1)) : 0.f;
+      const int32_t* bt = a.block_table + (size_t)it.b * a.max_pages;
+      const int seg = P < TILE_KEYS ? P : TILE_KEYS;
+      // Does some page holding a key of the item lie outside the pool?  (Checked once per
+      // item; only then are per-tile masks of unreadable keys built.)
+      bool item_bad = false;
+      {
+        const int p0 = it.lo_min >> a.log2_page, p1 = it.k_hi >> a.log2_page;
+#pragma unroll 1
+        for (int pi = p0 + lane; pi <= p1; pi += 32) {
+          const int page = __ldg(bt + pi);
+          item_bad |= page < 0 || page >= a.num_pages;
+        }
+        item_bad = __any_sync(0xffffffffu, item_bad);
+      }
+      auto tile_bad = [&](int k0) {
+        uint64_t bad = 0;
+#pragma unroll 1
+        for (int sg = 0; sg < TILE_KEYS / seg; ++sg) {
+          const int ks = k0 + sg * seg;
+          if (ks > it.k_hi || ks + seg - 1 < it.lo_min) continue;
+          const int page = __ldg(bt + min(ks >> a.log2_page, it.k_hi >> a.log2_page));
+          if (page < 0 || page >= a.num_pages) bad |= (seg == 64 ? ~0ull : (((1ull << seg) - 1) << (sg * seg)));
+        }
+        return bad;
+      };
+      float m = -INFINITY, l = 0.f;
+      uint8_t* prow = smem + L_::pst + (size_t)hs * S::P_BYTES + (size_t)r * 128;   // this row of P_h
+      const uint64_t scale2 = f2_pack(a.sm_scale, a.sm_scale);
+      const uint64_t log2e2 = f2_pack(LOG2E, LOG2E);
+      for (int j = 0; j < it.ntile; ++j, ++th) {
+        const int k0 = (it.kt0 + j) * TILE_KEYS;
+        const bool needs = pp_tile_needs_bias(it.pos0, k0, a.E);
+        const uint64_t bad = item_bad ? tile_bad(k0) : 0ull;
+        go = pp_wait_warp(&s_full[hs], (uint32_t)th & 1u, abort_flag, a);
+        if (!go) break;
+        tc_fence_after();
+        uint32_t sr[64];
+        {
+          uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+          uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+          tmem_ld32(tm_s, lo);
+          tmem_ld32(tm_s + 32, hi);
+          tmem_wait_ld();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[hs]);   // the MMA may compute the next S into this buffer
+        // visible columns of this row: [kmin - k0, kmax - k0] less unreadable keys
+        int kmin, kmax;
+        pp_row_keys(a, it, pr, k0, kmin, kmax);
+        uint64_t vis = 0;
+        if (rv && kmax >= kmin) vis = (~0ull >> (TILE_KEYS - 1 - (kmax - k0))) & (~0ull << (kmin - k0));
+        vis &= ~bad;
+        // key c sits at distance dmin + 63 - c; columns c <= cc read bucket E - 1
+        const int dmin = pr - (k0 + TILE_KEYS - 1);
+        const int cc = dmin + TILE_KEYS - a.E;
+        const int bslot_i = hs * NB + bcnt % NB;
+        const BT* bslot = reinterpret_cast<const BT*>(smem + L_::bias + (size_t)bslot_i * BS::SLOT_BYTES);
+        // bucket of key c at brow[-c]; any address in the slot when the tile reads no bucket from it
+        const BT* brow = bslot + (TILE_KEYS - 1);
+        if (needs) {
+          go = pp_wait_warp(&b_full[bslot_i], (uint32_t)(bcnt / NB) & 1u, abort_flag, a);
+          if (!go) break;
+          const int gr = r / BR;
+          brow = bslot + gr * BS::GROUP + (r % BR) * BS::COLS + (dmin - pp_group_x<BS::ALIGN>(dmin - r, gr)) +
+                 (TILE_KEYS - 1);
+        }
+        float mxv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        const bool all_vis = vis == ~0ull;
+        if (__all_sync(0xffffffffu, all_vis && cc < 0)) {
+          // every key visible, every bucket from the tile's bias rows
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            float x, y;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2,
+                             f2_pack(to_float_b(brow[-c]), to_float_b(brow[-c - 1]))), x, y);
+            sr[c] = __float_as_uint(x);
+            sr[c + 1] = __float_as_uint(y);
+            mxv[(c >> 1) & 3] = fmax3(mxv[(c >> 1) & 3], x, y);
+          }
+        } else if (__all_sync(0xffffffffu, all_vis && cc >= TILE_KEYS - 1)) {
+          // every key visible at distance >= E - 1
+          const uint64_t cl2 = f2_pack(clampv, clampv);
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            float x, y;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2, cl2), x, y);
+            sr[c] = __float_as_uint(x);
+            sr[c + 1] = __float_as_uint(y);
+            mxv[(c >> 1) & 3] = fmax3(mxv[(c >> 1) & 3], x, y);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const float b0 = c <= cc ? clampv : to_float_b(brow[-c]);
+            const float b1 = c + 1 <= cc ? clampv : to_float_b(brow[-c - 1]);
+            float x, y;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2, f2_pack(b0, b1)), x, y);
+            x = ((vis >> c) & 1ull) ? x : -INFINITY;
+            y = ((vis >> (c + 1)) & 1ull) ? y : -INFINITY;
+            sr[c] = __float_as_uint(x);
+            sr[c + 1] = __float_as_uint(y);
+            mxv[(c >> 1) & 3] = fmax3(mxv[(c >> 1) & 3], x, y);
+          }
+        }
+        const float mx = fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3]));
+        if (needs) {
+          // every bias value this thread read is consumed (mx depends on all of them)
+          asm volatile("" ::"f"(mx) : "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&b_empty[bslot_i]);
+          ++bcnt;
+        }
+        const float m_new = fmaxf(m, mx);
+        if (j == 0) {
+          m = m_new;
+        } else {
+          const bool mine = m_new > m + RESCALE_NAT;
+          if (__any_sync(0xffffffffu, mine)) {
+            // O_h must hold every earlier tile's P V product before it is rescaled
+            go = pp_wait_warp(&pv_done[hs], (uint32_t)(th - 1) & 1u, abort_flag, a);
+            if (!go) break;
+            tc_fence_after();
+            const float f = mine ? fast_exp2((m - m_new) * LOG2E) : 1.f;
+#pragma unroll 1
+            for (int c2 = 0; c2 < D / 32; ++c2) {
+              uint32_t ov[32];
+              tmem_ld32(tm_o + c2 * 32, ov);
+              tmem_wait_ld();
+#pragma unroll
+              for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * f);
+              tmem_st32(tm_o + c2 * 32, ov);
+            }
+            tmem_wait_st();
+            l *= f;
+            if (mine) m = m_new;
+          }
+        }
+        // p = 2^(s log2(e) - m log2(e)); masked keys (s = -inf) give exactly 0
+        const float mb = m == -INFINITY ? 0.f : m * LOG2E;
+        const uint64_t nmb2 = f2_pack(-mb, -mb);
+        uint32_t pk[32];
+        uint64_t ls2[2] = {0ull, 0ull};   // two packed partial sums (+0.0f pairs)
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), log2e2, nmb2), t0, t1);
+          const float p0 = fast_exp2(t0);
+          const float p1 = fast_exp2(t1);
+          ls2[c & 1] = f2_add(ls2[c & 1], f2_pack(p0, p1));
+          pk[c] = pack_bf16(p0, p1);
+        }
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(ls2[0], a0, a1);
+          f2_unpack(ls2[1], b0, b1);
+          l += (a0 + b0) + (a1 + b1);
+        }
+        // P_h of the previous tile has been read by its P V product: the buffer is free
+        if (th > 0) {
+          go = pp_wait_warp(&pv_done[hs], (uint32_t)(th - 1) & 1u, abort_flag, a);
+          if (!go) break;
+        }
+        // P row r: 128 bytes (64 keys), 16-byte chunk c at chunk position c ^ (r & 7)
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[hs]);
+      }
+      if (!go) break;
+      // ---- epilogue: O_h / l -> bf16 -> out, once the item's last P V product is done
+      go = pp_wait_warp(&pv_done[hs], (uint32_t)(th - 1) & 1u, abort_flag, a);
+      ++ic;
+      if (!go) break;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint4* orow = reinterpret_cast<uint4*>(out + ((size_t)(it.t0 + r) * a.Hq + h) * D);
+#pragma unroll 1
+      for (int c2 = 0; c2 < D / 16; ++c2) {
+        uint32_t ov[16];
+        tmem_ld16(tm_o + c2 * 16, ov);
+        tmem_wait_ld();
+        if (rv) {
+#pragma unroll
+          for (int q4 = 0; q4 < 2; ++q4) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(ov[8 * q4 + 0]) * inv, __uint_as_float(ov[8 * q4 + 1]) * inv);
+            v.y = pack_bf16(__uint_as_float(ov[8 * q4 + 2]) * inv, __uint_as_float(ov[8 * q4 + 3]) * inv);
+            v.z = pack_bf16(__uint_as_float(ov[8 * q4 + 4]) * inv, __uint_as_float(ov[8 * q4 + 5]) * inv);
+            v.w = pack_bf16(__uint_as_float(ov[8 * q4 + 6]) * inv, __uint_as_float(ov[8 * q4 + 7]) * inv);
+            orow[c2 * 2 + q4] = v;
+          }
+        }
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(512));
+  }
+}
+
+int num_sms_pp() {
+  int dev = 0;
+  const int n = current_device_sms(&dev);
+  return n > 0 ? n : 148;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_pair_t(const PrefillMaps& m, const PrefillArgs& a, cudaStream_t stream) {
+  constexpr size_t smem = PPSmem<D, BF16>::alloc;
+  static_assert(smem <= 227 * 1024, "shared memory budget");
+  static std::atomic<unsigned long long> opted{0};
+  cudaError_t e = smem_opt_in_once(prefill_pair_kernel<D, BF16>, (int)smem, opted);
+  if (e != cudaSuccess) return e;
+  const long long items = (long long)a.num_q_tiles * a.B * a.Hkv * ((a.G + 1) / 2);
+  const int grid = (int)std::min<long long>(items, num_sms_pp());
+  prefill_pair_kernel<D, BF16><<<grid, PP_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.bias, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_pair(const PrefillMaps& m, const PrefillArgs& a, int head_dim, cudaStream_t stream) {
+  if (a.bias_bf16)
+    return head_dim == 128 ? launch_pair_t<128, true>(m, a, stream) : launch_pair_t<64, true>(m, a, stream);
+  return head_dim == 128 ? launch_pair_t<128, false>(m, a, stream) : launch_pair_t<64, false>(m, a, stream);
+}
+
+}  // namespace ink

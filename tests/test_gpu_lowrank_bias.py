@@ -57,7 +57,7 @@ def test_lowrank_bias_edge_shapes(case):
 def test_lowrank_bias_matches_the_materialised_bias_entry():
     """The low-rank entry against the fp32 entry fed rel = r x proj (built in fp32 by a
     library GEMM): the same attention up to the rounding of the bias (fp16 in the low-rank
-    path) and of the bf16 output."""
+    path), the summation order of each kernel and the bf16 output."""
     prob = W.mixed_layer("swa", 0, DEV)[0]
     lr = W.make_problem(num_q_heads=prob.num_q_heads, num_kv_heads=prob.num_kv_heads, head_dim=prob.head_dim,
                         page_size=prob.page_size, rel_extent=prob.rel_extent, window=prob.window,
@@ -71,8 +71,10 @@ def test_lowrank_bias_matches_the_materialised_bias_entry():
     d = a.float() - b.float()
     diff = d.abs().max().item()
     rel = (d.norm() / b.float().norm()).item()
-    # the low-rank path keeps each tile's bias in fp16: outputs may differ by an ulp of bf16
-    assert diff <= 2e-2 and rel <= 2e-3, f"low-rank vs materialised bias: max diff {diff}, rel RMS {rel}"
+    # Two kernels with different fp32 summation orders (the materialised bias runs the
+    # head-pair prefill), each within max-abs 2e-2 and relative RMS 5e-3 of the fp64 oracle:
+    # their difference is held to the same bounds.
+    assert diff <= 2e-2 and rel <= 5e-3, f"low-rank vs materialised bias: max diff {diff}, rel RMS {rel}"
     lr.r, lr.rel_proj_t = r_saved, p_saved
 
 

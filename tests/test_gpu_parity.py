@@ -81,6 +81,9 @@ EDGE = [
     (4, 2, 128, 64, 1, 4, [70, 3], [70, 90]),                   # window 1: own value
     (8, 2, 128, 256, 512, 512, [300, 1], [1500, 777]),          # P256, SWA
     (8, 4, 64, 64, -1, 100, [0, 17, 1], [0, 17, 0]),            # zero-length sequences
+    (6, 2, 128, 64, -1, 64, [200, 129], [900, 129]),            # G3: a head pair and a lone head
+    (12, 4, 64, 16, 100, 256, [257, 3, 128], [400, 3, 128]),    # G3, D64, window 100
+    (2, 2, 128, 64, 512, 512, [520, 64], [1100, 64]),           # MHA, SWA, two q tiles
 ]
 
 
