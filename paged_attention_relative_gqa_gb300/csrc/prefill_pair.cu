@@ -40,38 +40,18 @@
 // issuing copies and MMAs, waits for the copies and MMAs already issued, and exits.
 #include <type_traits>
 
-#include "common.cuh"
-#include "kernels.h"
+#include "prefill_common.cuh"
 
 namespace ink {
 
 namespace {
 
 constexpr int PP_THREADS = 384;
-constexpr int PP_ROWS = PREFILL_ROWS;          // new tokens per item
-constexpr int BR = PAIR_BIAS_ROWS;             // tokens per bias box
-constexpr int NGR = PP_ROWS / BR;              // bias boxes per tile and head
-constexpr float RESCALE_NAT = 5.545177444479562f;   // rescale O when a max grows by > 2^8
+using namespace pf;
 
-
-// Bias slot of one head and one tile: NGR boxes of BR rows; box gr holds buckets
-// [x_gr, x_gr + COLS) of its rows, row i at +COLS i, x_gr = ALIGN floor((dmin0 + BR gr) / ALIGN)
-// where dmin0 = pos0 - (k0 + 63) is row 0's smallest distance in the tile (x_gr is 16-byte
-// aligned, as TMA wants).  Row r = BR gr + i finds the bucket of key k0 + c at
-// offset (dmin_r - x_gr) + 63 - c, dmin_r - x_gr in [i, i + ALIGN - 1].  The row pitch plus the
-// one-bucket skew between rows is odd (fp32: 101 words), so the 32 rows of a warp read 32
-// different banks (bf16: at most two rows per bank).
+// Bias ring slots per head: two for the bf16 bias, one for fp32 (shared-memory budget).
 template <bool BF16>
-struct PBias {
-  using T = typename std::conditional<BF16, __nv_bfloat16, float>::type;
-  static constexpr int COLS = BF16 ? PAIR_BIAS_COLS_BF16 : PAIR_BIAS_COLS_F32;
-  static constexpr int ALIGN = 16 / (int)sizeof(T);
-  static constexpr int GROUP = BR * COLS;                       // elements per box
-  static constexpr int SLOT_BYTES = NGR * GROUP * (int)sizeof(T);
-  static constexpr int NB = BF16 ? 2 : 1;                       // slots per head
-  static_assert(COLS >= TILE_KEYS + BR - 1 + ALIGN - 1, "bias box too narrow");
-  static_assert((COLS * (int)sizeof(T)) % 16 == 0 && SLOT_BYTES % 1024 == 0, "TMA alignment");
-};
+using PairBias = PBias<BF16, BF16 ? 2 : 1>;
 
 template <int D>
 struct PPShape {
@@ -91,7 +71,7 @@ struct PPShape {
 template <int D, bool BF16>
 struct PPSmem {
   using S = PPShape<D>;
-  using B = PBias<BF16>;
+  using B = PairBias<BF16>;
   static constexpr size_t kst = 0;
   static constexpr size_t vst = kst + (size_t)S::NK * S::KV_TILE;
   static constexpr size_t pst = vst + (size_t)S::NV * S::KV_TILE;
@@ -106,123 +86,85 @@ struct PPSmem {
   static constexpr size_t alloc = total + 1024;
 };
 
-struct PPItem {
-  int b, kvh, h0, nh, t0, rows, n, L, pos0, lo_min, k_hi, kt0, ntile;
-  bool bad_len;
-};
+// S_h = Q_h K^T of one 64-key tile (A = Q from TMEM, B = the K tile, K-major with the 128-byte
+// swizzle), D / 16 K-steps; descriptors of later K-steps add the byte offset / 16 to the
+// start-address field.  Executed by a converged warp; one elected lane issues.
+template <int D>
+__device__ __forceinline__ void pair_issue_s(uint32_t d, uint32_t a0, uint64_t b0, uint64_t* done) {
+  constexpr uint32_t IDESC_S = umma_idesc_bf16(PP_ROWS, TILE_KEYS, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk)
+    umma_ts_warp(d, a0 + kk * 8, b0 + (uint64_t)((((kk >> 2) * TILE_KEYS * 128) + (kk & 3) * 32) >> 4), IDESC_S,
+                 kk > 0 ? 1u : 0u);
+  umma_commit_warp(done);
+}
 
-// Item i: q-tile level (longest first), then sequence, KV head and head pair.
-__device__ __forceinline__ bool pp_item(const PrefillArgs& a, int i, PPItem& it) {
-  const int npair = (a.G + 1) >> 1;
-  const int per_qt = a.B * a.Hkv * npair;
-  const int qrev = i / per_qt;
-  int r = i - qrev * per_qt;
-  it.b = r / (a.Hkv * npair);
-  r -= it.b * (a.Hkv * npair);
-  it.kvh = r / npair;
-  const int pair = r - it.kvh * npair;
-  it.h0 = it.kvh * a.G + 2 * pair;
-  it.nh = min(2, a.G - 2 * pair);
-  const int qt = a.num_q_tiles - 1 - qrev;
-  const int cu0 = __ldg(a.cu_q + it.b);
-  it.n = __ldg(a.cu_q + it.b + 1) - cu0;
-  if (qt * PP_ROWS >= it.n) return false;
-  it.L = __ldg(a.seq_lens + it.b);
-  it.t0 = cu0 + qt * PP_ROWS;
-  it.rows = min(PP_ROWS, it.n - qt * PP_ROWS);
-  it.bad_len = it.n > it.L;
-  if (it.bad_len) {
-    it.ntile = 0;
-    return true;
+// O_h += P_h V of one 64-key tile (A = P from shared memory, B = the V tile, MN-major), four
+// K-steps of 16 keys; the first product of an item overwrites O_h.
+template <int D>
+__device__ __forceinline__ void pair_issue_pv(uint32_t d, uint64_t a0, uint64_t b0, uint32_t acc0, uint64_t* done) {
+  constexpr uint32_t IDESC_PV = umma_idesc_bf16(PP_ROWS, D, false, true);
+#pragma unroll
+  for (int ks = 0; ks < TILE_KEYS / 16; ++ks)
+    umma_ss_warp(d, a0 + (uint64_t)((ks * 32) >> 4), b0 + (uint64_t)((ks * 16 * 128) >> 4), IDESC_PV,
+                 (acc0 || ks > 0) ? 1u : 0u);
+  umma_commit_warp(done);
+}
+
+// Load this thread's Q row (rows past the item's last are zero) into TMEM (D / 2 columns).
+template <int D>
+__device__ __forceinline__ void pair_load_q(const uint4* qsrc, bool rv, uint32_t tm_q) {
+#pragma unroll
+  for (int half = 0; half < D / 64; ++half) {
+    uint32_t qv[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 x = rv ? __ldg(qsrc + half * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
+      qv[4 * c] = x.x;
+      qv[4 * c + 1] = x.y;
+      qv[4 * c + 2] = x.z;
+      qv[4 * c + 3] = x.w;
+    }
+    tmem_st32(tm_q + 32 * half, qv);
   }
-  it.pos0 = it.L - it.n + qt * PP_ROWS;
-  const int p_max = it.pos0 + it.rows - 1;
-  it.lo_min = a.W > 0 ? max(0, it.pos0 - a.W + 1) : 0;
-  const long long cap = (long long)a.max_pages << a.log2_page;
-  const int k_reach = (int)min((long long)it.L, cap) - 1;
-  it.k_hi = min(p_max, k_reach);
-  it.kt0 = it.lo_min / TILE_KEYS;
-  it.ntile = it.k_hi >= it.lo_min ? it.k_hi / TILE_KEYS - it.kt0 + 1 : 0;
-  return true;
+  tmem_wait_st();
 }
 
-// Visible keys of row position pr within tile k0 (kmin > kmax: none).
-__device__ __forceinline__ void pp_row_keys(const PrefillArgs& a, const PPItem& it, int pr, int k0, int& kmin,
-                                            int& kmax) {
-  const int lor = a.W > 0 ? max(0, pr - a.W + 1) : 0;
-  kmin = max(k0, lor);
-  kmax = min(min(k0 + TILE_KEYS - 1, pr), it.k_hi);
-}
-
-// Every visible (row, key) pair of tile k0 is at distance >= E - 1: the tile reads bucket E - 1 only.
-__device__ __forceinline__ bool pp_tile_needs_bias(int pos0, int k0, int E) {
-  return pos0 - (k0 + TILE_KEYS - 1) < E - 1;
-}
-
-// Does bias box gr (rows BR gr .. BR gr + BR - 1) read any bucket below E - 1 in tile k0?
-__device__ __forceinline__ bool pp_group_needed(const PrefillArgs& a, const PPItem& it, int k0, int gr) {
-  const int r0 = BR * gr;
-  if (r0 >= it.rows) return false;
-  const int p_lo = it.pos0 + r0, p_hi = it.pos0 + min(r0 + BR - 1, it.rows - 1);
-  const int lo_lo = a.W > 0 ? max(0, p_lo - a.W + 1) : 0;
-  const bool any_key = p_hi >= k0 && lo_lo <= min(k0 + TILE_KEYS - 1, it.k_hi);
-  const bool all_clamped = p_lo - (k0 + TILE_KEYS - 1) >= a.E - 1;
-  return any_key && !all_clamped;
-}
-
-template <int ALIGN>
-__device__ __forceinline__ int pp_group_x(int dmin0, int gr) {
-  return (dmin0 + BR * gr) & ~(ALIGN - 1);
-}
-
-// Two fp32 lanes in one 64-bit register: packed FMA and add (sm_100-family), three-input max.
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// Bounded wait with the call's limit; gives up at once when another warp has timed out.
-__device__ __forceinline__ bool pp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                       const PrefillArgs& a) {
-  if (mbar_try_wait(bar, parity)) return true;
-  if (*abort_flag) return false;
-  if (mbar_wait_limit(bar, parity, a.wait_ns)) return true;
-  record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
-  *abort_flag = 1;
-  return false;
-}
-
-// The same, with every lane of the warp waiting and one answer for the whole warp.
-__device__ __forceinline__ bool pp_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                            const PrefillArgs& a) {
-  return __all_sync(0xffffffffu, pp_wait(bar, parity, abort_flag, a));
-}
-
-// After an abort: wait (with the full limit) until fill n of a ring slot has landed, for
-// the last min(depth, issued) fills of the ring, so no copy is in flight at exit.
-__device__ __forceinline__ void pp_drain_ring(uint64_t* full, int depth, int issued, uint32_t* err) {
+// Multiply this thread's row of O (D fp32 TMEM columns) by f.
+template <int D>
+__device__ __forceinline__ void pair_rescale_o(uint32_t tm_o, float f) {
 #pragma unroll 1
-  for (int n = max(0, issued - depth); n < issued; ++n)
-    if (!mbar_wait_bounded(&full[n % depth], (uint32_t)(n / depth) & 1u)) record_error(err, INK_DEVERR_WAIT_TIMEOUT);
+  for (int c2 = 0; c2 < D / 32; ++c2) {
+    uint32_t ov[32];
+    tmem_ld32(tm_o + c2 * 32, ov);
+    tmem_wait_ld();
+#pragma unroll
+    for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * f);
+    tmem_st32(tm_o + c2 * 32, ov);
+  }
+  tmem_wait_st();
+}
+
+// out row = O / l in bf16 (written only when `store`).
+template <int D>
+__device__ __forceinline__ void pair_store_o(uint32_t tm_o, float inv, uint4* orow, bool store) {
+#pragma unroll 1
+  for (int c2 = 0; c2 < D / 16; ++c2) {
+    uint32_t ov[16];
+    tmem_ld16(tm_o + c2 * 16, ov);
+    tmem_wait_ld();
+    if (store) {
+#pragma unroll
+      for (int q4 = 0; q4 < 2; ++q4) {
+        uint4 v;
+        v.x = pack_bf16(__uint_as_float(ov[8 * q4 + 0]) * inv, __uint_as_float(ov[8 * q4 + 1]) * inv);
+        v.y = pack_bf16(__uint_as_float(ov[8 * q4 + 2]) * inv, __uint_as_float(ov[8 * q4 + 3]) * inv);
+        v.z = pack_bf16(__uint_as_float(ov[8 * q4 + 4]) * inv, __uint_as_float(ov[8 * q4 + 5]) * inv);
+        v.w = pack_bf16(__uint_as_float(ov[8 * q4 + 6]) * inv, __uint_as_float(ov[8 * q4 + 7]) * inv);
+        orow[c2 * 2 + q4] = v;
+      }
+    }
+  }
 }
 
 template <int D, bool BF16>
@@ -232,11 +174,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                     const __grid_constant__ CUtensorMap tmB, const PrefillArgs a) {
   using S = PPShape<D>;
   using L_ = PPSmem<D, BF16>;
-  using BS = PBias<BF16>;
+  using BS = PairBias<BF16>;
   using BT = typename BS::T;
   constexpr int NK = S::NK, NV = S::NV, NB = BS::NB;
-  constexpr uint32_t IDESC_S = umma_idesc_bf16(PP_ROWS, TILE_KEYS, false, false);
-  constexpr uint32_t IDESC_PV = umma_idesc_bf16(PP_ROWS, D, false, true);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -394,13 +334,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     auto issue_s = [&](int h, int kslot) -> bool {
       if (sn[h] > 0 && !pp_wait_warp(&s_empty[h], (uint32_t)(sn[h] - 1) & 1u, abort_flag, a)) return false;
       tc_fence_after();
-      const uint32_t kbase = smem_u32(smem + L_::kst + (size_t)kslot * S::KV_TILE);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t bd = umma_desc_sw128(kbase + (kk >> 2) * S::KV_SUB + (kk & 3) * 32, 16, 1024);
-        umma_ts_warp(tmem + S::TS + 64u * h, tmem + S::TQ + S::QC * h + kk * 8, bd, IDESC_S, kk > 0 ? 1u : 0u);
-      }
-      umma_commit_warp(&s_full[h]);
+      pair_issue_s<D>(tmem + S::TS + 64u * h, tmem + S::TQ + S::QC * h,
+                      umma_desc_sw128(smem_u32(smem + L_::kst + (size_t)kslot * S::KV_TILE), 16, 1024), &s_full[h]);
+      __syncwarp();
       ++sn[h];
       return true;
     };
@@ -458,14 +394,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           ++pc[h];
           if (!go) break;
           tc_fence_after();
-          const uint32_t pbase = smem_u32(smem + L_::pst + (size_t)h * S::P_BYTES);
-#pragma unroll
-          for (int ks = 0; ks < TILE_KEYS / 16; ++ks) {
-            const uint64_t adesc = umma_desc_sw128(pbase + ks * 32, 16, 1024);
-            const uint64_t bdesc = umma_desc_sw128(vbase + ks * 16 * 128, S::KV_SUB, 1024);
-            umma_ss_warp(tmem + S::TO + (uint32_t)(D * h), adesc, bdesc, IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
-          }
-          umma_commit_warp(&pv_done[h]);
+          pair_issue_pv<D>(tmem + S::TO + (uint32_t)(D * h),
+                           umma_desc_sw128(smem_u32(smem + L_::pst + (size_t)h * S::P_BYTES), 16, 1024),
+                           umma_desc_sw128(vbase, S::KV_SUB, 1024), j > 0 ? 1u : 0u, &pv_done[h]);
           if (h == it.nh - 1) umma_commit_warp(&v_empty[vs]);
           __syncwarp();
         }
@@ -546,22 +477,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       // ---- Q row into TMEM (rows past the item's last are zero); the previous item's S
       // products that read Q_h are complete (their s_full was seen), and its O_h has been read
       {
-        const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
-                                                           ((size_t)(it.t0 + (rv ? r : 0)) * a.Hq + h) * D);
-#pragma unroll
-        for (int half = 0; half < D / 64; ++half) {
-          uint32_t qv[32];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 x = rv ? __ldg(qsrc + half * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
-            qv[4 * c] = x.x;
-            qv[4 * c + 1] = x.y;
-            qv[4 * c + 2] = x.z;
-            qv[4 * c + 3] = x.w;
-          }
-          tmem_st32(tm_q + 32 * half, qv);
-        }
-        tmem_wait_st();
+        pair_load_q<D>(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                      ((size_t)(it.t0 + (rv ? r : 0)) * a.Hq + h) * D),
+                       rv, tm_q);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&q_ready[hs]);
@@ -694,16 +612,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             if (!go) break;
             tc_fence_after();
             const float f = mine ? fast_exp2((m - m_new) * LOG2E) : 1.f;
-#pragma unroll 1
-            for (int c2 = 0; c2 < D / 32; ++c2) {
-              uint32_t ov[32];
-              tmem_ld32(tm_o + c2 * 32, ov);
-              tmem_wait_ld();
-#pragma unroll
-              for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * f);
-              tmem_st32(tm_o + c2 * 32, ov);
-            }
-            tmem_wait_st();
+            pair_rescale_o<D>(tm_o, f);
             l *= f;
             if (mine) m = m_new;
           }
@@ -748,25 +657,8 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       ++ic;
       if (!go) break;
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* orow = reinterpret_cast<uint4*>(out + ((size_t)(it.t0 + r) * a.Hq + h) * D);
-#pragma unroll 1
-      for (int c2 = 0; c2 < D / 16; ++c2) {
-        uint32_t ov[16];
-        tmem_ld16(tm_o + c2 * 16, ov);
-        tmem_wait_ld();
-        if (rv) {
-#pragma unroll
-          for (int q4 = 0; q4 < 2; ++q4) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(ov[8 * q4 + 0]) * inv, __uint_as_float(ov[8 * q4 + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(ov[8 * q4 + 2]) * inv, __uint_as_float(ov[8 * q4 + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(ov[8 * q4 + 4]) * inv, __uint_as_float(ov[8 * q4 + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(ov[8 * q4 + 6]) * inv, __uint_as_float(ov[8 * q4 + 7]) * inv);
-            orow[c2 * 2 + q4] = v;
-          }
-        }
-      }
+      pair_store_o<D>(tm_o, l > 0.f ? 1.f / l : 0.f, reinterpret_cast<uint4*>(out + ((size_t)(it.t0 + r) * a.Hq + h) * D),
+                      rv);
       tc_fence_before();
     }
   }
