@@ -335,6 +335,7 @@ ink_status_t inkling_attn_decode(const ink_attn_params_t* params, const void* q,
   a.scale_log2 = params->sm_scale * 1.4426950408889634f;
   a.tiles_per_split = plan.tiles_per_split;
   a.num_splits = plan.num_splits;
+  a.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   if (ink::launch_decode(maps, a, params->head_dim, (cudaStream_t)stream) != cudaSuccess)
     return INK_ERR_CUDA;
   return INK_OK;
@@ -513,6 +514,7 @@ ink_status_t inkling_attn_kv_conv_write(const ink_attn_params_t* params, const v
   a.max_pages = params->max_pages_per_seq;
   a.num_pages = params->num_pages;
   a.nvec = nvec;
+  a.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   if (total_q == 0 && (params->num_seqs == 0 || !has_state)) return INK_OK;   // nothing to write
   int dev = 0;
   const int sms = ink::current_device_sms(&dev);

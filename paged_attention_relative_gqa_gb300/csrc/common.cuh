@@ -63,12 +63,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One probe that never suspends the thread.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The first probe of a wait limited to `limit_ns`: try_wait may suspend the thread for a
+// short time of the hardware's choosing, so a zero limit probes with test_wait instead
+// (only a phase already complete counts).
+__device__ __forceinline__ bool mbar_probe(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+  return limit_ns != 0 ? mbar_try_wait(bar, parity) : mbar_test_wait(bar, parity);
+}
+
 // Wait for phase `parity` of `bar` to complete; give up after `limit_ns` nanoseconds
 // (0: give up as soon as one probe finds the phase incomplete).  Returns false on timeout
 // (the caller records INK_DEVERR_WAIT_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+  if (limit_ns == 0) return mbar_test_wait(bar, parity);
   if (mbar_try_wait(bar, parity)) return true;
-  if (limit_ns == 0) return false;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1

@@ -147,9 +147,9 @@ __device__ __forceinline__ void named_barrier_consumers() {
 // Wait on an mbarrier phase unless the CTA has aborted; on timeout, record the error
 // and abort the CTA (every later wait returns at once).
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              uint32_t* err) {
+                                              uint32_t* err, unsigned long long limit_ns) {
   if (*abort_flag) return false;
-  if (mbar_wait_bounded(bar, parity)) return true;
+  if (mbar_wait_limit(bar, parity, limit_ns)) return true;
   record_error(err, INK_DEVERR_WAIT_TIMEOUT);
   *abort_flag = 1;
   return false;
@@ -259,13 +259,13 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmKs, const __grid_
       const int hkvp = a.Hkv << a.log2_page;
       constexpr uint32_t WHOLE_BYTES = 2u * TILE_KEYS * D * 2u;
       if (uc >= 2) {
-        if (lane == 0) go = wait_or_abort(&qempty[slot], (uint32_t)((uc >> 1) - 1) & 1u, abort_flag, a.err);
+        if (lane == 0) go = wait_or_abort(&qempty[slot], (uint32_t)((uc >> 1) - 1) & 1u, abort_flag, a.err, a.wait_ns);
         go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
       }
       for (int i = 0; i < cur.n_my && go; ++i, ++n) {
         const int st = n % NSTAGE;
         if (n >= NSTAGE) {
-          if (lane == 0) go = wait_or_abort(&empty[st], (uint32_t)((n / NSTAGE) - 1) & 1u, abort_flag, a.err);
+          if (lane == 0) go = wait_or_abort(&empty[st], (uint32_t)((n / NSTAGE) - 1) & 1u, abort_flag, a.err, a.wait_ns);
           go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
           if (!go) break;
         }
@@ -435,8 +435,8 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmKs, const __grid_
 
     for (int i = 0; i < cur.n_my; ++i, ++n) {
       const int st = n % NSTAGE;
-      const bool ok = wait_or_abort(&full[st], (uint32_t)(n / NSTAGE) & 1u, abort_flag, a.err) &&
-                      wait_or_abort(&bfull[n % BIAS_SLOTS], (uint32_t)(n / BIAS_SLOTS) & 1u, abort_flag, a.err);
+      const bool ok = wait_or_abort(&full[st], (uint32_t)(n / NSTAGE) & 1u, abort_flag, a.err, a.wait_ns) &&
+                      wait_or_abort(&bfull[n % BIAS_SLOTS], (uint32_t)(n / BIAS_SLOTS) & 1u, abort_flag, a.err, a.wait_ns);
       if (i == 0) {
         const uint32_t qbase = smem_u32(smem + L_::q + qslot * S::QSLOT_BYTES);
 #pragma unroll

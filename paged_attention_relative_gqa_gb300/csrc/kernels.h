@@ -29,6 +29,7 @@ struct DecodeArgs {
   int log2_page, max_pages, num_pages, E, W;
   float scale_log2;           // sm_scale * log2(e)
   int tiles_per_split, num_splits;
+  unsigned long long wait_ns; // limit of one pipeline wait (the drain waits keep 2 s)
 };
 
 struct PrefillArgs {
@@ -132,6 +133,7 @@ struct KvConvArgs {
   long long state_items;       // 2 * B * (ks-1) * nvec threads of state copy
   int tile_tokens;             // staged kernel: new rows per tile (<= 32)
   int stages;                  // staged kernel: ring depth (0: use the per-thread kernel)
+  unsigned long long wait_ns;  // limit of one pipeline wait (the drain waits keep 2 s)
 };
 
 // Largest dynamic shared memory of the staged K/V kernel.

@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(KVS_THREADS, 1) kv_conv_staged_kernel(const Kv
     int issued = 0;
     for (int u = blockIdx.x + ps * gridDim.x; u < units; u += NS * gridDim.x, k += NS) {
       const int s = ps;
-      if (k >= NS && !mbar_wait_bounded(&empty[s], ((k / NS) - 1) & 1)) {
+      if (k >= NS && !mbar_wait_limit(&empty[s], ((k / NS) - 1) & 1, a.wait_ns)) {
         if (lane == 0) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
         *reinterpret_cast<volatile int*>(abort_flag) = 1;
         break;
@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(KVS_THREADS, 1) kv_conv_staged_kernel(const Kv
   int k = 0;
   for (int u = blockIdx.x; u < units; u += gridDim.x, ++k) {
     const int s = k % NS;
-    const bool ok = mbar_wait_bounded(&full[s], (k / NS) & 1);
+    const bool ok = mbar_wait_limit(&full[s], (k / NS) & 1, a.wait_ns);
     if (!ok || *reinterpret_cast<volatile int*>(abort_flag)) {
       if (!ok) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
       break;

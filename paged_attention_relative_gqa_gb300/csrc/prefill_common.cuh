@@ -152,7 +152,7 @@ __device__ __noinline__ bool pp_wait_slow(uint64_t* bar, uint32_t parity, volati
 // Bounded wait with the call's limit; gives up at once when another warp has timed out.
 __device__ __forceinline__ bool pp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                        const PrefillArgs& a) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_probe(bar, parity, a.wait_ns)) return true;
   return pp_wait_slow(bar, parity, abort_flag, a.err, a.wait_ns);
 }
 

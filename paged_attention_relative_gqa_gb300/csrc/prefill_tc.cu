@@ -128,8 +128,8 @@ struct PtSmem {
   static constexpr size_t bars = lr_p + (BM == BM_LOWRANK ? (size_t)3 * LOWRANK_CHUNK * LOWRANK_MAX_D * 2 : 0);
   // q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2],
   // s_empty[2], o_done[2], o_free, b_full[NB], b_empty[NB], ml_full, ml_free,
-  // pt_full[3], r_full, bc_full, bc_empty
-  static constexpr int NBAR = 2 + 2 * S::NK + 2 * S::NV + 2 + 2 + 2 + 1 + 2 * BS::SLOTS + 2 + 6;
+  // pt_full[3], r_full, bc_full, bc_empty, drain[4] (one per MMA-issuing warp)
+  static constexpr int NBAR = 2 + 2 * S::NK + 2 * S::NV + 2 + 2 + 2 + 1 + 2 * BS::SLOTS + 2 + 6 + 4;
   static constexpr size_t vbad = bars + NBAR * 8;
   static constexpr size_t ml1 = vbad + S::NV * 8;          // float2 [128]
   static constexpr size_t misc = ml1 + PT_ROWS * 8;
@@ -260,10 +260,11 @@ __device__ __forceinline__ void lr_advance(const PrefillArgs& a, int total_items
 
 // A completed phase returns at once; otherwise give up at once if another warp of the
 // CTA has timed out, else wait (bounded) and on a timeout record it and tell the others.
-__device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __forceinline__ bool wait_flag(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err,
+                                          unsigned long long limit_ns) {
+  if (mbar_probe(bar, parity, limit_ns)) return true;
   if (*abort_flag) return false;
-  if (mbar_wait_bounded(bar, parity)) return true;
+  if (mbar_wait_limit(bar, parity, limit_ns)) return true;
   record_error(err, INK_DEVERR_WAIT_TIMEOUT);
   *abort_flag = 1;
   return false;
@@ -308,6 +309,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   uint64_t* r_full = pt_full + 3;
   uint64_t* bc_full = r_full + 1;
   uint64_t* bc_empty = bc_full + 1;
+  // every MMA a warp issued is complete before tensor memory is released: [0] the S issuer,
+  // [1] the low-rank bias product issuer, [2 + wg] the P V issuer of softmax warpgroup wg
+  uint64_t* drains = bc_empty + 1;
   float2* ml1 = reinterpret_cast<float2*>(smem + L_::ml1);
   uint64_t* vbad = reinterpret_cast<uint64_t*>(smem + L_::vbad);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L_::misc);
@@ -340,6 +344,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     mbar_init(r_full, 1);
     mbar_init(bc_full, 1);
     mbar_init(bc_empty, 4);
+    for (int x = 0; x < 4; ++x) mbar_init(&drains[x], 1);
     for (int x = 0; x < BS::SLOTS; ++x) {
       mbar_init(&b_full[x], BM == BM_LOWRANK ? 128 : (a.bias_bulk ? 1 : 32));
       mbar_init(&b_empty[x], 4);
@@ -374,28 +379,37 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       if (P >= TILE_KEYS) prefetch_tensormap(tm3);
       if (is_k) prefetch_tensormap(&tmQ3);
     }
-    int icount = 0, g = 0;
+    int icount = 0, g = 0, q_issued = 0;   // items, ring fills issued (g), Q tiles issued
     int chunk_b = -1, chunk_base = 0, chunk_val = -1;
     const int seg = P < TILE_KEYS ? P : TILE_KEYS;
     const int nseg = TILE_KEYS / seg;
-    for (int i = blockIdx.x; i < total_items && !*abort_flag; i += gridDim.x) {
+    bool go = true;
+    for (int i = blockIdx.x; i < total_items && go; i += gridDim.x) {
       PItem it;
       if (!get_item(a, i, it) || it.ntile == 0) continue;
-      if (is_k && lane == 0) {
-        bool ok = icount == 0 || wait_flag(q_empty, (uint32_t)(icount - 1) & 1u, abort_flag, a.err);
-        if (ok) {
-          mbar_arrive_expect_tx(q_full, (uint32_t)S::Q_BYTES);
-          tma_load_3d(smem + L_::q, &tmQ3, 0, it.t0, it.h * S::CB, q_full);   // 128 rows x all column blocks
+      if (is_k) {
+        bool ok = true;
+        if (lane == 0) {
+          ok = icount == 0 || wait_flag(q_empty, (uint32_t)(icount - 1) & 1u, abort_flag, a.err, a.wait_ns);
+          if (ok) {
+            mbar_arrive_expect_tx(q_full, (uint32_t)S::Q_BYTES);
+            tma_load_3d(smem + L_::q, &tmQ3, 0, it.t0, it.h * S::CB, q_full);   // 128 rows x all column blocks
+          }
         }
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+        ++q_issued;
       }
       const int32_t* bt = a.block_table + (size_t)it.b * a.max_pages;
       const int last_idx = it.k_hi >> a.log2_page;  // never read the table past here
       for (int j = 0; j < it.ntile; ++j, ++g) {
         const int st = g % NR;
         bool ok = true;
-        if (lane == 0 && g >= NR) ok = wait_flag(&empty[st], (uint32_t)((g / NR) - 1) & 1u, abort_flag, a.err);
+        if (lane == 0 && g >= NR) ok = wait_flag(&empty[st], (uint32_t)((g / NR) - 1) & 1u, abort_flag, a.err, a.wait_ns);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
+        if (!ok) {
+          go = false;
+          break;
+        }
         const int k0 = (it.kt0 + j) * TILE_KEYS;
         // lane sg < nseg takes segment sg of the tile: seg keys on one page
         const int pfirst = k0 >> a.log2_page, plast = (k0 + TILE_KEYS - 1) >> a.log2_page;
@@ -443,6 +457,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       }
       ++icount;
     }
+    // the copies issued last into each ring slot (and the last Q tile) may still be landing
+    // after an abort: wait for them (2 s each) so none is in flight when the CTA exits
+    if (lane == 0) {
+#pragma unroll 1
+      for (int n = max(0, g - NR); n < g; ++n)
+        if (!mbar_wait_bounded(&full[n % NR], (uint32_t)(n / NR) & 1u)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
+      if (q_issued > 0 && !mbar_wait_bounded(q_full, (uint32_t)(q_issued - 1) & 1u))
+        record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
+    }
   } else if (warp == 1) {
     if constexpr (BM == BM_LOWRANK) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(LR_REGS_PRODUCERS));
     // -------------------------------------------------------------- S issuer
@@ -451,15 +474,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     // warpgroup finds its next S computed when it finishes a P.  Q is freed after the
     // item's last S.
     int icount = 0, g = 0;
-    for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
+    bool go = true;
+    for (int i = blockIdx.x; i < total_items && go; i += gridDim.x) {
       PItem it;
       if (!get_item(a, i, it) || it.ntile == 0) continue;
-      (void)wait_flag(q_full, (uint32_t)icount & 1u, abort_flag, a.err);
+      go = __all_sync(0xffffffffu, wait_flag(q_full, (uint32_t)icount & 1u, abort_flag, a.err, a.wait_ns));
 #pragma unroll 1
-      for (int j = 0; j < it.ntile; ++j, ++g) {
+      for (int j = 0; j < it.ntile && go; ++j, ++g) {
         const int ks_ = g % NK;
-        (void)wait_flag(&k_full[ks_], (uint32_t)(g / NK) & 1u, abort_flag, a.err);
-        if (g >= 2) (void)wait_flag(&s_empty[g & 1], (uint32_t)((g >> 1) - 1) & 1u, abort_flag, a.err);
+        go = __all_sync(0xffffffffu, wait_flag(&k_full[ks_], (uint32_t)(g / NK) & 1u, abort_flag, a.err, a.wait_ns));
+        if (go && g >= 2)
+          go = __all_sync(0xffffffffu,
+                          wait_flag(&s_empty[g & 1], (uint32_t)((g >> 1) - 1) & 1u, abort_flag, a.err, a.wait_ns));
+        if (!go) break;   // after an abort no MMA is issued
         tc_fence_after();
         const uint32_t qbase = smem_u32(smem + L_::q);
         const uint32_t kbase = smem_u32(smem + L_::kst + (size_t)ks_ * S::KV_TILE);
@@ -476,6 +503,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       }
       ++icount;
     }
+    umma_commit_warp(&drains[0]);
+    __syncwarp();
+    if (!mbar_wait_bounded(&drains[0], 0)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
   } else if (warp == 2) {
     if constexpr (BM == BM_LOWRANK) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(LR_REGS_PRODUCERS));
     // -------------------------------------------------------------- bias loader
@@ -519,18 +549,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         bool ok = true;
         // the product of chunk n - 1 has been read out of TMEM: its MMA is complete, so
         // TMEM, the r rows and chunk slot (n - 1) % 3 are free
-        if (n >= 1) ok = wait_flag(bc_empty, (uint32_t)(n - 1) & 1u, abort_flag, a.err);
+        if (n >= 1) ok = wait_flag(bc_empty, (uint32_t)(n - 1) & 1u, abort_flag, a.err, a.wait_ns);
         if (ok && cur.first) {
           if (lane == 0) {
             mbar_arrive_expect_tx(r_full, (uint32_t)(PT_ROWS * LOWRANK_MAX_D * 2));
             tma_load_3d(smem + L_::lr_r, &tmR, 0, cur.it.h, cur.it.t0, r_full);
           }
           r_pending = true;
-          ok = wait_flag(r_full, (uint32_t)ritems & 1u, abort_flag, a.err);
+          ok = wait_flag(r_full, (uint32_t)ritems & 1u, abort_flag, a.err, a.wait_ns);
           ++ritems;
           r_pending = !ok;
         }
-        if (ok) ok = wait_flag(&pt_full[n % 3], (uint32_t)(n / 3) & 1u, abort_flag, a.err);
+        if (ok) ok = wait_flag(&pt_full[n % 3], (uint32_t)(n / 3) & 1u, abort_flag, a.err, a.wait_ns);
         if (!ok) break;
         tc_fence_after();
         const uint32_t rb = smem_u32(smem + L_::lr_r);
@@ -563,20 +593,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
           if (!mbar_wait_bounded(&pt_full[e % 3], (uint32_t)(e / 3) & 1u)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
         if (r_pending && !mbar_wait_bounded(r_full, (uint32_t)(ritems - 1) & 1u)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
       }
+      umma_commit_warp(&drains[1]);
+      __syncwarp();
+      if (!mbar_wait_bounded(&drains[1], 0)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
     } else {
     int bcnt[2] = {0, 0};   // bias tiles loaded per warpgroup
     int g = 0;
-    for (int i = blockIdx.x; i < total_items; i += gridDim.x) {
+    bool go = true;
+    for (int i = blockIdx.x; i < total_items && go; i += gridDim.x) {
       PItem it;
       if (!get_item(a, i, it) || it.ntile == 0) continue;
       for (int j = 0; j < it.ntile; ++j, ++g) {
         const int k0 = (it.kt0 + j) * TILE_KEYS;
         if (!tile_needs_bias(it.pos0, k0, a.E)) continue;
-        const int u = bcnt[g & 1]++;
+        const int u = bcnt[g & 1];
         const int slot = (g & 1) * BS::PER_WG + u % BS::PER_WG, use = u / BS::PER_WG;
         BT* sb = reinterpret_cast<BT*>(smem + L_::bias + (size_t)slot * BS::SLOT_BYTES);
         const int dmin0 = it.pos0 - (k0 + TILE_KEYS - 1);
-        if (use >= 1) (void)wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err);
+        if (use >= 1 &&
+            !__all_sync(0xffffffffu, wait_flag(&b_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, a.err, a.wait_ns))) {
+          go = false;
+          break;
+        }
+        ++bcnt[g & 1];
         if (a.bias_bulk) {
           // lane gr < NGROUP decides whether group gr of this tile is read; the warp loads those
           const uint32_t nm =
@@ -612,6 +651,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
+    // TMA path: the last fill of each slot may still be landing after an abort
+    if (a.bias_bulk && lane == 0) {
+#pragma unroll 1
+      for (int w = 0; w < 2; ++w)
+#pragma unroll 1
+        for (int u = max(0, bcnt[w] - BS::PER_WG); u < bcnt[w]; ++u)
+          if (!mbar_wait_bounded(&b_full[w * BS::PER_WG + u % BS::PER_WG], (uint32_t)(u / BS::PER_WG) & 1u))
+            record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
+    }
     }
   } else if (warp >= 12) {
     if constexpr (BM == BM_LOWRANK) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(LR_REGS_BIAS));
@@ -635,7 +683,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
           const int nch = j == jb ? 3 : 1;
 #pragma unroll 1
           for (int m = 0; m < nch; ++m) {
-            const bool ok = wait_flag(bc_full, (uint32_t)n & 1u, abort_flag, a.err);
+            const bool ok = wait_flag(bc_full, (uint32_t)n & 1u, abort_flag, a.err, a.wait_ns);
             ++n;
             tc_fence_after();
             uint32_t h[32];   // this row's 64 buckets of the chunk, fp16 pairs
@@ -662,7 +710,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
               if (off >= 3 * LOWRANK_CHUNK || j + k >= it.ntile) break;
               const int tt = t + k, sl = tt & 3;
               if (tt > waited) {
-                if (tt >= 4) (void)wait_flag(&b_empty[sl], (uint32_t)((tt >> 2) - 1) & 1u, abort_flag, a.err);
+                if (tt >= 4) (void)wait_flag(&b_empty[sl], (uint32_t)((tt >> 2) - 1) & 1u, abort_flag, a.err, a.wait_ns);
                 waited = tt;
               }
               __half* dst = reinterpret_cast<__half*>(smem + L_::bias + (size_t)sl * BS::SLOT_BYTES) +
@@ -780,7 +828,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         const uint32_t bpar = BM == BM_LOWRANK ? (uint32_t)(my_bt >> 2) & 1u : (uint32_t)(buse / BS::PER_WG) & 1u;
         const BT* bslot = reinterpret_cast<const BT*>(smem + L_::bias + (size_t)bslot_i * BS::SLOT_BYTES);
         uint64_t bad = item_bad ? tile_bad(k0) : 0ull;
-        bool ok = wait_flag(&s_full[g & 1], (uint32_t)(g >> 1) & 1u, abort_flag, a.err);
+        bool ok = wait_flag(&s_full[g & 1], (uint32_t)(g >> 1) & 1u, abort_flag, a.err, a.wait_ns);
         tc_fence_after();
         uint32_t sr[64];
         {
@@ -807,7 +855,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         // slot when the tile reads no bucket from it
         const BT* brow = bslot + (TILE_KEYS - 1);
         if (needs) {
-          (void)wait_flag(&b_full[bslot_i], bpar, abort_flag, a.err);
+          (void)wait_flag(&b_full[bslot_i], bpar, abort_flag, a.err, a.wait_ns);
           const int gr = r / BIAS_BOX_ROWS;
           brow = bslot + gr * BS::GROUP + (r % BIAS_BOX_ROWS) * BS::COLS + (dmin - bias_group_x<BS::ALIGN>(dmin - r, gr)) +
                  (TILE_KEYS - 1);
@@ -854,7 +902,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
           const bool mine = m_new > m + RESCALE_NAT;
           if (__any_sync(0xffffffffu, mine)) {
             // this warpgroup's O must be stable: its previous P V product (tile g - 2) is done
-            (void)wait_flag(&o_done[g & 1], (uint32_t)((g - 2) >> 1) & 1u, abort_flag, a.err);
+            (void)wait_flag(&o_done[g & 1], (uint32_t)((g - 2) >> 1) & 1u, abort_flag, a.err, a.wait_ns);
             tc_fence_after();
             const float f = mine ? fast_exp2((m - m_new) * LOG2E) : 1.f;
 #pragma unroll 1
@@ -884,7 +932,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
         l += (lsv[0] + lsv[1]) + (lsv[2] + lsv[3]);
         // P buffer g & 1 was last read by the P V product of tile g - 2
-        if (g >= 2) (void)wait_flag(&o_done[g & 1], (uint32_t)((g - 2) >> 1) & 1u, abort_flag, a.err);
+        if (g >= 2) (void)wait_flag(&o_done[g & 1], (uint32_t)((g - 2) >> 1) & 1u, abort_flag, a.err, a.wait_ns);
         tmem_st32(tlane + TM_P + (g & 1) * 32, pk);
         tmem_wait_st();
         tc_fence_before();
@@ -892,10 +940,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         if (sw == 0) {
           // O[wg] += P(g) V(g), issued by this warpgroup's first warp
           const int vs = g % NV;   // NV is even: this warpgroup's own V slots
-          bool pv_ok = wait_flag(&v_full[vs], (uint32_t)(g / NV) & 1u, abort_flag, a.err);
+          bool pv_ok = wait_flag(&v_full[vs], (uint32_t)(g / NV) & 1u, abort_flag, a.err, a.wait_ns);
           // warpgroup 1's first product of an item overwrites O[1], which the previous
           // item's epilogue (warpgroup 0) reads: wait until it has
-          if (fresh && wg == 1 && icount > 0) pv_ok = wait_flag(o_free, (uint32_t)(icount - 1) & 1u, abort_flag, a.err) && pv_ok;
+          if (fresh && wg == 1 && icount > 0) pv_ok = wait_flag(o_free, (uint32_t)(icount - 1) & 1u, abort_flag, a.err, a.wait_ns) && pv_ok;
           // zero the V rows of keys that no row of this item may read
           const uint64_t vb = pv_ok ? vbad[vs] : ~0ull;
           uint8_t* vt = smem + L_::vst + (size_t)vs * S::KV_TILE;
@@ -935,7 +983,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       // ---- item epilogue
       const int g_last = g - 1;
       if (wg == 1) {
-        if (icount > 0) (void)wait_flag(ml_free, (uint32_t)(icount - 1) & 1u, abort_flag, a.err);
+        if (icount > 0) (void)wait_flag(ml_free, (uint32_t)(icount - 1) & 1u, abort_flag, a.err, a.wait_ns);
         ml1[r] = make_float2(m, l);
         __syncwarp();
         if (lane == 0) mbar_arrive(ml_full);
@@ -944,11 +992,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         // product two tiles back, so o_done[1] is at most one phase short of the count
         // awaited below.  Waiting on o_done[1] earlier could see a phase two behind,
         // whose parity matches, and read O_1 before its last product lands.
-        (void)wait_flag(ml_full, (uint32_t)icount & 1u, abort_flag, a.err);
+        (void)wait_flag(ml_full, (uint32_t)icount & 1u, abort_flag, a.err, a.wait_ns);
         // both warpgroups' last P V products of the item are done
-        (void)wait_flag(&o_done[g_last & 1], (uint32_t)(g_last >> 1) & 1u, abort_flag, a.err);
+        (void)wait_flag(&o_done[g_last & 1], (uint32_t)(g_last >> 1) & 1u, abort_flag, a.err, a.wait_ns);
         if (g_last > g0)
-          (void)wait_flag(&o_done[(g_last - 1) & 1], (uint32_t)((g_last - 1) >> 1) & 1u, abort_flag, a.err);
+          (void)wait_flag(&o_done[(g_last - 1) & 1], (uint32_t)((g_last - 1) >> 1) & 1u, abort_flag, a.err, a.wait_ns);
         tc_fence_after();
         const float2 o1 = ml1[r];
         __syncwarp();
@@ -963,13 +1011,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         const float c0 = f0 * inv, c1 = f1 * inv;
         uint4* orow = reinterpret_cast<uint4*>(out + ((size_t)(it.t0 + r) * a.Hq + it.h) * D);
         const uint32_t t_o0 = tlane + TM_O, t_o1 = tlane + TM_O + D;
+        const bool store = rv && !*abort_flag;   // after an abort the rows are left untouched
 #pragma unroll 1
         for (int cc = 0; cc < D / 16; ++cc) {
           uint32_t ov[16], ow[16];
           tmem_ld16(t_o0 + cc * 16, ov);
           tmem_ld16(t_o1 + cc * 16, ow);
           tmem_wait_ld();
-          if (rv) {
+          if (store) {
 #pragma unroll
             for (int q4 = 0; q4 < 2; ++q4) {
               float y[8];
@@ -993,6 +1042,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         if (lane == 0) mbar_arrive(o_free);
       }
       ++icount;
+    }
+    if (sw == 0) {   // this warpgroup's P V products are complete before tensor memory is released
+      umma_commit_warp(&drains[2 + wg]);
+      __syncwarp();
+      if (!mbar_wait_bounded(&drains[2 + wg], 0)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
     }
   }
 
