@@ -30,9 +30,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from paged_attention_relative_gqa_gb300 import workloads as W  # noqa: E402
+from paged_attention_relative_gqa_gb300 import overlap  # noqa: E402
 
 METRIC = "decode attn HBM GB/s (% of 8 TB/s); prefill attn TFLOP/s (% bf16 peak); tok/s"
 HEADLINE = "swa_decode"
+DATA = "synthetic (seeded; Q/K/V ~N(0,1) bf16, bias ~N(0,0.5) fp32)"
 
 
 # ---------------------------------------------------------------- algorithmic work
@@ -319,10 +321,11 @@ WORKLOAD_DESC = {
              "and one decode call (128 requests, contexts log-uniform 512..16384)",
     "mixed_kv_graph": "mixed serving step with each layer's K/V write, replayed from one CUDA graph (24 calls): "
                       "5 SWA + 1 global layer, each: K/V short convolution (ks 4) + paged write of the prefill "
-                      "rows (8 x 2048) and of the decode rows (128), then the prefill call and the decode call",
+                      "rows (8 x 2048) and of the decode rows (128), then the prefill call and the decode call; "
+                      "per layer the prefill side and the decode side on two streams (fork/join)",
     "mixed_graph": "mixed serving step replayed from one CUDA graph (its 12 calls captured once): 5 SWA + "
                    "1 global layer, each one prefill call (8 x 2048 tokens) and one decode call (128 "
-                   "requests, contexts log-uniform 512..16384)",
+                   "requests, contexts log-uniform 512..16384), the two on two streams (fork/join per layer)",
 }
 
 
@@ -389,35 +392,40 @@ def measure(binding, name, dev, steps, warmup, stream, hbm_peak, bf16_peak):
         return measure_kv(binding, name, dev, steps, warmup, stream, hbm_peak)
     if name in ("mixed", "mixed_graph", "mixed_kv_graph"):
         layers = [W.mixed_layer(k, i, dev) for i, k in enumerate(W.MIXED_STACK)]
-        calls, keep = [], []
+        lay, keep = [], []   # per layer: (prefill-side calls, decode-side calls)
         for li, (pre, dec) in enumerate(layers):
-            if name == "mixed_kv_graph":
-                # the layer's K/V write comes first: prefill rows, then decode rows
-                for j, prob in enumerate((pre, dec)):
+            sides = []
+            for j, prob in enumerate((pre, dec)):
+                side = []
+                if name == "mixed_kv_graph":
+                    # the rows' K/V write comes before the attention that reads them
                     fn, ws = kv_call(binding, W.kv_step_for(prob, W.KV_CONV_KERNEL, seed=7000 + 10 * li + j), dev)
                     keep.append((ws, None))
-                    calls.append(fn)
-            for prob in (pre, dec):
+                    side.append(fn)
                 params = binding.params_of(prob)
                 ws = binding.alloc_workspace(params, True, dev)
                 out = torch.empty_like(prob.q)
                 keep.append((ws, out))
-                calls.append(make_call(binding, prob, out, ws))
-
-        def mixed_step():
-            for c in calls:
-                c()
+                side.append(make_call(binding, prob, out, ws))
+                sides.append(side)
+            lay.append((sides[0], sides[1]))
+        calls = overlap.serial(lay)
 
         if name in ("mixed_graph", "mixed_kv_graph"):
+            # each layer's prefill on the capturing stream, its decode on a side stream
+            two = overlap.LayerStreams(dev)
             with torch.cuda.stream(stream):
-                mixed_step()               # eager once: one-time per-device setup
+                two.run(lay)               # eager once: one-time per-device setup
             torch.cuda.synchronize()
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
-                mixed_step()
+                two.run(lay)
             m = time_steps([graph.replay], steps, warmup, stream)
             del graph
         else:
+            def mixed_step():
+                for c in calls:
+                    c()
             m = time_steps([mixed_step], steps, warmup, stream)
         per_call = [round(time_steps([c], 3, 1, stream), 4) for c in calls]
         for ws, _ in keep:
@@ -489,10 +497,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 2), "unit": r["unit"], "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded; Q/K/V ~N(0,1) bf16, bias ~N(0,0.5) fp32)",
-        "config": {"workload": WORKLOAD_DESC[name],
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (decode: two alternating 0.3-2.7 GB instances)"},
+        "data": DATA,
+        "config": config_of(name, world),
         "tok_s": round(r["tok_s"] * scale * world, 1),
         "gpu_launches": args.steps * r["launches_per_step"],
         "clocks": clk,
@@ -637,6 +643,13 @@ def e2e_kv(binding, step, steps, warmup, stream):
     return ms, h2d, d2h
 
 
+def config_of(name, world):
+    """The `config` object of a line; both arms print the same one for the same workload."""
+    return {"workload": WORKLOAD_DESC[name],
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (decode: two alternating 0.3-2.7 GB instances)"}
+
+
 # ---------------------------------------------------------------- reference arm (the oracle)
 
 def run_reference(args, rank, world):
@@ -668,10 +681,8 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)",
-        "config": {"workload": "swa_decode: batch 64, 64 q heads / 16 kv heads, head_dim 128, "
-                               "window 512, contexts U{1024..8192}, page 64, bias [64,64,512] fp32",
-                   "global_batch": B, "seq_len": "1024-8192 (context)", "parallelism": "host cores"},
+        "data": DATA,
+        "config": config_of(HEADLINE, world),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"{rows_per_step} of {total_rows} (sequence, head) rows per step "
                                    "(the whole workload)"},

@@ -121,3 +121,44 @@ def test_layer_step_with_kv_write_replays_and_matches_the_oracle():
     assert binding.inkling_attn_read_device_error(ws_kv) == 0
     assert binding.inkling_attn_read_device_error(ws) == 0
     sampled_check(pre, out, 9, "layer step with K/V write (sampled rows)")
+
+
+def test_two_stream_layers_replay_bitwise_from_a_cuda_graph():
+    """Per layer, the prefill on the capturing stream and the decode on a side stream (fork and
+    join per layer): the graph's replays give the bits of the serial eager calls."""
+    from paged_attention_relative_gqa_gb300 import overlap
+    layers, outs, keep = [], [], []
+    for i, kind in enumerate(["swa", "global"]):
+        pre, dec = W.mixed_layer(kind, i, DEV, n_prefill=2, n_decode=32)
+        sides = []
+        for prob in (pre, dec):
+            out = torch.empty_like(prob.q)
+            ws = binding.alloc_workspace(binding.params_of(prob), True, torch.device(DEV))
+            outs.append(out)
+            keep.append((prob, ws))
+            sides.append([_calls(prob, out, ws)])
+        layers.append((sides[0], sides[1]))
+    for c in overlap.serial(layers):
+        c()
+    torch.cuda.synchronize()
+    eager = [o.clone() for o in outs]
+    two = overlap.LayerStreams(torch.device(DEV))
+    capture = torch.cuda.Stream()
+    with torch.cuda.stream(capture):
+        two.run(layers)                  # eager on two streams once
+    torch.cuda.synchronize()
+    assert all(torch.equal(o, e) for o, e in zip(outs, eager))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=capture):
+        two.run(layers)
+    for _ in range(3):
+        for o in outs:
+            o.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        for o, e in zip(outs, eager):
+            assert torch.equal(o, e)
+    for _, ws in keep:
+        assert binding.inkling_attn_read_device_error(ws) == 0
+    del graph, layers, outs, eager, keep
+    torch.cuda.empty_cache()
