@@ -17,23 +17,25 @@
 //
 // Tensor memory (512 columns): Q of head 0 and 1 (the A operand of S = Q K^T, D/2 columns
 // each), S of head 0 and 1 (64 fp32 columns each), O of head 0 and 1 (D fp32 columns each).
-// P (softmax numerators, bf16) goes to shared memory, one 16 KB tile per head, so the next S
-// of a head can be computed while its softmax still works on the current one.
+// P (softmax numerators, bf16 pairs) overwrites the first 32 columns of its head's S and is
+// the A operand of O += P V, so neither P nor its product touches shared memory.  The next S
+// of a head is computed once that product has read P; meanwhile the tensor cores work on the
+// other head, whose softmax runs half a tile out of step.
 //
 // Warp roles (384 threads):
 //   warp 0   K and V producer: one TMA box per 64-key tile (or one per page segment when
 //            pages are shorter than a tile), block-table entries held 32 at a time in lanes.
-//   warp 1   MMA issuer: S_h(j+1) = Q_h K(j+1)^T (M 128, N 64, A from TMEM) as soon as the
-//            softmax of head h has read S_h(j) out of TMEM, then O_h += P_h(j) V(j) (A = P from
-//            shared memory) once P_h(j) is written.  Before the P V products of a tile it zeroes
-//            the V rows of keys that no row of the item may see (window edges, sequence end,
-//            unreadable pages).
-//   warps 2, 3  bias producers of head 0 and head 1: per tile that reads any bucket below
-//            E - 1, up to four 3-D TMA boxes (32 tokens x COLS buckets) into the head's ring.
+//   warps 1, 3  MMA issuers of head 0 and head 1, per tile: O_h += P_h(j) V(j) (M 128, N D,
+//            A = P from TMEM) once the softmax has written P_h(j), then S_h(j+1) = Q_h K(j+1)^T
+//            (M 128, N 64, A = Q from TMEM) once that product is complete.  Before its P V
+//            product each zeroes the V rows of keys that no row of the item may see (window
+//            edges, sequence end, unreadable pages).
+//   warp 2   bias producer: per tile that reads any bucket below E - 1 and per head, up to four
+//            3-D TMA boxes (32 tokens x COLS buckets) into the head's ring.
 //   warps 4-7, 8-11  softmax of head 0 and head 1: thread r owns row r (TMEM lane r).  Per
 //            item it loads its Q row into TMEM; per tile it reads its 64 scores, adds the bias,
 //            masks, keeps the running max and sum (O rescaled in TMEM only when the max grows
-//            by more than 2^8), writes P; at the end it normalises O and stores bf16.  Pairs of
+//            by more than 2^8), writes P into TMEM; at the end it normalises O and stores bf16.  Pairs of
 //            scores go through packed two-lane fp32 FMA and add (the same rounding as scalar
 //            FMA and add), maxima through three-input max.
 // Every wait is bounded; after a timeout the CTA records INK_DEVERR_WAIT_TIMEOUT, stops
@@ -60,10 +62,9 @@ struct PPShape {
   static constexpr int KV_TILE = CB * KV_SUB;
   static constexpr int NK = D == 128 ? 2 : 4;   // K ring (freed when both S products are done)
   static constexpr int NV = D == 128 ? 2 : 4;   // V ring (freed when both P V products are done)
-  static constexpr int P_BYTES = PP_ROWS * TILE_KEYS * 2;   // one head's P tile (bf16, 128-byte swizzle)
   static constexpr uint32_t QC = D / 2;          // TMEM columns of one Q tile (bf16 pairs)
   static constexpr uint32_t TQ = 0;              // Q_h at TQ + h QC
-  static constexpr uint32_t TS = 2 * QC;         // S_h at TS + 64 h
+  static constexpr uint32_t TS = 2 * QC;         // S_h at TS + 64 h; P_h in its first 32 columns
   static constexpr uint32_t TO = 2 * QC + 128;   // O_h at TO + D h
   static_assert(TO + 2 * D <= 512, "tensor memory budget");
 };
@@ -74,12 +75,11 @@ struct PPSmem {
   using B = PairBias<BF16>;
   static constexpr size_t kst = 0;
   static constexpr size_t vst = kst + (size_t)S::NK * S::KV_TILE;
-  static constexpr size_t pst = vst + (size_t)S::NV * S::KV_TILE;
-  static constexpr size_t bias = pst + (size_t)2 * S::P_BYTES;
+  static constexpr size_t bias = vst + (size_t)S::NV * S::KV_TILE;
   static constexpr size_t bars = bias + (size_t)2 * B::NB * B::SLOT_BYTES;
-  // k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], q_ready[2], s_full[2], s_empty[2],
-  // p_full[2], pv_done[2], b_full[2 NB], b_empty[2 NB], drain
-  static constexpr int NBAR = 2 * S::NK + 2 * S::NV + 10 + 4 * B::NB + 1;
+  // k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], q_ready[2], s_full[2], p_full[2],
+  // pv_done[2], b_full[2 NB], b_empty[2 NB], drain[2]
+  static constexpr int NBAR = 2 * S::NK + 2 * S::NV + 8 + 4 * B::NB + 2;
   static constexpr size_t vbad = bars + NBAR * 8;
   static constexpr size_t misc = vbad + S::NV * 8;
   static constexpr size_t total = misc + 32;
@@ -99,15 +99,14 @@ __device__ __forceinline__ void pair_issue_s(uint32_t d, uint32_t a0, uint64_t b
   umma_commit_warp(done);
 }
 
-// O_h += P_h V of one 64-key tile (A = P from shared memory, B = the V tile, MN-major), four
-// K-steps of 16 keys; the first product of an item overwrites O_h.
+// O_h += P_h V of one 64-key tile (A = P from TMEM, 8 columns of bf16 pairs per 16 keys; B = the
+// V tile, MN-major), four K-steps of 16 keys; the first product of an item overwrites O_h.
 template <int D>
-__device__ __forceinline__ void pair_issue_pv(uint32_t d, uint64_t a0, uint64_t b0, uint32_t acc0, uint64_t* done) {
+__device__ __forceinline__ void pair_issue_pv(uint32_t d, uint32_t a0, uint64_t b0, uint32_t acc0, uint64_t* done) {
   constexpr uint32_t IDESC_PV = umma_idesc_bf16(PP_ROWS, D, false, true);
 #pragma unroll
   for (int ks = 0; ks < TILE_KEYS / 16; ++ks)
-    umma_ss_warp(d, a0 + (uint64_t)((ks * 32) >> 4), b0 + (uint64_t)((ks * 16 * 128) >> 4), IDESC_PV,
-                 (acc0 || ks > 0) ? 1u : 0u);
+    umma_ts_warp(d, a0 + ks * 8, b0 + (uint64_t)((ks * 16 * 128) >> 4), IDESC_PV, (acc0 || ks > 0) ? 1u : 0u);
   umma_commit_warp(done);
 }
 
@@ -167,6 +166,29 @@ __device__ __forceinline__ void pair_store_o(uint32_t tm_o, float inv, uint4* or
   }
 }
 
+// One row's bias in a ring slot, read as pairs (b[c], b[c + 1]) for even c; key c's bucket is
+// element 63 - c counted from `k63`.
+template <bool BF16>
+struct BiasRow {   // fp32: one 32-bit load per key (the 32 rows of a warp hit 32 banks)
+  const float* k63;
+  __device__ __forceinline__ void at(const float* p) { k63 = p; }
+  __device__ __forceinline__ uint64_t pair(int c) const { return f2_pack(k63[63 - c], k63[62 - c]); }
+};
+template <>
+struct BiasRow<true> {   // bf16: 33 aligned 32-bit loads per row, each pair funnel-shifted into place
+  const uint32_t* w;     // the word holding element 0
+  uint32_t sh;           // 16 when element 0 is the high half of its word
+  __device__ __forceinline__ void at(const __nv_bfloat16* p) {
+    w = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(p) & ~uintptr_t(3));
+    sh = (uint32_t)(reinterpret_cast<uintptr_t>(p) & 2u) << 3;
+  }
+  __device__ __forceinline__ uint64_t pair(int c) const {
+    const int q = 31 - (c >> 1);   // elements 2q, 2q + 1: keys c + 1, c
+    const uint32_t v = __funnelshift_r(w[q], w[q + 1], sh);
+    return f2_pack(__uint_as_float(v & 0xffff0000u), __uint_as_float(v << 16));
+  }
+};
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(PP_THREADS, 1)
 prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -187,13 +209,12 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   uint64_t* v_full = k_empty + NK;
   uint64_t* v_empty = v_full + NV;
   uint64_t* q_ready = v_empty + NV;   // [2] Q of the item in TMEM, O of the previous item read
-  uint64_t* s_full = q_ready + 2;     // [2] S_h in TMEM
-  uint64_t* s_empty = s_full + 2;     // [2] S_h read out by the softmax
-  uint64_t* p_full = s_empty + 2;     // [2] P_h in shared memory
-  uint64_t* pv_done = p_full + 2;     // [2] O_h += P_h V done (P_h may be rewritten; O_h stable)
+  uint64_t* s_full = q_ready + 2;     // [2] S_h in TMEM (and every earlier product of the MMA warp done)
+  uint64_t* p_full = s_full + 2;      // [2] P_h in TMEM
+  uint64_t* pv_done = p_full + 2;     // [2] O_h += P_h V done (S_h may be rewritten; O_h stable)
   uint64_t* b_full = pv_done + 2;     // [2 NB] head h's slot s at h NB + s
   uint64_t* b_empty = b_full + 2 * NB;
-  uint64_t* drain = b_empty + 2 * NB;
+  uint64_t* drain = b_empty + 2 * NB;   // [2] one per MMA-issuing warp
   uint64_t* vbad = reinterpret_cast<uint64_t*>(smem + L_::vbad);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L_::misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L_::misc + 4);
@@ -205,16 +226,15 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   if (tid == 0) {
     for (int x = 0; x < NK; ++x) {
       mbar_init(&k_full[x], 1);
-      mbar_init(&k_empty[x], 1);
+      mbar_init(&k_empty[x], 2);   // one tcgen05.commit from each MMA warp
     }
     for (int x = 0; x < NV; ++x) {
       mbar_init(&v_full[x], 1);
-      mbar_init(&v_empty[x], 1);
+      mbar_init(&v_empty[x], 2);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&q_ready[x], 4);
       mbar_init(&s_full[x], 1);
-      mbar_init(&s_empty[x], 4);
       mbar_init(&p_full[x], 4);
       mbar_init(&pv_done[x], 1);
     }
@@ -222,7 +242,8 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       mbar_init(&b_full[x], 1);
       mbar_init(&b_empty[x], 4);
     }
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     fence_mbar_init();
     *abort_flag = 0;
   }
@@ -321,34 +342,38 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       pp_drain_ring(k_full, NK, gk, a.err);
       pp_drain_ring(v_full, NV, gv, a.err);
     }
-  } else if (warp == 1) {
-    // -------------------------------------------------------------- MMA issuer
-    // Per head h a count n_h of S tiles issued: S_h(n) goes into the head's one S buffer after
-    // the softmax has read S_h(n - 1) (s_empty phase n - 1), so every phase of s_empty, p_full
-    // and q_ready is waited for in order.
+  } else if (warp == 1 || warp == 3) {
+    // -------------------------------------------------------------- MMA issuers
+    // Warp 1 issues head 0's products, warp 3 head 1's, so that neither head waits behind the
+    // other's barriers.  Per tile: O_h += P_h(j) V(j) once the softmax has written P_h(j)
+    // (p_full), then S_h(j+1) into the same TMEM columns once that product has read P_h(j)
+    // (pv_done).  K and V slots are released by one commit from each warp (a warp whose head is
+    // absent from an item commits without products).  Every phase of the barriers a warp waits
+    // on is waited for in order.
+    const int h = warp == 1 ? 0 : 1;
     int g = 0;                     // tiles walked
-    int qc[2] = {0, 0};            // items per head
-    int sn[2] = {0, 0};            // S tiles issued per head
-    int pc[2] = {0, 0};            // P tiles consumed per head
+    int qc = 0;                    // items of head h
+    int pc = 0;                    // P V products issued for head h
     bool go = true;
-    auto issue_s = [&](int h, int kslot) -> bool {
-      if (sn[h] > 0 && !pp_wait_warp(&s_empty[h], (uint32_t)(sn[h] - 1) & 1u, abort_flag, a)) return false;
+    // S_h of K slot kslot, after the last P V product of head h has read P_h
+    auto issue_s = [&](int kslot) -> bool {
+      if (pc > 0 && !pp_wait_warp(&pv_done[h], (uint32_t)(pc - 1) & 1u, abort_flag, a)) return false;
       tc_fence_after();
       pair_issue_s<D>(tmem + S::TS + 64u * h, tmem + S::TQ + S::QC * h,
                       umma_desc_sw128(smem_u32(smem + L_::kst + (size_t)kslot * S::KV_TILE), 16, 1024), &s_full[h]);
       __syncwarp();
-      ++sn[h];
       return true;
     };
     for (int i = blockIdx.x; i < total_items && go; i += gridDim.x) {
       PPItem it;
       if (!pp_item(a, i, it) || it.ntile == 0) continue;
-      // S of tile 0 for each head once its Q is in TMEM
+      const bool mine = h < it.nh;
+      // S of tile 0 once Q_h is in TMEM
       go = pp_wait_warp(&k_full[g % NK], (uint32_t)(g / NK) & 1u, abort_flag, a);
-      for (int h = 0; h < it.nh && go; ++h) {
-        go = pp_wait_warp(&q_ready[h], (uint32_t)qc[h] & 1u, abort_flag, a);
-        ++qc[h];
-        if (go) go = issue_s(h, g % NK);
+      if (go && mine) {
+        go = pp_wait_warp(&q_ready[h], (uint32_t)qc & 1u, abort_flag, a);
+        ++qc;
+        if (go) go = issue_s(g % NK);
       }
       if (!go) break;
       umma_commit_warp(&k_empty[g % NK]);
@@ -356,19 +381,12 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       for (int j = 0; j < it.ntile && go; ++j) {
         const int gj = g + j;
         const int k0 = (it.kt0 + j) * TILE_KEYS;
-        // S of the next tile for each head, as soon as its softmax has read this tile's S
-        if (j + 1 < it.ntile) {
-          go = pp_wait_warp(&k_full[(gj + 1) % NK], (uint32_t)((gj + 1) / NK) & 1u, abort_flag, a);
-          for (int h = 0; h < it.nh && go; ++h) go = issue_s(h, (gj + 1) % NK);
-          if (!go) break;
-          umma_commit_warp(&k_empty[(gj + 1) % NK]);
-        }
-        // O_h += P_h V for this tile once P_h is in shared memory
         const int vs = gj % NV;
         go = pp_wait_warp(&v_full[vs], (uint32_t)(gj / NV) & 1u, abort_flag, a);
         if (!go) break;
-        {
-          // zero the V rows of keys that no row of the item may read
+        if (mine) {
+          // zero the V rows of keys that no row of the item may read (both warps write the same
+          // zeros to the same rows, each before its own product)
           const uint64_t vb = vbad[vs];
           if (k0 < it.lo_min || k0 + TILE_KEYS - 1 > it.k_hi || vb) {
             uint8_t* vt = smem + L_::vst + (size_t)vs * S::KV_TILE;
@@ -387,61 +405,69 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
           }
-        }
-        const uint32_t vbase = smem_u32(smem + L_::vst + (size_t)vs * S::KV_TILE);
-        for (int h = 0; h < it.nh && go; ++h) {
-          go = pp_wait_warp(&p_full[h], (uint32_t)pc[h] & 1u, abort_flag, a);
-          ++pc[h];
+          go = pp_wait_warp(&p_full[h], (uint32_t)pc & 1u, abort_flag, a);
           if (!go) break;
           tc_fence_after();
-          pair_issue_pv<D>(tmem + S::TO + (uint32_t)(D * h),
-                           umma_desc_sw128(smem_u32(smem + L_::pst + (size_t)h * S::P_BYTES), 16, 1024),
-                           umma_desc_sw128(vbase, S::KV_SUB, 1024), j > 0 ? 1u : 0u, &pv_done[h]);
-          if (h == it.nh - 1) umma_commit_warp(&v_empty[vs]);
+          pair_issue_pv<D>(tmem + S::TO + (uint32_t)(D * h), tmem + S::TS + 64u * h,
+                           umma_desc_sw128(smem_u32(smem + L_::vst + (size_t)vs * S::KV_TILE), S::KV_SUB, 1024),
+                           j > 0 ? 1u : 0u, &pv_done[h]);
+          ++pc;
+        }
+        umma_commit_warp(&v_empty[vs]);
+        __syncwarp();
+        // S of the next tile, into the columns P_h(j) occupies
+        if (j + 1 < it.ntile) {
+          go = pp_wait_warp(&k_full[(gj + 1) % NK], (uint32_t)((gj + 1) / NK) & 1u, abort_flag, a);
+          if (go && mine) go = issue_s((gj + 1) % NK);
+          if (!go) break;
+          umma_commit_warp(&k_empty[(gj + 1) % NK]);
           __syncwarp();
         }
       }
       g += it.ntile;
     }
-    // every MMA issued so far is complete before tensor memory is released
-    umma_commit_warp(drain);
+    // every MMA this warp issued is complete before tensor memory is released
+    umma_commit_warp(&drain[h]);
     __syncwarp();
-    if (!mbar_wait_bounded(drain, 0)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
-  } else if (warp == 2 || warp == 3) {
-    // -------------------------------------------------------------- bias producers
-    // Warp 2 + hs loads the bias of head slot hs: for each tile that reads any bucket below
-    // E - 1, the boxes of the 32-row groups that do, into the head's next ring slot.  Out-of-
-    // range buckets and tokens arrive as zeros and are never used.
-    const int hs = warp - 2;
+    if (!mbar_wait_bounded(&drain[h], 0)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
+  } else if (warp == 2) {
+    // -------------------------------------------------------------- bias producer
+    // For each tile that reads any bucket below E - 1, and each head of the item, the boxes of
+    // the 32-row groups that do, into that head's next ring slot.  Out-of-range buckets and
+    // tokens arrive as zeros and are never used.
     if (lane == 0) prefetch_tensormap(&tmB);
-    int cnt = 0;
+    int cnt[2] = {0, 0};
     bool go = true;
     for (int i = blockIdx.x; i < total_items && go; i += gridDim.x) {
       PPItem it;
-      if (!pp_item(a, i, it) || it.ntile == 0 || hs >= it.nh) continue;
-      const int h = it.h0 + hs;
-      for (int j = 0; j < it.ntile; ++j) {
+      if (!pp_item(a, i, it) || it.ntile == 0) continue;
+      for (int j = 0; j < it.ntile && go; ++j) {
         const int k0 = (it.kt0 + j) * TILE_KEYS;
         if (!pp_tile_needs_bias(it.pos0, k0, a.E)) continue;
-        const int slot = cnt % NB;
-        if (cnt >= NB && !pp_wait_warp(&b_empty[hs * NB + slot], (uint32_t)((cnt / NB) - 1) & 1u, abort_flag, a)) {
-          go = false;
-          break;
-        }
-        BT* sb = reinterpret_cast<BT*>(smem + L_::bias + (size_t)(hs * NB + slot) * BS::SLOT_BYTES);
         const int dmin0 = it.pos0 - (k0 + TILE_KEYS - 1);
         const uint32_t nm = __ballot_sync(0xffffffffu, lane < NGR && pp_group_needed(a, it, k0, lane));
-        mbar_arrive_expect_tx_warp(&b_full[hs * NB + slot], (uint32_t)__popc(nm) * (uint32_t)(BS::GROUP * sizeof(BT)));
+        for (int hs = 0; hs < it.nh; ++hs) {
+          const int slot = hs * NB + cnt[hs] % NB;
+          if (cnt[hs] >= NB && !pp_wait_warp(&b_empty[slot], (uint32_t)((cnt[hs] / NB) - 1) & 1u, abort_flag, a)) {
+            go = false;
+            break;
+          }
+          BT* sb = reinterpret_cast<BT*>(smem + L_::bias + (size_t)slot * BS::SLOT_BYTES);
+          mbar_arrive_expect_tx_warp(&b_full[slot], (uint32_t)__popc(nm) * (uint32_t)(BS::GROUP * sizeof(BT)));
 #pragma unroll 1
-        for (uint32_t mm = nm; mm; mm &= mm - 1) {
-          const int gr = __ffs(mm) - 1;
-          tma_load_3d_warp(sb + gr * BS::GROUP, &tmB, pp_group_x<BS::ALIGN>(dmin0, gr), h, it.t0 + BR * gr,
-                           &b_full[hs * NB + slot]);
+          for (uint32_t mm = nm; mm; mm &= mm - 1) {
+            const int gr = __ffs(mm) - 1;
+            tma_load_3d_warp(sb + gr * BS::GROUP, &tmB, pp_group_x<BS::ALIGN>(dmin0, gr), it.h0 + hs, it.t0 + BR * gr,
+                             &b_full[slot]);
+          }
+          ++cnt[hs];
         }
-        ++cnt;
       }
     }
-    if (lane == 0) pp_drain_ring(b_full + hs * NB, NB, cnt, a.err);
+    if (lane == 0) {
+      pp_drain_ring(b_full, NB, cnt[0], a.err);
+      pp_drain_ring(b_full + NB, NB, cnt[1], a.err);
+    }
   } else {
     // -------------------------------------------------------------- softmax warpgroups
     const int hs = (warp - 4) >> 2;   // head slot
@@ -514,7 +540,6 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         return bad;
       };
       float m = -INFINITY, l = 0.f;
-      uint8_t* prow = smem + L_::pst + (size_t)hs * S::P_BYTES + (size_t)r * 128;   // this row of P_h
       const uint64_t scale2 = f2_pack(a.sm_scale, a.sm_scale);
       const uint64_t log2e2 = f2_pack(LOG2E, LOG2E);
       for (int j = 0; j < it.ntile; ++j, ++th) {
@@ -532,9 +557,6 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           tmem_ld32(tm_s + 32, hi);
           tmem_wait_ld();
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[hs]);   // the MMA may compute the next S into this buffer
         // visible columns of this row: [kmin - k0, kmax - k0] less unreadable keys
         int kmin, kmax;
         pp_row_keys(a, it, pr, k0, kmin, kmax);
@@ -546,14 +568,14 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         const int cc = dmin + TILE_KEYS - a.E;
         const int bslot_i = hs * NB + bcnt % NB;
         const BT* bslot = reinterpret_cast<const BT*>(smem + L_::bias + (size_t)bslot_i * BS::SLOT_BYTES);
-        // bucket of key c at brow[-c]; any address in the slot when the tile reads no bucket from it
-        const BT* brow = bslot + (TILE_KEYS - 1);
+        // bucket of key c at element 63 - c of brow; anywhere in the slot when the tile reads no bucket from it
+        BiasRow<BF16> brow;
+        brow.at(bslot);
         if (needs) {
           go = pp_wait_warp(&b_full[bslot_i], (uint32_t)(bcnt / NB) & 1u, abort_flag, a);
           if (!go) break;
           const int gr = r / BR;
-          brow = bslot + gr * BS::GROUP + (r % BR) * BS::COLS + (dmin - pp_group_x<BS::ALIGN>(dmin - r, gr)) +
-                 (TILE_KEYS - 1);
+          brow.at(bslot + gr * BS::GROUP + (r % BR) * BS::COLS + (dmin - pp_group_x<BS::ALIGN>(dmin - r, gr)));
         }
         float mxv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         const bool all_vis = vis == ~0ull;
@@ -562,8 +584,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
             float x, y;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2,
-                             f2_pack(to_float_b(brow[-c]), to_float_b(brow[-c - 1]))), x, y);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2, brow.pair(c)), x, y);
             sr[c] = __float_as_uint(x);
             sr[c + 1] = __float_as_uint(y);
             mxv[(c >> 1) & 3] = fmax3(mxv[(c >> 1) & 3], x, y);
@@ -582,8 +603,10 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         } else {
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
-            const float b0 = c <= cc ? clampv : to_float_b(brow[-c]);
-            const float b1 = c + 1 <= cc ? clampv : to_float_b(brow[-c - 1]);
+            float b0, b1;
+            f2_unpack(brow.pair(c), b0, b1);
+            b0 = c <= cc ? clampv : b0;
+            b1 = c + 1 <= cc ? clampv : b1;
             float x, y;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2, f2_pack(b0, b1)), x, y);
             x = ((vis >> c) & 1ull) ? x : -INFINITY;
@@ -607,10 +630,8 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         } else {
           const bool mine = m_new > m + RESCALE_NAT;
           if (__any_sync(0xffffffffu, mine)) {
-            // O_h must hold every earlier tile's P V product before it is rescaled
-            go = pp_wait_warp(&pv_done[hs], (uint32_t)(th - 1) & 1u, abort_flag, a);
-            if (!go) break;
-            tc_fence_after();
+            // O_h holds every earlier tile's P V product: S_h(j) was issued after the last of
+            // them completed, and s_full covers every product the MMA warp issued before it
             const float f = mine ? fast_exp2((m - m_new) * LOG2E) : 1.f;
             pair_rescale_o<D>(tm_o, f);
             l *= f;
@@ -637,17 +658,10 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           f2_unpack(ls2[1], b0, b1);
           l += (a0 + b0) + (a1 + b1);
         }
-        // P_h of the previous tile has been read by its P V product: the buffer is free
-        if (th > 0) {
-          go = pp_wait_warp(&pv_done[hs], (uint32_t)(th - 1) & 1u, abort_flag, a);
-          if (!go) break;
-        }
-        // P row r: 128 bytes (64 keys), 16-byte chunk c at chunk position c ^ (r & 7)
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        // P row r over the first 32 columns of S_h (this thread has read S_h(j) already)
+        tmem_st32(tm_s, pk);
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[hs]);
       }
