@@ -167,8 +167,7 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmKs, const __grid_
   static_assert(HB == 8 || HB == 16, "heads per unit");
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L_::bars);
   uint64_t* empty = full + NSTAGE;
   uint64_t* qempty = empty + NSTAGE;  // [2]

@@ -166,25 +166,55 @@ __device__ __forceinline__ void pair_store_o(uint32_t tm_o, float inv, uint4* or
   }
 }
 
-// One row's bias in a ring slot, read as pairs (b[c], b[c + 1]) for even c; key c's bucket is
-// element 63 - c counted from `k63`.
+// 32-bit shared-memory load, kept after the barrier wait that precedes it.
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// One row's bias in a ring slot.  Key c's bucket is element 63 - c counted from the element of
+// key 63 (`at`).  load(hh) brings keys 32 hh .. 32 hh + 31 into registers (bf16: every key at
+// once), each load of a batch issued together; pair(c) hands out (b[c], b[c + 1]) for even c.
 template <bool BF16>
 struct BiasRow {   // fp32: one 32-bit load per key (the 32 rows of a warp hit 32 banks)
-  const float* k63;
-  __device__ __forceinline__ void at(const float* p) { k63 = p; }
-  __device__ __forceinline__ uint64_t pair(int c) const { return f2_pack(k63[63 - c], k63[62 - c]); }
-};
-template <>
-struct BiasRow<true> {   // bf16: 33 aligned 32-bit loads per row, each pair funnel-shifted into place
-  const uint32_t* w;     // the word holding element 0
-  uint32_t sh;           // 16 when element 0 is the high half of its word
-  __device__ __forceinline__ void at(const __nv_bfloat16* p) {
-    w = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(p) & ~uintptr_t(3));
-    sh = (uint32_t)(reinterpret_cast<uintptr_t>(p) & 2u) << 3;
+  uint32_t k63;    // shared address of key 63's element
+  float fv[32];    // keys 32 hh + i at fv[31 - i]
+  __device__ __forceinline__ void at(const float* p) { k63 = smem_u32(p); }
+  __device__ __forceinline__ void load(int hh) {
+#pragma unroll
+    for (int u = 0; u < 32; ++u) fv[u] = __uint_as_float(lds32(k63 + 4u * (uint32_t)(32 - 32 * hh + u)));
+  }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int u = 0; u < 32; ++u) fv[u] = 0.f;
   }
   __device__ __forceinline__ uint64_t pair(int c) const {
-    const int q = 31 - (c >> 1);   // elements 2q, 2q + 1: keys c + 1, c
-    const uint32_t v = __funnelshift_r(w[q], w[q + 1], sh);
+    const int i = c & 31;
+    return f2_pack(fv[31 - i], fv[30 - i]);
+  }
+};
+template <>
+struct BiasRow<true> {   // bf16: 33 aligned 32-bit loads per row, pairs funnel-shifted into place
+  uint32_t w0;           // shared address of the word holding key 63's element
+  uint32_t sh;           // 16 when that element is the high half of its word
+  uint32_t wv[33];
+  __device__ __forceinline__ void at(const __nv_bfloat16* p) {
+    const uint32_t a = smem_u32(p);
+    w0 = a & ~3u;
+    sh = (a & 2u) << 3;
+  }
+  __device__ __forceinline__ void load(int) {
+#pragma unroll
+    for (int u = 0; u < 33; ++u) wv[u] = lds32(w0 + 4u * (uint32_t)u);
+  }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int u = 0; u < 33; ++u) wv[u] = 0u;
+  }
+  __device__ __forceinline__ uint64_t pair(int c) const {
+    const int q = 31 - (c >> 1);   // elements 2q, 2q + 1 from key 63's: keys c + 1, c
+    const uint32_t v = __funnelshift_r(wv[q], wv[q + 1], sh);
     return f2_pack(__uint_as_float(v & 0xffff0000u), __uint_as_float(v << 16));
   }
 };
@@ -201,8 +231,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   constexpr int NK = S::NK, NV = S::NV, NB = BS::NB;
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L_::bars);
   uint64_t* k_full = bars;
   uint64_t* k_empty = k_full + NK;
@@ -546,17 +575,6 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         const int k0 = (it.kt0 + j) * TILE_KEYS;
         const bool needs = pp_tile_needs_bias(it.pos0, k0, a.E);
         const uint64_t bad = item_bad ? tile_bad(k0) : 0ull;
-        go = pp_wait_warp(&s_full[hs], (uint32_t)th & 1u, abort_flag, a);
-        if (!go) break;
-        tc_fence_after();
-        uint32_t sr[64];
-        {
-          uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-          uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-          tmem_ld32(tm_s, lo);
-          tmem_ld32(tm_s + 32, hi);
-          tmem_wait_ld();
-        }
         // visible columns of this row: [kmin - k0, kmax - k0] less unreadable keys
         int kmin, kmax;
         pp_row_keys(a, it, pr, k0, kmin, kmax);
@@ -568,14 +586,28 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         const int cc = dmin + TILE_KEYS - a.E;
         const int bslot_i = hs * NB + bcnt % NB;
         const BT* bslot = reinterpret_cast<const BT*>(smem + L_::bias + (size_t)bslot_i * BS::SLOT_BYTES);
-        // bucket of key c at element 63 - c of brow; anywhere in the slot when the tile reads no bucket from it
+        // The tile's bias comes into registers while its scores are still being computed
         BiasRow<BF16> brow;
-        brow.at(bslot);
         if (needs) {
           go = pp_wait_warp(&b_full[bslot_i], (uint32_t)(bcnt / NB) & 1u, abort_flag, a);
           if (!go) break;
           const int gr = r / BR;
           brow.at(bslot + gr * BS::GROUP + (r % BR) * BS::COLS + (dmin - pp_group_x<BS::ALIGN>(dmin - r, gr)));
+          brow.load(0);
+        } else {
+          brow.at(bslot);
+          brow.zero();
+        }
+        go = pp_wait_warp(&s_full[hs], (uint32_t)th & 1u, abort_flag, a);
+        if (!go) break;
+        tc_fence_after();
+        uint32_t sr[64];
+        {
+          uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+          uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+          tmem_ld32(tm_s, lo);
+          tmem_ld32(tm_s + 32, hi);
+          tmem_wait_ld();
         }
         float mxv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         const bool all_vis = vis == ~0ull;
@@ -583,6 +615,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           // every key visible, every bucket from the tile's bias rows
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
+            if (!BF16 && c == 32) brow.load(1);
             float x, y;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2, brow.pair(c)), x, y);
             sr[c] = __float_as_uint(x);
@@ -603,6 +636,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         } else {
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
+            if (!BF16 && c == 32) {
+              if (needs) brow.load(1);
+            }
             float b0, b1;
             f2_unpack(brow.pair(c), b0, b1);
             b0 = c <= cc ? clampv : b0;

@@ -286,8 +286,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   constexpr uint32_t IDESC_PV = umma_idesc_bf16(PT_ROWS, D, false, true);
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L_::bars);
   uint64_t* q_full = bars;
   uint64_t* q_empty = bars + 1;
