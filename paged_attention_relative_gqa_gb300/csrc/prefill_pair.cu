@@ -15,25 +15,26 @@
 // in order of decreasing causal length (static round-robin); the two heads of an item share
 // their tokens, hence their visible keys, masks and K/V tiles.
 //
-// Tensor memory (512 columns): Q of head 0 and 1 (the A operand of S = Q K^T, D/2 columns
-// each), S of head 0 and 1 (64 fp32 columns each), O of head 0 and 1 (D fp32 columns each).
-// P (softmax numerators, bf16 pairs) overwrites the first 32 columns of its head's S and is
-// the A operand of O += P V, so neither P nor its product touches shared memory.  The next S
-// of a head is computed once that product has read P; meanwhile the tensor cores work on the
-// other head, whose softmax runs half a tile out of step.
+// Tensor memory (512 columns for D = 128): Q of head 0 (the A operand of S_0 = Q_0 K^T, D/2
+// columns), S of head 0 and 1 (64 fp32 columns each), P of head 0 and 1 (softmax numerators,
+// 32 columns of bf16 pairs each: the A operand of O += P V), O of head 0 and 1 (D fp32 columns
+// each).  Q of head 1 does not fit and sits in shared memory (S_1 = Q_1 K^T reads both
+// operands from there).  With P apart from S, the next S of a head is computed as soon as the
+// softmax has read the current one, so the softmax never waits for its own P V product.
 //
 // Warp roles (384 threads):
 //   warp 0   K and V producer: one TMA box per 64-key tile (or one per page segment when
 //            pages are shorter than a tile), block-table entries held 32 at a time in lanes.
-//   warps 1, 3  MMA issuers of head 0 and head 1, per tile: O_h += P_h(j) V(j) (M 128, N D,
-//            A = P from TMEM) once the softmax has written P_h(j), then S_h(j+1) = Q_h K(j+1)^T
-//            (M 128, N 64, A = Q from TMEM) once that product is complete.  Before its P V
-//            product each zeroes the V rows of keys that no row of the item may see (window
-//            edges, sequence end, unreadable pages).
+//   warps 1, 3  MMA issuers of head 0 and head 1, per tile: S_h(j+1) = Q_h K(j+1)^T (M 128,
+//            N 64) as soon as the softmax has read S_h(j), then O_h += P_h(j) V(j) (M 128, N D,
+//            A = P from TMEM) once P_h(j) is written.  Before its P V product each zeroes the V
+//            rows of keys that no row of the item may see (window edges, sequence end,
+//            unreadable pages).
 //   warp 2   bias producer: per tile that reads any bucket below E - 1 and per head, up to four
 //            3-D TMA boxes (32 tokens x COLS buckets) into the head's ring.
 //   warps 4-7, 8-11  softmax of head 0 and head 1: thread r owns row r (TMEM lane r).  Per
-//            item it loads its Q row into TMEM; per tile it reads its 64 scores, adds the bias,
+//            item it loads its Q row (head 0: into TMEM; head 1: into shared memory, in the
+//            128-byte-swizzled layout of an MMA operand); per tile it reads its 64 scores, adds the bias,
 //            masks, keeps the running max and sum (O rescaled in TMEM only when the max grows
 //            by more than 2^8), writes P into TMEM; at the end it normalises O and stores bf16.  Pairs of
 //            scores go through packed two-lane fp32 FMA and add (the same rounding as scalar
@@ -55,7 +56,13 @@ using namespace pf;
 template <bool BF16>
 using PairBias = PBias<BF16, BF16 ? 2 : 1>;
 
-template <int D>
+constexpr int PP_Q1_SUB = PP_ROWS * 128;   // Q_1 in shared memory: blocks of 128 rows x 64 bf16
+
+// ES (early S, the bf16-bias kernel): Q_0 in TMEM, Q_1 in shared memory, P_h apart from S_h,
+// so that S_h(j+1) follows as soon as the softmax has read S_h(j).  Otherwise (the fp32-bias
+// kernel, whose bias ring takes the shared memory Q_1 would need): Q_h in TMEM and P_h over
+// the first 32 columns of S_h, so that S_h(j+1) follows once O_h += P_h(j) V(j) is done.
+template <int D, bool ES>
 struct PPShape {
   static constexpr int CB = D / 64;
   static constexpr int KV_SUB = TILE_KEYS * 128;
@@ -63,39 +70,49 @@ struct PPShape {
   static constexpr int NK = D == 128 ? 2 : 4;   // K ring (freed when both S products are done)
   static constexpr int NV = D == 128 ? 2 : 4;   // V ring (freed when both P V products are done)
   static constexpr uint32_t QC = D / 2;          // TMEM columns of one Q tile (bf16 pairs)
-  static constexpr uint32_t TQ = 0;              // Q_h at TQ + h QC
-  static constexpr uint32_t TS = 2 * QC;         // S_h at TS + 64 h; P_h in its first 32 columns
-  static constexpr uint32_t TO = 2 * QC + 128;   // O_h at TO + D h
+  static constexpr uint32_t TQ = 0;              // Q_h at TQ + h QC (ES: Q_0 only)
+  static constexpr uint32_t TS = ES ? QC : 2 * QC;            // S_h at TS + 64 h
+  static constexpr uint32_t TP = ES ? QC + 128 : 2 * QC;      // P_h at TP + PSTRIDE h
+  static constexpr uint32_t PSTRIDE = ES ? 32 : 64;
+  static constexpr uint32_t TO = ES ? QC + 192 : 2 * QC + 128;   // O_h at TO + D h
   static_assert(TO + 2 * D <= 512, "tensor memory budget");
+  static constexpr int Q1_BYTES = ES ? CB * PP_Q1_SUB : 0;
 };
 
 template <int D, bool BF16>
 struct PPSmem {
-  using S = PPShape<D>;
+  using S = PPShape<D, BF16>;
   using B = PairBias<BF16>;
   static constexpr size_t kst = 0;
   static constexpr size_t vst = kst + (size_t)S::NK * S::KV_TILE;
-  static constexpr size_t bias = vst + (size_t)S::NV * S::KV_TILE;
+  static constexpr size_t q1 = vst + (size_t)S::NV * S::KV_TILE;
+  static constexpr size_t bias = q1 + (size_t)S::Q1_BYTES;
   static constexpr size_t bars = bias + (size_t)2 * B::NB * B::SLOT_BYTES;
-  // k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], q_ready[2], s_full[2], p_full[2],
-  // pv_done[2], b_full[2 NB], b_empty[2 NB], drain[2]
-  static constexpr int NBAR = 2 * S::NK + 2 * S::NV + 8 + 4 * B::NB + 2;
+  // k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], q_ready[2], s_full[2], s_empty[2],
+  // p_full[2], pv_done[2], b_full[2 NB], b_empty[2 NB], drain[2]
+  static constexpr int NBAR = 2 * S::NK + 2 * S::NV + 10 + 4 * B::NB + 2;
   static constexpr size_t vbad = bars + NBAR * 8;
   static constexpr size_t misc = vbad + S::NV * 8;
   static constexpr size_t total = misc + 32;
   static constexpr size_t alloc = total + 1024;
 };
 
-// S_h = Q_h K^T of one 64-key tile (A = Q from TMEM, B = the K tile, K-major with the 128-byte
-// swizzle), D / 16 K-steps; descriptors of later K-steps add the byte offset / 16 to the
-// start-address field.  Executed by a converged warp; one elected lane issues.
-template <int D>
+// S_h = Q_h K^T of one 64-key tile, D / 16 K-steps (B = the K tile, K-major with the 128-byte
+// swizzle; descriptors of later K-steps add the byte offset / 16 to the start-address field).
+// A = Q_0 from TMEM (QS false, a0 its column) or Q_1 from shared memory (QS true, a0 the
+// address of its first block).  Executed by a converged warp; one elected lane issues.
+template <int D, bool QS>
 __device__ __forceinline__ void pair_issue_s(uint32_t d, uint32_t a0, uint64_t b0, uint64_t* done) {
   constexpr uint32_t IDESC_S = umma_idesc_bf16(PP_ROWS, TILE_KEYS, false, false);
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk)
-    umma_ts_warp(d, a0 + kk * 8, b0 + (uint64_t)((((kk >> 2) * TILE_KEYS * 128) + (kk & 3) * 32) >> 4), IDESC_S,
-                 kk > 0 ? 1u : 0u);
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t bk = b0 + (uint64_t)((((kk >> 2) * TILE_KEYS * 128) + (kk & 3) * 32) >> 4);
+    if constexpr (QS)
+      umma_ss_warp(d, umma_desc_sw128(a0 + (uint32_t)((kk >> 2) * PP_Q1_SUB + (kk & 3) * 32), 16, 1024), bk,
+                   IDESC_S, kk > 0 ? 1u : 0u);
+    else
+      umma_ts_warp(d, a0 + kk * 8, bk, IDESC_S, kk > 0 ? 1u : 0u);
+  }
   umma_commit_warp(done);
 }
 
@@ -127,6 +144,18 @@ __device__ __forceinline__ void pair_load_q(const uint4* qsrc, bool rv, uint32_t
     tmem_st32(tm_q + 32 * half, qv);
   }
   tmem_wait_st();
+}
+
+// Store this thread's Q row (rows past the item's last are zero) into shared memory as row r of
+// an MMA operand tile: CB blocks of 128 rows x 128 bytes, 16-byte chunk c of a row at chunk
+// position c ^ (r & 7) (the 128-byte swizzle).
+template <int D>
+__device__ __forceinline__ void pair_store_q_smem(const uint4* qsrc, bool rv, uint8_t* qtile, int r) {
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) {
+    const uint4 x = rv ? __ldg(qsrc + c) : make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(qtile + (c >> 3) * PP_Q1_SUB + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = x;
+  }
 }
 
 // Multiply this thread's row of O (D fp32 TMEM columns) by f.
@@ -224,7 +253,8 @@ __global__ void __launch_bounds__(PP_THREADS, 1)
 prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmK3, const __grid_constant__ CUtensorMap tmV3,
                     const __grid_constant__ CUtensorMap tmB, const PrefillArgs a) {
-  using S = PPShape<D>;
+  constexpr bool ES = BF16;
+  using S = PPShape<D, ES>;
   using L_ = PPSmem<D, BF16>;
   using BS = PairBias<BF16>;
   using BT = typename BS::T;
@@ -239,8 +269,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   uint64_t* v_empty = v_full + NV;
   uint64_t* q_ready = v_empty + NV;   // [2] Q of the item in TMEM, O of the previous item read
   uint64_t* s_full = q_ready + 2;     // [2] S_h in TMEM (and every earlier product of the MMA warp done)
-  uint64_t* p_full = s_full + 2;      // [2] P_h in TMEM
-  uint64_t* pv_done = p_full + 2;     // [2] O_h += P_h V done (S_h may be rewritten; O_h stable)
+  uint64_t* s_empty = s_full + 2;     // [2] S_h read by the softmax
+  uint64_t* p_full = s_empty + 2;     // [2] P_h in TMEM
+  uint64_t* pv_done = p_full + 2;     // [2] O_h += P_h V done (P_h may be rewritten; O_h stable)
   uint64_t* b_full = pv_done + 2;     // [2 NB] head h's slot s at h NB + s
   uint64_t* b_empty = b_full + 2 * NB;
   uint64_t* drain = b_empty + 2 * NB;   // [2] one per MMA-issuing warp
@@ -264,6 +295,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     for (int x = 0; x < 2; ++x) {
       mbar_init(&q_ready[x], 4);
       mbar_init(&s_full[x], 1);
+      mbar_init(&s_empty[x], 4);
       mbar_init(&p_full[x], 4);
       mbar_init(&pv_done[x], 1);
     }
@@ -296,108 +328,150 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         prefetch_tensormap(&tmV3);
       }
     }
-    int g = 0, gk = 0, gv = 0;   // tiles walked, K and V fills issued
-    int chunk_b = -1, chunk_base = 0, chunk_val = -1;
+    // Two cursors walk the same sequence of tiles, K one tile ahead of V: the S product of a
+    // tile is issued about a tile before its P V product, and a V slot that is still busy must
+    // not hold back the next K.
     const int seg = P < TILE_KEYS ? P : TILE_KEYS;
     const int nseg = TILE_KEYS / seg;
-    bool go = true;
-    for (int i = blockIdx.x; i < total_items && go; i += gridDim.x) {
+    struct Cursor {
+      int i, j;                           // item index, tile within it
       PPItem it;
-      if (!pp_item(a, i, it) || it.ntile == 0) continue;
+      int chunk_b, chunk_base, chunk_val; // block-table entries chunk_base + lane
+      int n;                              // fills issued
+    };
+    // the next tile of the walk (false when none is left)
+    auto advance = [&](Cursor& c) -> bool {
+      if (++c.j < c.it.ntile) return true;
+      for (c.i += gridDim.x; c.i < total_items; c.i += gridDim.x)
+        if (pp_item(a, c.i, c.it) && c.it.ntile > 0) {
+          c.j = 0;
+          return true;
+        }
+      return false;
+    };
+    // one K or V fill of the cursor's tile into the next ring slot (false after an abort)
+    auto issue = [&](Cursor& c, bool is_k) -> bool {
+      const PPItem& it = c.it;
       const int32_t* bt = a.block_table + (size_t)it.b * a.max_pages;
       const int last_idx = it.k_hi >> a.log2_page;   // never read the table past here
-      for (int j = 0; j < it.ntile; ++j, ++g) {
-        const int k0 = (it.kt0 + j) * TILE_KEYS;
-        // lane sg < nseg takes segment sg of the tile: seg keys on one page
-        const int pfirst = k0 >> a.log2_page, plast = (k0 + TILE_KEYS - 1) >> a.log2_page;
-        if (chunk_b != it.b || pfirst < chunk_base || plast >= chunk_base + 32) {
-          chunk_b = it.b;
-          chunk_base = pfirst;
-          const int idx = chunk_base + lane;
-          const int v = __ldg(bt + min(idx, last_idx));   // in bounds even past the last entry
-          chunk_val = idx <= last_idx ? v : -1;
-        }
-        const int ks = k0 + lane * seg;
-        const bool want = lane < nseg && ks <= it.k_hi && ks + seg - 1 >= it.lo_min;
-        const int page = __shfl_sync(0xffffffffu, chunk_val, min(max((ks >> a.log2_page) - chunk_base, 0), 31));
-        const bool bad_seg = want && (page < 0 || page >= a.num_pages);
-        const bool load = want && !bad_seg;
-        const uint32_t lmask = __ballot_sync(0xffffffffu, load);
-        const uint32_t bmask = __ballot_sync(0xffffffffu, bad_seg);
-        const int my_row = ((page * a.Hkv + it.kvh) << a.log2_page) + (ks & (P - 1));
-        const uint32_t bytes = (uint32_t)__popc(lmask) * (uint32_t)(seg * D * 2);
-#pragma unroll 1
-        for (int kv = 0; kv < 2; ++kv) {
-          const bool is_k = kv == 0;
-          const int NR = is_k ? NK : NV;
-          const int n = is_k ? gk : gv;
-          const int st = n % NR;
-          uint64_t* full = is_k ? k_full : v_full;
-          if (n >= NR && !pp_wait_warp(is_k ? &k_empty[st] : &v_empty[st], (uint32_t)((n / NR) - 1) & 1u,
-                                       abort_flag, a)) {
-            go = false;
-            break;
-          }
-          if (!is_k && lane == 0) {   // keys whose page is outside the pool: the MMA warp zeroes their V rows
-            uint64_t bad = 0;
-#pragma unroll 1
-            for (uint32_t mm = bmask; mm; mm &= mm - 1)
-              bad |= seg == 64 ? ~0ull : (((1ull << seg) - 1) << ((__ffs(mm) - 1) * seg));
-            vbad[st] = bad;
-          }
-          if (is_k && bmask && lane == 0) record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
-          __syncwarp();
-          mbar_arrive_expect_tx_warp(&full[st], bytes);
-          uint8_t* ring = smem + (is_k ? L_::kst : L_::vst) + (size_t)st * S::KV_TILE;
-#pragma unroll 1
-          for (uint32_t mm = lmask; mm; mm &= mm - 1) {
-            const int sg = __ffs(mm) - 1;
-            const int row = __shfl_sync(0xffffffffu, my_row, sg);
-            uint8_t* dst = ring + sg * seg * 128;
-            if (seg == TILE_KEYS) {
-              tma_load_3d_warp(dst, is_k ? &tmK3 : &tmV3, 0, row, 0, &full[st]);   // whole tile: one box
-            } else {
-#pragma unroll
-              for (int cb = 0; cb < S::CB; ++cb)
-                tma_load_2d_warp(dst + cb * S::KV_SUB, is_k ? &tmK : &tmV, cb * 64, row, &full[st]);
-            }
-          }
-          if (is_k) ++gk; else ++gv;
-        }
-        if (!go) break;
+      const int k0 = (it.kt0 + c.j) * TILE_KEYS;
+      // lane sg < nseg takes segment sg of the tile: seg keys on one page
+      const int pfirst = k0 >> a.log2_page, plast = (k0 + TILE_KEYS - 1) >> a.log2_page;
+      if (c.chunk_b != it.b || pfirst < c.chunk_base || plast >= c.chunk_base + 32) {
+        c.chunk_b = it.b;
+        c.chunk_base = pfirst;
+        const int idx = c.chunk_base + lane;
+        const int v = __ldg(bt + min(idx, last_idx));   // in bounds even past the last entry
+        c.chunk_val = idx <= last_idx ? v : -1;
       }
+      const int ks = k0 + lane * seg;
+      const bool want = lane < nseg && ks <= it.k_hi && ks + seg - 1 >= it.lo_min;
+      const int page = __shfl_sync(0xffffffffu, c.chunk_val, min(max((ks >> a.log2_page) - c.chunk_base, 0), 31));
+      const bool bad_seg = want && (page < 0 || page >= a.num_pages);
+      const bool load = want && !bad_seg;
+      const uint32_t lmask = __ballot_sync(0xffffffffu, load);
+      const uint32_t bmask = __ballot_sync(0xffffffffu, bad_seg);
+      const int my_row = ((page * a.Hkv + it.kvh) << a.log2_page) + (ks & (P - 1));
+      const uint32_t bytes = (uint32_t)__popc(lmask) * (uint32_t)(seg * D * 2);
+      const int NR = is_k ? NK : NV;
+      const int st = c.n % NR;
+      uint64_t* full = is_k ? k_full : v_full;
+      if (c.n >= NR && !pp_wait_warp(is_k ? &k_empty[st] : &v_empty[st], (uint32_t)((c.n / NR) - 1) & 1u, abort_flag, a))
+        return false;
+      if (!is_k && lane == 0) {   // keys whose page is outside the pool: the MMA warps zero their V rows
+        uint64_t bad = 0;
+#pragma unroll 1
+        for (uint32_t mm = bmask; mm; mm &= mm - 1)
+          bad |= seg == 64 ? ~0ull : (((1ull << seg) - 1) << ((__ffs(mm) - 1) * seg));
+        vbad[st] = bad;
+      }
+      if (is_k && bmask && lane == 0) record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
+      __syncwarp();
+      mbar_arrive_expect_tx_warp(&full[st], bytes);
+      uint8_t* ring = smem + (is_k ? L_::kst : L_::vst) + (size_t)st * S::KV_TILE;
+#pragma unroll 1
+      for (uint32_t mm = lmask; mm; mm &= mm - 1) {
+        const int sg = __ffs(mm) - 1;
+        const int row = __shfl_sync(0xffffffffu, my_row, sg);
+        uint8_t* dst = ring + sg * seg * 128;
+        if (seg == TILE_KEYS) {
+          tma_load_3d_warp(dst, is_k ? &tmK3 : &tmV3, 0, row, 0, &full[st]);   // whole tile: one box
+        } else {
+#pragma unroll
+          for (int cb = 0; cb < S::CB; ++cb)
+            tma_load_2d_warp(dst + cb * S::KV_SUB, is_k ? &tmK : &tmV, cb * 64, row, &full[st]);
+        }
+      }
+      ++c.n;
+      return true;
+    };
+    Cursor ck, cv;
+    ck.i = blockIdx.x - (int)gridDim.x;
+    ck.j = 0;
+    ck.it.ntile = 0;
+    ck.chunk_b = -1;
+    ck.chunk_base = 0;
+    ck.chunk_val = -1;
+    ck.n = 0;
+    cv = ck;
+    bool hk = advance(ck), hv = advance(cv);
+    bool go = true;
+    if (hk) {
+      go = issue(ck, true);
+      hk = advance(ck);
+    }
+    while (go && hv) {
+      if (hk) {
+        go = issue(ck, true);
+        if (!go) break;
+        hk = advance(ck);
+      }
+      go = issue(cv, false);
+      if (!go) break;
+      hv = advance(cv);
     }
     if (lane == 0) {
-      pp_drain_ring(k_full, NK, gk, a.err);
-      pp_drain_ring(v_full, NV, gv, a.err);
+      pp_drain_ring(k_full, NK, ck.n, a.err);
+      pp_drain_ring(v_full, NV, cv.n, a.err);
     }
   } else if (warp == 1 || warp == 3) {
     // -------------------------------------------------------------- MMA issuers
     // Warp 1 issues head 0's products, warp 3 head 1's, so that neither head waits behind the
-    // other's barriers.  Per tile: O_h += P_h(j) V(j) once the softmax has written P_h(j)
-    // (p_full), then S_h(j+1) into the same TMEM columns once that product has read P_h(j)
-    // (pv_done).  K and V slots are released by one commit from each warp (a warp whose head is
-    // absent from an item commits without products).  Every phase of the barriers a warp waits
-    // on is waited for in order.
+    // other's barriers.  Per tile j: S_h(j+1) once the softmax has read S_h(j) (s_empty) and
+    // K(j+1) has landed, then O_h += P_h(j) V(j) once P_h(j) is written (p_full).  K and V
+    // slots are released by one commit from each warp (a warp whose head is absent from an
+    // item commits without products).  Every phase of the barriers a warp waits on is waited
+    // for in order.
     const int h = warp == 1 ? 0 : 1;
     int g = 0;                     // tiles walked
     int qc = 0;                    // items of head h
+    int sn = 0;                    // S products issued for head h
     int pc = 0;                    // P V products issued for head h
     bool go = true;
-    // S_h of K slot kslot, after the last P V product of head h has read P_h
+    const uint32_t q1addr = smem_u32(smem + L_::q1);
+    // S_h of K slot kslot, once S_h is free: read by the softmax (ES), or, with P_h over S_h,
+    // read by the last P V product
     auto issue_s = [&](int kslot) -> bool {
-      if (pc > 0 && !pp_wait_warp(&pv_done[h], (uint32_t)(pc - 1) & 1u, abort_flag, a)) return false;
+      if (ES) {
+        if (sn > 0 && !pp_wait_warp(&s_empty[h], (uint32_t)(sn - 1) & 1u, abort_flag, a)) return false;
+      } else {
+        if (pc > 0 && !pp_wait_warp(&pv_done[h], (uint32_t)(pc - 1) & 1u, abort_flag, a)) return false;
+      }
       tc_fence_after();
-      pair_issue_s<D>(tmem + S::TS + 64u * h, tmem + S::TQ + S::QC * h,
-                      umma_desc_sw128(smem_u32(smem + L_::kst + (size_t)kslot * S::KV_TILE), 16, 1024), &s_full[h]);
+      const uint64_t kd = umma_desc_sw128(smem_u32(smem + L_::kst + (size_t)kslot * S::KV_TILE), 16, 1024);
+      if (ES && h == 1)
+        pair_issue_s<D, true>(tmem + S::TS + 64u, q1addr, kd, &s_full[1]);
+      else
+        pair_issue_s<D, false>(tmem + S::TS + 64u * h, tmem + S::TQ + S::QC * h, kd, &s_full[h]);
       __syncwarp();
+      ++sn;
       return true;
     };
     for (int i = blockIdx.x; i < total_items && go; i += gridDim.x) {
       PPItem it;
       if (!pp_item(a, i, it) || it.ntile == 0) continue;
       const bool mine = h < it.nh;
-      // S of tile 0 once Q_h is in TMEM
+      // S of tile 0 once Q_h is in place
       go = pp_wait_warp(&k_full[g % NK], (uint32_t)(g / NK) & 1u, abort_flag, a);
       if (go && mine) {
         go = pp_wait_warp(&q_ready[h], (uint32_t)qc & 1u, abort_flag, a);
@@ -411,6 +485,19 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         const int gj = g + j;
         const int k0 = (it.kt0 + j) * TILE_KEYS;
         const int vs = gj % NV;
+        // S of the next tile (ES: before this tile's P V product; otherwise after it)
+        auto next_s = [&]() -> bool {
+          if (j + 1 >= it.ntile) return true;
+          if (!pp_wait_warp(&k_full[(gj + 1) % NK], (uint32_t)((gj + 1) / NK) & 1u, abort_flag, a)) return false;
+          if (mine && !issue_s((gj + 1) % NK)) return false;
+          umma_commit_warp(&k_empty[(gj + 1) % NK]);
+          __syncwarp();
+          return true;
+        };
+        if (ES) {
+          go = next_s();
+          if (!go) break;
+        }
         go = pp_wait_warp(&v_full[vs], (uint32_t)(gj / NV) & 1u, abort_flag, a);
         if (!go) break;
         if (mine) {
@@ -437,21 +524,14 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           go = pp_wait_warp(&p_full[h], (uint32_t)pc & 1u, abort_flag, a);
           if (!go) break;
           tc_fence_after();
-          pair_issue_pv<D>(tmem + S::TO + (uint32_t)(D * h), tmem + S::TS + 64u * h,
+          pair_issue_pv<D>(tmem + S::TO + (uint32_t)(D * h), tmem + S::TP + S::PSTRIDE * h,
                            umma_desc_sw128(smem_u32(smem + L_::vst + (size_t)vs * S::KV_TILE), S::KV_SUB, 1024),
                            j > 0 ? 1u : 0u, &pv_done[h]);
           ++pc;
         }
         umma_commit_warp(&v_empty[vs]);
         __syncwarp();
-        // S of the next tile, into the columns P_h(j) occupies
-        if (j + 1 < it.ntile) {
-          go = pp_wait_warp(&k_full[(gj + 1) % NK], (uint32_t)((gj + 1) / NK) & 1u, abort_flag, a);
-          if (go && mine) go = issue_s((gj + 1) % NK);
-          if (!go) break;
-          umma_commit_warp(&k_empty[(gj + 1) % NK]);
-          __syncwarp();
-        }
+        if (!ES) go = next_s();
       }
       g += it.ntile;
     }
@@ -475,6 +555,16 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         if (!pp_tile_needs_bias(it.pos0, k0, a.E)) continue;
         const int dmin0 = it.pos0 - (k0 + TILE_KEYS - 1);
         const uint32_t nm = __ballot_sync(0xffffffffu, lane < NGR && pp_group_needed(a, it, k0, lane));
+        if constexpr (!BF16) {
+          // fp32: one ring slot per head, so the slot frees late; start the boxes towards L2 now
+#pragma unroll 1
+          for (int hs = 0; hs < it.nh; ++hs)
+#pragma unroll 1
+            for (uint32_t mm = nm; mm; mm &= mm - 1) {
+              const int gr = __ffs(mm) - 1;
+              tma_prefetch_l2_3d_warp(&tmB, pp_group_x<BS::ALIGN>(dmin0, gr), it.h0 + hs, it.t0 + BR * gr);
+            }
+        }
         for (int hs = 0; hs < it.nh; ++hs) {
           const int slot = hs * NB + cnt[hs] % NB;
           if (cnt[hs] >= NB && !pp_wait_warp(&b_empty[slot], (uint32_t)((cnt[hs] / NB) - 1) & 1u, abort_flag, a)) {
@@ -505,9 +595,10 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     const uint32_t tlane = tmem + ((uint32_t)(sw * 32) << 16);
     const uint32_t tm_q = tlane + S::TQ + S::QC * hs;
     const uint32_t tm_s = tlane + S::TS + 64u * hs;
+    const uint32_t tm_p = tlane + S::TP + S::PSTRIDE * hs;
     const uint32_t tm_o = tlane + S::TO + (uint32_t)(D * hs);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-    int th = 0, ic = 0, bcnt = 0;   // tiles, items and bias tiles of this head slot
+    int th = 0, bcnt = 0, pvw = 0;   // tiles, bias tiles and pv_done phases seen, of this head slot
     bool go = true;
     for (int i = blockIdx.x; i < total_items && go; i += gridDim.x) {
       PPItem it;
@@ -529,13 +620,19 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         }
         continue;
       }
-      // ---- Q row into TMEM (rows past the item's last are zero); the previous item's S
-      // products that read Q_h are complete (their s_full was seen), and its O_h has been read
+      // ---- Q row (rows past the item's last are zero): head 0 into TMEM, head 1 into shared
+      // memory; the previous item's S products that read Q_h are complete (their s_full was
+      // seen), and its O_h has been read
       {
-        pair_load_q<D>(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
-                                                      ((size_t)(it.t0 + (rv ? r : 0)) * a.Hq + h) * D),
-                       rv, tm_q);
-        tc_fence_before();
+        const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                           ((size_t)(it.t0 + (rv ? r : 0)) * a.Hq + h) * D);
+        if (!ES || hs == 0) {
+          pair_load_q<D>(qsrc, rv, tm_q);
+          tc_fence_before();
+        } else {
+          pair_store_q_smem<D>(qsrc, rv, smem + L_::q1, r);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&q_ready[hs]);
       }
@@ -609,6 +706,20 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           tmem_ld32(tm_s + 32, hi);
           tmem_wait_ld();
         }
+        if (ES) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[hs]);   // the MMA warp may compute the next S here
+        }
+        // ES: O_h and P_h are free once the previous tile's P V product is done (waited once per
+        // tile).  Otherwise S_h(j) was issued after that product completed, and s_full covers it.
+        auto wait_pv = [&]() -> bool {
+          if (!ES || pvw >= th) return true;
+          if (!pp_wait_warp(&pv_done[hs], (uint32_t)pvw & 1u, abort_flag, a)) return false;
+          ++pvw;
+          tc_fence_after();
+          return true;
+        };
         float mxv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         const bool all_vis = vis == ~0ull;
         if (__all_sync(0xffffffffu, all_vis && cc < 0)) {
@@ -666,8 +777,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         } else {
           const bool mine = m_new > m + RESCALE_NAT;
           if (__any_sync(0xffffffffu, mine)) {
-            // O_h holds every earlier tile's P V product: S_h(j) was issued after the last of
-            // them completed, and s_full covers every product the MMA warp issued before it
+            // O_h must hold every earlier tile's P V product before it is rescaled
+            go = wait_pv();
+            if (!go) break;
             const float f = mine ? fast_exp2((m - m_new) * LOG2E) : 1.f;
             pair_rescale_o<D>(tm_o, f);
             l *= f;
@@ -694,8 +806,10 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           f2_unpack(ls2[1], b0, b1);
           l += (a0 + b0) + (a1 + b1);
         }
-        // P row r over the first 32 columns of S_h (this thread has read S_h(j) already)
-        tmem_st32(tm_s, pk);
+        // P row r (P_h free once the previous tile's product has read it)
+        go = wait_pv();
+        if (!go) break;
+        tmem_st32(tm_p, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -703,9 +817,11 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       }
       if (!go) break;
       // ---- epilogue: O_h / l -> bf16 -> out, once the item's last P V product is done
-      go = pp_wait_warp(&pv_done[hs], (uint32_t)(th - 1) & 1u, abort_flag, a);
-      ++ic;
-      if (!go) break;
+      if (!ES || pvw < th) {
+        go = pp_wait_warp(&pv_done[hs], (uint32_t)(th - 1) & 1u, abort_flag, a);
+        if (!go) break;
+        pvw = th;
+      }
       tc_fence_after();
       pair_store_o<D>(tm_o, l > 0.f ? 1.f / l : 0.f, reinterpret_cast<uint4*>(out + ((size_t)(it.t0 + r) * a.Hq + h) * D),
                       rv);
