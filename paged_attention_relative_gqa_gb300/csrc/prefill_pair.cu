@@ -790,26 +790,34 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         const float mb = m == -INFINITY ? 0.f : m * LOG2E;
         const uint64_t nmb2 = f2_pack(-mb, -mb);
         uint32_t pk[32];
-        uint64_t ls2[2] = {0ull, 0ull};   // two packed partial sums (+0.0f pairs)
+        uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};   // four packed partial sums (+0.0f pairs)
+        auto exp_pairs = [&](int c0) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float t0, t1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), log2e2, nmb2), t0, t1);
-          const float p0 = fast_exp2(t0);
-          const float p1 = fast_exp2(t1);
-          ls2[c & 1] = f2_add(ls2[c & 1], f2_pack(p0, p1));
-          pk[c] = pack_bf16(p0, p1);
-        }
-        {
-          float a0, a1, b0, b1;
-          f2_unpack(ls2[0], a0, a1);
-          f2_unpack(ls2[1], b0, b1);
-          l += (a0 + b0) + (a1 + b1);
-        }
-        // P row r (P_h free once the previous tile's product has read it)
+          for (int c = c0; c < c0 + 16; ++c) {
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), log2e2, nmb2), t0, t1);
+            const float p0 = fast_exp2(t0);
+            const float p1 = fast_exp2(t1);
+            ls2[c & 3] = f2_add(ls2[c & 3], f2_pack(p0, p1));
+            pk[c] = pack_bf16(p0, p1);
+          }
+        };
+        // P row r in two halves, the first stored while the second is computed (P_h is free
+        // once the previous tile's product has read it)
+        exp_pairs(0);
         go = wait_pv();
         if (!go) break;
-        tmem_st32(tm_p, pk);
+        tmem_st16(tm_p, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+        exp_pairs(16);
+        tmem_st16(tm_p + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+        {
+          float a0, a1, b0, b1, c0, c1, d0, d1;
+          f2_unpack(ls2[0], a0, a1);
+          f2_unpack(ls2[1], b0, b1);
+          f2_unpack(ls2[2], c0, c1);
+          f2_unpack(ls2[3], d0, d1);
+          l += ((a0 + b0) + (c0 + d0)) + ((a1 + b1) + (c1 + d1));
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
