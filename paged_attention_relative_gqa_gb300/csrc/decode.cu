@@ -20,7 +20,9 @@
 //     rows (TMA over q viewed as [B*Hq, D]).  The producer runs ahead across units.
 //   warps 0-3 (consumers): each takes 16 keys of every tile: S = Q K^T (mma.sync,
 //     query heads are the 16 MMA rows), s2 = S * sm_scale * log2(e) + bias * log2(e),
-//     keys outside [lo, p] or in unreadable pages -> -inf, online softmax in base 2,
+//     keys outside [lo, p] or in unreadable pages -> -inf, online softmax in base 2 (the
+//     running max moves only when a score passes it by more than 8, so most tiles skip
+//     the cross-lane max and the rescale of O),
 //     O += P V with V rows of masked keys zeroed in registers.  The bias values of the
 //     next tile are prefetched into registers while the current one is computed.
 // Unit epilogue: the 4 warps' (max, sum, O) are merged through shared memory; a
@@ -518,27 +520,43 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmKs, const __grid_
         uint32_t pb0[NB], pb1[NB];
 #pragma unroll
         for (int j = 0; j < NB; ++j) {
+          // Scores in base 2.  The running max m_r moves only when a score passes it by more than
+          // 8 (so p = 2^(s - m_r) < 256): most tiles skip the cross-lane max and the rescale of O.
+          float sv[2][2];
+          bool up = false;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            sv[e][0] = v0 ? fmaf(acc[j][e], a.scale_log2, bias[j][e] * LOG2E) : -INFINITY;
+            sv[e][1] = v1 ? fmaf(acc[j][2 + e], a.scale_log2, bias[j][2 + e] * LOG2E) : -INFINITY;
+            up |= fmaxf(sv[e][0], sv[e][1]) > m_r[j][e] + 8.f;
+          }
+          if (__any_sync(0xffffffffu, up)) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float mx = fmaxf(sv[e][0], sv[e][1]);
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+              const float mn = fmaxf(m_r[j][e], mx);   // the same in the 8 lanes of this head
+              if (mn > m_r[j][e]) {
+                const float al = fast_exp2(m_r[j][e] - mn);
+                m_r[j][e] = mn;
+                l_r[j][e] *= al;
+#pragma unroll
+                for (int dn = 0; dn < D / 16; ++dn) {
+                  o[dn][j][e] *= al;
+                  o[dn][j][2 + e] *= al;
+                }
+              }
+            }
+          }
           float pr[4];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const float s0 = v0 ? fmaf(acc[j][e], a.scale_log2, bias[j][e] * LOG2E) : -INFINITY;
-            const float s1 = v1 ? fmaf(acc[j][2 + e], a.scale_log2, bias[j][2 + e] * LOG2E) : -INFINITY;
-            float mx = fmaxf(s0, s1);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float mn = fmaxf(m_r[j][e], mx);
-            const float mu = mn == -INFINITY ? 0.f : mn;
-            const float al = fast_exp2(m_r[j][e] - mu);
-            m_r[j][e] = mn;
-            pr[e] = fast_exp2(s0 - mu);
-            pr[2 + e] = fast_exp2(s1 - mu);
-            l_r[j][e] = l_r[j][e] * al + pr[e] + pr[2 + e];
-#pragma unroll
-            for (int dn = 0; dn < D / 16; ++dn) {
-              o[dn][j][e] *= al;
-              o[dn][j][2 + e] *= al;
-            }
+            const float mu = m_r[j][e] == -INFINITY ? 0.f : m_r[j][e];
+            pr[e] = fast_exp2(sv[e][0] - mu);
+            pr[2 + e] = fast_exp2(sv[e][1] - mu);
+            l_r[j][e] += pr[e] + pr[2 + e];
           }
           // P^T into the B-fragment layout: thread (g, c) needs keys 2c, 2c+1 (and +8) of head g
           const uint32_t X = pack_bf16(pr[0], pr[1]);  // key gq,   heads 2cq, 2cq+1
