@@ -21,10 +21,13 @@ class LayerStreams:
     """Issues each layer's (prefill calls, decode calls) on two streams.
 
     Every call must launch on the current stream (the binding's calls do when given no
-    stream).  ``decode_first`` issues the side stream's calls before the main stream's.
+    stream).  ``decode_first`` issues the side stream's calls before the main stream's.  With
+    the persistent one-CTA-per-SM prefill, prefill first is the better order: the decode's
+    CTAs then take the SMs the prefill's last wave leaves (decode first delays the whole
+    prefill wave behind the decode's CTAs).
     """
 
-    def __init__(self, device=None, decode_first: bool = True):
+    def __init__(self, device=None, decode_first: bool = False):
         self.side = torch.cuda.Stream(device=device)
         self.decode_first = decode_first
 
