@@ -515,7 +515,12 @@ def run_ours(args, rank, world, local_rank):
         del step
     elif name not in ("mixed", "mixed_graph", "mixed_kv_graph"):
         decode = "flops" not in r
-        src, kernel = ("decode.cu", "decode_persistent_kernel") if decode else ("prefill_tc.cu", "prefill_tc_kernel")
+        if decode:
+            src, kernel = "decode.cu", "decode_persistent_kernel"
+        elif "lowrank" in name:
+            src, kernel = "prefill_tc.cu", "prefill_tc_kernel"
+        else:   # the materialised bias runs the head-pair kernel
+            src, kernel = "prefill_pair.cu", "prefill_pair_kernel"
         if r["bound"] == "hbm":
             line["roofline"] = {"bound": "hbm", "achieved": round(r["GB/s"], 2), "peak": hbm_peak,
                                 "unit": "GB/s", "frac": round(r["GB/s"] / hbm_peak, 4),
