@@ -374,16 +374,23 @@ def measure_kv(binding, name, dev, steps, warmup, stream, hbm_peak):
     fn, ws = kv_call(binding, step, dev)
     if name == "kv_prefill_global":
         m = time_steps([fn], steps, warmup, stream)          # 268 MB read + 268 MB written per call > L2
-    else:
+    floor = None
+    if name != "kv_prefill_global":
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         m = time_flushed(fn, steps, warmup, stream, flush)
-        del flush
+        # the same timing of a one-element kernel: what launch and event latency alone cost
+        tiny = torch.zeros(1, device=dev)
+        floor = time_flushed(lambda: tiny.add_(1), steps, warmup, stream, flush)
+        del flush, tiny
     assert binding.inkling_attn_read_device_error(ws) == 0
     nbytes = kv_write_bytes(step)
     gbs = nbytes / m / 1e6
-    return {"ms": m, "value": gbs, "unit": "GB/s", "GB/s": gbs, "hbm_frac": gbs / hbm_peak,
-            "tok_s": step.total_q / m * 1e3, "bytes": nbytes, "launches_per_step": 1, "bound": "hbm",
-            "kv_step": step}
+    r = {"ms": m, "value": gbs, "unit": "GB/s", "GB/s": gbs, "hbm_frac": gbs / hbm_peak,
+         "tok_s": step.total_q / m * 1e3, "bytes": nbytes, "launches_per_step": 1, "bound": "hbm",
+         "kv_step": step}
+    if floor is not None:
+        r["one_element_kernel_ms"] = round(floor, 5)
+    return r
 
 
 def measure(binding, name, dev, steps, warmup, stream, hbm_peak, bf16_peak):

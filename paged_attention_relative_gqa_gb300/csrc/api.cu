@@ -520,7 +520,7 @@ ink_status_t inkling_attn_kv_conv_write(const ink_attn_params_t* params, const v
   const int sms = ink::current_device_sms(&dev);
   if (sms <= 0) return INK_ERR_CUDA;
   ink::kv_conv_plan(a, kernel_size, sms);
-  a.state_items = has_state ? 2ll * a.B * (kernel_size - 1) * nvec : 0;
+  a.state_items = has_state ? 2ll * a.B * nvec : 0;   // each copies all ks - 1 rows of a vector
   if ((a.conv_items + a.state_items + 255) / 256 >= (1ll << 31)) return INK_ERR_TOO_LARGE;
   if (ink::launch_kv_conv(a, kernel_size, (cudaStream_t)stream) != cudaSuccess) return INK_ERR_CUDA;
   return INK_OK;

@@ -130,7 +130,7 @@ struct KvConvArgs {
   int tok;                     // tokens per thread (1 or 8)
   int nchunks;                 // ceil(T / tok)
   long long conv_items;        // 2 * nchunks * nvec threads of convolution
-  long long state_items;       // 2 * B * (ks-1) * nvec threads of state copy
+  long long state_items;       // 2 * B * nvec threads of state copy (each all ks-1 rows)
   int tile_tokens;             // staged kernel: new rows per tile (<= 32)
   int stages;                  // staged kernel: ring depth (0: use the per-thread kernel)
   unsigned long long wait_ns;  // limit of one pipeline wait (the drain waits keep 2 s)

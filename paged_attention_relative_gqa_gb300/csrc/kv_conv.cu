@@ -23,7 +23,8 @@
 //    starts or crosses into the next request.  Consecutive threads take consecutive vectors
 //    of a row, so every load and store of a warp is 512 contiguous bytes of one row (or 256
 //    bytes per KV head in the cache).
-// In both, extra threads of the same launch copy the carried state rows.
+// In both, extra threads of the same launch copy the carried state: one thread per 16-byte
+// vector of a request's state, all KS - 1 rows (loads issued together).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -82,6 +83,36 @@ __device__ __forceinline__ int find_seq_shared(const int* cu_q, int B, int t) {
     if (cu_q[mid] <= t) lo = mid; else hi = mid;
   }
   return lo;
+}
+
+// Carried state of item sid = (tensor z, request b, vector v): the KS - 1 rows after the step,
+// the last KS - 1 rows of [state before; the request's new rows].  All loads are issued
+// before the stores.  cu holds cu_q (in shared memory when `cached`, else global).
+template <int KS>
+__device__ __forceinline__ void copy_state_item(const KvConvArgs& a, long long sid, const int* cu_s, bool cached,
+                                                int row_elems) {
+  const int v = (int)(sid % a.nvec);
+  const long long rest = sid / a.nvec;
+  const int b = (int)(rest % a.B);
+  const int z = (int)(rest / a.B);
+  const int col = v * 8;
+  const int seq_start = cached ? cu_s[b] : __ldg(a.cu_q + b);
+  const int n = max((cached ? cu_s[b + 1] : __ldg(a.cu_q + b + 1)) - seq_start, 0);
+  uint4 rows[KS - 1];
+#pragma unroll
+  for (int r = 0; r < KS - 1; ++r) {
+    rows[r] = make_uint4(0, 0, 0, 0);
+    if (r + n < KS - 1) {
+      rows[r] = ld_row16(a.st_in[z] + ((size_t)b * (KS - 1) + (r + n)) * row_elems + col);
+    } else {
+      const int t = seq_start + r + n - (KS - 1);
+      if (t >= 0 && t < a.T) rows[r] = ld_row16(a.x[z] + (size_t)t * row_elems + col);
+      else record_error(a.err, INK_DEVERR_BAD_ROWS);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < KS - 1; ++r)
+    *reinterpret_cast<uint4*>(a.st_out[z] + ((size_t)b * (KS - 1) + r) * row_elems + col) = rows[r];
 }
 
 // Requests whose offsets and lengths the per-thread kernel stages in shared memory (one
@@ -208,27 +239,8 @@ __global__ void __launch_bounds__(KV_CONV_THREADS, 2) kv_conv_write_kernel(const
     return;
   }
   if constexpr (KS > 1) {
-    if (gid >= a.conv_items + a.state_items) return;
     // ---------------------------------------------------------------- carried state
-    const long long sid = gid - a.conv_items;
-    const int v = (int)(sid % a.nvec);
-    long long rest = sid / a.nvec;
-    const int r = (int)(rest % (KS - 1));
-    rest /= (KS - 1);
-    const int b = (int)(rest % a.B);
-    const int z = (int)(rest / a.B);
-    const int col = v * 8;
-    const int seq_start = cached ? cu_s[b] : __ldg(a.cu_q + b);
-    const int n = max((cached ? cu_s[b + 1] : __ldg(a.cu_q + b + 1)) - seq_start, 0);
-    uint4 row = make_uint4(0, 0, 0, 0);
-    if (r + n < KS - 1) {
-      row = ld_row16(a.st_in[z] + ((size_t)b * (KS - 1) + (r + n)) * row_elems + col);
-    } else {
-      const int t = seq_start + r + n - (KS - 1);
-      if (t >= 0 && t < a.T) row = ld_row16(a.x[z] + (size_t)t * row_elems + col);
-      else record_error(a.err, INK_DEVERR_BAD_ROWS);
-    }
-    *reinterpret_cast<uint4*>(a.st_out[z] + ((size_t)b * (KS - 1) + r) * row_elems + col) = row;
+    if (gid < a.conv_items + a.state_items) copy_state_item<KS>(a, gid - a.conv_items, cu_s, cached, row_elems);
   }
 }
 
@@ -401,26 +413,8 @@ __global__ void __launch_bounds__(KVS_THREADS, 1) kv_conv_staged_kernel(const Kv
   // carried-state rows first (plain copies, a few per thread)
   if constexpr (KS > 1) {
     for (long long sid = (long long)blockIdx.x * KVS_CONSUMERS + threadIdx.x; sid < a.state_items;
-         sid += (long long)gridDim.x * KVS_CONSUMERS) {
-      const int v = (int)(sid % a.nvec);
-      long long rest = sid / a.nvec;
-      const int r = (int)(rest % (KS - 1));
-      rest /= (KS - 1);
-      const int b = (int)(rest % a.B);
-      const int z = (int)(rest / a.B);
-      const int col = v * 8;
-      const int seq_start = cached ? cu_s[b] : __ldg(a.cu_q + b);
-      const int n = max((cached ? cu_s[b + 1] : __ldg(a.cu_q + b + 1)) - seq_start, 0);
-      uint4 row = make_uint4(0, 0, 0, 0);
-      if (r + n < KS - 1) {
-        row = ld_row16(a.st_in[z] + ((size_t)b * (KS - 1) + (r + n)) * row_elems + col);
-      } else {
-        const int t = seq_start + r + n - (KS - 1);
-        if (t >= 0 && t < a.T) row = ld_row16(a.x[z] + (size_t)t * row_elems + col);
-        else record_error(a.err, INK_DEVERR_BAD_ROWS);
-      }
-      *reinterpret_cast<uint4*>(a.st_out[z] + ((size_t)b * (KS - 1) + r) * row_elems + col) = row;
-    }
+         sid += (long long)gridDim.x * KVS_CONSUMERS)
+      copy_state_item<KS>(a, sid, cu_s, cached, row_elems);
   }
 
   const int nseg = max(1, KVS_CONSUMERS / a.nvec);
