@@ -152,7 +152,8 @@ ink_status_t inkling_attn_prefill_bf16bias(const ink_attn_params_t* params, cons
  *   r           device, bf16 [total_q, Hq, d_rel], 16-byte aligned
  *   rel_proj_t  device, bf16 [E, d_rel]: rel_logits_proj transposed (bucket-major, so each
  *               bucket's d_rel coefficients are contiguous), 16-byte aligned
- *   d_rel       64 (else INK_ERR_BAD_SHAPE); the pages do not give it
+ *   d_rel       a multiple of 8 in [8, 64] (else INK_ERR_BAD_SHAPE); the pages do not give it.
+ *               The bias products run with K = 64; columns past d_rel are zeros.
  * The products are summed in fp32 from the bf16 operands (tensor-core MMA for the buckets
  * of a tile, a plain fp32 dot product for the clamped bucket E - 1) and the tile's bias
  * values are kept in fp16 until they are added to the fp32 scores (relative rounding

@@ -196,10 +196,11 @@ bool make_bias_map(CUtensorMap* map, const void* rel, bool bf16, const ink_attn_
   return r == CUDA_SUCCESS;
 }
 
-// Low-rank bias operands (d_rel 64): r [total_q, Hq, 64] as {64, Hq, total_q} with boxes of
-// 128 tokens of one head, and proj_t [E, 64] as {64, E} with boxes of LOWRANK_CHUNK buckets;
-// 128-byte rows with the 128-byte swizzle, as the bias MMA's K-major operands want them.
-// Out-of-range rows (tokens past total_q, buckets outside [0, E)) read as zeros.
+// Low-rank bias operands: r [total_q, Hq, d_rel] as {d_rel, Hq, total_q} with boxes of 64
+// columns x 128 tokens of one head, and proj_t [E, d_rel] as {d_rel, E} with boxes of 64
+// columns x LOWRANK_CHUNK buckets; 128-byte rows with the 128-byte swizzle, as the bias MMA's
+// K-major operands (K = 64) want them.  Columns past d_rel, tokens past total_q and buckets
+// outside [0, E) read as zeros, so a smaller d_rel adds zero products.
 bool make_lowrank_maps(ink::PrefillMaps* m, const void* r, const void* proj_t, const ink_attn_params_t* p,
                        int total_q, int d_rel) {
   auto fn = encode_fn();
@@ -207,7 +208,7 @@ bool make_lowrank_maps(ink::PrefillMaps* m, const void* r, const void* proj_t, c
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
   cuuint64_t dims_r[3] = {(cuuint64_t)d_rel, (cuuint64_t)p->num_q_heads, (cuuint64_t)total_q};
   cuuint64_t str_r[2] = {(cuuint64_t)d_rel * 2, (cuuint64_t)d_rel * 2 * p->num_q_heads};
-  cuuint32_t box_r[3] = {(cuuint32_t)d_rel, 1, (cuuint32_t)ink::PREFILL_ROWS};
+  cuuint32_t box_r[3] = {(cuuint32_t)ink::LOWRANK_MAX_D, 1, (cuuint32_t)ink::PREFILL_ROWS};
   cuuint32_t e3[3] = {1, 1, 1};
   CUresult e = fn(&m->lr_r, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(r), dims_r, str_r, box_r, e3,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -215,7 +216,7 @@ bool make_lowrank_maps(ink::PrefillMaps* m, const void* r, const void* proj_t, c
   if (e != CUDA_SUCCESS) return false;
   cuuint64_t dims_p[2] = {(cuuint64_t)d_rel, (cuuint64_t)p->rel_extent};
   cuuint64_t str_p[1] = {(cuuint64_t)d_rel * 2};
-  cuuint32_t box_p[2] = {(cuuint32_t)d_rel, (cuuint32_t)ink::LOWRANK_CHUNK};
+  cuuint32_t box_p[2] = {(cuuint32_t)ink::LOWRANK_MAX_D, (cuuint32_t)ink::LOWRANK_CHUNK};
   cuuint32_t e2[2] = {1, 1};
   e = fn(&m->lr_p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(proj_t), dims_p, str_p, box_p, e2,
          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -361,7 +362,7 @@ ink_status_t prefill_impl(const ink_attn_params_t* params, const void* q, const 
     return INK_ERR_NULL_PTR;
   if (lowrank ? (!lr_r || !lr_proj_t) : !rel_logits) return INK_ERR_NULL_PTR;
   if (max_q_len < 0 || total_q < 0) return INK_ERR_BAD_SHAPE;
-  if (lowrank && d_rel != ink::LOWRANK_MAX_D) return INK_ERR_BAD_SHAPE;
+  if (lowrank && (d_rel < 8 || d_rel > ink::LOWRANK_MAX_D || d_rel % 8 != 0)) return INK_ERR_BAD_SHAPE;
   if ((long long)total_q * params->num_q_heads >= (1ll << 31)) return INK_ERR_TOO_LARGE;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(cu_q_lens, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))

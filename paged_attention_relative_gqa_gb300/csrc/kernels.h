@@ -50,7 +50,7 @@ struct PrefillArgs {
   int bias_lowrank;           // bias from r and proj_t (rel unused)
   const void* lr_r;           // bf16 [total_q, Hq, d_rel]
   const void* lr_proj_t;      // bf16 [E, d_rel]
-  int d_rel;                  // 64
+  int d_rel;                  // a multiple of 8 in [8, 64]
   unsigned long long wait_ns; // limit of one pipeline wait (the drain waits keep 2 s)
 };
 
@@ -100,7 +100,7 @@ constexpr int BIAS_BOX_ROWS = 16;   // tokens per bias box
 constexpr int BIAS_BOX_COLS_BF16 = 88;   // buckets per bias box row, bf16 bias
 constexpr int PREFILL_ROWS = 128;        // new tokens per prefill work item
 constexpr int LOWRANK_CHUNK = 64;        // projection rows per TMA box (one key tile's new buckets)
-constexpr int LOWRANK_MAX_D = 64;        // d_rel of the low-rank bias (the MMA's K: four K-steps of 16)
+constexpr int LOWRANK_MAX_D = 64;        // largest d_rel of the low-rank bias (the MMA's K: four K-steps of 16)
 
 cudaError_t launch_prefill_tc(const PrefillMaps& maps, const PrefillArgs& a, int head_dim,
                               cudaStream_t stream);

@@ -40,6 +40,9 @@ EDGE_LR = [
     (8, 2, 64, 8, -1, 7, [1, 5, 70], [1, 40, 200], 64),           # P8, D64, E7 (clamp)
     (4, 4, 128, 64, -1, 1, [200], [300], 64),                     # E1: every key clamped
     (8, 2, 128, 64, -1, 4096, [700, 0, 130], [5000, 3, 130], 64), # long cached prefix, empty row
+    (8, 2, 128, 64, 512, 512, [300, 1], [1500, 777], 32),         # d_rel 32 (zero columns 32-63)
+    (8, 4, 64, 16, -1, 100, [150, 40], [150, 300], 16),           # d_rel 16, D64, P16
+    (16, 2, 128, 64, -1, 1024, [257], [900], 48),                 # d_rel 48
 ]
 
 
@@ -52,6 +55,18 @@ def test_lowrank_bias_edge_shapes(case):
     out, err = run_gpu(prob)
     assert err == 0
     compare(out.float().cpu().numpy(), oracle_full(prob), f"low-rank bias edge prefill {EDGE_LR[case]}")
+
+
+@pytest.mark.parametrize("d_rel", [64, 32])
+def test_lowrank_bias_with_std4_bias(d_rel):
+    """A bias of standard deviation 4 (the scores are dominated by it): the tile's bias is
+    held in fp16 on its way to the fp32 score, so this is where that rounding shows most."""
+    prob = W.make_problem(num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=64, rel_extent=1024,
+                          window=-1, q_lens=[700, 300], seq_lens=[700, 900], seed=88 + d_rel, device=DEV,
+                          rel_std=4.0, lowrank_d=d_rel)
+    out, err = run_gpu(prob)
+    assert err == 0
+    compare(out.float().cpu().numpy(), oracle_full(prob), f"low-rank bias, std 4, d_rel {d_rel}")
 
 
 def test_lowrank_bias_matches_the_materialised_bias_entry():
