@@ -76,7 +76,8 @@ struct DecSmem {
   static constexpr size_t bias = q + 2 * S::QSLOT_BYTES;
   static constexpr size_t obuf = bias + (size_t)DEC_CONSUMERS * BIAS_SLOTS * HB * BIAS_PITCH * 4;
   static constexpr size_t red = obuf + (size_t)DEC_CONSUMERS * HB * S::OPITCH * 4;
-  static constexpr size_t wts = red + 2 * DEC_CONSUMERS * 16 * 4;
+  static_assert((size_t)DEC_CONSUMERS * HB * S::OPITCH * 4 >= 16 * MAX_DECODE_SPLITS * 8, "merge scratch in obuf");
+  static constexpr size_t wts = red + (2 * DEC_CONSUMERS * 16 + 2 * 16) * 4;
   static constexpr size_t bars = wts + 16 * MAX_DECODE_SPLITS * 4;  // 8-byte aligned
   static constexpr size_t badmask = bars + (2 * NSTAGE + 4 + DEC_CONSUMERS * BIAS_SLOTS) * 8;
   static constexpr size_t flags = badmask + NSTAGE * 8;
@@ -157,6 +158,66 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
+// One split of a unit has its partials in the workspace: take the unit's ticket, and the
+// last of its splits to arrive merges all of them in split order and resets the ticket.
+// Run by the 128 consumer threads alike.  Out of line: it is off the tile loop's path.
+// Ordering: every thread's partial stores come before the CTA barrier, thread 0's ticket
+// add releases them at GPU scope and acquires the other splits' (the pattern of a
+// grid-wide semaphore), and the barrier after it hands that on to the threads that read.
+// The (max, sum) pairs of all splits are read at once into `scratch` (shared memory of at
+// least 16 x MAX_DECODE_SPLITS float2, free at this point), so the merge costs two round
+// trips to L2 rather than one per split.
+template <int D>
+__device__ __noinline__ void finish_split_unit(const float* part_o, const float* part_ml, int32_t* tickets,
+                                               __nv_bfloat16* out, int Hq, int Hkv, int head_chunks, int num_splits,
+                                               int b, int kvh, int hc, int h0, int nh, int nact, int tid,
+                                               int* flags, float* wts, float2* scratch) {
+  const size_t rowbase = (size_t)b * Hq + h0;
+  named_barrier_consumers();
+  const size_t ticket = ((size_t)b * Hkv + kvh) * head_chunks + hc;
+  if (tid == 0) {
+    int prev;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(tickets + ticket) : "memory");
+    flags[0] = prev == nact - 1;
+  }
+  named_barrier_consumers();
+  if (!flags[0]) return;
+  // scratch[r * MAX_DECODE_SPLITS + sp] <- (max, sum) of split sp of row r
+  for (int i = tid; i < nh * nact; i += DEC_CONSUMERS * 32) {
+    const int r = i / nact, sp = i - r * nact;
+    scratch[r * MAX_DECODE_SPLITS + sp] = __ldcg(reinterpret_cast<const float2*>(part_ml) + (rowbase + r) * num_splits + sp);
+  }
+  named_barrier_consumers();
+  if (tid < nh) {
+    const float2* row = scratch + tid * MAX_DECODE_SPLITS;
+    float M = -INFINITY;
+    for (int sp = 0; sp < nact; ++sp) M = fmaxf(M, row[sp].x);
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float Lt = 0.f;
+    for (int sp = 0; sp < nact; ++sp) Lt += row[sp].y * fast_exp2(row[sp].x - Mu);
+    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+    for (int sp = 0; sp < nact; ++sp) wts[tid * MAX_DECODE_SPLITS + sp] = fast_exp2(row[sp].x - Mu) * inv;
+  }
+  named_barrier_consumers();
+  for (int idx = tid; idx < nh * (D / 4); idx += DEC_CONSUMERS * 32) {
+    const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
+    const size_t pi0 = (rowbase + r) * num_splits;
+    const float* w = wts + r * MAX_DECODE_SPLITS;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int sp = 0; sp < nact; ++sp) {
+      const float wt = w[sp];
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(part_o + (pi0 + sp) * D + d));
+      acc.x += wt * v.x;
+      acc.y += wt * v.y;
+      acc.z += wt * v.z;
+      acc.w += wt * v.w;
+    }
+    *reinterpret_cast<uint2*>(out + (rowbase + r) * D + d) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+  }
+  if (tid == 0) tickets[ticket] = 0;  // ready for the next call
+}
+
 template <int D, int NSTAGE, int HB>
 __global__ void __launch_bounds__(DEC_THREADS, dec_ctas_per_sm<HB>())
 decode_persistent_kernel(const __grid_constant__ CUtensorMap tmKs, const __grid_constant__ CUtensorMap tmVs,
@@ -177,6 +238,7 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmKs, const __grid_
   int* flags = reinterpret_cast<int*>(smem + L_::flags);  // [0] ticket winner, [1] abort
   float* red_m = reinterpret_cast<float*>(smem + L_::red);
   float* red_l = red_m + DEC_CONSUMERS * 16;
+  float* head_ml = red_l + DEC_CONSUMERS * 16;  // [16][2]: a unit's (max, sum) per head
   float* obuf = reinterpret_cast<float*>(smem + L_::obuf);
   float* wts = reinterpret_cast<float*>(smem + L_::wts);
   volatile int* abort_flag = flags + 1;
@@ -596,6 +658,10 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmKs, const __grid_
         }
       }
     named_barrier_consumers();
+    // Each thread weighs its own heads' O rows: 2^(m_w - M) over the unit's sum (the sum
+    // alone when the unit is one split of several); then the 4 warps' rows are added,
+    // 4 channels per thread.
+    const bool single = cur.nact == 1;
 #pragma unroll
     for (int j = 0; j < NB; ++j)
 #pragma unroll
@@ -605,7 +671,16 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmKs, const __grid_
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < DEC_CONSUMERS; ++w) M = fmaxf(M, red_m[w * 16 + h]);
-        const float f = fast_exp2(m_r[j][e] - (M == -INFINITY ? 0.f : M));
+        const float Mu = M == -INFINITY ? 0.f : M;
+        float Lt = 0.f;
+#pragma unroll
+        for (int w = 0; w < DEC_CONSUMERS; ++w) Lt += red_l[w * 16 + h] * fast_exp2(red_m[w * 16 + h] - Mu);
+        float f = fast_exp2(m_r[j][e] - Mu);
+        if (single) f *= Lt > 0.f ? 1.f / Lt : 0.f;
+        if (warp == 0 && gq == 0) {
+          head_ml[2 * h] = M;
+          head_ml[2 * h + 1] = Lt;
+        }
         float* row = obuf + (warp * HB + h) * S::OPITCH;
 #pragma unroll
         for (int dn = 0; dn < D / 16; ++dn) {
@@ -614,64 +689,32 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmKs, const __grid_
         }
       }
     named_barrier_consumers();
-    const bool single = cur.nact == 1;
     const size_t rowbase = (size_t)cur.b * a.Hq + cur.h0;
-    for (int idx = tid; idx < cur.nh * D; idx += DEC_CONSUMERS * 32) {
-      const int r = idx / D, d = idx % D;
-      float M = -INFINITY;
+    for (int idx = tid; idx < cur.nh * (D / 4); idx += DEC_CONSUMERS * 32) {
+      const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
+      float4 acc = *reinterpret_cast<const float4*>(obuf + r * S::OPITCH + d);
 #pragma unroll
-      for (int w = 0; w < DEC_CONSUMERS; ++w) M = fmaxf(M, red_m[w * 16 + r]);
-      const float Mu = M == -INFINITY ? 0.f : M;
-      float acc = 0.f, Lt = 0.f;
-#pragma unroll
-      for (int w = 0; w < DEC_CONSUMERS; ++w) {
-        acc += obuf[(w * HB + r) * S::OPITCH + d];
-        Lt += red_l[w * 16 + r] * fast_exp2(red_m[w * 16 + r] - Mu);
+      for (int w = 1; w < DEC_CONSUMERS; ++w) {
+        const float4 v = *reinterpret_cast<const float4*>(obuf + (w * HB + r) * S::OPITCH + d);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
       }
       if (single) {
-        out[(rowbase + r) * D + d] = __float2bfloat16(Lt > 0.f ? acc / Lt : 0.f);
+        *reinterpret_cast<uint2*>(out + (rowbase + r) * D + d) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
       } else {
         const size_t pi = (rowbase + r) * a.num_splits + cur.s;
-        a.part_o[pi * D + d] = acc;
+        *reinterpret_cast<float4*>(a.part_o + pi * D + d) = acc;
         if (d == 0) {
-          a.part_ml[pi * 2 + 0] = M;
-          a.part_ml[pi * 2 + 1] = Lt;
+          a.part_ml[pi * 2 + 0] = head_ml[2 * r];
+          a.part_ml[pi * 2 + 1] = head_ml[2 * r + 1];
         }
       }
     }
-    if (!single) {
-      // split-K ticket: the last CTA of this (sequence, KV head, head chunk) merges
-      __threadfence();
-      named_barrier_consumers();
-      const size_t ticket = ((size_t)cur.b * a.Hkv + cur.kvh) * a.head_chunks + cur.hc;
-      if (tid == 0) flags[0] = (atomicAdd(&a.tickets[ticket], 1) == cur.nact - 1);
-      named_barrier_consumers();
-      if (flags[0]) {
-        __threadfence();
-        if (tid < cur.nh) {
-          const size_t pi0 = (rowbase + tid) * a.num_splits;
-          float M = -INFINITY;
-          for (int sp = 0; sp < cur.nact; ++sp) M = fmaxf(M, __ldcg(a.part_ml + (pi0 + sp) * 2));
-          const float Mu = M == -INFINITY ? 0.f : M;
-          float Lt = 0.f;
-          for (int sp = 0; sp < cur.nact; ++sp)
-            Lt += __ldcg(a.part_ml + (pi0 + sp) * 2 + 1) * fast_exp2(__ldcg(a.part_ml + (pi0 + sp) * 2) - Mu);
-          const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
-          for (int sp = 0; sp < cur.nact; ++sp)
-            wts[tid * MAX_DECODE_SPLITS + sp] = fast_exp2(__ldcg(a.part_ml + (pi0 + sp) * 2) - Mu) * inv;
-        }
-        named_barrier_consumers();
-        for (int idx = tid; idx < cur.nh * D; idx += DEC_CONSUMERS * 32) {
-          const int r = idx / D, d = idx % D;
-          const size_t pi0 = (rowbase + r) * a.num_splits;
-          float acc = 0.f;
-          for (int sp = 0; sp < cur.nact; ++sp)
-            acc += wts[r * MAX_DECODE_SPLITS + sp] * __ldcg(a.part_o + (pi0 + sp) * D + d);
-          out[(rowbase + r) * D + d] = __float2bfloat16(acc);
-        }
-        if (tid == 0) a.tickets[ticket] = 0;  // ready for the next call
-      }
-    }
+    if (!single)
+      finish_split_unit<D>(a.part_o, a.part_ml, a.tickets, out, a.Hq, a.Hkv, a.head_chunks, a.num_splits, cur.b,
+                           cur.kvh, cur.hc, cur.h0, cur.nh, cur.nact, tid, flags, wts, reinterpret_cast<float2*>(obuf));
     named_barrier_consumers();  // red/obuf/wts/flags are reused by the next unit
     cur = nxt;
     ucur = unxt;

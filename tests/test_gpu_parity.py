@@ -126,6 +126,31 @@ def test_long_decode_many_splits():
     full_check(prob, "long decode 64k")
 
 
+@pytest.mark.parametrize("head_dim", [128, 64])
+def test_decode_window_ragged_lengths(head_dim):
+    # Window-bound decode with more units than CTAs: ragged lengths (one key, under a tile,
+    # window-sized, one past it, misaligned) and 16-key pages (partial tiles); then
+    # zero-length sequences leave every other row's bits unchanged (the work split does
+    # not depend on the lengths).
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Hq, Hkv = 16, 8
+    B = -(-2 * sms // Hkv) + 5   # units > 2 CTAs per SM x SMs
+    rng = np.random.default_rng(77)
+    sl = [int(x) for x in rng.choice([1, 7, 63, 64, 65, 300, 511, 512, 513, 1000, 2999], size=B)]
+    prob = W.make_problem(num_q_heads=Hq, num_kv_heads=Hkv, head_dim=head_dim, page_size=16,
+                          rel_extent=600, window=512, q_lens=[1] * B, seq_lens=sl, seed=31,
+                          device=DEV, max_pages=200)
+    out1, _ = run_gpu(prob)
+    compare(out1.float().cpu().numpy(), oracle_full(prob), f"window decode B{B} D{head_dim}")
+    zero = [3, 4, B - 1]
+    for b in zero:
+        prob.seq_lens[b] = 0
+    out2, _ = run_gpu(prob)
+    keep = [b for b in range(B) if b not in zero]
+    assert torch.all(out2[zero] == 0)
+    assert np.array_equal(bits(out2[keep]), bits(out1[keep]))
+
+
 # ------------------------------------------------------------------ invariants on the GPU
 
 def _mid_problem(window=48, decode=False, seed=21):
