@@ -49,6 +49,7 @@ constexpr int DEC_THREADS = (DEC_CONSUMERS + 1) * 32;
 constexpr int QROWS = 16;       // query-head rows per unit (MMA M)
 constexpr int SEG_ROWS = 16;    // fine TMA box rows for partial tiles
 constexpr int PTAB = 576;       // staged block-table entries per unit (>= 64 tiles x 64/8 + 2)
+constexpr int L2_AHEAD = 1;     // whole tiles prefetched into L2 ahead of their loads
 
 template <int D>
 struct DecShape {
@@ -321,6 +322,21 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmKs, const __grid_
       const int row_kv = cur.kvh << a.log2_page;       // + page * Hkv * P
       const int hkvp = a.Hkv << a.log2_page;
       constexpr uint32_t WHOLE_BYTES = 2u * TILE_KEYS * D * 2u;
+      // The ring holds NSTAGE tiles; each load issue also starts the K and V boxes of the
+      // whole tile L2_AHEAD tiles on (in this unit or the next, whose table slice is staged)
+      // towards L2, so that the loads into the ring find them there.
+      int nfirst = 0, ncount = 0;
+      if (unxt < total_units) unit_page_span(a, nxt, nfirst, ncount);
+      const int* ntab = ptab + ((uc + 1) % 3) * PTAB;
+      auto prefetch_whole = [&](const Unit& w, const int* wtab, int wfirst, int i) {
+        const int k0 = (w.tb + i) * TILE_KEYS;
+        if (P < TILE_KEYS || k0 < w.lo || k0 + TILE_KEYS - 1 > w.p) return;
+        const int page = wtab[(k0 >> a.log2_page) - wfirst];
+        if (page < 0 || page >= a.num_pages) return;
+        const int row = page * hkvp + (w.kvh << a.log2_page) + (k0 & (P - 1));
+        tma_prefetch_l2_4d(&tmKt, 0, 0, 0, row >> 4);
+        tma_prefetch_l2_4d(&tmVt, 0, 0, 0, row >> 4);
+      };
       if (uc >= 2) {
         if (lane == 0) go = wait_or_abort(&qempty[slot], (uint32_t)((uc >> 1) - 1) & 1u, abort_flag, a.err, a.wait_ns);
         go = __shfl_sync(0xffffffffu, go ? 1 : 0, 0) != 0;
@@ -334,6 +350,10 @@ decode_persistent_kernel(const __grid_constant__ CUtensorMap tmKs, const __grid_
         }
         const int k0 = (cur.tb + i) * TILE_KEYS;
         if (lane == 0) {
+          if (i + L2_AHEAD < cur.n_my)
+            prefetch_whole(cur, tab, pfirst, i + L2_AHEAD);
+          else if (unxt < total_units && i + L2_AHEAD - cur.n_my < nxt.n_my)
+            prefetch_whole(nxt, ntab, nfirst, i + L2_AHEAD - cur.n_my);
           uint8_t* kdst = smem + L_::stages + (size_t)st * S::STAGE_BYTES;
           uint8_t* vdst = kdst + S::TILE_BYTES;
           const uint32_t qbytes = i == 0 ? (uint32_t)(S::COL_BLOCKS * QROWS * 128) : 0u;
