@@ -60,13 +60,36 @@ def test_lowrank_bias_edge_shapes(case):
 @pytest.mark.parametrize("d_rel", [64, 32])
 def test_lowrank_bias_with_std4_bias(d_rel):
     """A bias of standard deviation 4 (the scores are dominated by it): the tile's bias is
-    held in fp16 on its way to the fp32 score, so this is where that rounding shows most."""
+    held in fp16 on its way to the fp32 score, so this is where that rounding would show."""
     prob = W.make_problem(num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=64, rel_extent=1024,
                           window=-1, q_lens=[700, 300], seq_lens=[700, 900], seed=88 + d_rel, device=DEV,
                           rel_std=4.0, lowrank_d=d_rel)
     out, err = run_gpu(prob)
     assert err == 0
     compare(out.float().cpu().numpy(), oracle_full(prob), f"low-rank bias, std 4, d_rel {d_rel}")
+
+
+@pytest.mark.parametrize("std,d_rel", [(4.0, 64), (0.5, 64), (4.0, 32)])
+def test_lowrank_bias_error_is_that_of_the_fp32_bias(std, d_rel):
+    """The bias tile passes through fp16 in the low-rank path (fp32 products, rounded to fp16
+    in the ring, back to fp32 for the score).  Against the fp64 oracle its error must be no
+    larger than the fp32-bias entry's on the same bias (built in fp64, rounded to fp32): the
+    budget goes to the bf16 P and output, which both paths share, not to the fp16 step."""
+    import numpy as np
+    prob = W.make_problem(num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=64, rel_extent=1024,
+                          window=-1, q_lens=[700, 300], seq_lens=[700, 900], seed=88 + d_rel, device=DEV,
+                          rel_std=std, lowrank_d=d_rel)
+    ref = oracle_full(prob)
+    a, err_a = run_gpu(prob)
+    mat = (prob.r.double().reshape(-1, d_rel) @ prob.rel_proj_t.double().t()).float()
+    prob.r, prob.rel_proj_t, prob.rel_logits = None, None, mat.reshape(prob.total_q, prob.num_q_heads, -1).contiguous()
+    b, err_b = run_gpu(prob)
+    assert err_a == 0 and err_b == 0
+    ea, eb = a.float().cpu().numpy() - ref, b.float().cpu().numpy() - ref
+    ma, mb = float(np.abs(ea).max()), float(np.abs(eb).max())
+    ra, rb = float(np.linalg.norm(ea) / np.linalg.norm(ref)), float(np.linalg.norm(eb) / np.linalg.norm(ref))
+    print(f"std {std} d_rel {d_rel}: low-rank max_abs {ma:.3e} rel_rms {ra:.3e}; fp32 bias max_abs {mb:.3e} rel_rms {rb:.3e}")
+    assert ma <= 1.1 * mb + 1e-3 and ra <= 1.1 * rb + 1e-4
 
 
 def test_lowrank_bias_matches_the_materialised_bias_entry():
