@@ -418,6 +418,17 @@ def measure_kv(binding, name, dev, steps, warmup, stream, hbm_peak):
         for _, w in calls:
             assert binding.inkling_attn_read_device_error(w) == 0
         del graph, calls
+        # the same graph timing of as many one-element kernels: what a graph node alone costs
+        tiny = torch.zeros(1, device=dev)
+        with torch.cuda.stream(stream):
+            tiny.add_(1)
+        torch.cuda.synchronize()
+        g1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1, stream=stream):
+            for _ in range(n_inst):
+                tiny.add_(1)
+        extra["graph_one_element_kernel_ms"] = round(time_steps([g1.replay], replays, warmup, stream) / n_inst, 5)
+        del g1, tiny
         # one call alone, L2 flushed before it, and the same timing of a one-element kernel:
         # what launch and event latency alone cost
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)

@@ -126,6 +126,45 @@ __global__ void __launch_bounds__(KV_CONV_THREADS, 2) kv_conv_write_kernel(const
   __shared__ int cu_s[KV_SMALL_CACHED_SEQS + 1];
   __shared__ int len_s[KV_SMALL_CACHED_SEQS];
   const bool cached = a.B <= KV_SMALL_CACHED_SEQS;
+  const bool conv = gid < a.conv_items;
+  // A convolution thread's rows and taps depend on nothing else: their loads go out before
+  // the block stages the request offsets, so the two round trips overlap.
+  int v = 0, chunk = 0, z = 0;
+  if (conv) {
+    v = (int)(gid % a.nvec);
+    const long long rest = gid / a.nvec;
+    chunk = (int)(rest % a.nchunks);
+    z = (int)(rest / a.nchunks);                     // 0: K, 1: V
+  }
+  const uint16_t* __restrict__ x = a.x[z];
+  const int col = v * 8;                             // element offset inside a row
+  const int g = col / a.D, d = col % a.D;
+  const int t0 = chunk * TOK;
+  // this run's raw rows, loaded first so that TOK loads are in flight together, and the
+  // taps of these 8 channels: w[g, d + e, j] at ((g*D + d + e) * KS + j).  Threads past the
+  // convolution items issue no load (T may be 0, and x then points at nothing).
+  uint4 raw[TOK];
+  float flat[8 * KS];
+#pragma unroll
+  for (int k = 0; k < TOK; ++k) raw[k] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int q = 0; q < 8 * KS; ++q) flat[q] = 0.f;
+  if (conv) {
+#pragma unroll
+    for (int k = 0; k < TOK; ++k)
+      if (t0 + k < a.T) raw[k] = ld_row16(x + (size_t)(t0 + k) * row_elems + col);
+    const float4* wp = reinterpret_cast<const float4*>(a.w[z] + (size_t)(g * a.D + d) * KS);
+#pragma unroll
+    for (int q = 0; q < 2 * KS; ++q) {
+      const float4 f = __ldg(wp + q);
+      flat[4 * q] = f.x; flat[4 * q + 1] = f.y; flat[4 * q + 2] = f.z; flat[4 * q + 3] = f.w;
+    }
+  }
+  float w[KS][8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+#pragma unroll
+    for (int j = 0; j < KS; ++j) w[j][e] = flat[e * KS + j];
   if (cached) {
     for (int j = threadIdx.x; j <= a.B; j += KV_CONV_THREADS) {
       cu_s[j] = __ldg(a.cu_q + j);
@@ -133,40 +172,9 @@ __global__ void __launch_bounds__(KV_CONV_THREADS, 2) kv_conv_write_kernel(const
     }
   }
   __syncthreads();
-  if (gid < a.conv_items) {
+  if (conv) {
     // ---------------------------------------------------------------- convolution
-    const int v = (int)(gid % a.nvec);
-    const long long rest = gid / a.nvec;
-    const int chunk = (int)(rest % a.nchunks);
-    const int z = (int)(rest / a.nchunks);          // 0: K, 1: V
-    const uint16_t* __restrict__ x = a.x[z];
     uint16_t* __restrict__ cache = a.cache[z];
-    const int col = v * 8;                           // element offset inside a row
-    const int g = col / a.D, d = col % a.D;
-    const int t0 = chunk * TOK;
-
-    // this run's raw rows, loaded first so that TOK loads are in flight together
-    uint4 raw[TOK];
-#pragma unroll
-    for (int k = 0; k < TOK; ++k) {
-      const int t = t0 + k;
-      raw[k] = t < a.T ? ld_row16(x + (size_t)t * row_elems + col) : make_uint4(0, 0, 0, 0);
-    }
-    // taps of these 8 channels: w[g, d + e, j] at ((g*D + d + e) * KS + j)
-    float w[KS][8];
-    {
-      const float4* wp = reinterpret_cast<const float4*>(a.w[z] + (size_t)(g * a.D + d) * KS);
-      float flat[8 * KS];
-#pragma unroll
-      for (int q = 0; q < 2 * KS; ++q) {
-        const float4 f = __ldg(wp + q);
-        flat[4 * q] = f.x; flat[4 * q + 1] = f.y; flat[4 * q + 2] = f.z; flat[4 * q + 3] = f.w;
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-#pragma unroll
-        for (int j = 0; j < KS; ++j) w[j][e] = flat[e * KS + j];
-    }
 
     float win[KS > 1 ? KS - 1 : 1][8];   // rows at positions p - (KS-1) .. p - 1
     // The run is cut at request boundaries into segments [k, k_end); each segment loads
@@ -193,6 +201,11 @@ __global__ void __launch_bounds__(KV_CONV_THREADS, 2) kv_conv_write_kernel(const
       const bool seq_ok = n <= L;
       if (!seq_ok) record_error(a.err, INK_DEVERR_QLEN_EXCEEDS_KV);
       const int i0 = t - seq_start;                   // index of token t among the request's new rows
+      const int pos_t0 = L - n - seq_start + t0;      // position of run token 0 if it were in b
+      const int* bt_row = a.block_table + (size_t)b * a.max_pages;
+      // the page of the segment's first token, loaded beside the window rows
+      const int pidx0 = (pos_t0 + k) >> a.log2_page;
+      const int page0 = seq_ok && pidx0 >= 0 && pidx0 < a.max_pages ? __ldg(bt_row + pidx0) : -1;
 #pragma unroll
       for (int m = 0; m < KS - 1; ++m) {
         const int r = i0 - (KS - 1) + m;              // row of the new rows, or of the state if < 0
@@ -200,8 +213,6 @@ __global__ void __launch_bounds__(KV_CONV_THREADS, 2) kv_conv_write_kernel(const
                                      : a.st_in[z] + ((size_t)b * (KS - 1) + (KS - 1 + r)) * row_elems + col;
         unpack8(ld_row16(src), win[m]);
       }
-      const int pos_t0 = L - n - seq_start + t0;      // position of run token 0 if it were in b
-      const int* bt_row = a.block_table + (size_t)b * a.max_pages;
 #pragma unroll
       for (int kk = 0; kk < TOK; ++kk) {
         if (kk < k || kk >= k_end) continue;
@@ -226,7 +237,7 @@ __global__ void __launch_bounds__(KV_CONV_THREADS, 2) kv_conv_write_kernel(const
         if (!seq_ok) continue;
         const int p = pos_t0 + kk;
         const int pidx = p >> a.log2_page;
-        const int page = pidx < a.max_pages ? __ldg(bt_row + pidx) : -1;
+        const int page = pidx == pidx0 ? page0 : (pidx < a.max_pages ? __ldg(bt_row + pidx) : -1);
         if (page < 0 || page >= a.num_pages) {
           record_error(a.err, INK_DEVERR_PAGE_OUT_OF_RANGE);
           continue;
