@@ -668,6 +668,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       float m = -INFINITY, l = 0.f;
       const uint64_t scale2 = f2_pack(a.sm_scale, a.sm_scale);
       const uint64_t log2e2 = f2_pack(LOG2E, LOG2E);
+      const uint64_t scalelog2e2 = f2_pack(a.sm_scale * LOG2E, a.sm_scale * LOG2E);
       for (int j = 0; j < it.ntile; ++j, ++th) {
         const int k0 = (it.kt0 + j) * TILE_KEYS;
         const bool needs = pp_tile_needs_bias(it.pos0, k0, a.E);
@@ -722,6 +723,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         };
         float mxv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         const bool all_vis = vis == ~0ull;
+        bool raw_clamp = false;   // sr holds the raw scores, every key reading bucket E - 1
         if (__all_sync(0xffffffffu, all_vis && cc < 0)) {
           // every key visible, every bucket from the tile's bias rows
 #pragma unroll
@@ -734,16 +736,12 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             mxv[(c >> 1) & 3] = fmax3(mxv[(c >> 1) & 3], x, y);
           }
         } else if (__all_sync(0xffffffffu, all_vis && cc >= TILE_KEYS - 1)) {
-          // every key visible at distance >= E - 1
-          const uint64_t cl2 = f2_pack(clampv, clampv);
+          // every key visible at distance >= E - 1: s sm_scale + clampv for every key, so the max
+          // is taken over the raw scores and the row's constant goes into the exponent's FMA
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            float x, y;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2, cl2), x, y);
-            sr[c] = __float_as_uint(x);
-            sr[c + 1] = __float_as_uint(y);
-            mxv[(c >> 1) & 3] = fmax3(mxv[(c >> 1) & 3], x, y);
-          }
+          for (int c = 0; c < 64; c += 2)
+            mxv[(c >> 1) & 3] = fmax3(mxv[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+          raw_clamp = true;
         } else {
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
@@ -763,7 +761,8 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             mxv[(c >> 1) & 3] = fmax3(mxv[(c >> 1) & 3], x, y);
           }
         }
-        const float mx = fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3]));
+        float mx = fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3]));
+        if (raw_clamp) mx = fmaf(mx, a.sm_scale, clampv);
         if (needs) {
           // every bias value this thread read is consumed (mx depends on all of them)
           asm volatile("" ::"f"(mx) : "memory");
@@ -786,16 +785,19 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             if (mine) m = m_new;
           }
         }
-        // p = 2^(s log2(e) - m log2(e)); masked keys (s = -inf) give exactly 0
+        // p = 2^(s log2(e) - m log2(e)); masked keys (s = -inf) give exactly 0.  With raw
+        // scores: 2^(raw sm_scale log2(e) + clampv log2(e) - m log2(e)).
         const float mb = m == -INFINITY ? 0.f : m * LOG2E;
-        const uint64_t nmb2 = f2_pack(-mb, -mb);
+        const float addv = (raw_clamp ? clampv * LOG2E : 0.f) - mb;
+        const uint64_t nmb2 = f2_pack(addv, addv);
+        const uint64_t mul2 = raw_clamp ? scalelog2e2 : log2e2;
         uint32_t pk[32];
         uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};   // four packed partial sums (+0.0f pairs)
         auto exp_pairs = [&](int c0) {
 #pragma unroll
           for (int c = c0; c < c0 + 16; ++c) {
             float t0, t1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), log2e2, nmb2), t0, t1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), mul2, nmb2), t0, t1);
             const float p0 = fast_exp2(t0);
             const float p1 = fast_exp2(t1);
             ls2[c & 3] = f2_add(ls2[c & 3], f2_pack(p0, p1));
