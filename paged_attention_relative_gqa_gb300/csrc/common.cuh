@@ -54,6 +54,19 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
 // The first 1024-byte-aligned byte of dynamic shared memory, reached by pointer arithmetic on
 // the shared array itself so that the compiler still knows the pointer is in shared memory
 // (accesses through it compile to shared loads and stores, not generic ones).
+// Persistent kernels hand out work items round-robin: CTA c takes walk positions c,
+// c + gridDim.x, ...  Position i names item sched_item(i) of a list sorted longest first.
+// Every odd round that is not the last is handed out in reverse, so that a CTA that took the
+// longest item of one round takes the shortest of the next: every CTA's total is then within
+// about one item's length of the mean, where the plain order leaves CTA 0 a whole round's
+// spread of lengths ahead of the last CTA for every round.  A bijection on [0, total).
+__device__ __forceinline__ int sched_item(int i, int total) {
+  const int g = (int)gridDim.x;
+  const int k = i / g;
+  const int c = i - k * g;
+  return ((k & 1) && (k + 1) * g <= total) ? k * g + (g - 1 - c) : i;
+}
+
 __device__ __forceinline__ uint8_t* smem_align1024(uint8_t* raw) {
   return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
 }

@@ -7,7 +7,8 @@
 // ("Inkling attn backend cleanup fake registry", TensorRT-LLM PR #17860).
 //
 // Work item: 128 consecutive new tokens of one sequence and one query head.  One CTA
-// per SM walks items in order of decreasing causal length (static round-robin).
+// per SM walks items in order of decreasing causal length (static round-robin, every other
+// round reversed: sched_item).
 // Warp roles (384 threads):
 //   warps 0, 3  producers: TMA of the item's 128 query rows (q viewed as [tokens, Hq*D])
 //           and of 64-key K tiles (warp 0) and V tiles (warp 3) into separate rings (K is
@@ -142,8 +143,9 @@ struct PItem {
   bool bad_len;
 };
 
-__device__ __forceinline__ bool get_item(const PrefillArgs& a, int i, PItem& it) {
+__device__ __forceinline__ bool get_item(const PrefillArgs& a, int i_walk, PItem& it) {
   const int per_qt = a.B * a.Hq;
+  const int i = sched_item(i_walk, a.num_q_tiles * per_qt);
   const int qrev = i / per_qt;
   const int r = i - qrev * per_qt;
   it.b = r / a.Hq;
