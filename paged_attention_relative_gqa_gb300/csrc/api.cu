@@ -414,6 +414,7 @@ ink_status_t prefill_impl(const ink_attn_params_t* params, const void* q, const 
   a.d_rel = d_rel;
   a.bias_bulk = !lowrank && (bias_bf16 || ((params->rel_extent % 4 == 0) && aligned(rel_logits, 16)));
   a.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  a.io32 = aligned(q, 32) && aligned(out, 32) ? 1 : 0;
   std::memset(&maps.bias, 0, sizeof maps.bias);
   std::memset(&maps.lr_r, 0, sizeof maps.lr_r);
   std::memset(&maps.lr_p, 0, sizeof maps.lr_p);

@@ -52,6 +52,7 @@ struct PrefillArgs {
   const void* lr_proj_t;      // bf16 [E, d_rel]
   int d_rel;                  // a multiple of 8 in [8, 64]
   unsigned long long wait_ns; // limit of one pipeline wait (the drain waits keep 2 s)
+  int io32;                   // q and out 32-byte aligned: rows move in 256-bit loads and stores
 };
 
 // TMA descriptors of one decode call: K/V pools viewed as [num_pages*Hkv*P rows, D]

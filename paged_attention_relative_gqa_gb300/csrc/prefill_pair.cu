@@ -34,7 +34,9 @@
 //            3-D TMA boxes (32 tokens x COLS buckets) into the head's ring.
 //   warps 4-7, 8-11  softmax of head 0 and head 1: thread r owns row r (TMEM lane r).  Per
 //            item it loads its Q row (head 0: into TMEM; head 1: into shared memory, in the
-//            128-byte-swizzled layout of an MMA operand); per tile it reads its 64 scores, adds the bias,
+//            128-byte-swizzled layout of an MMA operand), the next item's as soon as the
+//            current item's last P is written, so that the next S overlaps the last P V
+//            product and the epilogue; per tile it reads its 64 scores, adds the bias,
 //            masks, keeps the running max and sum (O rescaled in TMEM only when the max grows
 //            by more than 2^8), writes P into TMEM; at the end it normalises O and stores bf16.  Pairs of
 //            scores go through packed two-lane fp32 FMA and add (the same rounding as scalar
@@ -127,35 +129,73 @@ __device__ __forceinline__ void pair_issue_pv(uint32_t d, uint32_t a0, uint64_t 
   umma_commit_warp(done);
 }
 
-// Load this thread's Q row (rows past the item's last are zero) into TMEM (D / 2 columns).
-template <int D>
-__device__ __forceinline__ void pair_load_q(const uint4* qsrc, bool rv, uint32_t tm_q) {
-#pragma unroll
-  for (int half = 0; half < D / 64; ++half) {
-    uint32_t qv[32];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 x = rv ? __ldg(qsrc + half * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
-      qv[4 * c] = x.x;
-      qv[4 * c + 1] = x.y;
-      qv[4 * c + 2] = x.z;
-      qv[4 * c + 3] = x.w;
-    }
-    tmem_st32(tm_q + 32 * half, qv);
+// 32 bytes of a row (p 32-byte aligned when IO32, else 16): one 256-bit load, or two 128-bit
+// ones.  A thread owns a whole row, so each load of a warp touches 32 rows; the wider load
+// halves the L1 requests of a row.
+template <bool IO32>
+__device__ __forceinline__ void ldg_row32(const uint4* p, uint32_t (&r)[8]) {
+  if constexpr (IO32) {
+    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "l"(p));
+  } else {
+    const uint4 x = __ldg(p), y = __ldg(p + 1);
+    r[0] = x.x; r[1] = x.y; r[2] = x.z; r[3] = x.w;
+    r[4] = y.x; r[5] = y.y; r[6] = y.z; r[7] = y.w;
   }
+}
+template <bool IO32>
+__device__ __forceinline__ void stg_row32(uint4* p, const uint32_t (&r)[8]) {
+  if constexpr (IO32) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]),
+                 "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+  } else {
+    p[0] = make_uint4(r[0], r[1], r[2], r[3]);
+    p[1] = make_uint4(r[4], r[5], r[6], r[7]);
+  }
+}
+
+// Load this thread's Q row (rows past the item's last are zero) into TMEM (D / 2 columns).
+// Every load of the row is issued before the first store.
+template <int D, bool IO32>
+__device__ __forceinline__ void pair_load_q(const uint4* qsrc, bool rv, uint32_t tm_q) {
+  uint32_t qv[D / 64][32];
+#pragma unroll
+  for (int c = 0; c < D / 16; ++c) {
+    uint32_t (&w)[8] = *reinterpret_cast<uint32_t(*)[8]>(&qv[c >> 2][8 * (c & 3)]);
+    if (rv) {
+      ldg_row32<IO32>(qsrc + 2 * c, w);
+    } else {
+#pragma unroll
+      for (int x = 0; x < 8; ++x) w[x] = 0u;
+    }
+  }
+#pragma unroll
+  for (int half = 0; half < D / 64; ++half) tmem_st32(tm_q + 32 * half, qv[half]);
   tmem_wait_st();
 }
 
 // Store this thread's Q row (rows past the item's last are zero) into shared memory as row r of
 // an MMA operand tile: CB blocks of 128 rows x 128 bytes, 16-byte chunk c of a row at chunk
 // position c ^ (r & 7) (the 128-byte swizzle).
-template <int D>
+template <int D, bool IO32>
 __device__ __forceinline__ void pair_store_q_smem(const uint4* qsrc, bool rv, uint8_t* qtile, int r) {
+  uint32_t x[D / 16][8];
 #pragma unroll
-  for (int c = 0; c < D / 8; ++c) {
-    const uint4 x = rv ? __ldg(qsrc + c) : make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(qtile + (c >> 3) * PP_Q1_SUB + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = x;
+  for (int c = 0; c < D / 16; ++c) {
+    if (rv) {
+      ldg_row32<IO32>(qsrc + 2 * c, x[c]);
+    } else {
+#pragma unroll
+      for (int y = 0; y < 8; ++y) x[c][y] = 0u;
+    }
   }
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c)
+    *reinterpret_cast<uint4*>(qtile + (c >> 3) * PP_Q1_SUB + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
+        make_uint4(x[c >> 1][4 * (c & 1)], x[c >> 1][4 * (c & 1) + 1], x[c >> 1][4 * (c & 1) + 2],
+                   x[c >> 1][4 * (c & 1) + 3]);
 }
 
 // Multiply this thread's row of O (D fp32 TMEM columns) by f.
@@ -173,23 +213,22 @@ __device__ __forceinline__ void pair_rescale_o(uint32_t tm_o, float f) {
   tmem_wait_st();
 }
 
-// out row = O / l in bf16 (written only when `store`).
-template <int D>
+// out row = O / l in bf16 (written only when `store`), 32 columns per TMEM load.
+template <int D, bool IO32>
 __device__ __forceinline__ void pair_store_o(uint32_t tm_o, float inv, uint4* orow, bool store) {
 #pragma unroll 1
-  for (int c2 = 0; c2 < D / 16; ++c2) {
-    uint32_t ov[16];
-    tmem_ld16(tm_o + c2 * 16, ov);
+  for (int c2 = 0; c2 < D / 32; ++c2) {
+    uint32_t ov[32];
+    tmem_ld32(tm_o + c2 * 32, ov);
     tmem_wait_ld();
     if (store) {
 #pragma unroll
-      for (int q4 = 0; q4 < 2; ++q4) {
-        uint4 v;
-        v.x = pack_bf16(__uint_as_float(ov[8 * q4 + 0]) * inv, __uint_as_float(ov[8 * q4 + 1]) * inv);
-        v.y = pack_bf16(__uint_as_float(ov[8 * q4 + 2]) * inv, __uint_as_float(ov[8 * q4 + 3]) * inv);
-        v.z = pack_bf16(__uint_as_float(ov[8 * q4 + 4]) * inv, __uint_as_float(ov[8 * q4 + 5]) * inv);
-        v.w = pack_bf16(__uint_as_float(ov[8 * q4 + 6]) * inv, __uint_as_float(ov[8 * q4 + 7]) * inv);
-        orow[c2 * 2 + q4] = v;
+      for (int q8 = 0; q8 < 2; ++q8) {
+        uint32_t w[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+          w[x] = pack_bf16(__uint_as_float(ov[16 * q8 + 2 * x]) * inv, __uint_as_float(ov[16 * q8 + 2 * x + 1]) * inv);
+        stg_row32<IO32>(orow + c2 * 4 + 2 * q8, w);
       }
     }
   }
@@ -248,12 +287,16 @@ struct BiasRow<true> {   // bf16: 33 aligned 32-bit loads per row, pairs funnel-
   }
 };
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool IO32>
 __global__ void __launch_bounds__(PP_THREADS, 1)
 prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmK3, const __grid_constant__ CUtensorMap tmV3,
                     const __grid_constant__ CUtensorMap tmB, const PrefillArgs a) {
   constexpr bool ES = BF16;
+  // fp32 bias: the next item's facts (its bucket E - 1, its page check) are read at the end
+  // of the current item along with its Q row.  (With the bf16 bias the kernel measured
+  // slower that way, and reads them at the item's start.)
+  constexpr bool CARRY = !BF16;
   using S = PPShape<D, ES>;
   using L_ = PPSmem<D, BF16>;
   using BS = PairBias<BF16>;
@@ -267,7 +310,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   uint64_t* k_empty = k_full + NK;
   uint64_t* v_full = k_empty + NK;
   uint64_t* v_empty = v_full + NV;
-  uint64_t* q_ready = v_empty + NV;   // [2] Q of the item in TMEM, O of the previous item read
+  uint64_t* q_ready = v_empty + NV;   // [2] Q_h of the item in place
   uint64_t* s_full = q_ready + 2;     // [2] S_h in TMEM (and every earlier product of the MMA warp done)
   uint64_t* s_empty = s_full + 2;     // [2] S_h read by the softmax
   uint64_t* p_full = s_empty + 2;     // [2] P_h in TMEM
@@ -599,10 +642,57 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     const uint32_t tm_o = tlane + S::TO + (uint32_t)(D * hs);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
     int th = 0, bcnt = 0, pvw = 0;   // tiles, bias tiles and pv_done phases seen, of this head slot
+    int q_in = -1;                   // item whose Q row went in at the end of the previous one
+    PPItem nx;                       // item q_in, with its row's bucket E - 1 and page check
+    float nx_clamp = 0.f;
+    bool nx_bad = false;
+    // This thread's Q row of item qi (rows past the item's last are zero): head 0 into TMEM,
+    // head 1 into shared memory (ES), then q_ready
+    auto load_q = [&](const PPItem& qi) {
+      const bool qv = r < qi.rows;
+      const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                         ((size_t)(qi.t0 + (qv ? r : 0)) * a.Hq + qi.h0 + hs) * D);
+      if (!ES || hs == 0) {
+        pair_load_q<D, IO32>(qsrc, qv, tm_q);
+        tc_fence_before();
+      } else {
+        pair_store_q_smem<D, IO32>(qsrc, qv, smem + L_::q1, r);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_ready[hs]);
+    };
+    // Bucket E - 1 of this thread's row of item qi (rows past the item's last read its last
+    // row: in bounds), and whether some page holding a key of the item lies outside the pool
+    // (then per-tile masks of unreadable keys are built); the table entries are read four
+    // per lane at a time.
+    auto item_clamp = [&](const PPItem& qi) -> float {
+      const bool qv = r < qi.rows;
+      const BT* relrow =
+          static_cast<const BT*>(a.rel) + ((size_t)(qi.t0 + (qv ? r : qi.rows - 1)) * a.Hq + qi.h0 + hs) * a.E;
+      return qv ? to_float_b(__ldg(relrow + a.E - 1)) : 0.f;
+    };
+    auto item_pages_bad = [&](const PPItem& qi) -> bool {
+      const int32_t* bq = a.block_table + (size_t)qi.b * a.max_pages;
+      const int p0 = qi.lo_min >> a.log2_page, p1 = qi.k_hi >> a.log2_page;
+      bool bad = false;
+#pragma unroll 1
+      for (int pi = p0 + lane; pi <= p1; pi += 128) {
+        int pg[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) pg[u] = __ldg(bq + min(pi + 32 * u, p1));
+#pragma unroll
+        for (int u = 0; u < 4; ++u) bad |= pg[u] < 0 || pg[u] >= a.num_pages;
+      }
+      return __any_sync(0xffffffffu, bad);
+    };
     bool go = true;
     for (int i = blockIdx.x; i < total_items && go; i += gridDim.x) {
       PPItem it;
-      if (!pp_item(a, i, it)) continue;
+      if (CARRY && q_in == i)
+        it = nx;
+      else if (!pp_item(a, i, it))
+        continue;
       if (hs == 0 && sw == 0 && lane == 0 && it.t0 == __ldg(a.cu_q + it.b) && it.h0 == 0) {
         if (it.n > a.max_q_len) record_error(a.err, INK_DEVERR_QLEN_EXCEEDS_MAX);
         if (it.bad_len) record_error(a.err, INK_DEVERR_QLEN_EXCEEDS_KV);
@@ -620,40 +710,34 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         }
         continue;
       }
-      // ---- Q row (rows past the item's last are zero): head 0 into TMEM, head 1 into shared
-      // memory; the previous item's S products that read Q_h are complete (their s_full was
-      // seen), and its O_h has been read
-      {
-        const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
-                                                           ((size_t)(it.t0 + (rv ? r : 0)) * a.Hq + h) * D);
-        if (!ES || hs == 0) {
-          pair_load_q<D>(qsrc, rv, tm_q);
-          tc_fence_before();
-        } else {
-          pair_store_q_smem<D>(qsrc, rv, smem + L_::q1, r);
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&q_ready[hs]);
-      }
-      const int pr = it.pos0 + r;
-      // bucket E - 1 of this row (rows past the item's last read its last row: in bounds)
-      const BT* relrow = static_cast<const BT*>(a.rel) + ((size_t)(it.t0 + (rv ? r : it.rows - 1)) * a.Hq + h) * a.E;
-      const float clampv = rv ? to_float_b(__ldg(relrow + a.E - 1)) : 0.f;
-      const int32_t* bt = a.block_table + (size_t)it.b * a.max_pages;
-      const int seg = P < TILE_KEYS ? P : TILE_KEYS;
-      // Does some page holding a key of the item lie outside the pool?  (Checked once per
-      // item; only then are per-tile masks of unreadable keys built.)
+      // ---- Q row and the item's facts, unless they came in at the end of the previous item
+      // (the previous item's S products that read Q_h are complete: their s_full was seen)
+      float clampv;
       bool item_bad = false;
-      {
+      if constexpr (CARRY) {
+        if (q_in == i) {
+          clampv = nx_clamp;
+          item_bad = nx_bad;
+        } else {
+          clampv = item_clamp(it);
+          load_q(it);
+          item_bad = item_pages_bad(it);
+        }
+      } else {
+        if (q_in != i) load_q(it);
+        clampv = item_clamp(it);
         const int p0 = it.lo_min >> a.log2_page, p1 = it.k_hi >> a.log2_page;
+        const int32_t* bq = a.block_table + (size_t)it.b * a.max_pages;
 #pragma unroll 1
         for (int pi = p0 + lane; pi <= p1; pi += 32) {
-          const int page = __ldg(bt + pi);
+          const int page = __ldg(bq + pi);
           item_bad |= page < 0 || page >= a.num_pages;
         }
         item_bad = __any_sync(0xffffffffu, item_bad);
       }
+      const int pr = it.pos0 + r;
+      const int32_t* bt = a.block_table + (size_t)it.b * a.max_pages;
+      const int seg = P < TILE_KEYS ? P : TILE_KEYS;
       auto tile_bad = [&](int k0) {
         uint64_t bad = 0;
 #pragma unroll 1
@@ -826,6 +910,33 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         if (lane == 0) mbar_arrive(&p_full[hs]);
       }
       if (!go) break;
+      // ---- the next item's Q row goes in now, so that its first S product overlaps this
+      // item's last P V product and epilogue (S_h(last), the last reader of Q_h, is complete;
+      // the next item's first P V product, which overwrites O_h, follows this epilogue)
+      {
+        int ni = i + (int)gridDim.x;
+        if constexpr (CARRY) {
+          nx = PPItem{};   // (written on every path: nothing of it lives through the tile loop)
+          nx_clamp = 0.f;
+          nx_bad = false;
+          for (; ni < total_items; ni += gridDim.x)
+            if (pp_item(a, ni, nx) && hs < nx.nh && nx.ntile > 0) break;
+          if (ni < total_items) {
+            nx_clamp = item_clamp(nx);
+            load_q(nx);
+            nx_bad = item_pages_bad(nx);
+            q_in = ni;
+          }
+        } else {
+          PPItem nq;
+          for (; ni < total_items; ni += gridDim.x)
+            if (pp_item(a, ni, nq) && hs < nq.nh && nq.ntile > 0) break;
+          if (ni < total_items) {
+            load_q(nq);
+            q_in = ni;
+          }
+        }
+      }
       // ---- epilogue: O_h / l -> bf16 -> out, once the item's last P V product is done
       if (!ES || pvw < th) {
         go = pp_wait_warp(&pv_done[hs], (uint32_t)(th - 1) & 1u, abort_flag, a);
@@ -833,8 +944,8 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         pvw = th;
       }
       tc_fence_after();
-      pair_store_o<D>(tm_o, l > 0.f ? 1.f / l : 0.f, reinterpret_cast<uint4*>(out + ((size_t)(it.t0 + r) * a.Hq + h) * D),
-                      rv);
+      pair_store_o<D, IO32>(tm_o, l > 0.f ? 1.f / l : 0.f, reinterpret_cast<uint4*>(out + ((size_t)(it.t0 + r) * a.Hq + h) * D),
+                            rv);
       tc_fence_before();
     }
   }
@@ -853,25 +964,30 @@ int num_sms_pp() {
   return n > 0 ? n : 148;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool IO32>
 cudaError_t launch_pair_t(const PrefillMaps& m, const PrefillArgs& a, cudaStream_t stream) {
   constexpr size_t smem = PPSmem<D, BF16>::alloc;
   static_assert(smem <= 227 * 1024, "shared memory budget");
   static std::atomic<unsigned long long> opted{0};
-  cudaError_t e = smem_opt_in_once(prefill_pair_kernel<D, BF16>, (int)smem, opted);
+  cudaError_t e = smem_opt_in_once(prefill_pair_kernel<D, BF16, IO32>, (int)smem, opted);
   if (e != cudaSuccess) return e;
   const long long items = (long long)a.num_q_tiles * a.B * a.Hkv * ((a.G + 1) / 2);
   const int grid = (int)std::min<long long>(items, num_sms_pp());
-  prefill_pair_kernel<D, BF16><<<grid, PP_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.bias, a);
+  prefill_pair_kernel<D, BF16, IO32><<<grid, PP_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.bias, a);
   return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_pair_io(const PrefillMaps& m, const PrefillArgs& a, cudaStream_t stream) {
+  return a.io32 ? launch_pair_t<D, BF16, true>(m, a, stream) : launch_pair_t<D, BF16, false>(m, a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_pair(const PrefillMaps& m, const PrefillArgs& a, int head_dim, cudaStream_t stream) {
   if (a.bias_bf16)
-    return head_dim == 128 ? launch_pair_t<128, true>(m, a, stream) : launch_pair_t<64, true>(m, a, stream);
-  return head_dim == 128 ? launch_pair_t<128, false>(m, a, stream) : launch_pair_t<64, false>(m, a, stream);
+    return head_dim == 128 ? launch_pair_io<128, true>(m, a, stream) : launch_pair_io<64, true>(m, a, stream);
+  return head_dim == 128 ? launch_pair_io<128, false>(m, a, stream) : launch_pair_io<64, false>(m, a, stream);
 }
 
 }  // namespace ink

@@ -318,3 +318,35 @@ def test_error_word_is_clear_after_good_calls():
     prob = _mid_problem()
     _, err = run_gpu(prob)
     assert err == 0
+
+
+def _at_16_byte_offset(t: torch.Tensor) -> torch.Tensor:
+    """A copy of `t` whose storage starts 16 bytes past a 32-byte boundary."""
+    step = 16 // t.element_size()
+    buf = torch.empty(t.numel() + 32 // t.element_size(), dtype=t.dtype, device=t.device)
+    base = (-buf.data_ptr() % 32) // t.element_size()
+    view = buf[base + step:base + step + t.numel()].view(t.shape)
+    view.copy_(t)
+    assert view.data_ptr() % 32 == 16
+    return view
+
+
+@pytest.mark.parametrize("bias_dtype", [torch.float32, torch.bfloat16])
+def test_prefill_with_q_and_out_only_16_byte_aligned(bias_dtype):
+    """The C ABI asks 16-byte alignment of q and out.  The head-pair prefill moves rows in
+    256-bit loads and stores when both are 32-byte aligned and in 128-bit ones otherwise; the
+    two give the same bits, and the oracle agrees."""
+    prob = W.make_problem(num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=64, rel_extent=600,
+                          window=-1, q_lens=[300, 129, 1], seq_lens=[700, 129, 40], seed=31, device=DEV,
+                          bias_dtype=bias_dtype)
+    ref, _ = run_gpu(prob)
+    q_aligned = prob.q
+    prob.q = _at_16_byte_offset(q_aligned)
+    params = binding.params_of(prob)
+    ws = binding.alloc_workspace(params, True, prob.q.device)
+    out = _at_16_byte_offset(torch.full_like(prob.q, float("nan")))
+    binding.run(prob, out=out, workspace=ws)
+    assert binding.inkling_attn_read_device_error(ws) == 0
+    assert np.array_equal(bits(out), bits(ref))
+    prob.q = q_aligned
+    compare(out.float().cpu().numpy(), oracle_full(prob), f"prefill, q/out at 16-byte offsets, {bias_dtype}")
