@@ -78,7 +78,9 @@ struct PPShape {
   static constexpr uint32_t PSTRIDE = ES ? 32 : 64;
   static constexpr uint32_t TO = ES ? QC + 192 : 2 * QC + 128;   // O_h at TO + D h
   static_assert(TO + 2 * D <= 512, "tensor memory budget");
-  static constexpr int Q1_BYTES = ES ? CB * PP_Q1_SUB : 0;
+  // ES: Q_1, an MMA operand.  Otherwise the staging tile through which TMA brings each Q_h
+  // tile on its way into TMEM.
+  static constexpr int Q1_BYTES = CB * PP_Q1_SUB;
 };
 
 template <int D, bool BF16>
@@ -91,8 +93,8 @@ struct PPSmem {
   static constexpr size_t bias = q1 + (size_t)S::Q1_BYTES;
   static constexpr size_t bars = bias + (size_t)2 * B::NB * B::SLOT_BYTES;
   // k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], q_ready[2], s_full[2], s_empty[2],
-  // p_full[2], pv_done[2], b_full[2 NB], b_empty[2 NB], drain[2]
-  static constexpr int NBAR = 2 * S::NK + 2 * S::NV + 10 + 4 * B::NB + 2;
+  // p_full[2], pv_done[2], b_full[2 NB], b_empty[2 NB], drain[2], qs_full[2], qs_empty[2]
+  static constexpr int NBAR = 2 * S::NK + 2 * S::NV + 10 + 4 * B::NB + 6;
   static constexpr size_t vbad = bars + NBAR * 8;
   static constexpr size_t misc = vbad + S::NV * 8;
   static constexpr size_t total = misc + 32;
@@ -291,7 +293,8 @@ template <int D, bool BF16, bool IO32>
 __global__ void __launch_bounds__(PP_THREADS, 1)
 prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmK3, const __grid_constant__ CUtensorMap tmV3,
-                    const __grid_constant__ CUtensorMap tmB, const PrefillArgs a) {
+                    const __grid_constant__ CUtensorMap tmQ3, const __grid_constant__ CUtensorMap tmB,
+                    const PrefillArgs a) {
   constexpr bool ES = BF16;
   // fp32 bias: the next item's facts (its bucket E - 1, its page check) are read at the end
   // of the current item along with its Q row.  (With the bf16 bias the kernel measured
@@ -318,9 +321,12 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   uint64_t* b_full = pv_done + 2;     // [2 NB] head h's slot s at h NB + s
   uint64_t* b_empty = b_full + 2 * NB;
   uint64_t* drain = b_empty + 2 * NB;   // [2] one per MMA-issuing warp
+  uint64_t* qs_full = drain + 2;        // [2] (fp32 bias) Q_h tile staged in shared memory
+  uint64_t* qs_empty = qs_full + 2;     // [2] (fp32 bias) head h's warps have read it
   uint64_t* vbad = reinterpret_cast<uint64_t*>(smem + L_::vbad);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L_::misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L_::misc + 4);
+  int* qs_issued = reinterpret_cast<int*>(smem + L_::misc + 8);   // [2] staged tiles issued per head
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = 1 << a.log2_page;
@@ -348,6 +354,11 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     }
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&qs_full[x], 1);
+      mbar_init(&qs_empty[x], 4);
+      qs_issued[x] = 0;
+    }
     fence_mbar_init();
     *abort_flag = 0;
   }
@@ -646,9 +657,64 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     PPItem nx;                       // item q_in, with its row's bucket E - 1 and page check
     float nx_clamp = 0.f;
     bool nx_bad = false;
-    // This thread's Q row of item qi (rows past the item's last are zero): head 0 into TMEM,
-    // head 1 into shared memory (ES), then q_ready
-    auto load_q = [&](const PPItem& qi) {
+    // fp32 bias: Q tiles reach TMEM through one shared-memory staging tile, by TMA (128
+    // rows, all column blocks, the 128-byte swizzle), in the order (item, head 0), (item,
+    // head 1), (next item, head 0), ...  The warps of the head that has read a tile issue the
+    // next one, so one tile is in flight at a time: head 0's tile of the next item arrives
+    // while the current item is still running.  Rows past an item's last are other tokens'
+    // queries (or zeros past the tensor): their scores are masked and never stored.
+    constexpr bool QSTAGE = !ES;
+    int qsn = 0;   // staged tiles this head slot has taken
+    auto stage_q = [&](const PPItem& qi, int hq) {   // one thread
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive_expect_tx(&qs_full[hq], (uint32_t)S::Q1_BYTES);
+      tma_load_3d(smem + L_::q1, &tmQ3, 0, qi.t0, (qi.h0 + hq) * S::CB, &qs_full[hq]);
+      atomicAdd(&qs_issued[hq], 1);
+    };
+    // This thread's Q row of item qi (index qidx) into TMEM (fp32 bias: from the staging tile;
+    // bf16 bias: head 0 from global memory, rows past the item's last zero; head 1 into shared
+    // memory), then q_ready.  False after an abort.
+    auto load_q = [&](const PPItem& qi, int qidx) -> bool {
+      if constexpr (QSTAGE) {
+        if (hs == 0 && qsn == 0 && sw == 0 && lane == 0) stage_q(qi, 0);   // the first tile
+        if (!pp_wait_warp(&qs_full[hs], (uint32_t)qsn & 1u, abort_flag, a)) return false;
+        ++qsn;
+        {
+          const uint8_t* st = smem + L_::q1;
+          uint32_t qv[D / 64][32];
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            const uint4 x = *reinterpret_cast<const uint4*>(st + (c >> 3) * PP_Q1_SUB + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+            qv[c >> 3][4 * (c & 7)] = x.x;
+            qv[c >> 3][4 * (c & 7) + 1] = x.y;
+            qv[c >> 3][4 * (c & 7) + 2] = x.z;
+            qv[c >> 3][4 * (c & 7) + 3] = x.w;
+          }
+#pragma unroll
+          for (int half = 0; half < D / 64; ++half) tmem_st32(tm_q + 32 * half, qv[half]);
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&q_ready[hs]);
+          mbar_arrive(&qs_empty[hs]);
+        }
+        if (sw == 0) {   // the next tile, once this head's four warps have read this one
+          if (!pp_wait_warp(&qs_empty[hs], (uint32_t)(qsn - 1) & 1u, abort_flag, a)) return false;
+          if (hs == 0 && qi.nh == 2) {
+            if (lane == 0) stage_q(qi, 1);
+          } else {
+            PPItem nq;
+            for (int ni = qidx + (int)gridDim.x; ni < total_items; ni += gridDim.x)
+              if (pp_item(a, ni, nq) && nq.ntile > 0) {
+                if (lane == 0) stage_q(nq, 0);
+                break;
+              }
+          }
+        }
+        return true;
+      }
       const bool qv = r < qi.rows;
       const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
                                                          ((size_t)(qi.t0 + (qv ? r : 0)) * a.Hq + qi.h0 + hs) * D);
@@ -661,6 +727,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_ready[hs]);
+      return true;
     };
     // Bucket E - 1 of this thread's row of item qi (rows past the item's last read its last
     // row: in bounds), and whether some page holding a key of the item lies outside the pool
@@ -720,11 +787,14 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           item_bad = nx_bad;
         } else {
           clampv = item_clamp(it);
-          load_q(it);
+          if (!load_q(it, i)) {
+            go = false;
+            break;
+          }
           item_bad = item_pages_bad(it);
         }
       } else {
-        if (q_in != i) load_q(it);
+        if (q_in != i) load_q(it, i);
         clampv = item_clamp(it);
         const int p0 = it.lo_min >> a.log2_page, p1 = it.k_hi >> a.log2_page;
         const int32_t* bq = a.block_table + (size_t)it.b * a.max_pages;
@@ -910,6 +980,25 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         if (lane == 0) mbar_arrive(&p_full[hs]);
       }
       if (!go) break;
+      // ---- epilogue: O_h / l -> bf16 -> out, once the item's last P V product is done
+      auto epilogue = [&]() -> bool {
+        if (!ES || pvw < th) {
+          if (!pp_wait_warp(&pv_done[hs], (uint32_t)(th - 1) & 1u, abort_flag, a)) return false;
+          pvw = th;
+        }
+        tc_fence_after();
+        pair_store_o<D, IO32>(tm_o, l > 0.f ? 1.f / l : 0.f,
+                              reinterpret_cast<uint4*>(out + ((size_t)(it.t0 + r) * a.Hq + h) * D), rv);
+        tc_fence_before();
+        return true;
+      };
+      // Head 1's staged tile is issued once head 0 has read its own: head 1 writes its output
+      // first, while that tile is on its way.
+      const bool epilogue_first = QSTAGE && hs == 1;
+      if (epilogue_first && !epilogue()) {
+        go = false;
+        break;
+      }
       // ---- the next item's Q row goes in now, so that its first S product overlaps this
       // item's last P V product and epilogue (S_h(last), the last reader of Q_h, is complete;
       // the next item's first P V product, which overwrites O_h, follows this epilogue)
@@ -923,7 +1012,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             if (pp_item(a, ni, nx) && hs < nx.nh && nx.ntile > 0) break;
           if (ni < total_items) {
             nx_clamp = item_clamp(nx);
-            load_q(nx);
+            go = load_q(nx, ni);
             nx_bad = item_pages_bad(nx);
             q_in = ni;
           }
@@ -932,26 +1021,28 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
           for (; ni < total_items; ni += gridDim.x)
             if (pp_item(a, ni, nq) && hs < nq.nh && nq.ntile > 0) break;
           if (ni < total_items) {
-            load_q(nq);
+            go = load_q(nq, ni);
             q_in = ni;
           }
         }
       }
-      // ---- epilogue: O_h / l -> bf16 -> out, once the item's last P V product is done
-      if (!ES || pvw < th) {
-        go = pp_wait_warp(&pv_done[hs], (uint32_t)(th - 1) & 1u, abort_flag, a);
-        if (!go) break;
-        pvw = th;
+      if (!go) break;
+      if (!epilogue_first && !epilogue()) {
+        go = false;
+        break;
       }
-      tc_fence_after();
-      pair_store_o<D, IO32>(tm_o, l > 0.f ? 1.f / l : 0.f, reinterpret_cast<uint4*>(out + ((size_t)(it.t0 + r) * a.Hq + h) * D),
-                            rv);
-      tc_fence_before();
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  // a staged Q tile still in flight (after an abort) lands before the CTA exits
+  if (!ES && tid == 0) {
+    for (int x = 0; x < 2; ++x) {
+      const int n = qs_issued[x];
+      if (n > 0 && !mbar_wait_bounded(&qs_full[x], (uint32_t)(n - 1) & 1u)) record_error(a.err, INK_DEVERR_WAIT_TIMEOUT);
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(512));
@@ -973,7 +1064,7 @@ cudaError_t launch_pair_t(const PrefillMaps& m, const PrefillArgs& a, cudaStream
   if (e != cudaSuccess) return e;
   const long long items = (long long)a.num_q_tiles * a.B * a.Hkv * ((a.G + 1) / 2);
   const int grid = (int)std::min<long long>(items, num_sms_pp());
-  prefill_pair_kernel<D, BF16, IO32><<<grid, PP_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.bias, a);
+  prefill_pair_kernel<D, BF16, IO32><<<grid, PP_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.q3, m.bias, a);
   return cudaGetLastError();
 }
 
