@@ -630,7 +630,10 @@ def run_ours(args, rank, world, local_rank):
                 continue
             st = steps_x if other in ("global_decode", "swa_prefill_tiny", "kv_prefill_global",
                                       "kv_decode_swa") else max(3, steps_x // 2)
+            ck = Clocks(local_rank)
+            ck.start()
             o = measure(binding, other, dev, st, min(args.warmup, 3), stream, hbm_peak, bf16_peak)
+            o["clocks"] = ck.stop()   # sampled over the workload's setup and its timed calls
             o.pop("probs", None)
             o.pop("kv_step", None)
             wl[other] = {k: (round(v, 5) if isinstance(v, float) else v) for k, v in o.items()
