@@ -15,12 +15,15 @@
 // in order of decreasing causal length (static round-robin); the two heads of an item share
 // their tokens, hence their visible keys, masks and K/V tiles.
 //
-// Tensor memory (512 columns for D = 128): Q of head 0 (the A operand of S_0 = Q_0 K^T, D/2
-// columns), S of head 0 and 1 (64 fp32 columns each), P of head 0 and 1 (softmax numerators,
-// 32 columns of bf16 pairs each: the A operand of O += P V), O of head 0 and 1 (D fp32 columns
-// each).  Q of head 1 does not fit and sits in shared memory (S_1 = Q_1 K^T reads both
-// operands from there).  With P apart from S, the next S of a head is computed as soon as the
-// softmax has read the current one, so the softmax never waits for its own P V product.
+// Tensor memory (512 columns for D = 128), bf16 bias: Q of head 0 (the A operand of
+// S_0 = Q_0 K^T, D/2 columns), S of head 0 and 1 (64 fp32 columns each), P of head 0 and 1
+// (softmax numerators, 32 columns of bf16 pairs each: the A operand of O += P V), O of head 0
+// and 1 (D fp32 columns each).  Q of head 1 does not fit and sits in shared memory
+// (S_1 = Q_1 K^T reads both operands from there).  With P apart from S, the next S of a head
+// is computed as soon as the softmax has read the current one, so the softmax never waits
+// for its own P V product.  fp32 bias (whose bias ring leaves no room for Q of head 1): Q of
+// both heads in TMEM, P over the first columns of S, and the next S of a head after its P V
+// product; Q tiles come into TMEM through one shared-memory staging tile loaded by TMA.
 //
 // Warp roles (384 threads):
 //   warp 0   K and V producer: one TMA box per 64-key tile (or one per page segment when
@@ -33,10 +36,11 @@
 //   warp 2   bias producer: per tile that reads any bucket below E - 1 and per head, up to four
 //            3-D TMA boxes (32 tokens x COLS buckets) into the head's ring.
 //   warps 4-7, 8-11  softmax of head 0 and head 1: thread r owns row r (TMEM lane r).  Per
-//            item it loads its Q row (head 0: into TMEM; head 1: into shared memory, in the
-//            128-byte-swizzled layout of an MMA operand), the next item's as soon as the
-//            current item's last P is written, so that the next S overlaps the last P V
-//            product and the epilogue; per tile it reads its 64 scores, adds the bias,
+//            item it loads its Q row (bf16 bias, head 0: into TMEM; head 1: into shared
+//            memory, in the 128-byte-swizzled layout of an MMA operand; fp32 bias: from the
+//            staging tile into TMEM), the next item's as soon as the current item's last P is
+//            written, so that the next S overlaps the last P V product and the epilogue; per
+//            tile it reads its 64 scores, adds the bias,
 //            masks, keeps the running max and sum (O rescaled in TMEM only when the max grows
 //            by more than 2^8), writes P into TMEM; at the end it normalises O and stores bf16.  Pairs of
 //            scores go through packed two-lane fp32 FMA and add (the same rounding as scalar
