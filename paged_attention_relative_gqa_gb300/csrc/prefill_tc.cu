@@ -1020,21 +1020,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
           tmem_ld16(t_o1 + cc * 16, ow);
           tmem_wait_ld();
           if (store) {
+            uint32_t w[8];
 #pragma unroll
-            for (int q4 = 0; q4 < 2; ++q4) {
-              float y[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float a0 = has0 ? __uint_as_float(ov[8 * q4 + e]) * c0 : 0.f;
-                const float a1 = has1 ? __uint_as_float(ow[8 * q4 + e]) * c1 : 0.f;
-                y[e] = a0 + a1;
-              }
-              uint4 v;
-              v.x = pack_bf16(y[0], y[1]);
-              v.y = pack_bf16(y[2], y[3]);
-              v.z = pack_bf16(y[4], y[5]);
-              v.w = pack_bf16(y[6], y[7]);
-              orow[cc * 2 + q4] = v;
+            for (int e = 0; e < 8; ++e) {
+              const float a0 = has0 ? __uint_as_float(ov[2 * e]) * c0 : 0.f;
+              const float a1 = has1 ? __uint_as_float(ow[2 * e]) * c1 : 0.f;
+              const float b0 = has0 ? __uint_as_float(ov[2 * e + 1]) * c0 : 0.f;
+              const float b1 = has1 ? __uint_as_float(ow[2 * e + 1]) * c1 : 0.f;
+              w[e] = pack_bf16(a0 + a1, b0 + b1);
+            }
+            if (a.io32) {
+              asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(orow + cc * 2), "r"(w[0]),
+                           "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                           : "memory");
+            } else {
+              orow[cc * 2] = make_uint4(w[0], w[1], w[2], w[3]);
+              orow[cc * 2 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
             }
           }
         }

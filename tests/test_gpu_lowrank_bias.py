@@ -125,3 +125,23 @@ def test_lowrank_bias_global_prefill_sampled_rows_and_repeats():
     assert torch.equal(out, again)
     del prob, out, again
     torch.cuda.empty_cache()
+
+
+def test_lowrank_bias_with_q_and_out_only_16_byte_aligned():
+    """q and out 16-byte aligned but not 32 (the C ABI asks 16): the output rows then go out
+    in 128-bit stores instead of 256-bit ones, with the same bits."""
+    from tests.test_gpu_parity import _at_16_byte_offset
+    from tests.parity import bits
+    import numpy as np
+    prob = W.make_problem(num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=64, rel_extent=512,
+                          window=-1, q_lens=[300, 129], seq_lens=[700, 129], seed=41, device=DEV, lowrank_d=64)
+    ref, _ = run_gpu(prob)
+    q_aligned = prob.q
+    prob.q = _at_16_byte_offset(q_aligned)
+    params = binding.params_of(prob)
+    ws = binding.alloc_workspace(params, True, prob.q.device)
+    out = _at_16_byte_offset(torch.full_like(prob.q, float("nan")))
+    binding.run(prob, out=out, workspace=ws)
+    assert binding.inkling_attn_read_device_error(ws) == 0
+    assert np.array_equal(bits(out), bits(ref))
+    prob.q = q_aligned
