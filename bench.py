@@ -349,6 +349,14 @@ def e2e_decode_pipelined(binding, prob, steps, warmup, stream):
     torch.cuda.synchronize()
     assert binding.inkling_attn_read_device_error(ws) == 0
     del graph
+    # every step decodes the same inputs: both host copies of the output hold the bits of a
+    # plain device-resident call
+    ref = torch.empty_like(prob.q)
+    binding.inkling_attn_decode(params, prob.q, prob.k_cache, prob.v_cache, prob.block_table, prob.seq_lens,
+                                prob.rel_logits, ref, ws, stream)
+    torch.cuda.synchronize()
+    ref_h = ref.cpu()
+    assert all(torch.equal(o.view(torch.int16), ref_h.view(torch.int16)) for o in out_h), "e2e output differs"
     return start.elapsed_time(end) / (reps * E2E_GRAPH_STEPS)
 
 
