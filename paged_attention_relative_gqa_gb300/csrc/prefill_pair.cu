@@ -293,7 +293,7 @@ struct BiasRow<true> {   // bf16: 33 aligned 32-bit loads per row, pairs funnel-
   }
 };
 
-template <int D, bool BF16, bool IO32>
+template <int D, bool BF16, bool IO32, bool AHEAD2>
 __global__ void __launch_bounds__(PP_THREADS, 1)
 prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmK3, const __grid_constant__ CUtensorMap tmV3,
@@ -613,7 +613,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         if (!pp_tile_needs_bias(it.pos0, k0, a.E)) continue;
         const int dmin0 = it.pos0 - (k0 + TILE_KEYS - 1);
         const uint32_t nm = __ballot_sync(0xffffffffu, lane < NGR && pp_group_needed(a, it, k0, lane));
-        if constexpr (!BF16) {
+        if constexpr (!BF16 && !AHEAD2) {
           // fp32: one ring slot per head, so the slot frees late; start the boxes towards L2 now
 #pragma unroll 1
           for (int hs = 0; hs < it.nh; ++hs)
@@ -622,6 +622,26 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
               const int gr = __ffs(mm) - 1;
               tma_prefetch_l2_3d_warp(&tmB, pp_group_x<BS::ALIGN>(dmin0, gr), it.h0 + hs, it.t0 + BR * gr);
             }
+        }
+        if constexpr (!BF16 && AHEAD2) {
+          // the same a tile earlier (window layers, whose short items leave the first tiles
+          // of each item little time): the next tile's boxes at every tile, and this tile's
+          // when no earlier tile sent them
+          const bool sent = j > 0 && pp_tile_needs_bias(it.pos0, k0 - TILE_KEYS, a.E);
+#pragma unroll 1
+          for (int jj = sent ? 1 : 0; jj <= 1; ++jj) {
+            const int kp = k0 + jj * TILE_KEYS;
+            if (j + jj >= it.ntile || !pp_tile_needs_bias(it.pos0, kp, a.E)) continue;
+            const int dp = it.pos0 - (kp + TILE_KEYS - 1);
+            const uint32_t np = jj == 0 ? nm : __ballot_sync(0xffffffffu, lane < NGR && pp_group_needed(a, it, kp, lane));
+#pragma unroll 1
+            for (int hs = 0; hs < it.nh; ++hs)
+#pragma unroll 1
+              for (uint32_t mm = np; mm; mm &= mm - 1) {
+                const int gr = __ffs(mm) - 1;
+                tma_prefetch_l2_3d_warp(&tmB, pp_group_x<BS::ALIGN>(dp, gr), it.h0 + hs, it.t0 + BR * gr);
+              }
+          }
         }
         for (int hs = 0; hs < it.nh; ++hs) {
           const int slot = hs * NB + cnt[hs] % NB;
@@ -1059,22 +1079,29 @@ int num_sms_pp() {
   return n > 0 ? n : 148;
 }
 
-template <int D, bool BF16, bool IO32>
+template <int D, bool BF16, bool IO32, bool AHEAD2>
 cudaError_t launch_pair_t(const PrefillMaps& m, const PrefillArgs& a, cudaStream_t stream) {
   constexpr size_t smem = PPSmem<D, BF16>::alloc;
   static_assert(smem <= 227 * 1024, "shared memory budget");
   static std::atomic<unsigned long long> opted{0};
-  cudaError_t e = smem_opt_in_once(prefill_pair_kernel<D, BF16, IO32>, (int)smem, opted);
+  cudaError_t e = smem_opt_in_once(prefill_pair_kernel<D, BF16, IO32, AHEAD2>, (int)smem, opted);
   if (e != cudaSuccess) return e;
   const long long items = (long long)a.num_q_tiles * a.B * a.Hkv * ((a.G + 1) / 2);
   const int grid = (int)std::min<long long>(items, num_sms_pp());
-  prefill_pair_kernel<D, BF16, IO32><<<grid, PP_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.q3, m.bias, a);
+  prefill_pair_kernel<D, BF16, IO32, AHEAD2><<<grid, PP_THREADS, smem, stream>>>(m.k, m.v, m.k3, m.v3, m.q3,
+                                                                                 m.bias, a);
   return cudaGetLastError();
 }
 
+// The fp32-bias kernel of window layers sends its bias boxes towards L2 a tile earlier (a
+// kernel of its own, so that the global layers' code stays as it is).
 template <int D, bool BF16>
 cudaError_t launch_pair_io(const PrefillMaps& m, const PrefillArgs& a, cudaStream_t stream) {
-  return a.io32 ? launch_pair_t<D, BF16, true>(m, a, stream) : launch_pair_t<D, BF16, false>(m, a, stream);
+  if constexpr (!BF16) {
+    if (a.W > 0)
+      return a.io32 ? launch_pair_t<D, false, true, true>(m, a, stream) : launch_pair_t<D, false, false, true>(m, a, stream);
+  }
+  return a.io32 ? launch_pair_t<D, BF16, true, false>(m, a, stream) : launch_pair_t<D, BF16, false, false>(m, a, stream);
 }
 
 }  // namespace
