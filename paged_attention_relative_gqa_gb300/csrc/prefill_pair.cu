@@ -73,7 +73,7 @@ struct PPShape {
   static constexpr int CB = D / 64;
   static constexpr int KV_SUB = TILE_KEYS * 128;
   static constexpr int KV_TILE = CB * KV_SUB;
-  static constexpr int NK = D == 128 ? 2 : 4;   // K ring (freed when both S products are done)
+  static constexpr int NK = D == 128 ? (ES ? 3 : 2) : 4;   // K ring (freed when both S products are done)
   static constexpr int NV = D == 128 ? 2 : 4;   // V ring (freed when both P V products are done)
   static constexpr uint32_t QC = D / 2;          // TMEM columns of one Q tile (bf16 pairs)
   static constexpr uint32_t TQ = 0;              // Q_h at TQ + h QC (ES: Q_0 only)
